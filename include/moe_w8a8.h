@@ -1,0 +1,220 @@
+/*
+ * moe_w8a8.h -- C ABI of the W8A8 quantised mixture-of-experts layer for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The layer (one MoE feed-forward block of an LLM, serving-time forward):
+ *
+ *   router logits  l[t][e] = sum_h x[t][h] * Wr[h][e] (+ bias[e]), FP32
+ *   top-k          k largest logits per token (ties -> lower expert index),
+ *                  weights w = softmax over the selected logits
+ *   permutation    every (token, choice) gets a slot; expert e owns the
+ *                  contiguous slots [offsets[e], offsets[e+1]), tokens in
+ *                  ascending order
+ *   quantise       per token: s_x = amax_h |x| / 127,
+ *                  q_x = clamp(round_half_even(x / s_x), -128, 127)
+ *   GEMM1          acc1[s][n] = sum_h q_x[t(s)][h] * w13_q[e(s)][n][h]  (exact int32)
+ *   epilogue 1     g = (acc1[s][n] * s_x) * s_w13[e][n], u likewise at n + I,
+ *                  h = silu(g) * u = (g / (1 + exp(-g))) * u           (FP32)
+ *   requantise     per slot: s_h = amax_n |h| / 127, q_h = round(h / s_h)
+ *   GEMM2          acc2[s][c] = sum_n q_h[s][n] * w2_q[e(s)][c][n]      (exact int32)
+ *   epilogue 2     o[s][c] = (acc2[s][c] * s_h[s]) * s_w2[e][c]         (FP32)
+ *   combine        y[t][c] = bf16_rne(sum_j w[t][j] * o[slot(t, j)][c])
+ *
+ * Sources: the quantisation formula, per-channel weight scales, per-token
+ * dynamic activation scales and the scale outer product applied in the GEMM
+ * epilogue -- "W8A8 quantisation of MiniMax-M3 on K100AI" (mhpn.cn), section
+ * 2.1; FP32 accumulation with re-quantisation between operators -- "DeepSeek
+ * V4 950 FP8 inference on H100" (lpnh.cn), section 2.3; the FP32 router --
+ * same page, section 4.1; the gate -> top-k -> contiguous per-expert slots
+ * -> expert GEMMs -> weighted combine pipeline -- "Tencent Hunyuan AI Infra
+ * on Hopper" (pnsm.cn), section 1.3.
+ *
+ * Conventions for every call
+ *   - All data pointers are DEVICE pointers owned by the caller; the library
+ *     allocates and frees nothing.  bf16 tensors are passed as uint16_t bit
+ *     patterns.  Every pointer must be 16-byte aligned; tensors are dense and
+ *     row-major (last index contiguous).
+ *   - `stream` is a cudaStream_t (NULL = the legacy default stream).  Calls
+ *     only enqueue work on it and never synchronise, except
+ *     moe_w8a8_device_error.
+ *   - Arguments are checked on the host before anything is launched; a
+ *     failed check returns an error status and launches nothing.
+ *   - Calls on different streams are safe when their workspaces differ.
+ *   - The calls are deterministic: the same inputs give bit-identical
+ *     outputs.
+ */
+#ifndef MOE_W8A8_H
+#define MOE_W8A8_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define MOE_W8A8_API __attribute__((visibility("default")))
+#else
+#define MOE_W8A8_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+    MOE_OK = 0,
+    MOE_ERR_INVALID_ARG = -1,        /* null or misaligned pointer, bad count */
+    MOE_ERR_UNSUPPORTED_SHAPE = -2,  /* a dimension outside the supported set */
+    MOE_ERR_WORKSPACE_TOO_SMALL = -3,
+    MOE_ERR_CUDA = -4,               /* a CUDA runtime call or launch failed */
+    MOE_ERR_DEVICE_TIMEOUT = -5,     /* a device-side wait ran out of time */
+    MOE_ERR_NOT_IMPLEMENTED = -6,
+    MOE_ERR_DEVICE = -7              /* a device-side consistency check failed */
+} moe_status_t;
+
+/* Human-readable name of a status code (static string, never NULL). */
+MOE_W8A8_API const char* moe_w8a8_status_string(moe_status_t status);
+
+/* Library version as an integer major*10000 + minor*100 + patch. */
+MOE_W8A8_API int moe_w8a8_version(void);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_quantize_weights -- offline per-output-channel weight quantisation.
+ *
+ * For each of `rows` rows of length K:  s = max_k |w[k]| / 127 (binary32
+ * division), w_q[k] = clamp(round_half_even(w[k] / s), -128, 127); a row of
+ * zeros gives s = 0 and codes 0.  Weight scales are per output channel and
+ * computed once, offline ("W8A8 quantisation of MiniMax-M3 on K100AI",
+ * section 2.1).  Call it once per expert tensor: rows = E * 2I for w13
+ * (row order: expert, then gate rows 0..I-1, then up rows I..2I-1) and
+ * rows = E * H for w2.
+ *
+ *   w        fp32 [rows][K]  input
+ *   w_q      int8 [rows][K]  output
+ *   w_scale  fp32 [rows]     output
+ * Requirements: rows >= 0, 1 <= K <= 2^20.  rows == 0 is a no-op.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows, int64_t K, int8_t* w_q,
+                                       float* w_scale, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * Workspace of moe_w8a8_forward / moe_w8a8_forward_debug, in bytes, for the
+ * given shape.  Returns 0 for shapes the forward rejects.  The workspace is
+ * caller-owned device memory (256-byte aligned) that the forward uses for
+ * its intermediates (routing tables, quantised activations, the FP32 gate/up
+ * output, its requantised form and the per-slot expert outputs).  Its first
+ * 256 bytes hold the sticky device error word read by moe_w8a8_device_error;
+ * zero them once before the first call on a new workspace.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API size_t moe_w8a8_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_forward -- the whole MoE layer (see the top of this file).
+ *
+ *   x           bf16 [T][H]       activations
+ *   router_w    fp32 [H][E]       router weights (never quantised)
+ *   router_bias fp32 [E] or NULL  added to the logits before top-k
+ *   w13_q       int8 [E][2I][H]   gate rows 0..I-1 then up rows I..2I-1
+ *   w13_scale   fp32 [E][2I]
+ *   w2_q        int8 [E][H][I]    down projection
+ *   w2_scale    fp32 [E][H]
+ *   y           bf16 [T][H]       output
+ *   workspace   >= moe_w8a8_workspace_size(T, H, I, E, top_k) bytes
+ *
+ * Supported shapes: 0 <= T <= 2^20; H and I multiples of 128 with
+ * 128 <= H, I <= 16384; 1 <= E <= 256; 1 <= top_k <= min(E, 8).  T == 0 is a
+ * no-op that reads no pointer (NULL is accepted).  Integer results (routing, quantised codes, int32 accumulators)
+ * are exact; the router's binary32 sums can order two logits differently
+ * from an exact evaluation only when they differ by less than about 1e-6.
+ * Errors: MOE_ERR_INVALID_ARG (null/misaligned pointer), _UNSUPPORTED_SHAPE,
+ * _WORKSPACE_TOO_SMALL, _CUDA (launch failure).  Device-side timeouts are
+ * reported later through moe_w8a8_device_error.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_forward(const uint16_t* x, const float* router_w, const float* router_bias,
+                              const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                              const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                              int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                              void* stream);
+
+/* Device buffers that moe_w8a8_forward_debug fills with the intermediates
+ * (S = T * top_k).  Any field may be NULL (skipped).  The raw accumulators
+ * cost a full extra GEMM output each; use them on small shapes. */
+typedef struct {
+    int32_t* topk_ids;    /* [T][top_k]  selected experts, descending logit */
+    float* topk_w;        /* [T][top_k]  their weights */
+    int32_t* offsets;     /* [E+1]       slot offsets per expert */
+    int32_t* slot_of;     /* [T][top_k]  slot of each (token, choice) */
+    int32_t* slot_token;  /* [S]         token held by each slot */
+    float* s_x;           /* [T]         activation scales */
+    int8_t* q_x;          /* [T][H]      quantised activations */
+    int32_t* acc1;        /* [S][2I]     GEMM1 accumulators (gate | up) */
+    float* h;             /* [S][I]      FP32 gate/up output */
+    float* s_h;           /* [S]         requantisation scales */
+    int8_t* q_h;          /* [S][I]      requantised h */
+    int32_t* acc2;        /* [S][H]      GEMM2 accumulators */
+    float* o;             /* [S][H]      per-slot expert outputs */
+} moe_w8a8_debug_t;
+
+/* moe_w8a8_forward plus copies of the intermediates into `dbg` (same
+ * arguments and errors; `dbg` may be NULL). */
+MOE_W8A8_API moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float* router_w,
+                                    const float* router_bias, const int8_t* w13_q,
+                                    const float* w13_scale, const int8_t* w2_q,
+                                    const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                    int64_t E, int64_t top_k, uint16_t* y, void* workspace,
+                                    size_t workspace_bytes, void* stream,
+                                    const moe_w8a8_debug_t* dbg);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_linear -- one W8A8 linear layer, the dense form of the expert
+ * GEMM: per-token dynamic quantisation of x, exact INT8 GEMM, and the
+ * per-token x per-channel scale outer product in the epilogue
+ * ("W8A8 quantisation of MiniMax-M3 on K100AI", section 2.1):
+ *   y[m][n] = bf16_rne((acc[m][n] * s_x[m]) * w_scale[n]).
+ *
+ *   x        bf16 [M][K]
+ *   w_q      int8 [N][K]     per-output-channel quantised weights
+ *   w_scale  fp32 [N]
+ *   y        bf16 [M][N]
+ *   workspace >= moe_w8a8_linear_workspace_size(M, N, K) bytes
+ * Supported: 0 <= M <= 2^20; N, K multiples of 128 in [128, 65536].  M == 0
+ * is a no-op that reads no pointer.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API size_t moe_w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K);
+MOE_W8A8_API moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* w_scale, int64_t M,
+                             int64_t N, int64_t K, uint16_t* y, void* workspace,
+                             size_t workspace_bytes, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_device_error -- synchronise `stream`, then read and clear the
+ * sticky device error word in the first bytes of `workspace`.  Returns
+ * MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a pipeline wait inside a kernel gave up;
+ * the kernel released its resources and returned, its outputs are
+ * undefined), MOE_ERR_DEVICE (an internal consistency check failed) or
+ * MOE_ERR_CUDA (the synchronisation itself failed).
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_device_error(void* workspace, void* stream);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_set_wait_timeout_ns -- time limit of every spin-wait inside the
+ * kernels launched after this call (process-wide; default 2e9 ns = 2 s).
+ * A wait that runs out sets the device error word, abandons the kernel's
+ * remaining work, drains the copies it has in flight and returns.  Returns
+ * the previous limit.  0 restores the default.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_set_profile_events -- measurement hook.  While set (on the calling
+ * host thread), every moe_w8a8_forward records events[i] on its stream right
+ * before its i-th kernel launch (0 router/top-k, 1 scan, 2 permute+quantise,
+ * 3 GEMM1, 4 requantise, 5 GEMM2, 6 combine) and events[7] after the last,
+ * and moe_w8a8_linear records events[0] (quantise), events[1] (GEMM) and
+ * events[2] (end).  `events` holds `n` cudaEvent_t created by the caller
+ * (n >= 8); NULL turns the hook off.  Returns MOE_ERR_INVALID_ARG if n < 8.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_set_profile_events(void* const* events, int n);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_W8A8_H */

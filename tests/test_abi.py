@@ -1,0 +1,132 @@
+"""The C ABI without a GPU: the library loads, exports every function that
+include/moe_w8a8.h declares, and rejects bad arguments on the host before
+anything is launched."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from conftest import ROOT
+from w8a8_quantised_moe_gb300 import _lib
+from w8a8_quantised_moe_gb300 import build as lib_build
+
+HEADER = os.path.join(ROOT, "include", "moe_w8a8.h")
+OK, INVALID, SHAPE, WS_SMALL = 0, -1, -2, -3
+FAKE = 1 << 20  # an aligned, never dereferenced address
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return _lib.load()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(moe_w8a8_\w+)\s*\(", text)))
+
+
+def test_header_and_binding_agree():
+    assert sorted(_lib.EXPORTS) == declared_functions()
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.moe_w8a8_status_string(code).decode() == name
+    assert lib.moe_w8a8_status_string(12345).decode() == "MOE_ERR_UNKNOWN"
+    assert lib.moe_w8a8_version() >= 100
+
+
+@pytest.mark.parametrize("shape", [
+    (16, 100, 512, 8, 2),     # H not a multiple of 128
+    (16, 256, 500, 8, 2),     # I not a multiple of 128
+    (16, 256, 512, 0, 1),     # no experts
+    (16, 256, 512, 257, 2),   # too many experts
+    (16, 256, 512, 8, 0),     # top_k < 1
+    (16, 256, 512, 8, 9),     # top_k > 8
+    (16, 256, 512, 4, 5),     # top_k > E
+    (-1, 256, 512, 8, 2),     # negative T
+    (16, 32768, 512, 8, 2),   # H too large
+])
+def test_workspace_size_rejects_bad_shapes(lib, shape):
+    assert lib.moe_w8a8_workspace_size(*shape) == 0
+
+
+def test_workspace_size_grows_with_tokens(lib):
+    a = lib.moe_w8a8_workspace_size(16, 256, 512, 8, 2)
+    b = lib.moe_w8a8_workspace_size(32, 256, 512, 8, 2)
+    assert 0 < a < b
+    assert a % 256 == 0 and b % 256 == 0
+    # the largest configuration stays a few GB
+    big = lib.moe_w8a8_workspace_size(4096, 7168, 2048, 256, 8)
+    assert 0 < big < 4 << 30
+
+
+def _fwd(lib, T=16, H=256, I=512, E=8, k=2, ptrs=None, ws_bytes=None, bias=None):
+    p = dict(x=FAKE, rw=FAKE, w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, y=FAKE, ws=FAKE)
+    p.update(ptrs or {})
+    need = lib.moe_w8a8_workspace_size(T, H, I, E, k)
+    return lib.moe_w8a8_forward(p["x"], p["rw"], bias, p["w13"], p["s13"], p["w2"], p["s2"], T, H, I, E, k,
+                                p["y"], p["ws"], need if ws_bytes is None else ws_bytes, None)
+
+
+def test_forward_rejects_bad_arguments_without_launching(lib):
+    assert _fwd(lib, H=100) == SHAPE
+    assert _fwd(lib, k=9) == SHAPE
+    for name in ("x", "rw", "w13", "s13", "w2", "s2", "y", "ws"):
+        assert _fwd(lib, ptrs={name: None}) == INVALID, name
+        assert _fwd(lib, ptrs={name: FAKE + 4}) == INVALID, name  # misaligned
+    assert _fwd(lib, bias=FAKE + 8) == INVALID
+    assert _fwd(lib, ptrs={"ws": FAKE + 16}) == INVALID  # workspace must be 256-aligned
+    assert _fwd(lib, ws_bytes=1024) == WS_SMALL
+
+
+def test_forward_with_no_tokens_is_a_no_op(lib):
+    # T == 0 passes every check and returns before touching the device
+    assert _fwd(lib, T=0) == OK
+
+
+def test_linear_rejects_bad_arguments(lib):
+    need = lib.moe_w8a8_linear_workspace_size(64, 256, 256)
+    assert need > 0
+    assert lib.moe_w8a8_linear_workspace_size(64, 100, 256) == 0
+    assert lib.moe_w8a8_linear_workspace_size(64, 256, 0) == 0
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need - 1, None) == WS_SMALL
+    assert lib.moe_w8a8_linear(None, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need, None) == INVALID
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 200, 256, FAKE, FAKE, need, None) == SHAPE
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 0, 256, 256, FAKE, FAKE, need, None) == OK
+
+
+def test_quantize_weights_argument_checks(lib):
+    assert lib.moe_w8a8_quantize_weights(FAKE, 0, 64, FAKE, FAKE, None) == OK  # no rows
+    assert lib.moe_w8a8_quantize_weights(FAKE, 4, 0, FAKE, FAKE, None) == SHAPE
+    assert lib.moe_w8a8_quantize_weights(FAKE, -1, 64, FAKE, FAKE, None) == SHAPE
+    assert lib.moe_w8a8_quantize_weights(None, 4, 64, FAKE, FAKE, None) == INVALID
+    assert lib.moe_w8a8_quantize_weights(FAKE, 4, 64, FAKE + 1, FAKE, None) == INVALID
+
+
+def test_device_error_rejects_bad_workspace(lib):
+    assert lib.moe_w8a8_device_error(None, None) == INVALID
+    assert lib.moe_w8a8_device_error(FAKE + 16, None) == INVALID
+
+
+def test_wait_timeout_setting_round_trips(lib):
+    prev = lib.moe_w8a8_set_wait_timeout_ns(12345)
+    assert lib.moe_w8a8_set_wait_timeout_ns(prev) == 12345
+    assert lib.moe_w8a8_set_wait_timeout_ns(0) == prev  # 0 restores the default
+    assert lib.moe_w8a8_set_wait_timeout_ns(0) == 2_000_000_000
+
+
+def test_python_front_end_fails_loudly_without_library(tmp_path, monkeypatch):
+    import w8a8_quantised_moe_gb300 as moe
+    monkeypatch.setattr(_lib, "_lib", None)
+    with pytest.raises(ImportError):
+        _lib.load(str(tmp_path / "missing.so"))
+    assert moe.__name__  # the package itself imports without the library

@@ -1,0 +1,64 @@
+"""The benchmark's multi-rank bookkeeping on CPU (gloo, world size 2): the
+barrier, the max over ranks of the timed region, and the whole-job value.
+The layer itself is not sharded (replicas only), so this is all of the N > 1
+path apart from the per-rank GPU work."""
+import os
+import socket
+
+import pytest
+import torch.multiprocessing as mp
+
+import bench
+
+
+def _free_port():
+    with socket.socket() as s:
+        s.bind(("127.0.0.1", 0))
+        return s.getsockname()[1]
+
+
+def _worker(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), WORLD_SIZE=str(world),
+                      RANK=str(rank), LOCAL_RANK=str(rank))
+    ranks = bench.Ranks(backend="gloo")
+    try:
+        ranks.barrier()
+        seconds = 1.0 + rank  # rank 1 is the slow one
+        slowest = ranks.max(seconds)
+        value = bench.aggregate(units_per_rank=1000.0, world=ranks.world, max_seconds=slowest)
+        q.put((rank, ranks.world, slowest, value))
+    finally:
+        ranks.close()
+
+
+def test_two_rank_max_and_aggregate():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_worker, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    for p in procs:
+        p.join(timeout=120)
+        assert p.exitcode == 0
+    got = sorted(q.get(timeout=10) for _ in range(2))
+    for rank, world, slowest, value in got:
+        assert world == 2
+        assert slowest == 2.0
+        assert value == pytest.approx(1000.0 * 2 / 2.0)
+
+
+def test_single_rank_needs_no_process_group(monkeypatch):
+    for k in ("WORLD_SIZE", "RANK", "LOCAL_RANK"):
+        monkeypatch.delenv(k, raising=False)
+    r = bench.Ranks()
+    assert r.world == 1 and r.rank == 0 and r.dist is None
+    assert r.max(3.5) == 3.5
+    r.barrier()
+    assert bench.aggregate(100, 1, 0.5) == 200
+
+
+def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
+    monkeypatch.setenv("RANK", "1")
+    assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0"]) == 0
+    assert capsys.readouterr().out == ""

@@ -1,0 +1,220 @@
+"""Parity of the CUDA library with the CPU oracle, stage by stage, on seeded
+inputs that span several tiles and ragged tails.
+
+Integer results (routing, slots, quantised codes, int32 accumulators) must
+match bit for bit.  Float results are compared where the method is float:
+h differs only through expf; every later stage is checked bit-exactly on the
+GPU's own inputs to it (q_h from the GPU's h, acc2 from the GPU's q_h, o from
+the GPU's acc2, y from the GPU's o), and end to end within the layer's
+tolerance."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_quantised_moe_gb300 as moe
+from w8a8_quantised_moe_gb300 import build as lib_build
+from w8a8_quantised_moe_gb300 import workloads as wl
+from gpu_helpers import (H_RTOL, Layer, assert_y_close, bf16_from_dev, bf16_to_dev, bits_to_f32,
+                         y_errors)
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    moe._lib.load()
+
+
+TINY = wl.CONFIGS["tiny"]
+CASES = {
+    "tiny": TINY,
+    # S/E = 75 rows per expert: 128-row tiles, ragged tails
+    "wide_tiles": TINY.replace(T=300, H=512, I=384, E=8, k=2),
+    # 32-row tiles, router bias, top-4
+    "top4_bias": TINY.replace(T=77, H=384, I=256, E=16, k=4, bias="normal", bias_std=0.5),
+    # K > 1024 in both GEMMs: several exact accumulation chunks
+    "long_k": TINY.replace(T=100, H=1280, I=1152, E=4, k=2, n_outlier=13),
+    "single_expert": TINY.replace(T=45, H=256, I=256, E=1, k=1),
+    "one_token": TINY.replace(T=1, H=256, I=512, E=8, k=2),
+}
+
+
+def _stagewise(layer: Layer):
+    cfg = layer.cfg
+    names = ("topk_ids", "topk_w", "offsets", "slot_of", "slot_token", "s_x", "q_x", "acc1", "h",
+             "s_h", "q_h", "acc2", "o")
+    y_o, ref = layer.oracle(dump=names)
+    y_d, dev = moe.forward_debug(*layer.device_args())
+    torch.cuda.synchronize()
+    g = {k: v.cpu().numpy() for k, v in dev.items()}
+    y_g = bf16_from_dev(y_d)
+
+    # routing and permutation: exact
+    np.testing.assert_array_equal(g["topk_ids"], ref["topk_ids"])
+    np.testing.assert_allclose(g["topk_w"], ref["topk_w"], rtol=0, atol=1e-6)
+    np.testing.assert_array_equal(g["offsets"], ref["offsets"])
+    np.testing.assert_array_equal(g["slot_of"], ref["slot_of"])
+    np.testing.assert_array_equal(g["slot_token"], ref["slot_token"])
+    # activation quantisation: exact
+    np.testing.assert_array_equal(g["s_x"], ref["s_x"])
+    np.testing.assert_array_equal(g["q_x"], ref["q_x"])
+    # GEMM1 accumulators: exact
+    np.testing.assert_array_equal(g["acc1"], ref["acc1"])
+    # h: float, differs only through expf
+    np.testing.assert_allclose(g["h"], ref["h"], rtol=H_RTOL, atol=1e-30)
+    # requantisation of the GPU's own h: exact
+    q_h_ref, s_h_ref = oracle.quantize_rows(g["h"])
+    np.testing.assert_array_equal(g["s_h"], s_h_ref)
+    np.testing.assert_array_equal(g["q_h"], q_h_ref)
+    # GEMM2 on the GPU's own q_h, then its epilogue: exact
+    off = g["offsets"]
+    for e in range(cfg.E):
+        a, b = off[e], off[e + 1]
+        if a == b:
+            continue
+        acc2 = oracle.gemm_s8(g["q_h"][a:b], layer.w2_q[e])
+        np.testing.assert_array_equal(g["acc2"][a:b], acc2)
+        o = oracle.epilogue_scale(acc2, g["s_h"][a:b], layer.s2[e])
+        np.testing.assert_array_equal(g["o"][a:b], o)
+    # combine of the GPU's own o: exact
+    y_stage = oracle.combine(g["o"], g["slot_of"], g["topk_w"])
+    np.testing.assert_array_equal(y_g, y_stage)
+    # end to end: the layer's tolerance
+    assert_y_close(y_g, y_o)
+    mismatch = int((g["q_h"] != ref["q_h"]).sum())
+    return mismatch, y_errors(y_g, y_o)
+
+
+@pytest.mark.parametrize("name", list(CASES))
+def test_forward_matches_oracle_stage_by_stage(name):
+    mismatch, (max_err, max_ref, mean_rel) = _stagewise(Layer(CASES[name], seed=0))
+    cfg = CASES[name]
+    # end-to-end q_h codes can differ only where expf moved h across a
+    # rounding boundary: a vanishing fraction, each by one code
+    assert mismatch <= max(2, cfg.T * cfg.k * cfg.I // 10000)
+
+
+def test_forward_all_tokens_to_one_expert():
+    cfg = TINY.replace(T=150, H=256, I=256, E=6, k=1)
+    layer = Layer(cfg, seed=2)
+    layer.bias = np.array([0, 0, 0, 50, 0, 0], np.float32)  # every token picks expert 3
+    layer.d_bias = torch.from_numpy(layer.bias).cuda()
+    _stagewise(layer)
+
+
+def test_forward_plain_entry_equals_debug_entry_and_is_deterministic():
+    layer = Layer(CASES["wide_tiles"], seed=1)
+    y1 = moe.forward(*layer.device_args())
+    y2 = moe.forward(*layer.device_args())
+    y3, _ = moe.forward_debug(*layer.device_args(), fields=("h",))
+    torch.cuda.synchronize()
+    assert torch.equal(y1.view(torch.int16), y2.view(torch.int16))
+    assert torch.equal(y1.view(torch.int16), y3.view(torch.int16))
+
+
+def test_workspace_larger_than_needed_and_reused():
+    big = Layer(CASES["wide_tiles"], seed=3)
+    small = Layer(CASES["tiny"], seed=3)
+    ws = moe.new_workspace(moe.workspace_size(300, 512, 384, 8, 2))
+    y_big = moe.forward(*big.device_args(), workspace=ws)
+    y_small = moe.forward(*small.device_args(), workspace=ws)
+    assert moe.device_error(ws) == 0
+    assert_y_close(bf16_from_dev(y_big), big.oracle())
+    assert_y_close(bf16_from_dev(y_small), small.oracle())
+
+
+def test_empty_batch_is_a_no_op():
+    layer = Layer(TINY, seed=0)
+    x0 = torch.empty((0, TINY.H), dtype=torch.bfloat16, device="cuda")
+    y = moe.forward(x0, *layer.device_args()[1:])
+    assert y.shape == (0, TINY.H)
+
+
+# ------------------------------------------------------------------ weights
+
+def test_quantize_weights_bit_exact():
+    r = np.random.default_rng(11)
+    w = (r.standard_normal((300, 520)) * 0.02).astype(np.float32)
+    w[3] = 0.0
+    w[5] *= 1e-30
+    w[7] *= 1e20
+    w[9, 17] = 5.0  # one dominant channel
+    q_ref, s_ref = oracle.quantize_rows(w)
+    q, s = moe.quantize_weights(torch.from_numpy(w).cuda())
+    np.testing.assert_array_equal(s.cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(q.cpu().numpy(), q_ref)
+    # K not a multiple of 4 takes the scalar path
+    q2, s2 = moe.quantize_weights(torch.from_numpy(w[:, :131].copy()).cuda())
+    q2r, s2r = oracle.quantize_rows(w[:, :131])
+    np.testing.assert_array_equal(q2.cpu().numpy(), q2r)
+    np.testing.assert_array_equal(s2.cpu().numpy(), s2r)
+
+
+# ------------------------------------------------------------------- linear
+
+def _golden_linear_padded():
+    """The hand-worked 2x4 example of tests/golden/linear_2x4.txt, zero-padded
+    to K = N = 128 (padding changes neither the amax nor any sum)."""
+    x = np.zeros((2, 128), np.float32)
+    x[0, :4] = [1, -2, 0.5, 127]
+    x[1, :4] = [63.5, -1.25, 0.75, -0.25]
+    w = np.zeros((128, 128), np.int8)
+    w[0, :4] = [1, 1, 1, 1]
+    w[1, :4] = [-1, 0, 2, 1]
+    s_w = np.ones(128, np.float32)
+    s_w[:2] = [0.25, 0.125]
+    return x, w, s_w
+
+
+def test_linear_golden_example():
+    x, w, s_w = _golden_linear_padded()
+    xb = torch.from_numpy(x).to(torch.bfloat16).cuda()
+    y = moe.linear(xb, torch.from_numpy(w).cuda(), torch.from_numpy(s_w).cuda())
+    yf = y.float().cpu().numpy()
+    np.testing.assert_array_equal(yf[:, :2], np.array([[31.5, 15.75], [15.875, -7.6875]], np.float32))
+    assert (yf[:, 2:] == 0).all()
+
+
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 256, 384), (300, 384, 1280), (130, 128, 4096)])
+def test_linear_bit_exact(M, N, K):
+    cfg = wl.LINEAR
+    x = wl.draw_activations(7, cfg.cfg_id, M, K, max(1, K // 100))
+    w32 = (np.random.default_rng(M + N + K).standard_normal((N, K)) * 0.02).astype(np.float32)
+    w_q, s_w = oracle.quantize_rows(w32)
+    y_ref = oracle.linear(x, w_q, s_w)
+    y = moe.linear(bf16_to_dev(x), torch.from_numpy(w_q).cuda(), torch.from_numpy(s_w).cuda())
+    np.testing.assert_array_equal(bf16_from_dev(y), y_ref)
+
+
+# --------------------------------------------------------------- exactness
+
+def test_int32_accumulators_exact_on_worst_case_inputs():
+    """x = +-1 (every code +-127) against int8 weights spanning [-128, 127],
+    K = 7168: the exact sums run far beyond 2^24, so any fp32 rounding in the
+    tensor-core accumulation would show."""
+    T, H, I = 64, 7168, 128
+    r = np.random.default_rng(5)
+    x = np.where(r.random((T, H)) < 0.5, -1.0, 1.0).astype(np.float32)
+    x[:, :8] = 1.0  # some rows with long runs of one sign
+    x[0, :] = 1.0
+    xb = torch.from_numpy(x).to(torch.bfloat16)
+    w13 = r.integers(-128, 128, (1, 2 * I, H)).astype(np.int8)
+    w13[0, 0, :] = 127  # against row 0 of x: 7168 * 127 * 127 > 2^26
+    w13[0, 1, :] = -128
+    w2 = r.integers(-128, 128, (1, H, I)).astype(np.int8)
+    s13 = np.full((1, 2 * I), 1e-6, np.float32)
+    s2 = np.full((1, H), 1e-3, np.float32)
+    Wr = np.zeros((H, 1), np.float32)
+    args = (xb.cuda(), torch.from_numpy(Wr).cuda(), None, torch.from_numpy(w13).cuda(),
+            torch.from_numpy(s13).cuda(), torch.from_numpy(w2).cuda(), torch.from_numpy(s2).cuda(), 1)
+    _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
+    q_x = dev["q_x"].cpu().numpy()
+    assert (np.abs(q_x) == 127).all()
+    ref1 = q_x.astype(np.int64) @ w13[0].astype(np.int64).T
+    assert np.abs(ref1).max() > 2 ** 26
+    np.testing.assert_array_equal(dev["acc1"].cpu().numpy(), ref1)
+    q_h = dev["q_h"].cpu().numpy()
+    ref2 = q_h.astype(np.int64) @ w2[0].astype(np.int64).T
+    np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)

@@ -1,1 +1,190 @@
-"""W8A8 quantised mixture-of-experts layer for GB300 (sm_103a)."""
+"""W8A8 quantised mixture-of-experts layer for GB300 (sm_103a).
+
+Python front end of the C ABI in ``include/moe_w8a8.h``.  PyTorch provides
+device memory and streams; every step of the layer runs in the CUDA library
+``libmoe_w8a8.so`` (built in-tree by ``build.py``).  There is no CPU or
+PyTorch fallback: without the library every call raises.
+
+    import torch, w8a8_quantised_moe_gb300 as moe
+    w13_q, w13_s = moe.quantize_weights(w13_fp32.view(-1, H))   # offline
+    w2_q, w2_s = moe.quantize_weights(w2_fp32.view(-1, I))
+    y = moe.forward(x, router_w, None, w13_q.view(E, 2 * I, H), w13_s.view(E, 2 * I),
+                    w2_q.view(E, H, I), w2_s.view(E, H), top_k=2)
+"""
+from __future__ import annotations
+
+import ctypes
+
+from . import _lib
+from ._lib import MoeError, STATUS
+
+__all__ = [
+    "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward",
+    "forward_debug", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns",
+    "version",
+]
+
+
+def _torch():
+    import torch
+    return torch
+
+
+def _ptr(t):
+    return None if t is None else t.data_ptr()
+
+
+def _stream(stream):
+    torch = _torch()
+    s = torch.cuda.current_stream() if stream is None else stream
+    return s.cuda_stream
+
+
+def _need(t, dtype, shape, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_cuda or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous cuda {dtype} {tuple(shape)}, got {t.dtype} "
+                         f"{tuple(t.shape)} on {t.device}")
+
+
+def version() -> int:
+    return _lib.load().moe_w8a8_version()
+
+
+def set_wait_timeout_ns(ns: int) -> int:
+    """Time limit of every in-kernel wait for later launches; returns the previous one."""
+    return int(_lib.load().moe_w8a8_set_wait_timeout_ns(int(ns)))
+
+
+def quantize_weights(w, stream=None):
+    """Per-output-channel INT8 quantisation of fp32 ``w [rows, K]`` -> (int8 [rows, K], fp32 [rows])."""
+    torch = _torch()
+    rows, K = w.shape
+    _need(w, torch.float32, (rows, K), "w")
+    q = torch.empty((rows, K), dtype=torch.int8, device=w.device)
+    s = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    _lib.check(_lib.load().moe_w8a8_quantize_weights(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
+               "moe_w8a8_quantize_weights")
+    return q, s
+
+
+def workspace_size(T, H, I, E, top_k) -> int:
+    n = _lib.load().moe_w8a8_workspace_size(T, H, I, E, top_k)
+    if n == 0:
+        raise MoeError(-2, "moe_w8a8_workspace_size")
+    return int(n)
+
+
+def new_workspace(nbytes: int, device="cuda"):
+    """A zeroed device workspace (the error word starts cleared)."""
+    torch = _torch()
+    return torch.zeros(nbytes, dtype=torch.uint8, device=device)
+
+
+def _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k):
+    torch = _torch()
+    T, H = x.shape
+    E = router_w.shape[1]
+    I = w2_q.shape[2] if w2_q.dim() == 3 else 0
+    _need(x, torch.bfloat16, (T, H), "x")
+    _need(router_w, torch.float32, (H, E), "router_w")
+    if router_bias is not None:
+        _need(router_bias, torch.float32, (E,), "router_bias")
+    _need(w13_q, torch.int8, (E, 2 * I, H), "w13_q")
+    _need(w13_scale, torch.float32, (E, 2 * I), "w13_scale")
+    _need(w2_q, torch.int8, (E, H, I), "w2_q")
+    _need(w2_scale, torch.float32, (E, H), "w2_scale")
+    return T, H, I, E
+
+
+def forward(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, workspace=None, out=None,
+            stream=None):
+    """The MoE layer: bf16 x [T, H] -> bf16 y [T, H] (see include/moe_w8a8.h)."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k)
+    need = workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (T, H), "out")
+    _lib.check(_lib.load().moe_w8a8_forward(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "moe_w8a8_forward")
+    return y
+
+
+_DEBUG_FIELDS = {
+    # name: (dtype, shape(T, H, I, E, k))
+    "topk_ids": ("int32", lambda T, H, I, E, k: (T, k)),
+    "topk_w": ("float32", lambda T, H, I, E, k: (T, k)),
+    "offsets": ("int32", lambda T, H, I, E, k: (E + 1,)),
+    "slot_of": ("int32", lambda T, H, I, E, k: (T, k)),
+    "slot_token": ("int32", lambda T, H, I, E, k: (T * k,)),
+    "s_x": ("float32", lambda T, H, I, E, k: (T,)),
+    "q_x": ("int8", lambda T, H, I, E, k: (T, H)),
+    "acc1": ("int32", lambda T, H, I, E, k: (T * k, 2 * I)),
+    "h": ("float32", lambda T, H, I, E, k: (T * k, I)),
+    "s_h": ("float32", lambda T, H, I, E, k: (T * k,)),
+    "q_h": ("int8", lambda T, H, I, E, k: (T * k, I)),
+    "acc2": ("int32", lambda T, H, I, E, k: (T * k, H)),
+    "o": ("float32", lambda T, H, I, E, k: (T * k, H)),
+}
+
+
+def forward_debug(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, fields=None,
+                  workspace=None, stream=None):
+    """``forward`` plus the intermediates named in ``fields`` (default: all)
+    as device tensors.  Returns (y, dict)."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k)
+    need = workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    fields = tuple(_DEBUG_FIELDS) if fields is None else tuple(fields)
+    bufs = _lib.DebugBuffers()
+    out = {}
+    for name in fields:
+        dt, shape = _DEBUG_FIELDS[name]
+        t = torch.zeros(shape(T, H, I, E, top_k), dtype=getattr(torch, dt), device=x.device)
+        out[name] = t
+        setattr(bufs, name, t.data_ptr())
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _lib.check(_lib.load().moe_w8a8_forward_debug(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), ctypes.byref(bufs)), "moe_w8a8_forward_debug")
+    return y, out
+
+
+def linear_workspace_size(M, N, K) -> int:
+    n = _lib.load().moe_w8a8_linear_workspace_size(M, N, K)
+    if n == 0:
+        raise MoeError(-2, "moe_w8a8_linear_workspace_size")
+    return int(n)
+
+
+def linear(x, w_q, w_scale, workspace=None, out=None, stream=None):
+    """W8A8 linear layer: bf16 x [M, K], int8 w_q [N, K], fp32 w_scale [N] -> bf16 [M, N]."""
+    torch = _torch()
+    M, K = x.shape
+    N = w_q.shape[0]
+    _need(x, torch.bfloat16, (M, K), "x")
+    _need(w_q, torch.int8, (N, K), "w_q")
+    _need(w_scale, torch.float32, (N,), "w_scale")
+    need = linear_workspace_size(M, N, K)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    y = out if out is not None else torch.empty((M, N), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (M, N), "out")
+    _lib.check(_lib.load().moe_w8a8_linear(_ptr(x), _ptr(w_q), _ptr(w_scale), M, N, K, _ptr(y), _ptr(workspace),
+                                           workspace.numel() * workspace.element_size(), _stream(stream)),
+               "moe_w8a8_linear")
+    return y
+
+
+def device_error(workspace, stream=None) -> int:
+    """Synchronise the stream, read and clear the workspace's device error word (a status code)."""
+    return int(_lib.load().moe_w8a8_device_error(_ptr(workspace), _stream(stream)))

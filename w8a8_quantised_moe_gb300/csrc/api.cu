@@ -1,0 +1,360 @@
+// api.cu -- the C ABI (include/moe_w8a8.h): argument checks, workspace
+// layout and the launch sequence of the layer.
+//
+// Forward launch sequence on the caller's stream (no host synchronisation):
+//   1 router_topk      logits, top-k, weights, chunk counts and ranks
+//   2 scan             expert offsets, first slot of every (chunk, expert)
+//   3 permute_quant    slots; per-token quantisation scattered into slots
+//   4 grouped GEMM 1   gate/up GEMM + scale outer product + SiLU(gate)*up -> h
+//   5 requant          per-slot requantisation of h
+//   6 grouped GEMM 2   down GEMM + scale outer product -> o
+//   7 combine          weighted sum of each token's k slot rows -> y (bf16)
+#include <atomic>
+#include <cstring>
+
+#include "../../include/moe_w8a8.h"
+#include "internal.h"
+
+namespace moe {
+
+int num_sms() {
+    int dev = 0, n = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return 1;
+    if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n < 1) return 1;
+    return n;
+}
+
+namespace {
+
+std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+thread_local cudaEvent_t const* t_events = nullptr;  // measurement hook
+
+cudaError_t mark(int i, cudaStream_t st) {
+    return t_events ? cudaEventRecord(t_events[i], st) : cudaSuccess;
+}
+
+size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
+
+bool moe_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+    if (T < 0 || T > (int64_t(1) << 20)) return false;
+    if (H < 128 || H > 16384 || H % 128) return false;
+    if (I < 128 || I > 16384 || I % 128) return false;
+    if (E < 1 || E > kMaxExperts) return false;
+    if (k < 1 || k > kMaxTopK || k > E) return false;
+    return true;
+}
+
+int choose_bn(int64_t S, int64_t E) { return (S / E) >= 48 ? 128 : 32; }
+
+}  // namespace
+
+FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
+    FwdLayout L{};
+    const int64_t S = T * k;
+    const int64_t nchunk = (T + kRouterTokens - 1) / kRouterTokens;
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    L.err = take(256);
+    L.topk_ids = take(S * 4);
+    L.topk_w = take(S * 4);
+    L.rank = take(S * 4);
+    L.hist = take(nchunk * E * 4);
+    L.offsets = take((E + 1) * 4);
+    L.slot_of = take(S * 4);
+    L.slot_token = take(S * 4);
+    L.s_x = take(T * 4);
+    L.s_slot = take(S * 4);
+    L.q_x16 = take(S * H * 2);
+    L.h = take(S * I * 4);
+    L.s_h = take(S * 4);
+    L.q_h16 = take(S * I * 2);
+    L.o = take(S * H * 4);
+    L.total = off;
+    return L;
+}
+
+LinLayout lin_layout(int64_t M, int64_t N, int64_t K) {
+    (void)N;
+    LinLayout L{};
+    size_t off = 0;
+    auto take = [&](size_t bytes) {
+        const size_t at = off;
+        off = align256(off + bytes);
+        return at;
+    };
+    L.err = take(256);
+    L.s_x = take(M * 4);
+    L.q_x16 = take(M * K * 2);
+    L.total = off;
+    return L;
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+namespace {
+
+template <typename T>
+T* at(void* base, size_t off) {
+    return reinterpret_cast<T*>(static_cast<char*>(base) + off);
+}
+
+moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float* router_bias,
+                          const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                          const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                          int64_t k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                          void* stream, const moe_w8a8_debug_t* dbg) {
+    if (!moe_shape_ok(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;  // nothing is read or written
+    const void* ptrs[] = {x, router_w, w13_q, w13_scale, w2_q, w2_scale, y, workspace};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (router_bias != nullptr && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(T, H, I, E, k);
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int S = (int)(T * k);
+    const int nchunk = (int)((T + kRouterTokens - 1) / kRouterTokens);
+    int* err = at<int>(workspace, L.err);
+    int32_t* topk_ids = at<int32_t>(workspace, L.topk_ids);
+    float* topk_w = at<float>(workspace, L.topk_w);
+    int32_t* rank = at<int32_t>(workspace, L.rank);
+    int32_t* hist = at<int32_t>(workspace, L.hist);
+    int32_t* offsets = at<int32_t>(workspace, L.offsets);
+    int32_t* slot_of = at<int32_t>(workspace, L.slot_of);
+    int32_t* slot_token = at<int32_t>(workspace, L.slot_token);
+    float* s_x = at<float>(workspace, L.s_x);
+    float* s_slot = at<float>(workspace, L.s_slot);
+    uint16_t* q_x16 = at<uint16_t>(workspace, L.q_x16);
+    float* h = at<float>(workspace, L.h);
+    float* s_h = at<float>(workspace, L.s_h);
+    uint16_t* q_h16 = at<uint16_t>(workspace, L.q_h16);
+    float* o = at<float>(workspace, L.o);
+    const uint64_t timeout = g_timeout_ns.load();
+    const int bn = choose_bn(S, E);
+
+    cudaError_t e;
+    if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_router_topk(x, router_w, router_bias, (int)T, (int)H, (int)E, (int)k, topk_ids, topk_w,
+                           rank, hist, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_scan(hist, nchunk, (int)E, offsets, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
+                             s_x, s_slot, q_x16, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    GemmArgs g1{};
+    g1.K = (int)H;
+    g1.n_cb = (int)(I / 64);
+    g1.n_groups = (int)E;
+    g1.total_rows = S;
+    g1.offsets = offsets;
+    g1.w_rows_per_group = (int)(2 * I);
+    g1.up_offset = (int)I;
+    g1.w_scale = w13_scale;
+    g1.act_scale = s_slot;
+    g1.out = h;
+    g1.ld_out = (int)I;
+    g1.acc_out = dbg ? dbg->acc1 : nullptr;
+    g1.error = err;
+    g1.timeout_ns = timeout;
+    if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_grouped_gemm(Epi::GateUp, bn, g1, w13_q, q_x16, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    GemmArgs g2{};
+    g2.K = (int)I;
+    g2.n_cb = (int)(H / 128);
+    g2.n_groups = (int)E;
+    g2.total_rows = S;
+    g2.offsets = offsets;
+    g2.w_rows_per_group = (int)H;
+    g2.up_offset = 0;
+    g2.w_scale = w2_scale;
+    g2.act_scale = s_h;
+    g2.out = o;
+    g2.ld_out = (int)H;
+    g2.acc_out = dbg ? dbg->acc2 : nullptr;
+    g2.error = err;
+    g2.timeout_ns = timeout;
+    if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_grouped_gemm(Epi::ScaleF32, bn, g2, w2_q, q_h16, st);
+    if (e != cudaSuccess) return from_cuda(e);
+
+    if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_combine(o, slot_of, topk_w, (int)T, (int)H, (int)k, y, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    if ((e = mark(7, st)) != cudaSuccess) return from_cuda(e);
+
+    if (dbg) {
+        auto cp = [&](void* dst, const void* src, size_t bytes) -> cudaError_t {
+            if (!dst) return cudaSuccess;
+            return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+        };
+        const size_t Sb = (size_t)S * 4;
+        if ((e = cp(dbg->topk_ids, topk_ids, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->topk_w, topk_w, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->offsets, offsets, (size_t)(E + 1) * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->slot_of, slot_of, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->slot_token, slot_token, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_x, s_x, (size_t)T * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->h, h, (size_t)S * I * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_h, s_h, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->o, o, (size_t)S * H * 4)) != cudaSuccess) return from_cuda(e);
+        if (dbg->q_x) {
+            // token t's quantised row sits in each of its slots; take the first
+            e = launch_f16_rows_to_s8(q_x16, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+    }
+    return MOE_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+const char* moe_w8a8_status_string(moe_status_t s) {
+    switch (s) {
+        case MOE_OK: return "MOE_OK";
+        case MOE_ERR_INVALID_ARG: return "MOE_ERR_INVALID_ARG";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "MOE_ERR_UNSUPPORTED_SHAPE";
+        case MOE_ERR_WORKSPACE_TOO_SMALL: return "MOE_ERR_WORKSPACE_TOO_SMALL";
+        case MOE_ERR_CUDA: return "MOE_ERR_CUDA";
+        case MOE_ERR_DEVICE_TIMEOUT: return "MOE_ERR_DEVICE_TIMEOUT";
+        case MOE_ERR_NOT_IMPLEMENTED: return "MOE_ERR_NOT_IMPLEMENTED";
+        case MOE_ERR_DEVICE: return "MOE_ERR_DEVICE";
+    }
+    return "MOE_ERR_UNKNOWN";
+}
+
+int moe_w8a8_version(void) { return 100; }
+
+uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns) {
+    return g_timeout_ns.exchange(ns == 0 ? kDefaultTimeoutNs : ns);
+}
+
+moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows, int64_t K, int8_t* w_q,
+                                       float* w_scale, void* stream) {
+    if (rows < 0 || K < 1 || K > (int64_t(1) << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(launch_quantize_weights(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream)));
+}
+
+size_t moe_w8a8_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k) {
+    if (!moe_shape_ok(T, H, I, E, top_k)) return 0;
+    return fwd_layout(T, H, I, E, top_k).total;
+}
+
+moe_status_t moe_w8a8_forward(const uint16_t* x, const float* router_w, const float* router_bias,
+                              const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                              const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                              int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                              void* stream) {
+    return forward_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
+                        workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float* router_w,
+                                    const float* router_bias, const int8_t* w13_q,
+                                    const float* w13_scale, const int8_t* w2_q,
+                                    const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                    int64_t E, int64_t top_k, uint16_t* y, void* workspace,
+                                    size_t workspace_bytes, void* stream,
+                                    const moe_w8a8_debug_t* dbg) {
+    return forward_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
+                        workspace, workspace_bytes, stream, dbg);
+}
+
+size_t moe_w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {
+    if (M < 0 || M > (int64_t(1) << 20) || N < 128 || N > 65536 || N % 128 || K < 128 || K > 65536 || K % 128)
+        return 0;
+    return lin_layout(M, N, K).total;
+}
+
+moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* w_scale, int64_t M,
+                             int64_t N, int64_t K, uint16_t* y, void* workspace,
+                             size_t workspace_bytes, void* stream) {
+    const size_t need = moe_w8a8_linear_workspace_size(M, N, K);
+    if (need == 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (M == 0) return MOE_OK;  // nothing is read or written
+    const void* ptrs[] = {x, w_q, w_scale, y, workspace};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const LinLayout L = lin_layout(M, N, K);
+    float* s_x = at<float>(workspace, L.s_x);
+    uint16_t* q16 = at<uint16_t>(workspace, L.q_x16);
+    cudaError_t e;
+    if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
+    e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
+                             q16, st);
+    if (e != cudaSuccess) return from_cuda(e);
+    if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
+    GemmArgs g{};
+    g.K = (int)K;
+    g.n_cb = (int)(N / 128);
+    g.n_groups = 1;
+    g.total_rows = (int)M;
+    g.offsets = nullptr;
+    g.w_rows_per_group = (int)N;
+    g.w_scale = w_scale;
+    g.act_scale = s_x;
+    g.out = y;
+    g.ld_out = (int)N;
+    g.acc_out = nullptr;
+    g.error = at<int>(workspace, L.err);
+    g.timeout_ns = g_timeout_ns.load();
+    const int bn = M >= 48 ? 128 : 32;
+    if ((e = launch_grouped_gemm(Epi::ScaleBF16, bn, g, w_q, q16, st)) != cudaSuccess) return from_cuda(e);
+    return from_cuda(mark(2, st));
+}
+
+moe_status_t moe_w8a8_set_profile_events(void* const* events, int n) {
+    if (events == nullptr) {
+        t_events = nullptr;
+        return MOE_OK;
+    }
+    if (n < 8) return MOE_ERR_INVALID_ARG;
+    t_events = reinterpret_cast<cudaEvent_t const*>(events);
+    return MOE_OK;
+}
+
+moe_status_t moe_w8a8_device_error(void* workspace, void* stream) {
+    if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    if (cudaStreamSynchronize(st) != cudaSuccess) return MOE_ERR_CUDA;
+    int host = 0;
+    if (cudaMemcpy(&host, workspace, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (host != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(workspace, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (host & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    if (host & kErrDevice) return MOE_ERR_DEVICE;
+    return MOE_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,79 @@
+// internal.h -- declarations shared by the translation units of the library
+// (host launchers of every kernel, the forward's workspace layout).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+namespace moe {
+
+constexpr int kRouterTokens = 32;  // tokens per router CTA = tokens per routing chunk
+constexpr int kMaxExperts = 256;
+constexpr int kMaxTopK = 8;
+constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+
+// Bits of the sticky device error word (first int of a workspace).
+constexpr int kErrTimeout = 1;  // a pipeline wait ran out of time
+constexpr int kErrDevice = 2;   // a device-side consistency check failed
+
+// Epilogue variants of the grouped GEMM.
+enum class Epi : int {
+    GateUp = 0,    // h = silu(g) * u, fp32 out (first expert GEMM)
+    ScaleF32 = 1,  // (acc * s_act) * s_w, fp32 out (second expert GEMM)
+    ScaleBF16 = 2  // (acc * s_act) * s_w, bf16 out (linear layer)
+};
+
+struct GemmArgs {
+    int K;                   // reduction length (multiple of 128)
+    int n_cb;                // channel blocks per group
+    int n_groups;            // groups (experts); 1 for the linear layer
+    int total_rows;          // rows of the activation matrix
+    const int32_t* offsets;  // [n_groups + 1] group row offsets, or nullptr: one group
+    int w_rows_per_group;    // weight rows per group (2I, H or N)
+    int up_offset;           // GateUp only: row offset of the up half (I)
+    const float* w_scale;    // [n_groups * w_rows_per_group]
+    const float* act_scale;  // [total_rows]
+    void* out;               // fp32 or bf16 output
+    int ld_out;              // output row length in elements
+    int32_t* acc_out;        // optional raw accumulators [total_rows][w_rows_per_group]
+    int* error;              // sticky device error word
+    uint64_t timeout_ns;
+};
+
+// Forward workspace layout (byte offsets; every region 256-byte aligned).
+struct FwdLayout {
+    size_t err, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x, s_slot, q_x16,
+        h, s_h, q_h16, o, total;
+};
+FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
+
+struct LinLayout {
+    size_t err, s_x, q_x16, total;
+};
+LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
+
+// ---- launchers (return cudaSuccess or the launch error) ----
+cudaError_t launch_router_topk(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
+                               int E, int k, int32_t* topk_ids, float* topk_w, int32_t* rank,
+                               int32_t* hist, cudaStream_t st);
+cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, cudaStream_t st);
+cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
+                                 const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
+                                 int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16,
+                                 cudaStream_t st);
+cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
+                           cudaStream_t st);
+cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
+                           int H, int k, uint16_t* y, cudaStream_t st);
+cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
+                                    cudaStream_t st);
+cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
+                                  int row_stride_of, int8_t* q8, cudaStream_t st);
+cudaError_t launch_grouped_gemm(Epi epi, int bn, const GemmArgs& args, const void* w,
+                                const void* act16, cudaStream_t st);
+
+int num_sms();
+
+}  // namespace moe

@@ -1,0 +1,183 @@
+// pointwise.cu -- row-wise kernels around the expert GEMMs.
+//
+//   requant_kernel          per slot row of h: s_h = amax/127,
+//                           q_h = clamp(round(h/s_h)), written as exact fp16
+//                           values (the GEMM operand) and optionally int8.
+//   combine_kernel          y[t] = bf16_rne(sum_j w[t][j] * o[slot(t, j)]).
+//   quantize_weights_kernel per output channel: s = amax/127, q = round(w/s).
+//   f16_rows_to_s8_kernel   copies quantised rows out as int8 (debug dumps).
+//
+// Quantisation: "W8A8 quantisation of MiniMax-M3 on K100AI" (mhpn.cn),
+// section 2.1; re-quantising the FP32 result for the next operator:
+// "DeepSeek V4 950 FP8 inference on H100" (lpnh.cn), section 2.3; weighted
+// combine at the end of the layer: "Tencent Hunyuan AI Infra on Hopper"
+// (pnsm.cn), section 1.3.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "internal.h"
+
+namespace moe {
+namespace {
+
+__device__ __forceinline__ int quant_code(float v, float s) {
+    if (s == 0.f) return 0;
+    const int q = __float2int_rn(__fdiv_rn(v, s));
+    return min(127, max(-128, q));
+}
+
+__device__ __forceinline__ float warp_max(float v) {
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, off));
+    return v;
+}
+
+// One warp per row of h [S][I].
+__global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ h, int S, int I,
+                                                      float* __restrict__ s_h,
+                                                      uint16_t* __restrict__ q16,
+                                                      int8_t* __restrict__ q8) {
+    const int lane = threadIdx.x & 31;
+    const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    if (r >= S) return;
+    const float4* row = reinterpret_cast<const float4*>(h + (size_t)r * I);
+    const int nv = I / 4;
+    float amax = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+        const float4 v = row[i];
+        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
+    }
+    amax = warp_max(amax);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) s_h[r] = s;
+    for (int i = lane; i < nv; i += 32) {
+        const float4 v = row[i];
+        const int a = quant_code(v.x, s), b = quant_code(v.y, s), c = quant_code(v.z, s),
+                  d = quant_code(v.w, s);
+        uint2 o;
+        o.x = (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+        o.y = (uint32_t)__half_as_ushort(__int2half_rn(c)) | ((uint32_t)__half_as_ushort(__int2half_rn(d)) << 16);
+        reinterpret_cast<uint2*>(q16 + (size_t)r * I)[i] = o;
+        if (q8 != nullptr) {
+            const uint32_t packed = (uint32_t)(uint8_t)a | ((uint32_t)(uint8_t)b << 8) |
+                                    ((uint32_t)(uint8_t)c << 16) | ((uint32_t)(uint8_t)d << 24);
+            reinterpret_cast<uint32_t*>(q8 + (size_t)r * I)[i] = packed;
+        }
+    }
+}
+
+// One CTA of 256 threads per token; each thread handles float4 columns.
+__global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o,
+                                                      const int32_t* __restrict__ slot_of,
+                                                      const float* __restrict__ topk_w, int T,
+                                                      int H, int k, uint16_t* __restrict__ y) {
+    const int t = blockIdx.x;
+    if (t >= T) return;
+    __shared__ int32_t slot[kMaxTopK];
+    __shared__ float w[kMaxTopK];
+    if (threadIdx.x < k) {
+        slot[threadIdx.x] = slot_of[(size_t)t * k + threadIdx.x];
+        w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
+    }
+    __syncthreads();
+    const int nv = H / 4;
+    for (int i = threadIdx.x; i < nv; i += 256) {
+        float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+        for (int j = 0; j < k; ++j) {
+            const float4 v = reinterpret_cast<const float4*>(o + (size_t)slot[j] * H)[i];
+            const float wj = w[j];
+            a0 = __fadd_rn(a0, __fmul_rn(wj, v.x));
+            a1 = __fadd_rn(a1, __fmul_rn(wj, v.y));
+            a2 = __fadd_rn(a2, __fmul_rn(wj, v.z));
+            a3 = __fadd_rn(a3, __fmul_rn(wj, v.w));
+        }
+        uint2 out;
+        out.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a0)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a1)) << 16);
+        out.y = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a2)) |
+                ((uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a3)) << 16);
+        reinterpret_cast<uint2*>(y + (size_t)t * H)[i] = out;
+    }
+}
+
+// One warp per weight row; grid-stride over rows.
+__global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __restrict__ w,
+                                                               int64_t rows, int K,
+                                                               int8_t* __restrict__ q,
+                                                               float* __restrict__ s_out) {
+    const int lane = threadIdx.x & 31;
+    const int64_t nwarps = (int64_t)gridDim.x * 8;
+    for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += nwarps) {
+        const float* row = w + r * K;
+        float amax = 0.f;
+        if ((K & 3) == 0) {
+            for (int i = lane; i < K / 4; i += 32) {
+                const float4 v = reinterpret_cast<const float4*>(row)[i];
+                amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
+            }
+        } else {
+            for (int i = lane; i < K; i += 32) amax = fmaxf(amax, fabsf(row[i]));
+        }
+        amax = warp_max(amax);
+        const float s = __fdiv_rn(amax, 127.0f);
+        if (lane == 0) s_out[r] = s;
+        int8_t* qr = q + r * K;
+        if ((K & 3) == 0) {
+            for (int i = lane; i < K / 4; i += 32) {
+                const float4 v = reinterpret_cast<const float4*>(row)[i];
+                const uint32_t packed = (uint32_t)(uint8_t)quant_code(v.x, s) |
+                                        ((uint32_t)(uint8_t)quant_code(v.y, s) << 8) |
+                                        ((uint32_t)(uint8_t)quant_code(v.z, s) << 16) |
+                                        ((uint32_t)(uint8_t)quant_code(v.w, s) << 24);
+                reinterpret_cast<uint32_t*>(qr)[i] = packed;
+            }
+        } else {
+            for (int i = lane; i < K; i += 32) qr[i] = (int8_t)quant_code(row[i], s);
+        }
+    }
+}
+
+// q8[r][:] = int8(q16[row_of[r * stride]][:]) (row_of == nullptr: identity).
+__global__ void f16_rows_to_s8_kernel(const uint16_t* __restrict__ q16, const int32_t* __restrict__ row_of,
+                                      int rows, int K, int stride, int8_t* __restrict__ q8) {
+    const int r = blockIdx.x;
+    if (r >= rows) return;
+    const int src = row_of ? row_of[(size_t)r * stride] : r;
+    for (int i = threadIdx.x; i < K; i += blockDim.x)
+        q8[(size_t)r * K + i] = (int8_t)__half2int_rn(__ushort_as_half(q16[(size_t)src * K + i]));
+}
+
+}  // namespace
+
+cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
+                           cudaStream_t st) {
+    if (S == 0) return cudaSuccess;
+    requant_kernel<<<(S + 7) / 8, 256, 0, st>>>(h, S, I, s_h, q16, q8);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
+                           int H, int k, uint16_t* y, cudaStream_t st) {
+    if (T == 0) return cudaSuccess;
+    combine_kernel<<<T, 256, 0, st>>>(o, slot_of, topk_w, T, H, k, y);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
+                                    cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    int64_t blocks = (rows + 7) / 8;
+    const int64_t cap = (int64_t)num_sms() * 16;
+    if (blocks > cap) blocks = cap;
+    quantize_weights_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, rows, K, q, s);
+    return cudaGetLastError();
+}
+
+cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
+                                  int row_stride_of, int8_t* q8, cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    f16_rows_to_s8_kernel<<<rows, 256, 0, st>>>(q16, row_of, rows, K, row_stride_of, q8);
+    return cudaGetLastError();
+}
+
+}  // namespace moe

@@ -218,3 +218,58 @@ def test_int32_accumulators_exact_on_worst_case_inputs():
     q_h = dev["q_h"].cpu().numpy()
     ref2 = q_h.astype(np.int64) @ w2[0].astype(np.int64).T
     np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)
+
+
+def _boundary_rows(H):
+    """Rows whose codes equal x (amax 127 -> s = 1): L1 = 2^17 and 2^17 + 1."""
+    r = np.random.default_rng(9)
+    rows = []
+    for extra in (0, 1):
+        mag = np.full(H, 64.0)
+        mag[0] = 127.0
+        mag[1:64] = 63.0  # 127 + 63*63 + 1984*64 = 131072
+        if extra:
+            mag[1] = 64.0  # 131073
+        sign = np.where(r.random(H) < 0.5, -1.0, 1.0)
+        sign[0] = 1.0
+        rows.append(mag * sign)
+    return np.array(rows, np.float32)
+
+
+def test_exactness_certificate_boundary():
+    """A row with L1 = 2^17 against weights -128*sign(x) drives the partial
+    sums to exactly -2^24 on the tensor-core path; a row one above the bound
+    goes to the exact CUDA-core path.  Both must be exact."""
+    H, I = 2048, 128
+    x = _boundary_rows(H)
+    assert np.abs(x[0]).sum() == 2 ** 17 and np.abs(x[1]).sum() == 2 ** 17 + 1
+    w13 = np.random.default_rng(3).integers(-128, 128, (1, 2 * I, H)).astype(np.int8)
+    w13[0, 0] = (-128 * np.sign(x[0])).astype(np.int8)
+    w13[0, 1] = (-128 * np.sign(x[1])).astype(np.int8)
+    w13[0, 2] = (127 * np.sign(x[0])).astype(np.int8)
+    w2 = np.random.default_rng(4).integers(-128, 128, (1, H, I)).astype(np.int8)
+    args = (torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.zeros((H, 1), device="cuda"), None,
+            torch.from_numpy(w13).cuda(), torch.full((1, 2 * I), 1e-7, device="cuda"),
+            torch.from_numpy(w2).cuda(), torch.full((1, H), 1e-3, device="cuda"), 1)
+    _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
+    q_x = dev["q_x"].cpu().numpy()
+    np.testing.assert_array_equal(q_x, x.astype(np.int8))
+    ref1 = q_x.astype(np.int64) @ w13[0].astype(np.int64).T
+    assert ref1[0, 0] == -(2 ** 24)
+    np.testing.assert_array_equal(dev["acc1"].cpu().numpy(), ref1)
+    ref2 = dev["q_h"].cpu().numpy().astype(np.int64) @ w2[0].astype(np.int64).T
+    np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)
+
+
+def test_second_gemm_exact_path():
+    """Identical gate and up rows make h constant along I, so every q_h code
+    is +-127 and L1(q_h) = 127 * 2048 is far above the bound: GEMM2 runs on
+    the exact path for every row.  Compared with the oracle stage by stage."""
+    cfg = TINY.replace(T=8, H=256, I=2048, E=2, k=1)
+    layer = Layer(cfg, seed=4)
+    layer.w13_q[:] = 1
+    layer.d_w13 = torch.from_numpy(layer.w13_q).cuda()
+    mismatch, _ = _stagewise(layer)
+    _, dev = moe.forward_debug(*layer.device_args(), fields=("q_h",))
+    q_h = dev["q_h"].cpu().numpy()
+    assert (np.abs(q_h.astype(np.int64)).sum(axis=1) > 2 ** 17).all()

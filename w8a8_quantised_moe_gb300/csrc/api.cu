@@ -12,7 +12,7 @@
 #include <atomic>
 #include <cstring>
 
-#include "../../include/moe_w8a8.h"
+#include "moe_w8a8.h"
 #include "internal.h"
 
 namespace moe {
@@ -48,8 +48,6 @@ bool moe_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     return true;
 }
 
-int choose_bn(int64_t S, int64_t E) { return (S / E) >= 48 ? 128 : 32; }
-
 }  // namespace
 
 FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
@@ -63,6 +61,7 @@ FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
         return at;
     };
     L.err = take(256);
+    L.counts = take(2 * 4);
     L.topk_ids = take(S * 4);
     L.topk_w = take(S * 4);
     L.rank = take(S * 4);
@@ -72,6 +71,10 @@ FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     L.slot_token = take(S * 4);
     L.s_x = take(T * 4);
     L.s_slot = take(S * 4);
+    L.flag1 = take(S * 4);
+    L.list1 = take(S * 4);
+    L.flag2 = take(S * 4);
+    L.list2 = take(S * 4);
     L.q_x16 = take(S * H * 2);
     L.h = take(S * I * 4);
     L.s_h = take(S * 4);
@@ -91,7 +94,10 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K) {
         return at;
     };
     L.err = take(256);
+    L.counts = take(2 * 4);
     L.s_x = take(M * 4);
+    L.flag = take(M * 4);
+    L.list = take(M * 4);
     L.q_x16 = take(M * K * 2);
     L.total = off;
     return L;
@@ -136,13 +142,18 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     int32_t* slot_token = at<int32_t>(workspace, L.slot_token);
     float* s_x = at<float>(workspace, L.s_x);
     float* s_slot = at<float>(workspace, L.s_slot);
+    int32_t* counts = at<int32_t>(workspace, L.counts);
+    int32_t* flag1 = at<int32_t>(workspace, L.flag1);
+    int32_t* list1 = at<int32_t>(workspace, L.list1);
+    int32_t* flag2 = at<int32_t>(workspace, L.flag2);
+    int32_t* list2 = at<int32_t>(workspace, L.list2);
     uint16_t* q_x16 = at<uint16_t>(workspace, L.q_x16);
     float* h = at<float>(workspace, L.h);
     float* s_h = at<float>(workspace, L.s_h);
     uint16_t* q_h16 = at<uint16_t>(workspace, L.q_h16);
     float* o = at<float>(workspace, L.o);
     const uint64_t timeout = g_timeout_ns.load();
-    const int bn = choose_bn(S, E);
+    const GemmShape shape = choose_gemm_shape(S, E);
 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
@@ -150,14 +161,16 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
                            rank, hist, st);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_scan(hist, nchunk, (int)E, offsets, st);
+    e = launch_scan(hist, nchunk, (int)E, offsets, counts, st);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                             s_x, s_slot, q_x16, st);
+                             s_x, s_slot, q_x16, flag1, list1, counts + 0, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g1{};
+    g1.w = w13_q;
+    g1.act16 = q_x16;
     g1.K = (int)H;
     g1.n_cb = (int)(I / 64);
     g1.n_groups = (int)E;
@@ -170,17 +183,22 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.out = h;
     g1.ld_out = (int)I;
     g1.acc_out = dbg ? dbg->acc1 : nullptr;
+    g1.flags = flag1;
+    g1.fb_list = list1;
+    g1.fb_count = counts + 0;
     g1.error = err;
     g1.timeout_ns = timeout;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::GateUp, bn, g1, w13_q, q_x16, st);
+    e = launch_grouped_gemm(Epi::GateUp, shape, g1, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, st);
+    e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g2{};
+    g2.w = w2_q;
+    g2.act16 = q_h16;
     g2.K = (int)I;
     g2.n_cb = (int)(H / 128);
     g2.n_groups = (int)E;
@@ -193,10 +211,13 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.out = o;
     g2.ld_out = (int)H;
     g2.acc_out = dbg ? dbg->acc2 : nullptr;
+    g2.flags = flag2;
+    g2.fb_list = list2;
+    g2.fb_count = counts + 1;
     g2.error = err;
     g2.timeout_ns = timeout;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::ScaleF32, bn, g2, w2_q, q_h16, st);
+    e = launch_grouped_gemm(Epi::ScaleF32, shape, g2, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
@@ -306,14 +327,20 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const LinLayout L = lin_layout(M, N, K);
     float* s_x = at<float>(workspace, L.s_x);
+    int32_t* counts = at<int32_t>(workspace, L.counts);
+    int32_t* flag = at<int32_t>(workspace, L.flag);
+    int32_t* list = at<int32_t>(workspace, L.list);
     uint16_t* q16 = at<uint16_t>(workspace, L.q_x16);
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q16, st);
+                             q16, flag, list, counts, st);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
     GemmArgs g{};
+    g.w = w_q;
+    g.act16 = q16;
     g.K = (int)K;
     g.n_cb = (int)(N / 128);
     g.n_groups = 1;
@@ -325,10 +352,13 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     g.out = y;
     g.ld_out = (int)N;
     g.acc_out = nullptr;
+    g.flags = flag;
+    g.fb_list = list;
+    g.fb_count = counts;
     g.error = at<int>(workspace, L.err);
     g.timeout_ns = g_timeout_ns.load();
-    const int bn = M >= 48 ? 128 : 32;
-    if ((e = launch_grouped_gemm(Epi::ScaleBF16, bn, g, w_q, q16, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_grouped_gemm(Epi::ScaleBF16, choose_gemm_shape(M, 1), g, st)) != cudaSuccess)
+        return from_cuda(e);
     return from_cuda(mark(2, st));
 }
 

@@ -9,24 +9,31 @@
 // 2.1), and, for the first expert GEMM, h = silu(g) * u of the gate and up
 // halves.
 //
-// GB300 has no INT8 tcgen05 MMA (kind::i8 does not exist on sm_103a), so the
-// product runs on kind::f16: int8 values are exact in fp16, products of two
-// of them (|p| <= 2^14) are exact in the fp32 accumulator, and every TMEM
-// accumulation covers at most 1024 products, so every partial sum is an
-// integer of magnitude <= 2^24 and therefore exact.  After each 1024-long K
-// chunk the epilogue warps convert the fp32 accumulator to int32 and add it
-// to a running int32 sum, which makes the whole GEMM exact for any int8 input
-// and any K <= 131071.
+// Exactness.  GB300 has no INT8 tcgen05 MMA (kind::i8 does not exist on
+// sm_103a), so the product runs on kind::f16: int8 values are exact in fp16
+// and products of two of them (|p| <= 2^14) are exact in the fp32
+// accumulator.  Every partial sum of a row r is bounded by
+// 128 * sum_k |act[r][k]|, so when that L1 norm is at most 2^17 every
+// partial sum is an integer of magnitude <= 2^24, exactly representable, and
+// the fp32 accumulator holds the exact int32 result in any summation order.
+// The quantisation kernels compute the L1 norm of every row and list the
+// rows above the bound; this kernel skips them in its tensor-core epilogue
+// and recomputes them after its tile loop with exact int32 dot products on
+// the CUDA cores.  Typical activations stay far below the bound; the exact
+// path only costs time on adversarial inputs.
 //
 // Operand roles ("swap AB"): A = 128 weight rows per tile, converted from
 // int8 to fp16 by converter warps straight into tensor memory; B = a tile of
 // BN activation rows, already fp16, loaded by TMA (128-byte swizzle) into
 // shared memory; D = 128 x N fp32 accumulator in tensor memory, N = the
-// tile's valid rows rounded up to 16.  Warp roles of a CTA (320 threads):
+// tile's valid rows rounded up to 16.  One stage ring (NS stages of BK along
+// K) carries both: the producer refills stage s after the MMAs that read it
+// have completed, so the MMA thread waits once and commits once per stage.
+// Warp roles of a CTA (320 threads):
 //   warp 0      TMA producer (int8 weight tile + fp16 activation tile)
 //   warp 1      TMEM allocator and single-thread MMA issuer
 //   warps 2-5   converters: int8 weight rows -> fp16 pairs -> tcgen05.st
-//   warps 6-9   epilogue: tcgen05.ld, int32 chunk sums, scales, outputs
+//   warps 6-9   epilogue: tcgen05.ld, scales, SiLU gate, outputs
 // The grid is persistent; tiles are dealt round-robin.  Every wait is
 // bounded (see ptx.cuh); a timeout aborts the CTA cleanly.
 #include <cuda_bf16.h>
@@ -41,34 +48,40 @@ namespace moe {
 namespace {
 
 constexpr int kThreads = 320;
-constexpr int kBK = 64;         // K elements per pipeline stage
-constexpr int kChunkKB = 16;    // stages per exact accumulation chunk (1024 K)
-constexpr int kNumA = 4;        // TMEM stages of the converted A operand
-constexpr int kACols = kBK / 2; // TMEM columns of one A stage (two fp16 per column)
-constexpr int kTileM = 128;     // weight rows per tile
-constexpr int kStageA = kTileM * kBK;  // int8 bytes of one weight stage
+constexpr int kTileM = 128;   // weight rows per tile
+constexpr int kEpiWarp0 = 6;  // first epilogue warp
 
-template <int BN>
+template <int BN_, int BK_, int NS_, int ND_>
 struct Cfg {
-    static constexpr int kStageB = BN * kBK * 2;  // fp16 activation stage
+    static constexpr int BN = BN_;  // activation rows per tile (MMA N)
+    static constexpr int BK = BK_;  // K per stage
+    static constexpr int NS = NS_;  // stages
+    static constexpr int ND = ND_;  // accumulator buffers
+    static constexpr int kStageA = kTileM * BK;  // int8 weights
+    static constexpr int kStageB = BN * BK * 2;  // fp16 activations
     static constexpr int kStage = kStageA + kStageB;
-    static constexpr int kStages = BN >= 128 ? 6 : 8;
-    static constexpr int kXch = 64 * (BN + 1) * 4;  // gate/up exchange buffer
-    static constexpr int kAccCols = BN;
-    static constexpr int kTmemCols = kNumA * kACols + 2 * kAccCols;
+    static constexpr int kACols = BK / 2;       // TMEM columns of one A stage
+    static constexpr int kDCol0 = NS * kACols;  // first accumulator column
+    static constexpr int kTmemCols = NS * kACols + ND * BN;
     static constexpr int kTmemAlloc = kTmemCols <= 32 ? 32 : kTmemCols <= 64 ? 64 : kTmemCols <= 128 ? 128
                                       : kTmemCols <= 256 ? 256 : 512;
-    // shared memory layout (offsets from a 1024-aligned base)
-    static constexpr int kOffStages = 0;
-    static constexpr int kOffXch = kStages * kStage;
+    static constexpr int kXchStride = 33;
+    static constexpr int kXch = kTileM * kXchStride * 4;  // gate/up exchange, 32 columns
+    static constexpr int kOffXch = NS * kStage;
     static constexpr int kOffBars = kOffXch + kXch;
-    static constexpr int kNumBars = 2 * kStages + 2 * kNumA + 4 + 1 + 2;
+    static constexpr int kNumBars = 3 * NS + 2 * ND + 2;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffMisc = kOffTiles + (kMaxExperts + 1) * 4 * 2;
     static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
-    static_assert(kStageB % 1024 == 0, "B stage must keep 1024-byte alignment");
+    static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM budget");
+    static_assert(BK == 64 || BK == 128, "K per stage");
+    static_assert(kSmem <= 232448, "shared memory budget");
 };
+
+using CfgWide = Cfg<256, 64, 4, 1>;    // many rows per group
+using CfgMid = Cfg<128, 128, 4, 2>;    // about a hundred rows per group
+using CfgNarrow = Cfg<32, 128, 6, 2>;  // a few rows per group (decode)
 
 // Tile table of a launch: group g owns tiles [tile_start[g], tile_start[g+1]);
 // inside a group, tile = cb * ntb + tb (token blocks fastest, so CTAs running
@@ -80,15 +93,19 @@ struct Tiles {
     int n_cb;
 };
 
+__device__ __forceinline__ int last_le(const int* a, int n, int v) {  // last i < n with a[i] <= v
+    int lo = 0, hi = n - 1;
+    while (lo < hi) {
+        const int mid = (lo + hi + 1) >> 1;
+        if (a[mid] <= v) lo = mid; else hi = mid - 1;
+    }
+    return lo;
+}
+
 template <int BN>
 __device__ __forceinline__ void decode_tile(const Tiles& t, int tile, int& g, int& cb, int& row0,
                                             int& nvalid) {
-    int lo = 0, hi = t.n_groups - 1;
-    while (lo < hi) {  // last g with tile_start[g] <= tile
-        const int mid = (lo + hi + 1) >> 1;
-        if (t.tile_start[mid] <= tile) lo = mid; else hi = mid - 1;
-    }
-    g = lo;
+    g = last_le(t.tile_start, t.n_groups, tile);
     const int local = tile - t.tile_start[g];
     const int rows = t.row_start[g + 1] - t.row_start[g];
     const int ntb = (rows + BN - 1) / BN;
@@ -123,6 +140,15 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
     }
 }
 
+// Barrier of the four epilogue warps on an mbarrier of count 4 (bounded).
+__device__ __forceinline__ bool epi_sync(uint64_t* bar, uint32_t& it, const WaitCtl& ctl) {
+    __syncwarp();
+    if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+    const bool ok = warp_wait(bar, it & 1u, ctl);
+    ++it;
+    return ok;
+}
+
 // int8 x4 (one 32-bit word, element 0 in the low byte) -> two fp16x2 words
 // (element 0 in the low half).  (q + 128) is placed in the mantissa of
 // 1024.0h, giving 1024 + q + 128 exactly; subtracting 1152 leaves q.
@@ -137,27 +163,101 @@ __device__ __forceinline__ void s8x4_to_f16x4(uint32_t w, uint32_t& lo, uint32_t
     hi = *reinterpret_cast<uint32_t*>(&hb);
 }
 
+__device__ __forceinline__ void cvt_chunk(const uint4 w, uint32_t* v) {
+    s8x4_to_f16x4(w.x, v[0], v[1]);
+    s8x4_to_f16x4(w.y, v[2], v[3]);
+    s8x4_to_f16x4(w.z, v[4], v[5]);
+    s8x4_to_f16x4(w.w, v[6], v[7]);
+}
+
 __device__ __forceinline__ float silu_f32(float g) {
     return __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
 }
 
-template <int BN, int EPI>
+__device__ __forceinline__ float dequant(float acc, float s_act, float s_w) {
+    return __fmul_rn(__fmul_rn(acc, s_act), s_w);
+}
+
+// Exact CUDA-core path for the rows the certificate rejected: one warp per
+// (row, output channel), int32 dot products over K.
+template <int EPI>
+__device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_groups) {
+    const int n_fb = *args.fb_count;
+    if (n_fb <= 0) return;
+    const int lane = threadIdx.x & 31;
+    const int per_row = (EPI == (int)Epi::GateUp) ? args.up_offset : args.w_rows_per_group;
+    const long n_items = (long)n_fb * per_row;
+    const int warps = kThreads / 32;
+    const int8_t* w = static_cast<const int8_t*>(args.w);
+    const __half* act = static_cast<const __half*>(args.act16);
+    for (long item = (long)blockIdx.x * warps + (threadIdx.x >> 5); item < n_items;
+         item += (long)gridDim.x * warps) {
+        const int row = args.fb_list[item / per_row];
+        const int n = (int)(item % per_row);
+        const int g = last_le(row_start, n_groups, row);
+        const __half* a = act + (size_t)row * args.K;
+        const int8_t* w0 = w + ((size_t)g * args.w_rows_per_group + n) * args.K;
+        const int8_t* w1 = w0 + (size_t)args.up_offset * args.K;  // up row (GateUp only)
+        int acc0 = 0, acc1 = 0;
+        for (int k = lane * 8; k < args.K; k += 32 * 8) {
+            const uint4 av = *reinterpret_cast<const uint4*>(a + k);
+            const __half* ah = reinterpret_cast<const __half*>(&av);
+            const uint2 wv0 = *reinterpret_cast<const uint2*>(w0 + k);
+            const int8_t* wb0 = reinterpret_cast<const int8_t*>(&wv0);
+            int q[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) q[i] = __half2int_rn(ah[i]);
+#pragma unroll
+            for (int i = 0; i < 8; ++i) acc0 += q[i] * (int)wb0[i];
+            if (EPI == (int)Epi::GateUp) {
+                const uint2 wv1 = *reinterpret_cast<const uint2*>(w1 + k);
+                const int8_t* wb1 = reinterpret_cast<const int8_t*>(&wv1);
+#pragma unroll
+                for (int i = 0; i < 8; ++i) acc1 += q[i] * (int)wb1[i];
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            acc0 += __shfl_xor_sync(0xffffffffu, acc0, off);
+            acc1 += __shfl_xor_sync(0xffffffffu, acc1, off);
+        }
+        if (lane != 0) continue;
+        const float sa = args.act_scale[row];
+        const float* sw = args.w_scale + (size_t)g * args.w_rows_per_group;
+        if (EPI == (int)Epi::GateUp) {
+            const float gv = dequant(__int2float_rn(acc0), sa, sw[n]);
+            const float uv = dequant(__int2float_rn(acc1), sa, sw[args.up_offset + n]);
+            static_cast<float*>(args.out)[(size_t)row * args.ld_out + n] = __fmul_rn(silu_f32(gv), uv);
+            if (args.acc_out) {
+                args.acc_out[(size_t)row * args.w_rows_per_group + n] = acc0;
+                args.acc_out[(size_t)row * args.w_rows_per_group + args.up_offset + n] = acc1;
+            }
+        } else {
+            const float v = dequant(__int2float_rn(acc0), sa, sw[n]);
+            if (EPI == (int)Epi::ScaleF32)
+                static_cast<float*>(args.out)[(size_t)row * args.ld_out + n] = v;
+            else
+                static_cast<__nv_bfloat16*>(args.out)[(size_t)row * args.ld_out + n] = __float2bfloat16_rn(v);
+            if (args.acc_out) args.acc_out[(size_t)row * args.w_rows_per_group + n] = acc0;
+        }
+    }
+}
+
+template <class C, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
     grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
                         const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
-    using C = Cfg<BN>;
+    constexpr int BN = C::BN, BK = C::BK, NS = C::NS, ND = C::ND;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* raw_full = bars;
-    uint64_t* raw_empty = bars + C::kStages;
-    uint64_t* a_full = bars + 2 * C::kStages;
-    uint64_t* a_empty = a_full + kNumA;
-    uint64_t* acc_full = a_empty + kNumA;
-    uint64_t* acc_empty = acc_full + 2;
-    uint64_t* teardown = acc_empty + 2;
-    uint64_t* xch_full = teardown + 1;   // up-half warps -> gate-half warps
-    uint64_t* xch_empty = teardown + 2;  // gate-half warps -> up-half warps
+    uint64_t* full = bars;                // [NS] TMA landed
+    uint64_t* a_full = bars + NS;         // [NS] A stage converted into TMEM
+    uint64_t* empty = bars + 2 * NS;      // [NS] MMAs of the stage completed
+    uint64_t* acc_full = bars + 3 * NS;   // [ND]
+    uint64_t* acc_empty = acc_full + ND;  // [ND]
+    uint64_t* teardown = acc_empty + ND;
+    uint64_t* epi_bar = teardown + 1;
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -166,24 +266,20 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_groups = args.n_groups;
-    const int nkb = args.K / kBK;
+    const int nkb = args.K / BK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < C::kStages; ++s) {
-            mbar_init(&raw_full[s], 1);
-            mbar_init(&raw_empty[s], 4 + 1);
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&a_full[s], 4);
+            mbar_init(&empty[s], 1);
         }
-        for (int a = 0; a < kNumA; ++a) {
-            mbar_init(&a_full[a], 4);
-            mbar_init(&a_empty[a], 1);
-        }
-        for (int b = 0; b < 2; ++b) {
-            mbar_init(&acc_full[b], 1);
-            mbar_init(&acc_empty[b], 4);
+        for (int d = 0; d < ND; ++d) {
+            mbar_init(&acc_full[d], 1);
+            mbar_init(&acc_empty[d], 4);
         }
         mbar_init(teardown, 1);
-        mbar_init(xch_full, 2);
-        mbar_init(xch_empty, 2);
+        mbar_init(epi_bar, 4);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
@@ -204,7 +300,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 row_start[g] = r0;
                 if (g == n_groups - 1) row_start[n_groups] = r1;
             }
-            int v = (g < n_groups) ? ((r1 - r0 + BN - 1) / BN) * args.n_cb : 0;
+            const int v = (g < n_groups) ? ((r1 - r0 + BN - 1) / BN) * args.n_cb : 0;
             int incl = v;
 #pragma unroll
             for (int off = 1; off < 32; off <<= 1) {
@@ -241,187 +337,168 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wrow1 = wrow0 + 64;
                 }
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
-                    if (!mbar_wait(&raw_empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + C::kOffStages + s * C::kStage;
-                    mbar_arrive_expect_tx(&raw_full[s], C::kStage);
-                    tma_load_2d(st, &tmap_w, &raw_full[s], kb * kBK, wrow0);
-                    tma_load_2d(st + kStageA / 2, &tmap_w, &raw_full[s], kb * kBK, wrow1);
-                    tma_load_2d(st + kStageA, &tmap_b, &raw_full[s], kb * kBK, row0);
+                    const uint32_t s = it % NS, ph = (it / NS) & 1u;
+                    if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                    uint8_t* st = smem + s * C::kStage;
+                    mbar_arrive_expect_tx(&full[s], C::kStage);
+                    tma_load_2d(st, &tmap_w, &full[s], kb * BK, wrow0);
+                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kb * BK, wrow1);
+                    tma_load_2d(st + C::kStageA, &tmap_b, &full[s], kb * BK, row0);
+                    if (BK == 128) tma_load_2d(st + C::kStageA + BN * 128, &tmap_b, &full[s], kb * BK + 64, row0);
                 }
             }
             // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)C::kStages && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % C::kStages);
-                mbar_wait_drain(&raw_full[s], (last / C::kStages) & 1u);
+            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                mbar_wait_drain(&full[s], (last / NS) & 1u);
             }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
         if (lane == 0) {
-            uint32_t it = 0, acc_it = 0;
+            uint32_t it = 0, tl = 0;
             bool ok = true;
-            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+            for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tl) {
                 int g, cb, row0, nvalid;
                 decode_tile<BN>(tiles, tile, g, cb, row0, nvalid);
-                const uint32_t n_mma = (uint32_t)((nvalid + 15) & ~15);
-                const uint32_t idesc = idesc_f16_f32(kTileM, n_mma);
-                uint32_t d_col = 0;
+                const uint32_t idesc = idesc_f16_f32(kTileM, (uint32_t)((nvalid + 15) & ~15));
+                const uint32_t d = tl % ND;
+                if (!mbar_wait(&acc_empty[d], ((tl / ND) & 1u) ^ 1u, ctl)) break;
+                tc_fence_after();
+                const uint32_t d_col = (uint32_t)C::kDCol0 + d * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    if (kb % kChunkKB == 0) {
-                        const uint32_t b = acc_it & 1u, ph = (acc_it >> 1) & 1u;
-                        if (!mbar_wait(&acc_empty[b], ph ^ 1u, ctl)) { ok = false; break; }
-                        d_col = (uint32_t)(kNumA * kACols) + b * (uint32_t)C::kAccCols;
-                    }
-                    const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
-                    const uint32_t a = it % kNumA, aph = (it / kNumA) & 1u;
-                    if (!mbar_wait(&raw_full[s], ph, ctl)) { ok = false; break; }
-                    if (!mbar_wait(&a_full[a], aph, ctl)) { ok = false; break; }
+                    const uint32_t s = it % NS, ph = (it / NS) & 1u;
+                    // a_full implies full: the converters observed the TMA's
+                    // completion before they converted this stage
+                    if (!mbar_wait(&a_full[s], ph, ctl)) { ok = false; break; }
                     tc_fence_after();
-                    const uint64_t bdesc = smem_desc_sw128(smem_u32(smem + C::kOffStages + s * C::kStage + kStageA));
+                    const uint32_t b_base = smem_u32(smem + s * C::kStage + C::kStageA);
 #pragma unroll
-                    for (int ks = 0; ks < kBK / 16; ++ks) {
-                        mma_f16_tmem_a(tmem + d_col, tmem + a * kACols + ks * 8, bdesc + (uint64_t)(ks * 2), idesc,
-                                       (kb % kChunkKB != 0 || ks != 0) ? 1u : 0u);
+                    for (int ks = 0; ks < BK / 16; ++ks) {
+                        const uint64_t bdesc =
+                            smem_desc_sw128(b_base + (ks / 4) * BN * 128) + (uint64_t)((ks % 4) * 2);
+                        mma_f16_tmem_a(tmem + d_col, tmem + s * C::kACols + ks * 8, bdesc, idesc,
+                                       (kb != 0 || ks != 0) ? 1u : 0u);
                     }
-                    mma_commit(&raw_empty[s]);
-                    mma_commit(&a_empty[a]);
-                    if (kb % kChunkKB == kChunkKB - 1 || kb == nkb - 1) {
-                        mma_commit(&acc_full[acc_it & 1u]);
-                        ++acc_it;
-                    }
+                    mma_commit(&empty[s]);
                 }
+                if (!ok) break;
+                mma_commit(&acc_full[d]);
             }
             mma_commit(teardown);
             mbar_wait_drain(teardown, 0);
         }
-    } else if (warp < 6) {
+    } else if (warp < kEpiWarp0) {
         // ------------------------------------------------------- converters
         const int q = warp & 3;
         const int row = q * 32 + lane;
-        const uint32_t swz = (uint32_t)((row >> 1) & 3);
         uint32_t it = 0;
         bool ok = true;
         for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const uint32_t s = it % C::kStages, ph = (it / C::kStages) & 1u;
-                const uint32_t a = it % kNumA, aph = (it / kNumA) & 1u;
-                if (!warp_wait(&raw_full[s], ph, ctl)) { ok = false; break; }
-                if (!warp_wait(&a_empty[a], aph ^ 1u, ctl)) { ok = false; break; }
-                const uint8_t* src = smem + C::kOffStages + s * C::kStage + row * kBK;
-                uint32_t v[32];
+                const uint32_t s = it % NS, ph = (it / NS) & 1u;
+                // this fill was issued after the MMAs that last read TMEM stage
+                // s completed, so full[s] also frees the TMEM stage
+                if (!warp_wait(&full[s], ph, ctl)) { ok = false; break; }
+                const uint8_t* src = smem + s * C::kStage + row * BK;
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + s * C::kACols;
+                if (BK == 64) {  // 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3)
+                    const uint32_t swz = (uint32_t)((row >> 1) & 3);
+                    uint32_t v[32];
 #pragma unroll
-                for (int c = 0; c < 4; ++c) {  // 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3)
-                    const uint4 w = *reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4));
-                    s8x4_to_f16x4(w.x, v[c * 8 + 0], v[c * 8 + 1]);
-                    s8x4_to_f16x4(w.y, v[c * 8 + 2], v[c * 8 + 3]);
-                    s8x4_to_f16x4(w.z, v[c * 8 + 4], v[c * 8 + 5]);
-                    s8x4_to_f16x4(w.w, v[c * 8 + 6], v[c * 8 + 7]);
+                    for (int c = 0; c < 4; ++c)
+                        cvt_chunk(*reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4)), v + c * 8);
+                    tmem_st_32(taddr, v);
+                } else {  // 128-byte swizzle: chunk c sits at c ^ (row & 7)
+                    const uint32_t swz = (uint32_t)(row & 7);
+#pragma unroll
+                    for (int hh = 0; hh < 2; ++hh) {
+                        uint32_t v[32];
+#pragma unroll
+                        for (int c = 0; c < 4; ++c)
+                            cvt_chunk(*reinterpret_cast<const uint4*>(src + (((hh * 4 + c) ^ swz) << 4)), v + c * 8);
+                        tmem_st_32(taddr + hh * 32, v);
+                    }
                 }
-                tmem_st_32(tmem + ((uint32_t)(q * 32) << 16) + a * kACols, v);
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
-                if (lane == 0) {
-                    mbar_arrive(&a_full[a]);
-                    mbar_arrive(&raw_empty[s]);
-                }
+                if (lane == 0) mbar_arrive(&a_full[s]);
             }
         }
     } else {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;
-        const int row = q * 32 + lane;  // TMEM lane = weight row of the tile
+        const int ew = warp - kEpiWarp0;  // 0..3
+        const int row = q * 32 + lane;    // TMEM lane = weight row of the tile
         const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
-        uint32_t acc_it = 0, xch_it = 0;
+        uint32_t tl = 0, eit = 0;
         bool ok = true;
-        const int nchunks = (nkb + kChunkKB - 1) / kChunkKB;
-        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
+        for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x, ++tl) {
             int g, cb, row0, nvalid;
             decode_tile<BN>(tiles, tile, g, cb, row0, nvalid);
-            int32_t sum[BN];
-#pragma unroll
-            for (int j = 0; j < BN; ++j) sum[j] = 0;
-            for (int ch = 0; ch < nchunks; ++ch) {
-                const uint32_t b = acc_it & 1u, ph = (acc_it >> 1) & 1u;
-                if (!warp_wait(&acc_full[b], ph, ctl)) { ok = false; break; }
-                tc_fence_after();
-                const uint32_t col0 = (uint32_t)(kNumA * kACols) + b * (uint32_t)C::kAccCols;
-#pragma unroll
-                for (int cblk = 0; cblk < BN / 16; ++cblk) {
-                    if (cblk * 16 < nvalid) {
-                        uint32_t r[16];
-                        tmem_ld_16(tmem + lane_addr + col0 + cblk * 16, r);
-                        tmem_wait_ld();
-#pragma unroll
-                        for (int i = 0; i < 16; ++i) sum[cblk * 16 + i] += __float2int_rn(__uint_as_float(r[i]));
-                    }
+            const uint32_t d = tl % ND;
+            if (!warp_wait(&acc_full[d], (tl / ND) & 1u, ctl)) break;
+            tc_fence_after();
+            const uint32_t col0 = (uint32_t)C::kDCol0 + d * BN;
+            const int nch = (nvalid + 31) / 32;
+            int wrow;  // this thread's weight row within the group
+            if (EPI == (int)Epi::GateUp) wrow = (row >> 6) * args.up_offset + cb * 64 + (row & 63);
+            else wrow = cb * kTileM + row;
+            const float sw = args.w_scale[(size_t)g * args.w_rows_per_group + wrow];
+            for (int ch = 0; ch < nch; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32(tmem + lane_addr + col0 + ch * 32, r);
+                tmem_wait_ld();
+                if (ch == nch - 1) {  // every column is in registers: release the accumulator
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive(&acc_empty[d]);
                 }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(&acc_empty[b]);
-                ++acc_it;
-            }
-            if (!ok) break;
-
-            if (EPI == (int)Epi::GateUp) {
-                const int half = row >> 6;  // 0: gate rows, 1: up rows
-                const int c = row & 63;
-                const int chan = cb * 64 + c;
-                const int wrow = half * args.up_offset + chan;
-                const float sw = args.w_scale[(size_t)g * args.w_rows_per_group + wrow];
+                const int j0 = ch * 32;
                 if (args.acc_out) {
 #pragma unroll
-                    for (int j = 0; j < BN; ++j)
-                        if (j < nvalid) args.acc_out[(size_t)(row0 + j) * args.w_rows_per_group + wrow] = sum[j];
+                    for (int j = 0; j < 32; ++j)
+                        if (j0 + j < nvalid && args.flags[row0 + j0 + j] == 0)
+                            args.acc_out[(size_t)(row0 + j0 + j) * args.w_rows_per_group + wrow] =
+                                __float2int_rn(__uint_as_float(r[j]));
                 }
-                float* xrow = xch + c * (BN + 1);
-                const uint32_t xph = xch_it & 1u;
-                ++xch_it;
-                if (half && !warp_wait(xch_empty, xph ^ 1u, ctl)) break;
+                if (EPI == (int)Epi::GateUp) {
+                    float* xrow = xch + row * C::kXchStride;
 #pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    if (j < nvalid) {
-                        const float sa = __ldg(args.act_scale + row0 + j);
-                        const float v = __fmul_rn(__fmul_rn(__int2float_rn(sum[j]), sa), sw);
-                        if (half) xrow[j] = v; else sum[j] = __float_as_int(v);
+                    for (int j = 0; j < 32; ++j) {
+                        const int jj = min(j0 + j, nvalid - 1);
+                        xrow[j] = dequant(__uint_as_float(r[j]), __ldg(args.act_scale + row0 + jj), sw);
                     }
-                }
-                if (half) {
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xch_full);
-                } else {
-                    if (!warp_wait(xch_full, xph, ctl)) break;
-                    float* out = reinterpret_cast<float*>(args.out);
+                    if (!epi_sync(epi_bar, eit, ctl)) { ok = false; break; }
+                    // warp ew: tokens j0 + 8*ew .. +7; lanes: channels lane, lane + 32
+                    float* out = static_cast<float*>(args.out);
 #pragma unroll
-                    for (int j = 0; j < BN; ++j) {
-                        if (j < nvalid) {
-                            const float gv = __int_as_float(sum[j]);
-                            const float h = __fmul_rn(silu_f32(gv), xrow[j]);
-                            out[(size_t)(row0 + j) * args.ld_out + chan] = h;
+                    for (int t = 0; t < 8; ++t) {
+                        const int j = ew * 8 + t;
+                        const int rr = row0 + j0 + j;
+                        if (j0 + j < nvalid && args.flags[rr] == 0) {
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2) {
+                                const int c = lane + 32 * c2;
+                                const float gv = xch[c * C::kXchStride + j];
+                                const float uv = xch[(64 + c) * C::kXchStride + j];
+                                out[(size_t)rr * args.ld_out + cb * 64 + c] = __fmul_rn(silu_f32(gv), uv);
+                            }
                         }
                     }
-                    __syncwarp();
-                    if (lane == 0) mbar_arrive(xch_empty);
-                }
-            } else {
-                const int chan = cb * kTileM + row;
-                const float sw = args.w_scale[(size_t)g * args.w_rows_per_group + chan];
-                if (args.acc_out) {
+                    if (!epi_sync(epi_bar, eit, ctl)) { ok = false; break; }
+                } else {
 #pragma unroll
-                    for (int j = 0; j < BN; ++j)
-                        if (j < nvalid) args.acc_out[(size_t)(row0 + j) * args.w_rows_per_group + chan] = sum[j];
-                }
-#pragma unroll
-                for (int j = 0; j < BN; ++j) {
-                    if (j < nvalid) {
-                        const float sa = __ldg(args.act_scale + row0 + j);
-                        const float v = __fmul_rn(__fmul_rn(__int2float_rn(sum[j]), sa), sw);
-                        if (EPI == (int)Epi::ScaleF32) {
-                            reinterpret_cast<float*>(args.out)[(size_t)(row0 + j) * args.ld_out + chan] = v;
-                        } else {
-                            reinterpret_cast<__nv_bfloat16*>(args.out)[(size_t)(row0 + j) * args.ld_out + chan] =
-                                __float2bfloat16_rn(v);
+                    for (int j = 0; j < 32; ++j) {
+                        const int rr = row0 + j0 + j;
+                        if (j0 + j < nvalid && args.flags[rr] == 0) {
+                            const float v = dequant(__uint_as_float(r[j]), __ldg(args.act_scale + rr), sw);
+                            if (EPI == (int)Epi::ScaleF32)
+                                static_cast<float*>(args.out)[(size_t)rr * args.ld_out + wrow] = v;
+                            else
+                                static_cast<__nv_bfloat16*>(args.out)[(size_t)rr * args.ld_out + wrow] =
+                                    __float2bfloat16_rn(v);
                         }
                     }
                 }
@@ -436,6 +513,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_after();
         tmem_dealloc(tmem, C::kTmemAlloc);
     }
+    if (!*abort_flag) fallback_rows<EPI>(args, row_start, n_groups);
 }
 
 // ------------------------------------------------------------------ host side
@@ -470,10 +548,9 @@ bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int BN, int EPI>
-cudaError_t launch_impl(const GemmArgs& args, const void* w, const void* act16, cudaStream_t st) {
-    using C = Cfg<BN>;
-    auto kern = grouped_gemm_kernel<BN, EPI>;
+template <class C, int EPI>
+cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
+    auto kern = grouped_gemm_kernel<C, EPI>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
     std::call_once(once, [&] {
@@ -483,14 +560,14 @@ cudaError_t launch_impl(const GemmArgs& args, const void* w, const void* act16, 
 
     CUtensorMap tw, tb;
     const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
-    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, w, args.K, w_rows, kBK, 64,
-                     CU_TENSOR_MAP_SWIZZLE_64B))
+    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK, 64,
+                     C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, act16, args.K, (uint64_t)args.total_rows, kBK, BN,
-                     CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K, (uint64_t)args.total_rows, 64,
+                     C::BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
-    const long max_tiles = ((long)(args.total_rows + BN - 1) / BN + args.n_groups) * args.n_cb;
+    const long max_tiles = ((long)(args.total_rows + C::BN - 1) / C::BN + args.n_groups) * args.n_cb;
     int grid = num_sms();
     if (max_tiles < grid) grid = (int)max_tiles;
     if (grid < 1) grid = 1;
@@ -498,18 +575,31 @@ cudaError_t launch_impl(const GemmArgs& args, const void* w, const void* act16, 
     return cudaGetLastError();
 }
 
+template <int EPI>
+cudaError_t launch_epi(GemmShape shape, const GemmArgs& args, cudaStream_t st) {
+    switch (shape) {
+        case GemmShape::Wide: return launch_impl<CfgWide, EPI>(args, st);
+        case GemmShape::Mid: return launch_impl<CfgMid, EPI>(args, st);
+        case GemmShape::Narrow: return launch_impl<CfgNarrow, EPI>(args, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
 }  // namespace
 
-cudaError_t launch_grouped_gemm(Epi epi, int bn, const GemmArgs& args, const void* w, const void* act16,
-                                cudaStream_t st) {
+GemmShape choose_gemm_shape(long rows, long groups) {
+    const long per_group = rows / (groups > 0 ? groups : 1);
+    if (per_group >= 192) return GemmShape::Wide;
+    if (per_group >= 48) return GemmShape::Mid;
+    return GemmShape::Narrow;
+}
+
+cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st) {
     if (args.total_rows == 0) return cudaSuccess;
     switch (epi) {
-        case Epi::GateUp:
-            return bn == 128 ? launch_impl<128, 0>(args, w, act16, st) : launch_impl<32, 0>(args, w, act16, st);
-        case Epi::ScaleF32:
-            return bn == 128 ? launch_impl<128, 1>(args, w, act16, st) : launch_impl<32, 1>(args, w, act16, st);
-        case Epi::ScaleBF16:
-            return bn == 128 ? launch_impl<128, 2>(args, w, act16, st) : launch_impl<32, 2>(args, w, act16, st);
+        case Epi::GateUp: return launch_epi<0>(shape, args, st);
+        case Epi::ScaleF32: return launch_epi<1>(shape, args, st);
+        case Epi::ScaleBF16: return launch_epi<2>(shape, args, st);
     }
     return cudaErrorInvalidValue;
 }

@@ -25,7 +25,21 @@ enum class Epi : int {
     ScaleBF16 = 2  // (acc * s_act) * s_w, bf16 out (linear layer)
 };
 
+// Tile shapes of the grouped GEMM (activation rows per tile / K per stage).
+enum class GemmShape : int {
+    Wide = 0,    // 256 rows per tile: groups of a few hundred rows or more
+    Mid = 1,     // 128 rows per tile
+    Narrow = 2   // 32 rows per tile: a few rows per group (decode)
+};
+
+// Largest L1 norm of a quantised activation row for which the fp32
+// tensor-core accumulation of int8 x int8 products is exact: every partial
+// sum is then at most 128 * 2^17 = 2^24 in magnitude.
+constexpr int kExactL1 = 1 << 17;
+
 struct GemmArgs {
+    const void* w;           // int8 weights [n_groups * w_rows_per_group][K]
+    const void* act16;       // fp16 activation rows [total_rows][K] (exact int8 values)
     int K;                   // reduction length (multiple of 128)
     int n_cb;                // channel blocks per group
     int n_groups;            // groups (experts); 1 for the linear layer
@@ -38,19 +52,22 @@ struct GemmArgs {
     void* out;               // fp32 or bf16 output
     int ld_out;              // output row length in elements
     int32_t* acc_out;        // optional raw accumulators [total_rows][w_rows_per_group]
+    const int32_t* flags;    // [total_rows] nonzero: row above kExactL1, done by the exact path
+    const int32_t* fb_list;  // rows above kExactL1 (any order)
+    const int32_t* fb_count; // number of entries of fb_list
     int* error;              // sticky device error word
     uint64_t timeout_ns;
 };
 
 // Forward workspace layout (byte offsets; every region 256-byte aligned).
 struct FwdLayout {
-    size_t err, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x, s_slot, q_x16,
-        h, s_h, q_h16, o, total;
+    size_t err, counts, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x, s_slot,
+        flag1, list1, flag2, list2, q_x16, h, s_h, q_h16, o, total;
 };
 FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 
 struct LinLayout {
-    size_t err, s_x, q_x16, total;
+    size_t err, counts, s_x, flag, list, q_x16, total;
 };
 LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 
@@ -58,21 +75,22 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 cudaError_t launch_router_topk(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
                                int E, int k, int32_t* topk_ids, float* topk_w, int32_t* rank,
                                int32_t* hist, cudaStream_t st);
-cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, cudaStream_t st);
+cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
+                        cudaStream_t st);
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16,
-                                 cudaStream_t st);
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
-                           cudaStream_t st);
+                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
                            int H, int k, uint16_t* y, cudaStream_t st);
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
                                     cudaStream_t st);
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
                                   int row_stride_of, int8_t* q8, cudaStream_t st);
-cudaError_t launch_grouped_gemm(Epi epi, int bn, const GemmArgs& args, const void* w,
-                                const void* act16, cudaStream_t st);
+GemmShape choose_gemm_shape(long rows, long groups);
+cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st);
 
 int num_sms();
 

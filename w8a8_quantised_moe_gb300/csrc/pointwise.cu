@@ -32,11 +32,16 @@ __device__ __forceinline__ float warp_max(float v) {
     return v;
 }
 
-// One warp per row of h [S][I].
+// One warp per row of h [S][I].  Like the activation quantiser it certifies
+// every code row: rows whose L1 norm exceeds kExactL1 are flagged and listed
+// for the exact path of the second GEMM.
 __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ h, int S, int I,
                                                       float* __restrict__ s_h,
                                                       uint16_t* __restrict__ q16,
-                                                      int8_t* __restrict__ q8) {
+                                                      int8_t* __restrict__ q8,
+                                                      int32_t* __restrict__ flags,
+                                                      int32_t* __restrict__ fb_list,
+                                                      int32_t* __restrict__ fb_count) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (r >= S) return;
@@ -50,10 +55,12 @@ __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ 
     amax = warp_max(amax);
     const float s = __fdiv_rn(amax, 127.0f);
     if (lane == 0) s_h[r] = s;
+    int l1 = 0;
     for (int i = lane; i < nv; i += 32) {
         const float4 v = row[i];
         const int a = quant_code(v.x, s), b = quant_code(v.y, s), c = quant_code(v.z, s),
                   d = quant_code(v.w, s);
+        l1 += abs(a) + abs(b) + abs(c) + abs(d);
         uint2 o;
         o.x = (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
         o.y = (uint32_t)__half_as_ushort(__int2half_rn(c)) | ((uint32_t)__half_as_ushort(__int2half_rn(d)) << 16);
@@ -63,6 +70,13 @@ __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ 
                                     ((uint32_t)(uint8_t)c << 16) | ((uint32_t)(uint8_t)d << 24);
             reinterpret_cast<uint32_t*>(q8 + (size_t)r * I)[i] = packed;
         }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (lane == 0) {
+        const int flagged = l1 > kExactL1 ? 1 : 0;
+        flags[r] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = r;
     }
 }
 
@@ -150,9 +164,9 @@ __global__ void f16_rows_to_s8_kernel(const uint16_t* __restrict__ q16, const in
 }  // namespace
 
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
-                           cudaStream_t st) {
+                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {
     if (S == 0) return cudaSuccess;
-    requant_kernel<<<(S + 7) / 8, 256, 0, st>>>(h, S, I, s_h, q16, q8);
+    requant_kernel<<<(S + 7) / 8, 256, 0, st>>>(h, S, I, s_h, q16, q8, flags, fb_list, fb_count);
     return cudaGetLastError();
 }
 

@@ -160,13 +160,14 @@ constexpr int kScanSmemInts = 40960;
 
 __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict__ hist, int nchunk,
                                                             int E, int32_t* __restrict__ offsets,
-                                                            int use_smem) {
+                                                            int32_t* __restrict__ counts, int use_smem) {
     extern __shared__ int32_t tab_s[];
     __shared__ int32_t part_tot[kScanThreads];
     __shared__ int32_t total[kMaxExperts + 1];
     const int tid = threadIdx.x;
     const int n = nchunk * E;
     int32_t* tab = use_smem ? tab_s : hist;
+    if (tid < 2) counts[tid] = 0;  // rows listed for the exact GEMM path (GEMM1, GEMM2)
     if (use_smem) {
         for (int i = tid; i < n; i += kScanThreads) tab[i] = hist[i];
         __syncthreads();
@@ -221,12 +222,15 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
 }
 
 // One warp per token.  With topk_ids == nullptr the token's single "slot" is
-// the token itself (the dense linear layer).
+// the token itself (the dense linear layer).  Besides the codes, every token
+// gets the L1 norm of its code row; rows above kExactL1 are flagged in each
+// of their slots and listed for the exact path of the GEMM.
 __global__ void __launch_bounds__(256) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
-    float* __restrict__ s_slot, uint16_t* __restrict__ q16) {
+    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int32_t* __restrict__ flags,
+    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -258,6 +262,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
     if (lane < nk) s_slot[my_slot] = s;
+    int l1 = 0;
     for (int i = lane; i < nv; i += 32) {
         const uint4 v = __ldg(row + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
@@ -271,11 +276,19 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
                 q0 = min(127, max(-128, q0));
                 q1 = min(127, max(-128, q1));
             }
+            l1 += abs(q0) + abs(q1);
             out[j] = (uint32_t)__half_as_ushort(__int2half_rn(q0)) |
                      ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
         }
         const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
         for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    const int flagged = l1 > kExactL1 ? 1 : 0;
+    if (lane < nk) {
+        flags[my_slot] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = my_slot;
     }
 }
 
@@ -296,7 +309,8 @@ cudaError_t launch_router_topk(const uint16_t* x, const float* Wr, const float* 
     return cudaGetLastError();
 }
 
-cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, cudaStream_t st) {
+cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
+                        cudaStream_t st) {
     const long n = (long)nchunk * E;
     const int use_smem = n <= kScanSmemInts ? 1 : 0;
     const size_t smem = use_smem ? (size_t)n * sizeof(int32_t) : 0;
@@ -307,17 +321,17 @@ cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, cuda
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    scan_kernel<<<1, kScanThreads, smem, st>>>(hist, nchunk, E, offsets, use_smem);
+    scan_kernel<<<1, kScanThreads, smem, st>>>(hist, nchunk, E, offsets, counts, use_smem);
     return cudaGetLastError();
 }
 
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16,
-                                 cudaStream_t st) {
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {
     const int grid = (T + 7) / 8;
     permute_quant_kernel<<<grid, 256, 0, st>>>(x, topk_ids, rank, hist, T, H, E, k, slot_of, slot_token,
-                                               s_x, s_slot, q16);
+                                               s_x, s_slot, q16, flags, fb_list, fb_count);
     return cudaGetLastError();
 }
 

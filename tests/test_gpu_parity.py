@@ -30,11 +30,13 @@ def _built():
 TINY = wl.CONFIGS["tiny"]
 CASES = {
     "tiny": TINY,
-    # S/E = 75 rows per expert: 128-row tiles, ragged tails
+    # 75 rows per expert: 128-row tiles, ragged tails
     "wide_tiles": TINY.replace(T=300, H=512, I=384, E=8, k=2),
+    # 300 rows per expert: 256-row tiles, ragged tails
+    "rows_256": TINY.replace(T=600, H=384, I=256, E=4, k=2),
     # 32-row tiles, router bias, top-4
     "top4_bias": TINY.replace(T=77, H=384, I=256, E=16, k=4, bias="normal", bias_std=0.5),
-    # K > 1024 in both GEMMs: several exact accumulation chunks
+    # long reductions in both GEMMs
     "long_k": TINY.replace(T=100, H=1280, I=1152, E=4, k=2, n_outlier=13),
     "single_expert": TINY.replace(T=45, H=256, I=256, E=1, k=1),
     "one_token": TINY.replace(T=1, H=256, I=512, E=8, k=2),
@@ -230,23 +232,24 @@ def _boundary_rows(H):
         mag[1:64] = 63.0  # 127 + 63*63 + 1984*64 = 131072
         if extra:
             mag[1] = 64.0  # 131073
-        sign = np.where(r.random(H) < 0.5, -1.0, 1.0)
+        # row 0 positive (its weights -128 make every product -128 * |x|)
+        sign = np.where(r.random(H) < 0.5, -1.0, 1.0) if extra else np.ones(H)
         sign[0] = 1.0
         rows.append(mag * sign)
     return np.array(rows, np.float32)
 
 
 def test_exactness_certificate_boundary():
-    """A row with L1 = 2^17 against weights -128*sign(x) drives the partial
-    sums to exactly -2^24 on the tensor-core path; a row one above the bound
-    goes to the exact CUDA-core path.  Both must be exact."""
+    """A positive row with L1 = 2^17 against weights -128 drives the partial
+    sums down to exactly -2^24 on the tensor-core path; a row one above the
+    bound goes to the exact CUDA-core path.  Both must be exact."""
     H, I = 2048, 128
     x = _boundary_rows(H)
     assert np.abs(x[0]).sum() == 2 ** 17 and np.abs(x[1]).sum() == 2 ** 17 + 1
     w13 = np.random.default_rng(3).integers(-128, 128, (1, 2 * I, H)).astype(np.int8)
-    w13[0, 0] = (-128 * np.sign(x[0])).astype(np.int8)
-    w13[0, 1] = (-128 * np.sign(x[1])).astype(np.int8)
-    w13[0, 2] = (127 * np.sign(x[0])).astype(np.int8)
+    w13[0, 0] = -128   # partial sums of row 0 fall monotonically to -2^24
+    w13[0, 1] = -128
+    w13[0, 2] = 127
     w2 = np.random.default_rng(4).integers(-128, 128, (1, H, I)).astype(np.int8)
     args = (torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.zeros((H, 1), device="cuda"), None,
             torch.from_numpy(w13).cuda(), torch.full((1, 2 * I), 1e-7, device="cuda"),

@@ -2,7 +2,8 @@
 // layout and the launch sequence of the layer.
 //
 // Forward launch sequence on the caller's stream (no host synchronisation):
-//   1 router_topk      logits, top-k, weights, chunk counts and ranks
+//   1 router           split of the router weights into three bf16 parts,
+//                      tensor-core logits, top-k, weights, chunk counts/ranks
 //   2 scan             expert offsets, first slot of every (chunk, expert)
 //   3 permute_quant    slots; per-token quantisation scattered into slots
 //   4 grouped GEMM 1   gate/up GEMM + scale outer product + SiLU(gate)*up -> h
@@ -62,6 +63,9 @@ FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     };
     L.err = take(256);
     L.counts = take(2 * 4);
+    const RouterPlan rp = router_plan(T, H, E);
+    L.wsplit = take((size_t)3 * rp.E_pad * H * 2);
+    L.logits = take((size_t)rp.KS * T * rp.E_pad * 4);
     L.topk_ids = take(S * 4);
     L.topk_w = take(S * 4);
     L.rank = take(S * 4);
@@ -133,6 +137,8 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     const int S = (int)(T * k);
     const int nchunk = (int)((T + kRouterTokens - 1) / kRouterTokens);
     int* err = at<int>(workspace, L.err);
+    uint16_t* wsplit = at<uint16_t>(workspace, L.wsplit);
+    float* logits = at<float>(workspace, L.logits);
     int32_t* topk_ids = at<int32_t>(workspace, L.topk_ids);
     float* topk_w = at<float>(workspace, L.topk_w);
     int32_t* rank = at<int32_t>(workspace, L.rank);
@@ -153,12 +159,11 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     uint16_t* q_h16 = at<uint16_t>(workspace, L.q_h16);
     float* o = at<float>(workspace, L.o);
     const uint64_t timeout = g_timeout_ns.load();
-    const GemmShape shape = choose_gemm_shape(S, E);
 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_router_topk(x, router_w, router_bias, (int)T, (int)H, (int)E, (int)k, topk_ids, topk_w,
-                           rank, hist, st);
+    e = launch_router(x, router_w, router_bias, (int)T, (int)H, (int)E, (int)k, wsplit, logits, topk_ids,
+                      topk_w, rank, hist, err, timeout, st);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
     e = launch_scan(hist, nchunk, (int)E, offsets, counts, st);
@@ -189,7 +194,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.error = err;
     g1.timeout_ns = timeout;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::GateUp, shape, g1, st);
+    e = launch_grouped_gemm(Epi::GateUp, choose_gemm_shape(S, E, H), g1, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
@@ -217,7 +222,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.error = err;
     g2.timeout_ns = timeout;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::ScaleF32, shape, g2, st);
+    e = launch_grouped_gemm(Epi::ScaleF32, choose_gemm_shape(S, E, I), g2, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
@@ -357,7 +362,7 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     g.fb_count = counts;
     g.error = at<int>(workspace, L.err);
     g.timeout_ns = g_timeout_ns.load();
-    if ((e = launch_grouped_gemm(Epi::ScaleBF16, choose_gemm_shape(M, 1), g, st)) != cudaSuccess)
+    if ((e = launch_grouped_gemm(Epi::ScaleBF16, choose_gemm_shape(M, 1, K), g, st)) != cudaSuccess)
         return from_cuda(e);
     return from_cuda(mark(2, st));
 }

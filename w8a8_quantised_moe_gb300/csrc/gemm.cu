@@ -518,36 +518,6 @@ __global__ void __launch_bounds__(kThreads, 1)
 
 // ------------------------------------------------------------------ host side
 
-using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
-                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
-                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
-
-EncodeFn get_encode_fn() {
-    static EncodeFn fn = nullptr;
-    static std::once_flag once;
-    std::call_once(once, [] {
-        void* p = nullptr;
-        cudaDriverEntryPointQueryResult q;
-        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
-                cudaSuccess &&
-            q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<EncodeFn>(p);
-    });
-    return fn;
-}
-
-bool make_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
-                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
-    EncodeFn enc = get_encode_fn();
-    if (!enc) return false;
-    const cuuint64_t dims[2] = {inner, outer};
-    const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
-    const cuuint32_t box[2] = {box_inner, box_outer};
-    const cuuint32_t estr[2] = {1, 1};
-    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
-               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 template <class C, int EPI>
 cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
     auto kern = grouped_gemm_kernel<C, EPI>;
@@ -560,10 +530,10 @@ cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
 
     CUtensorMap tw, tb;
     const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
-    if (!make_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK, 64,
+    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK, 64,
                      C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K, (uint64_t)args.total_rows, 64,
+    if (!make_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K, (uint64_t)args.total_rows, 64,
                      C::BN, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
 
@@ -587,9 +557,41 @@ cudaError_t launch_epi(GemmShape shape, const GemmArgs& args, cudaStream_t st) {
 
 }  // namespace
 
-GemmShape choose_gemm_shape(long rows, long groups) {
+using EncodeFn = CUresult (*)(CUtensorMap*, CUtensorMapDataType, cuuint32_t, void*, const cuuint64_t*,
+                              const cuuint64_t*, const cuuint32_t*, const cuuint32_t*, CUtensorMapInterleave,
+                              CUtensorMapSwizzle, CUtensorMapL2promotion, CUtensorMapFloatOOBfill);
+
+static EncodeFn get_encode_fn() {
+    static EncodeFn fn = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+                cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            fn = reinterpret_cast<EncodeFn>(p);
+    });
+    return fn;
+}
+
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base, uint64_t inner,
+                 uint64_t outer, uint32_t box_inner, uint32_t box_outer, CUtensorMapSwizzle swz) {
+    EncodeFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t dims[2] = {inner, outer};
+    const cuuint64_t strides[1] = {inner * (uint64_t)elem_bytes};
+    const cuuint32_t box[2] = {box_inner, box_outer};
+    const cuuint32_t estr[2] = {1, 1};
+    return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+GemmShape choose_gemm_shape(long rows, long groups, long K) {
     const long per_group = rows / (groups > 0 ? groups : 1);
-    if (per_group >= 192) return GemmShape::Wide;
+    // the 256-row tile has one accumulator, so its epilogue is not hidden
+    // behind the next tile's MMAs: worth it only for long reductions
+    if (per_group >= 192 && K >= 3072) return GemmShape::Wide;
     if (per_group >= 48) return GemmShape::Mid;
     return GemmShape::Narrow;
 }

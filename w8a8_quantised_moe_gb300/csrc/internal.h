@@ -9,7 +9,9 @@
 
 namespace moe {
 
-constexpr int kRouterTokens = 32;  // tokens per router CTA = tokens per routing chunk
+constexpr int kRouterTokens = 32;  // tokens per top-k CTA = tokens per routing chunk
+constexpr int kRouterTargetCtas = 160;  // K slices of the router GEMM fill about this many CTAs
+constexpr int kRouterMaxSlices = 8;     // at most this many K slices (partial logits per token)
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -59,10 +61,18 @@ struct GemmArgs {
     uint64_t timeout_ns;
 };
 
+// Launch plan of the router GEMM: experts padded to E_pad (a multiple of 16,
+// or of 128 above 128), NB experts per CTA, the hidden dimension cut into KS
+// slices of kb_per_slice 64-wide steps.
+struct RouterPlan {
+    int E_pad, NB, n_eb, KS, kb_per_slice;
+};
+RouterPlan router_plan(int64_t T, int64_t H, int64_t E);
+
 // Forward workspace layout (byte offsets; every region 256-byte aligned).
 struct FwdLayout {
-    size_t err, counts, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x, s_slot,
-        flag1, list1, flag2, list2, q_x16, h, s_h, q_h16, o, total;
+    size_t err, counts, wsplit, logits, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x,
+        s_slot, flag1, list1, flag2, list2, q_x16, h, s_h, q_h16, o, total;
 };
 FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 
@@ -72,9 +82,10 @@ struct LinLayout {
 LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 
 // ---- launchers (return cudaSuccess or the launch error) ----
-cudaError_t launch_router_topk(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                               int E, int k, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                               int32_t* hist, cudaStream_t st);
+// Router: weight split, tensor-core logits (partials per K slice), top-k.
+cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
+                          uint16_t* wsplit, float* logits, int32_t* topk_ids, float* topk_w, int32_t* rank,
+                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
                         cudaStream_t st);
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
@@ -89,9 +100,14 @@ cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t*
                                     cudaStream_t st);
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
                                   int row_stride_of, int8_t* q8, cudaStream_t st);
-GemmShape choose_gemm_shape(long rows, long groups);
+GemmShape choose_gemm_shape(long rows, long groups, long K);
 cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st);
 
 int num_sms();
+
+// 2-D tiled tensor map (row-major, inner dimension contiguous).
+bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
+                        uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
+                        CUtensorMapSwizzle swz);
 
 }  // namespace moe

@@ -1,19 +1,12 @@
 // route.cu -- routing and activation quantisation.
 //
-//   router_topk_kernel   FP32 router logits, top-k with ties to the lower
-//                        expert index, softmax over the selected logits, and
-//                        per 32-token chunk: the count of tokens per expert and
-//                        each choice's rank among the chunk's tokens of that
-//                        expert.
 //   scan_kernel          expert offsets (exclusive prefix over experts) and the
 //                        first slot of every (chunk, expert).
 //   permute_quant_kernel slot of every (token, choice); per-token dynamic INT8
 //                        quantisation of x, scattered into the token's slots.
 //
-// Gate -> top-k -> routing pre-processing that reserves a contiguous slot
-// range per expert: "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section
-// 1.3.  FP32 router: "DeepSeek V4 950 FP8 inference on H100" (lpnh.cn),
-// section 4.1.  Per-token dynamic quantisation q = clamp(round(x/s)),
+// Routing pre-processing that reserves a contiguous slot range per expert:
+// "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section 1.3.  Per-token dynamic quantisation q = clamp(round(x/s)),
 // s = amax/127: "W8A8 quantisation of MiniMax-M3 on K100AI" (mhpn.cn),
 // section 2.1.
 #include <cuda_bf16.h>
@@ -24,131 +17,7 @@
 namespace moe {
 namespace {
 
-constexpr int RT = kRouterTokens;  // 32 tokens per CTA
-constexpr int HK = 32;             // hidden channels per smem chunk
-
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
-
-// Thread layout: warp w owns tokens 4w..4w+3 of the chunk; lane l owns
-// experts l + 32*i for i < EPT.  Each thread keeps 4 x EPT logits.
-template <int EPT>
-__global__ void __launch_bounds__(256) router_topk_kernel(const uint16_t* __restrict__ x,
-                                                          const float* __restrict__ Wr,
-                                                          const float* __restrict__ bias, int T,
-                                                          int H, int E, int k,
-                                                          int32_t* __restrict__ topk_ids,
-                                                          float* __restrict__ topk_w,
-                                                          int32_t* __restrict__ rank,
-                                                          int32_t* __restrict__ hist) {
-    constexpr int EP = 32 * EPT;  // padded expert count
-    __shared__ __align__(16) float xsT[HK][RT];  // [h][token]
-    __shared__ __align__(16) float ws[HK][EP];
-    __shared__ uint32_t mask[EP];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * RT;
-
-    float acc[4][EPT];
-#pragma unroll
-    for (int r = 0; r < 4; ++r)
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) acc[r][i] = 0.f;
-    for (int i = tid; i < EP; i += 256) mask[i] = 0u;
-
-    for (int h0 = 0; h0 < H; h0 += HK) {
-        {  // x chunk: 32 tokens x 32 channels; thread -> token tid/8, channels 4*(tid%8)..+3
-            const int r = tid >> 3, c = (tid & 7) * 4, t = t0 + r;
-            uint2 v = make_uint2(0u, 0u);
-            if (t < T) v = *reinterpret_cast<const uint2*>(x + (size_t)t * H + h0 + c);
-            xsT[c + 0][r] = bf16_bits_to_float(v.x & 0xffffu);
-            xsT[c + 1][r] = bf16_bits_to_float(v.x >> 16);
-            xsT[c + 2][r] = bf16_bits_to_float(v.y & 0xffffu);
-            xsT[c + 3][r] = bf16_bits_to_float(v.y >> 16);
-        }
-        for (int i = tid; i < HK * EP; i += 256) {
-            const int r = i / EP, e = i % EP;
-            ws[r][e] = (e < E) ? Wr[(size_t)(h0 + r) * E + e] : 0.f;
-        }
-        __syncthreads();
-#pragma unroll 8
-        for (int hh = 0; hh < HK; ++hh) {
-            const float4 xv = *reinterpret_cast<const float4*>(&xsT[hh][warp * 4]);
-            const float xr[4] = {xv.x, xv.y, xv.z, xv.w};
-#pragma unroll
-            for (int i = 0; i < EPT; ++i) {
-                const float w = ws[hh][lane + 32 * i];
-#pragma unroll
-                for (int r = 0; r < 4; ++r) acc[r][i] = __fmaf_rn(xr[r], w, acc[r][i]);
-            }
-        }
-        __syncthreads();
-    }
-
-    // top-k per token with warp-wide arg-max; ties go to the lower index
-#pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int t = t0 + warp * 4 + r;
-        float v[EPT];
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            const int e = lane + 32 * i;
-            v[i] = (e < E) ? (bias ? __fadd_rn(acc[r][i], bias[e]) : acc[r][i]) : -INFINITY;
-        }
-        bool taken[EPT];
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) taken[i] = (lane + 32 * i) >= E;
-        float sel_v[kMaxTopK];
-        int sel_e[kMaxTopK];
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < EPT; ++i) {
-                const int e = lane + 32 * i;
-                if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
-                    bv = v[i];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < EPT; ++i)
-                if (lane + 32 * i == be) taken[i] = true;
-            sel_v[j] = bv;
-            sel_e[j] = be;
-        }
-        if (t < T && lane == 0) {
-            float den = 0.f;
-            float ex[kMaxTopK];
-            for (int j = 0; j < k; ++j) {
-                ex[j] = expf(__fsub_rn(sel_v[j], sel_v[0]));
-                den = __fadd_rn(den, ex[j]);
-            }
-            for (int j = 0; j < k; ++j) {
-                topk_ids[(size_t)t * k + j] = sel_e[j];
-                topk_w[(size_t)t * k + j] = __fdiv_rn(ex[j], den);
-                atomicOr(&mask[sel_e[j]], 1u << (warp * 4 + r));
-            }
-        }
-    }
-    __syncthreads();
-    // chunk-local rank of each choice and the chunk's count per expert
-    for (int i = tid; i < RT * k; i += 256) {
-        const int r = i / k, t = t0 + r;
-        if (t < T) {
-            const int e = topk_ids[(size_t)t * k + (i % k)];
-            rank[(size_t)t * k + (i % k)] = __popc(mask[e] & ((1u << r) - 1u));
-        }
-    }
-    for (int e = tid; e < E; e += 256) hist[(size_t)blockIdx.x * E + e] = __popc(mask[e]);
-}
 
 // One CTA.  hist [nchunk][E] holds per-chunk counts on entry and the first
 // slot of every (chunk, expert) on exit; offsets[E+1] receives the exclusive
@@ -293,21 +162,6 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
 }
 
 }  // namespace
-
-cudaError_t launch_router_topk(const uint16_t* x, const float* Wr, const float* bias, int T, int H,
-                               int E, int k, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                               int32_t* hist, cudaStream_t st) {
-    const int grid = (T + RT - 1) / RT;
-    if (E <= 32)
-        router_topk_kernel<1><<<grid, 256, 0, st>>>(x, Wr, bias, T, H, E, k, topk_ids, topk_w, rank, hist);
-    else if (E <= 64)
-        router_topk_kernel<2><<<grid, 256, 0, st>>>(x, Wr, bias, T, H, E, k, topk_ids, topk_w, rank, hist);
-    else if (E <= 128)
-        router_topk_kernel<4><<<grid, 256, 0, st>>>(x, Wr, bias, T, H, E, k, topk_ids, topk_w, rank, hist);
-    else
-        router_topk_kernel<8><<<grid, 256, 0, st>>>(x, Wr, bias, T, H, E, k, topk_ids, topk_w, rank, hist);
-    return cudaGetLastError();
-}
 
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
                         cudaStream_t st) {

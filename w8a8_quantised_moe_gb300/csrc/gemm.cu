@@ -34,11 +34,19 @@
 //   warp 1      TMEM allocator and single-thread MMA issuer
 //   warps 2-5   converters: int8 weight rows -> fp16 pairs -> tcgen05.st
 //   warps 6-9   epilogue: tcgen05.ld, scales, SiLU gate, outputs
+// Shared-memory bandwidth (about 128 B/clk per SM, shared by TMA writes,
+// tensor-core operand reads and LSU traffic) bounds this 1-SM MMA design:
+// every stage moves the activation tile twice (TMA write, tensor-core read)
+// and the int8 weight tile twice (TMA write, converter read).  So each tile
+// loads only as many activation rows as it has valid rows (rounded up to a
+// box of 32, 64, 128 or BN rows), and the accumulators are double-buffered
+// so that the epilogue never holds up the MMAs.
 // The grid is persistent; tiles are dealt round-robin.  Every wait is
 // bounded (see ptx.cuh); a timeout aborts the CTA cleanly.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <cstdlib>
 #include <mutex>
 
 #include "internal.h"
@@ -71,7 +79,8 @@ struct Cfg {
     static constexpr int kOffBars = kOffXch + kXch;
     static constexpr int kNumBars = 3 * NS + 2 * ND + 2;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
-    static constexpr int kOffMisc = kOffTiles + (kMaxExperts + 1) * 4 * 2;
+    static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;  // [2][BN] scales, [2][BN] flags
+    static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
     static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM budget");
@@ -79,7 +88,7 @@ struct Cfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-using CfgWide = Cfg<256, 64, 4, 1>;    // many rows per group
+using CfgWide = Cfg<192, 64, 4, 2>;    // hundreds of rows per group (compute-bound)
 using CfgMid = Cfg<128, 128, 4, 2>;    // about a hundred rows per group
 using CfgNarrow = Cfg<32, 128, 6, 2>;  // a few rows per group (decode)
 
@@ -90,7 +99,6 @@ struct Tiles {
     const int* tile_start;  // smem, [n_groups + 1]
     const int* row_start;   // smem, [n_groups + 1]
     int n_groups;
-    int n_cb;
 };
 
 __device__ __forceinline__ int last_le(const int* a, int n, int v) {  // last i < n with a[i] <= v
@@ -243,10 +251,22 @@ __device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_
     }
 }
 
+// Box heights of the activation tensor maps: a tile with nvalid rows loads
+// the smallest box that covers them.
+template <int BN>
+__device__ __forceinline__ int box_index(int nvalid) {
+    return nvalid <= 32 ? 0 : nvalid <= 64 ? 1 : nvalid <= 128 ? 2 : 3;
+}
+template <int BN>
+__host__ __device__ constexpr int box_rows(int i) {
+    return i == 0 ? (BN < 32 ? BN : 32) : i == 1 ? (BN < 64 ? BN : 64) : i == 2 ? (BN < 128 ? BN : 128) : BN;
+}
+
 template <class C, int EPI>
 __global__ void __launch_bounds__(kThreads, 1)
-    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w,
-                        const __grid_constant__ CUtensorMap tmap_b, const GemmArgs args) {
+    grouped_gemm_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b0,
+                        const __grid_constant__ CUtensorMap tmap_b1, const __grid_constant__ CUtensorMap tmap_b2,
+                        const __grid_constant__ CUtensorMap tmap_b3, const GemmArgs args) {
     constexpr int BN = C::BN, BK = C::BK, NS = C::NS, ND = C::ND;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
@@ -263,6 +283,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
     float* xch = reinterpret_cast<float*>(smem + C::kOffXch);
+    float* row_scale_s = reinterpret_cast<float*>(smem + C::kOffRowInfo);       // [2][BN]
+    int* row_flag_s = reinterpret_cast<int*>(smem + C::kOffRowInfo + 2 * BN * 4);  // [2][BN]
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_groups = args.n_groups;
@@ -283,7 +305,10 @@ __global__ void __launch_bounds__(kThreads, 1)
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
-        tma_prefetch_desc(&tmap_b);
+        tma_prefetch_desc(&tmap_b0);
+        tma_prefetch_desc(&tmap_b1);
+        tma_prefetch_desc(&tmap_b2);
+        tma_prefetch_desc(&tmap_b3);
     }
     if (warp == 1) {
         tmem_alloc(tmem_slot, C::kTmemAlloc);
@@ -317,7 +342,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
     const int total_tiles = tile_start[n_groups];
-    const Tiles tiles{tile_start, row_start, n_groups, args.n_cb};
+    const Tiles tiles{tile_start, row_start, n_groups};
     const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
 
     if (warp == 0) {
@@ -336,15 +361,19 @@ __global__ void __launch_bounds__(kThreads, 1)
                     wrow0 = g * args.w_rows_per_group + cb * kTileM;
                     wrow1 = wrow0 + 64;
                 }
+                const int bi = box_index<BN>(nvalid);
+                const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
+                const uint32_t stage_bytes = (uint32_t)(C::kStageA + box_rows<BN>(bi) * 128 * (BK / 64));
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % NS, ph = (it / NS) & 1u;
                     if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                     uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(&full[s], C::kStage);
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
                     tma_load_2d(st, &tmap_w, &full[s], kb * BK, wrow0);
                     tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kb * BK, wrow1);
-                    tma_load_2d(st + C::kStageA, &tmap_b, &full[s], kb * BK, row0);
-                    if (BK == 128) tma_load_2d(st + C::kStageA + BN * 128, &tmap_b, &full[s], kb * BK + 64, row0);
+#pragma unroll
+                    for (int hh = 0; hh < BK / 64; ++hh)
+                        tma_load_2d(st + C::kStageA + hh * BN * 128, mb, &full[s], kb * BK + hh * 64, row0);
                 }
             }
             // drain: every fill issued must land before the CTA may exit
@@ -438,14 +467,25 @@ __global__ void __launch_bounds__(kThreads, 1)
             int g, cb, row0, nvalid;
             decode_tile<BN>(tiles, tile, g, cb, row0, nvalid);
             const uint32_t d = tl % ND;
+            int wrow;  // this thread's weight row within the group
+            if (EPI == (int)Epi::GateUp) wrow = (row >> 6) * args.up_offset + cb * 64 + (row & 63);
+            else wrow = cb * kTileM + row;
+            const float sw = __ldg(args.w_scale + (size_t)g * args.w_rows_per_group + wrow);
+            // stage the tile's activation scales and exact-path flags in shared
+            // memory while the MMAs run (buffer tl & 1: the previous user of it,
+            // tile tl - 2, finished before the last epilogue barrier)
+            float* sa = row_scale_s + (tl & 1u) * BN;
+            int* fl = row_flag_s + (tl & 1u) * BN;
+            for (int j = ew * 32 + lane; j < BN; j += 128) {
+                const bool in = j < nvalid;
+                sa[j] = in ? __ldg(args.act_scale + row0 + j) : 0.f;
+                fl[j] = in ? __ldg(args.flags + row0 + j) : 1;
+            }
+            if (!epi_sync(epi_bar, eit, ctl)) break;
             if (!warp_wait(&acc_full[d], (tl / ND) & 1u, ctl)) break;
             tc_fence_after();
             const uint32_t col0 = (uint32_t)C::kDCol0 + d * BN;
             const int nch = (nvalid + 31) / 32;
-            int wrow;  // this thread's weight row within the group
-            if (EPI == (int)Epi::GateUp) wrow = (row >> 6) * args.up_offset + cb * 64 + (row & 63);
-            else wrow = cb * kTileM + row;
-            const float sw = args.w_scale[(size_t)g * args.w_rows_per_group + wrow];
             for (int ch = 0; ch < nch; ++ch) {
                 uint32_t r[32];
                 tmem_ld_32(tmem + lane_addr + col0 + ch * 32, r);
@@ -459,7 +499,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 if (args.acc_out) {
 #pragma unroll
                     for (int j = 0; j < 32; ++j)
-                        if (j0 + j < nvalid && args.flags[row0 + j0 + j] == 0)
+                        if (fl[j0 + j] == 0)
                             args.acc_out[(size_t)(row0 + j0 + j) * args.w_rows_per_group + wrow] =
                                 __float2int_rn(__uint_as_float(r[j]));
                 }
@@ -467,8 +507,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     float* xrow = xch + row * C::kXchStride;
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
-                        const int jj = min(j0 + j, nvalid - 1);
-                        xrow[j] = dequant(__uint_as_float(r[j]), __ldg(args.act_scale + row0 + jj), sw);
+                        xrow[j] = dequant(__uint_as_float(r[j]), sa[j0 + j], sw);
                     }
                     if (!epi_sync(epi_bar, eit, ctl)) { ok = false; break; }
                     // warp ew: tokens j0 + 8*ew .. +7; lanes: channels lane, lane + 32
@@ -477,7 +516,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int t = 0; t < 8; ++t) {
                         const int j = ew * 8 + t;
                         const int rr = row0 + j0 + j;
-                        if (j0 + j < nvalid && args.flags[rr] == 0) {
+                        if (fl[j0 + j] == 0) {
 #pragma unroll
                             for (int c2 = 0; c2 < 2; ++c2) {
                                 const int c = lane + 32 * c2;
@@ -492,8 +531,8 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
                     for (int j = 0; j < 32; ++j) {
                         const int rr = row0 + j0 + j;
-                        if (j0 + j < nvalid && args.flags[rr] == 0) {
-                            const float v = dequant(__uint_as_float(r[j]), __ldg(args.act_scale + rr), sw);
+                        if (fl[j0 + j] == 0) {
+                            const float v = dequant(__uint_as_float(r[j]), sa[j0 + j], sw);
                             if (EPI == (int)Epi::ScaleF32)
                                 static_cast<float*>(args.out)[(size_t)rr * args.ld_out + wrow] = v;
                             else
@@ -528,20 +567,21 @@ cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
     });
     if (attr_err != cudaSuccess) return attr_err;
 
-    CUtensorMap tw, tb;
+    CUtensorMap tw, tb[4];
     const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
     if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK, 64,
-                     C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
+                            C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    if (!make_tensor_map_2d(&tb, CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K, (uint64_t)args.total_rows, 64,
-                     C::BN, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
+    for (int i = 0; i < 4; ++i)
+        if (!make_tensor_map_2d(&tb[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K,
+                                (uint64_t)args.total_rows, 64, box_rows<C::BN>(i), CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
 
     const long max_tiles = ((long)(args.total_rows + C::BN - 1) / C::BN + args.n_groups) * args.n_cb;
     int grid = num_sms();
     if (max_tiles < grid) grid = (int)max_tiles;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, C::kSmem, st>>>(tw, tb, args);
+    kern<<<grid, kThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], args);
     return cudaGetLastError();
 }
 
@@ -588,10 +628,9 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes
 }
 
 GemmShape choose_gemm_shape(long rows, long groups, long K) {
+    (void)K;
     const long per_group = rows / (groups > 0 ? groups : 1);
-    // the 256-row tile has one accumulator, so its epilogue is not hidden
-    // behind the next tile's MMAs: worth it only for long reductions
-    if (per_group >= 192 && K >= 3072) return GemmShape::Wide;
+    if (per_group >= 160) return GemmShape::Wide;
     if (per_group >= 48) return GemmShape::Mid;
     return GemmShape::Narrow;
 }

@@ -84,13 +84,39 @@ struct Cfg {
     static constexpr int kSmem = kOffMisc + 64 + 1024;  // + alignment slack
     static_assert(kStageB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(kTmemCols <= 512, "TMEM budget");
-    static_assert(BK == 64 || BK == 128, "K per stage");
+    static_assert(BK == 64 || BK == 128 || BK == 256, "K per stage");
+    // the int8 weight stage: one 64-byte-swizzled [128 x 64] tile for BK = 64,
+    // else BK/128 sub-tiles of [128 x 128] with the 128-byte swizzle
+    static constexpr int kSubA = BK == 64 ? kStageA : kTileM * 128;
+    static constexpr int kNumSubA = BK == 64 ? 1 : BK / 128;
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-using CfgWide = Cfg<192, 64, 4, 2>;    // hundreds of rows per group (compute-bound)
-using CfgMid = Cfg<128, 128, 4, 2>;    // about a hundred rows per group
-using CfgNarrow = Cfg<32, 128, 6, 2>;  // a few rows per group (decode)
+// Each stage costs the MMA thread one wait and one commit, about 255 cycles
+// that overlap the MMAs only by their ~45-cycle issue floor, so a stage
+// takes max(MMA work, 45 * MMAs + 255) cycles: deep stages (many MMAs per
+// wait) keep small tiles from paying the fixed cost many times.
+#ifndef MOE_W_BN  // tile shapes: rows per tile, K per stage, stages, accumulators
+#define MOE_W_BN 160
+#define MOE_W_BK 128
+#define MOE_W_NS 3
+#define MOE_W_ND 2
+#endif
+#ifndef MOE_M_BN
+#define MOE_M_BN 128
+#define MOE_M_BK 128
+#define MOE_M_NS 4
+#define MOE_M_ND 2
+#endif
+#ifndef MOE_N_BN
+#define MOE_N_BN 32
+#define MOE_N_BK 256
+#define MOE_N_NS 3
+#define MOE_N_ND 2
+#endif
+using CfgWide = Cfg<MOE_W_BN, MOE_W_BK, MOE_W_NS, MOE_W_ND>;    // hundreds of rows per group
+using CfgMid = Cfg<MOE_M_BN, MOE_M_BK, MOE_M_NS, MOE_M_ND>;     // about a hundred rows per group
+using CfgNarrow = Cfg<MOE_N_BN, MOE_N_BK, MOE_N_NS, MOE_N_ND>;  // a few rows per group (decode)
 
 // Tile table of a launch: group g owns tiles [tile_start[g], tile_start[g+1]);
 // inside a group, tile = cb * ntb + tb (token blocks fastest, so CTAs running
@@ -288,7 +314,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int n_groups = args.n_groups;
-    const int nkb = args.K / BK;
+    const int nkb = (args.K + BK - 1) / BK;  // a partial last stage reads zeros past K (TMA fill)
 
     if (threadIdx.x == 0) {
         for (int s = 0; s < NS; ++s) {
@@ -369,8 +395,12 @@ __global__ void __launch_bounds__(kThreads, 1)
                     if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
                     uint8_t* st = smem + s * C::kStage;
                     mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d(st, &tmap_w, &full[s], kb * BK, wrow0);
-                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kb * BK, wrow1);
+#pragma unroll
+                    for (int sa = 0; sa < C::kNumSubA; ++sa) {  // rows 0-63 and 64-127 of each sub-tile
+                        const int kx = kb * BK + sa * (BK == 64 ? 64 : 128);
+                        tma_load_2d(st + sa * C::kSubA, &tmap_w, &full[s], kx, wrow0);
+                        tma_load_2d(st + sa * C::kSubA + C::kSubA / 2, &tmap_w, &full[s], kx, wrow1);
+                    }
 #pragma unroll
                     for (int hh = 0; hh < BK / 64; ++hh)
                         tma_load_2d(st + C::kStageA + hh * BN * 128, mb, &full[s], kb * BK + hh * 64, row0);
@@ -429,7 +459,7 @@ __global__ void __launch_bounds__(kThreads, 1)
                 // this fill was issued after the MMAs that last read TMEM stage
                 // s completed, so full[s] also frees the TMEM stage
                 if (!warp_wait(&full[s], ph, ctl)) { ok = false; break; }
-                const uint8_t* src = smem + s * C::kStage + row * BK;
+                const uint8_t* src = smem + s * C::kStage + row * (BK == 64 ? 64 : 128);
                 const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + s * C::kACols;
                 if (BK == 64) {  // 64-byte swizzle: chunk c sits at c ^ ((row >> 1) & 3)
                     const uint32_t swz = (uint32_t)((row >> 1) & 3);
@@ -438,14 +468,16 @@ __global__ void __launch_bounds__(kThreads, 1)
                     for (int c = 0; c < 4; ++c)
                         cvt_chunk(*reinterpret_cast<const uint4*>(src + ((c ^ swz) << 4)), v + c * 8);
                     tmem_st_32(taddr, v);
-                } else {  // 128-byte swizzle: chunk c sits at c ^ (row & 7)
+                } else {  // 128-byte swizzle: chunk c of a sub-tile row sits at c ^ (row & 7)
                     const uint32_t swz = (uint32_t)(row & 7);
 #pragma unroll
-                    for (int hh = 0; hh < 2; ++hh) {
+                    for (int hh = 0; hh < BK / 64; ++hh) {  // 64 K per tcgen05.st
+                        const uint8_t* sub = src + (hh >> 1) * C::kSubA;
                         uint32_t v[32];
 #pragma unroll
                         for (int c = 0; c < 4; ++c)
-                            cvt_chunk(*reinterpret_cast<const uint4*>(src + (((hh * 4 + c) ^ swz) << 4)), v + c * 8);
+                            cvt_chunk(*reinterpret_cast<const uint4*>(sub + ((((hh & 1) * 4 + c) ^ swz) << 4)),
+                                      v + c * 8);
                         tmem_st_32(taddr + hh * 32, v);
                     }
                 }
@@ -569,7 +601,7 @@ cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
 
     CUtensorMap tw, tb[4];
     const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
-    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK, 64,
+    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, C::BK == 64 ? 64 : 128, 64,
                             C::BK == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     for (int i = 0; i < 4; ++i)

@@ -184,6 +184,37 @@ MOE_W8A8_API moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, 
                              size_t workspace_bytes, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * moe_w8a8_linear_static -- moe_w8a8_linear for callers that cannot
+ * allocate device memory.  The method's pages have no counterpart to it.
+ *
+ * Some callers cannot allocate when they run the layer: a plugin whose host
+ * framework gives it no allocator, or a serving loop that reserved all
+ * device memory for its own pool at start-up (a fresh cudaMalloc would fail,
+ * fragment the pool, or synchronise the device).  This entry point needs no
+ * workspace and allocates nothing, neither itself nor through a library
+ * routine: its scratch is a static device array of 8 MiB inside the library,
+ * which every GPU that loads the library holds until the process exits.
+ *
+ *   x, w_q, w_scale, y, M, N, K, stream: as for moe_w8a8_linear; the caller
+ *   still provides the inputs and the output.
+ * Limit: the scratch of a call, moe_w8a8_linear_workspace_size(M, N, K)
+ *   bytes (about 2*M*K + 12*M + 1 KiB; e.g. up to 1022 tokens at K = 4096), must
+ *   fit the 8 MiB; a larger shape is rejected with MOE_ERR_UNSUPPORTED_SHAPE
+ *   before anything is launched.
+ * Set-up: the first call on each device looks up that device's address of
+ *   the array (with the device current) and caches it; make that first call
+ *   before any stream capture.
+ * Sharing: every call on a device uses the same array, which keeps the last
+ *   call's contents (the call clears what must start at zero).  Calls that
+ *   overlap on the GPU -- on different streams, or from several host threads
+ *   -- race on the array and give undefined results; serialise them.
+ * Errors: as moe_w8a8_linear; a device-side timeout marks the output as
+ *   undefined but cannot be read back through moe_w8a8_device_error.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* w_q, const float* w_scale,
+                                                 int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream);
+
+/* ---------------------------------------------------------------------------
  * moe_w8a8_device_error -- synchronise `stream`, then read and clear the
  * sticky device error word in the first bytes of `workspace`.  Returns
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a pipeline wait inside a kernel gave up;

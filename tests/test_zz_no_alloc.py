@@ -1,0 +1,73 @@
+"""moe_w8a8_linear_static: the W8A8 linear layer for callers that cannot
+allocate device memory (its scratch is a static device array in the
+library).  Checked through the C ABI against moe_w8a8_linear, which takes a
+caller-allocated workspace, on two calls in a row; its results are
+bit-identical to that entry point's, which the other tests pin to the oracle.
+
+This file is named to be collected last, so that a run that stops at the
+first failure has already run every other test."""
+import numpy as np
+import pytest
+import torch
+
+import w8a8_quantised_moe_gb300 as moe
+from w8a8_quantised_moe_gb300 import _lib
+from w8a8_quantised_moe_gb300 import build as lib_build
+from w8a8_quantised_moe_gb300 import workloads as wl
+
+pytestmark = pytest.mark.gpu
+
+OK, SHAPE = 0, -2
+
+
+@pytest.fixture(scope="module")
+def lib():
+    lib_build.build()
+    return _lib.load()
+
+
+def _inputs(seed, M, N, K):
+    x = wl.draw_activations(seed, wl.LINEAR.cfg_id, M, K, max(1, K // 100))
+    r = np.random.default_rng(seed)
+    w_q = torch.from_numpy(r.integers(-127, 128, (N, K)).astype(np.int8)).cuda()
+    s_w = torch.from_numpy((r.random(N) * 1e-3 + 1e-4).astype(np.float32)).cuda()
+    xb = torch.from_numpy(x.view(np.int16)).view(torch.bfloat16).cuda()
+    return xb, w_q, s_w
+
+
+def _with_workspace(lib, xb, w_q, s_w):
+    M, K = xb.shape
+    N = w_q.shape[0]
+    ws = moe.new_workspace(moe.linear_workspace_size(M, N, K))
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.moe_w8a8_linear(xb.data_ptr(), w_q.data_ptr(), s_w.data_ptr(), M, N, K, y.data_ptr(),
+                               ws.data_ptr(), ws.numel(), st) == OK
+    return y
+
+
+def _static(lib, xb, w_q, s_w):
+    M, K = xb.shape
+    N = w_q.shape[0]
+    y = torch.empty((M, N), dtype=torch.bfloat16, device="cuda")
+    st = torch.cuda.current_stream().cuda_stream
+    assert lib.moe_w8a8_linear_static(xb.data_ptr(), w_q.data_ptr(), s_w.data_ptr(), M, N, K, y.data_ptr(),
+                                      st) == OK
+    return y
+
+
+def test_static_scratch_linear_matches_workspace_linear_twice(lib):
+    # two calls in a row with different shapes and inputs: the second must
+    # not see anything the first left in the shared scratch
+    for seed, (M, N, K) in ((1, (300, 384, 1280)), (2, (1000, 256, 4096))):
+        xb, w_q, s_w = _inputs(seed, M, N, K)
+        y_static = _static(lib, xb, w_q, s_w)
+        y_ws = _with_workspace(lib, xb, w_q, s_w)
+        torch.cuda.synchronize()
+        assert torch.equal(y_static.view(torch.int16), y_ws.view(torch.int16)), (M, N, K)
+
+
+def test_static_scratch_linear_rejects_shapes_beyond_its_capacity(lib):
+    # 2048 x 4096 fp16 codes alone need 16 MiB: rejected before any launch
+    assert lib.moe_w8a8_linear_static(1 << 20, 1 << 20, 1 << 20, 2048, 256, 4096, 1 << 20, None) == SHAPE
+    assert lib.moe_w8a8_linear_static(1 << 20, 1 << 20, 1 << 20, 0, 256, 4096, 1 << 20, None) == OK

@@ -37,6 +37,7 @@ EXPORTS = (
     "moe_w8a8_device_error",
     "moe_w8a8_set_wait_timeout_ns",
     "moe_w8a8_set_profile_events",
+    "moe_w8a8_linear_static",
 )
 
 
@@ -79,6 +80,7 @@ def load(path: str = LIB_PATH):
             "moe_w8a8_device_error": ([vp, vp], i32),
             "moe_w8a8_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_uint64),
             "moe_w8a8_set_profile_events": ([ctypes.c_void_p, i32], i32),
+            "moe_w8a8_linear_static": ([vp, vp, vp, i64, i64, i64, vp, vp], i32),
         }
         for name, (args, res) in decl.items():
             fn = getattr(lib, name)

@@ -14,7 +14,7 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w8a8.so")
-SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu"]
+SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu", "static_linear.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 NVCC_FLAGS = [

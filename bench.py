@@ -251,8 +251,8 @@ def oracle_sample_rate(cfg, inputs, oweights, target_s, max_tokens=None):
 
     n = min(lim, 8)
     dt = run(n)
-    while dt < 0.2 * target_s and n < lim:
-        n = min(lim, max(n * 2, int(n * 0.5 * target_s / max(dt, 1e-3))))
+    while dt < 0.5 * target_s and n < lim:
+        n = min(lim, max(n * 2, int(n * target_s / max(dt, 1e-3))))
         dt = run(n)
     return n / dt, n, dt
 

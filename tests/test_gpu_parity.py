@@ -40,6 +40,12 @@ CASES = {
     "long_k": TINY.replace(T=100, H=1280, I=1152, E=4, k=2, n_outlier=13),
     "single_expert": TINY.replace(T=45, H=256, I=256, E=1, k=1),
     "one_token": TINY.replace(T=1, H=256, I=512, E=8, k=2),
+    # about 500 rows per expert: CTA-pair tiles (192 rows), several per expert, ragged tails
+    "pair_tiles": TINY.replace(T=1000, H=512, I=256, E=4, k=2),
+    # CTA pairs with reductions longer than the stage ring in both GEMMs
+    "pair_long_k": TINY.replace(T=800, H=1280, I=640, E=4, k=2, n_outlier=13),
+    # CTA pairs under Zipf-skewed routing: experts from a few rows to several tiles
+    "pair_skewed": TINY.replace(T=1200, H=256, I=256, E=8, k=2, bias="zipf", zipf_s=1.2),
 }
 
 
@@ -179,7 +185,8 @@ def test_linear_golden_example():
     assert (yf[:, 2:] == 0).all()
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 256, 384), (300, 384, 1280), (130, 128, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 256, 384), (300, 384, 1280), (130, 128, 4096),
+                                   (500, 512, 1024)])
 def test_linear_bit_exact(M, N, K):
     cfg = wl.LINEAR
     x = wl.draw_activations(7, cfg.cfg_id, M, K, max(1, K // 100))
@@ -276,3 +283,27 @@ def test_second_gemm_exact_path():
     _, dev = moe.forward_debug(*layer.device_args(), fields=("q_h",))
     q_h = dev["q_h"].cpu().numpy()
     assert (np.abs(q_h.astype(np.int64)).sum(axis=1) > 2 ** 17).all()
+
+
+def test_exact_path_mixed_rows_on_cta_pairs():
+    """400 rows through one expert (CTA-pair tiles): four rows of +-1 (every
+    code +-127, L1 far above the bound) take the exact CUDA-core path, the
+    rest the tensor cores; both GEMMs' accumulators must be exact."""
+    T, H, I = 400, 2048, 256
+    r = np.random.default_rng(11)
+    x = (r.standard_normal((T, H)) * 0.5).astype(np.float32)
+    x[:4] = np.where(r.random((4, H)) < 0.5, -1.0, 1.0)
+    w13 = r.integers(-128, 128, (1, 2 * I, H)).astype(np.int8)
+    w2 = r.integers(-128, 128, (1, H, I)).astype(np.int8)
+    args = (torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.zeros((H, 1), device="cuda"), None,
+            torch.from_numpy(w13).cuda(), torch.full((1, 2 * I), 1e-6, device="cuda"),
+            torch.from_numpy(w2).cuda(), torch.full((1, H), 1e-3, device="cuda"), 1)
+    _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
+    q_x = dev["q_x"].cpu().numpy()
+    l1 = np.abs(q_x.astype(np.int64)).sum(axis=1)
+    assert (l1[:4] > 2 ** 17).all() and (l1[4:] <= 2 ** 17).all()
+    ref1 = q_x.astype(np.int64) @ w13[0].astype(np.int64).T
+    np.testing.assert_array_equal(dev["acc1"].cpu().numpy(), ref1)
+    q_h = dev["q_h"].cpu().numpy()
+    ref2 = q_h.astype(np.int64) @ w2[0].astype(np.int64).T
+    np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)

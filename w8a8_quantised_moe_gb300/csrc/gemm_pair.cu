@@ -1,0 +1,468 @@
+// gemm_pair.cu -- the exact INT8 grouped GEMM on CTA pairs (tcgen05
+// cta_group::2): the same product and epilogues as gemm.cu ("W8A8
+// quantisation of MiniMax-M3 on K100AI" (mhpn.cn), section 2.1; exactness
+// certificate and exact CUDA-core path as described there), for groups with
+// enough rows to fill wide tiles.
+//
+// A cluster of two CTAs on neighbouring SMs computes one 256 x N tile:
+//   A  256 weight rows = channel blocks 2p (even CTA) and 2p + 1 (odd CTA);
+//      each CTA converts its 128 int8 rows to fp16 in its own tensor memory.
+//   B  N activation rows of one group (N = valid rows rounded up to 16);
+//      rows [0, N/2) sit in the even CTA's shared memory, [N/2, N) in the odd
+//      CTA's, each loaded by that CTA's TMA producer.
+//   D  each CTA's tensor memory holds its 128 weight rows x N accumulators.
+// The even CTA's MMA thread issues M = 256 MMAs that read both CTAs' operands.
+// Against one CTA per tile this halves what each SM loads and keeps in
+// shared memory per MMA column (one half of B instead of all of it), and
+// every MMA instruction does twice the work for the same issue cost, which
+// matters because the issuing thread shares its SM sub-partition with a
+// converter and an epilogue warp.
+//
+// Synchronisation (every wait bounded; see ptx.cuh):
+//   full[s]       per CTA: its TMA bytes of stage s landed
+//   a_ready[j]    even CTA, 8 arrivals (4 converter warps x 2 CTAs): tensor-
+//                 memory A slot j holds the stage's weights in both CTAs.  A
+//                 converter waited on its own full[s] first, so this also
+//                 covers both halves of B.
+//   empty[s]      per CTA, committed by the even CTA's MMAs to both CTAs:
+//                 stage s's shared memory and A slot (it % NA) are free again
+//   acc_full[d]   per CTA, committed to both: accumulator d complete
+//   acc_empty[d]  even CTA, 8 arrivals (4 epilogue warps x 2 CTAs)
+// Shared memory of the odd CTA is read by the even CTA's MMAs, and both CTAs
+// arrive on each other's barriers, so neither leaves before a final cluster
+// barrier that every thread of both CTAs reaches on every path.
+#include <mutex>
+
+#include "gemm_common.cuh"
+
+namespace moe {
+namespace {
+
+constexpr int kPairBK = 128;  // K per stage
+constexpr int kPairND = 2;    // accumulator buffers
+
+template <int BN_, int NS_, int NA_>
+struct PairCfg {
+    static constexpr int BN = BN_;        // activation rows per pair tile (MMA N, at most)
+    static constexpr int NS = NS_;        // shared-memory stages
+    static constexpr int NA = NA_;        // tensor-memory A slots (at most NS)
+    static constexpr int kHalf = BN / 2;  // activation rows per CTA
+    static constexpr int kStageA = kTileM * kPairBK;    // int8 weights, [128 x 128] 128-byte swizzle
+    static constexpr int kSubB = kHalf * 128;           // one 64-wide K half of the fp16 rows
+    static constexpr int kStageB = 2 * kSubB;
+    static constexpr int kStage = kStageA + kStageB;
+    static constexpr int kACols = kPairBK / 2;          // TMEM columns of one A slot
+    static constexpr int kDCol0 = NA * kACols;          // first accumulator column
+    static constexpr int kTmemCols = kDCol0 + kPairND * BN;
+    static constexpr int kXchStride = 33;
+    static constexpr int kXch = kTileM * kXchStride * 4;
+    static constexpr int kOffXch = NS * kStage;
+    static constexpr int kOffBars = kOffXch + kXch;
+    static constexpr int kNumBars = 2 * NS + NA + 2 * kPairND + 2;
+    static constexpr int kOffTiles = kOffBars + kNumBars * 8;
+    static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;
+    static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
+    static constexpr int kSmem = kOffMisc + 64 + 1024;
+    static_assert(kSubB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
+    static_assert(kTmemCols <= 512, "TMEM budget");
+    // a converter learns that A slot (it % NA) is free from empty[] of stage
+    // it - NA, whose barrier cannot have moved on to a later phase when NS >= NA
+    static_assert(NS >= NA, "stage ring and A slots");
+    static_assert(kSmem <= 232448, "shared memory budget");
+};
+
+// Tensor memory holds the A slots and two accumulators.  Measured on the
+// prefill and linear workloads: 192-wide tiles with two A slots and four
+// stages beat 160-wide tiles with three A slots (wider MMAs amortise the
+// issuing thread's per-stage cost) and a fifth stage gains nothing.
+#ifndef MOE_P_BN  // pair tile width, shared-memory stages, A slots
+#define MOE_P_BN 192
+#define MOE_P_NS 4
+#define MOE_P_NA 2
+#endif
+using CfgPair = PairCfg<MOE_P_BN, MOE_P_NS, MOE_P_NA>;
+
+// Box heights of the per-CTA activation tensor maps: a CTA of a tile with
+// half-width h loads the smallest box that covers h rows.
+template <int HALF>
+__host__ __device__ constexpr int pair_box_rows(int i) {
+    return i == 0 ? (HALF < 16 ? HALF : 16) : i == 1 ? (HALF < 32 ? HALF : 32) : i == 2 ? (HALF < 64 ? HALF : 64)
+                                                                                       : HALF;
+}
+__device__ __forceinline__ int pair_box_index(int h) { return h <= 16 ? 0 : h <= 32 ? 1 : h <= 64 ? 2 : 3; }
+
+// Pair tile -> group, channel-block pair, first row, valid rows.  Inside a
+// group, tile = cp * ntb + tb (token blocks fastest).
+template <int BN>
+__device__ __forceinline__ void decode_pair_tile(const Tiles& t, int tile, int& g, int& cp, int& row0,
+                                                 int& nvalid) {
+    g = last_le(t.tile_start, t.n_groups, tile);
+    const int local = tile - t.tile_start[g];
+    const int rows = t.row_start[g + 1] - t.row_start[g];
+    const int ntb = (rows + BN - 1) / BN;
+    cp = local / ntb;
+    const int tb = local - cp * ntb;
+    row0 = t.row_start[g] + tb * BN;
+    nvalid = min(BN, t.row_start[g + 1] - row0);
+}
+
+template <class C, int EPI>
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+    grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b0,
+                             const __grid_constant__ CUtensorMap tmap_b1, const __grid_constant__ CUtensorMap tmap_b2,
+                             const __grid_constant__ CUtensorMap tmap_b3, const GemmArgs args) {
+    constexpr int BN = C::BN, NS = C::NS;
+    extern __shared__ uint8_t smem_raw[];
+    uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+    uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
+    uint64_t* full = bars;                     // [NS]
+    uint64_t* empty = bars + NS;               // [NS]
+    uint64_t* a_ready = bars + 2 * NS;         // [NA], used in the even CTA
+    uint64_t* acc_full = a_ready + C::NA;    // [ND]
+    uint64_t* acc_empty = acc_full + kPairND;  // [ND], used in the even CTA
+    uint64_t* teardown = acc_empty + kPairND;
+    uint64_t* epi_bar = teardown + 1;
+    int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
+    int* row_start = tile_start + (kMaxExperts + 1);
+    uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
+    volatile int* abort_flag = reinterpret_cast<volatile int*>(smem + C::kOffMisc + 8);
+    float* xch = reinterpret_cast<float*>(smem + C::kOffXch);
+    float* row_scale_s = reinterpret_cast<float*>(smem + C::kOffRowInfo);          // [2][BN]
+    int* row_flag_s = reinterpret_cast<int*>(smem + C::kOffRowInfo + 2 * BN * 4);  // [2][BN]
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t rank = cluster_ctarank();  // 0: issues the MMAs
+    const int cluster = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+    const int n_groups = args.n_groups;
+    const int n_cp = args.n_cb >> 1;
+    const int nkb = (args.K + kPairBK - 1) / kPairBK;
+
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < NS; ++s) {
+            mbar_init(&full[s], 1);
+            mbar_init(&empty[s], 1);
+        }
+        for (int j = 0; j < C::NA; ++j) mbar_init(&a_ready[j], 8);
+        for (int d = 0; d < kPairND; ++d) {
+            mbar_init(&acc_full[d], 1);
+            mbar_init(&acc_empty[d], 8);
+        }
+        mbar_init(teardown, 1);
+        mbar_init(epi_bar, 4);
+        *abort_flag = 0;
+        fence_barrier_init();
+        tma_prefetch_desc(&tmap_w);
+        tma_prefetch_desc(&tmap_b0);
+        tma_prefetch_desc(&tmap_b1);
+        tma_prefetch_desc(&tmap_b2);
+        tma_prefetch_desc(&tmap_b3);
+    }
+    if (warp == 1) {
+        tmem_alloc_pair(tmem_slot, 512);
+        tmem_relinquish_pair();
+    }
+    if (warp == 2) {  // tile table: pair tiles of group g = ceil(rows_g / BN) * n_cp
+        int carry = 0;
+        for (int base = 0; base < n_groups; base += 32) {
+            const int g = base + lane;
+            int r0 = 0, r1 = 0;
+            if (g < n_groups) {
+                r0 = args.offsets ? args.offsets[g] : 0;
+                r1 = args.offsets ? args.offsets[g + 1] : args.total_rows;
+                row_start[g] = r0;
+                if (g == n_groups - 1) row_start[n_groups] = r1;
+            }
+            const int v = (g < n_groups) ? ((r1 - r0 + BN - 1) / BN) * n_cp : 0;
+            int incl = v;
+#pragma unroll
+            for (int off = 1; off < 32; off <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, incl, off);
+                if (lane >= off) incl += o;
+            }
+            if (g < n_groups) tile_start[g] = carry + incl - v;
+            carry += __shfl_sync(0xffffffffu, incl, 31);
+        }
+        if (lane == 0) tile_start[n_groups] = carry;
+    }
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // both CTAs' barriers are initialised before anyone arrives remotely
+    tc_fence_after();
+    const uint32_t tmem = *tmem_slot;
+    const int total_tiles = tile_start[n_groups];
+    const Tiles tiles{tile_start, row_start, n_groups};
+    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
+
+    if (warp == 0) {
+        // ---------------------------------------------------------- producer
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+                int g, cp, row0, nvalid;
+                decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
+                const int cb = 2 * cp + (int)rank;
+                int wrow0, wrow1;
+                if (EPI == (int)Epi::GateUp) {
+                    wrow0 = g * args.w_rows_per_group + cb * 64;
+                    wrow1 = wrow0 + args.up_offset;
+                } else {
+                    wrow0 = g * args.w_rows_per_group + cb * kTileM;
+                    wrow1 = wrow0 + 64;
+                }
+                const int half = ((nvalid + 15) & ~15) >> 1;  // activation rows per CTA
+                const int bi = pair_box_index(half);
+                const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
+                const int brow = row0 + (int)rank * half;
+                const uint32_t stage_bytes = (uint32_t)(C::kStageA + 2 * pair_box_rows<C::kHalf>(bi) * 128);
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % NS, ph = (it / NS) & 1u;
+                    if (!mbar_wait_cluster(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                    uint8_t* st = smem + s * C::kStage;
+                    mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    const int kx = kb * kPairBK;
+                    tma_load_2d(st, &tmap_w, &full[s], kx, wrow0);
+                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kx, wrow1);
+                    tma_load_2d(st + C::kStageA, mb, &full[s], kx, brow);
+                    tma_load_2d(st + C::kStageA + C::kSubB, mb, &full[s], kx + 64, brow);
+                }
+            }
+            // drain: every fill issued must land before the CTA may exit
+            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                mbar_wait_drain(&full[s], (last / NS) & 1u);
+            }
+        }
+    } else if (warp == 1) {
+        // ------------------------------------------- MMA issuer (even CTA)
+        if (lane == 0 && rank == 0) {
+            uint32_t it = 0, tl = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters, ++tl) {
+                int g, cp, row0, nvalid;
+                decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
+                const uint32_t n_mma = (uint32_t)((nvalid + 15) & ~15);
+                const uint32_t idesc = idesc_f16_f32(2 * kTileM, n_mma);
+                const uint32_t d = tl % kPairND;
+                if (!mbar_wait_cluster(&acc_empty[d], ((tl / kPairND) & 1u) ^ 1u, ctl)) break;
+                tc_fence_after();
+                const uint32_t d_col = (uint32_t)C::kDCol0 + d * BN;
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % NS, j = it % C::NA;
+                    if (!mbar_wait_cluster(&a_ready[j], (it / C::NA) & 1u, ctl)) { ok = false; break; }
+                    tc_fence_after();
+                    const uint32_t b_base = smem_u32(smem + s * C::kStage + C::kStageA);
+#pragma unroll
+                    for (int ks = 0; ks < kPairBK / 16; ++ks) {
+                        const uint64_t bdesc =
+                            smem_desc_sw128(b_base + (ks / 4) * C::kSubB) + (uint64_t)((ks % 4) * 2);
+                        mma_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols + ks * 8, bdesc, idesc,
+                                            (kb != 0 || ks != 0) ? 1u : 0u);
+                    }
+                    mma_commit_pair(&empty[s], 3);
+                }
+                if (!ok) break;
+                mma_commit_pair(&acc_full[d], 3);
+            }
+            mma_commit_pair(teardown, 1);
+            mbar_wait_drain(teardown, 0);
+        }
+    } else if (warp < kEpiWarp0) {
+        // ------------------------------------------------------- converters
+        const int q = warp & 3;
+        const int row = q * 32 + lane;
+        const uint32_t a_ready_leader = cluster_addr(&a_ready[0], 0);
+        uint32_t it = 0;
+        bool ok = true;
+        for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+            for (int kb = 0; kb < nkb; ++kb, ++it) {
+                const uint32_t s = it % NS, ph = (it / NS) & 1u, j = it % C::NA;
+                // the even CTA's MMAs read this CTA's half of B once the
+                // arrival below is observed: it follows this wait
+                if (!warp_wait(&full[s], ph, ctl)) { ok = false; break; }
+                if (it >= (uint32_t)C::NA) {  // A slot j is free once the MMAs of stage it - NA completed
+                    const uint32_t p = it - C::NA;
+                    if (!warp_wait_cluster(&empty[p % NS], (p / NS) & 1u, ctl)) { ok = false; break; }
+                }
+                const uint8_t* src = smem + s * C::kStage + row * 128;
+                const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + j * C::kACols;
+                const uint32_t swz = (uint32_t)(row & 7);  // 128-byte swizzle: chunk c at c ^ (row & 7)
+#pragma unroll
+                for (int hh = 0; hh < 2; ++hh) {  // 64 K per tcgen05.st
+                    uint32_t v[32];
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+                        cvt_chunk(*reinterpret_cast<const uint4*>(src + (((hh * 4 + c) ^ swz) << 4)), v + c * 8);
+                    tmem_st_32(taddr + hh * 32, v);
+                }
+                tmem_wait_st();
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive_cluster(a_ready_leader + j * 8);
+            }
+        }
+    } else {
+        // --------------------------------------------------------- epilogue
+        const int q = warp & 3;
+        const int ew = warp - kEpiWarp0;  // 0..3
+        const int row = q * 32 + lane;    // TMEM lane = weight row of this CTA's channel block
+        const uint32_t lane_addr = (uint32_t)(q * 32) << 16;
+        const uint32_t acc_empty_leader = cluster_addr(&acc_empty[0], 0);
+        uint32_t tl = 0, eit = 0;
+        bool ok = true;
+        for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters, ++tl) {
+            int g, cp, row0, nvalid;
+            decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
+            const int cb = 2 * cp + (int)rank;
+            const uint32_t d = tl % kPairND;
+            int wrow;  // this thread's weight row within the group
+            if (EPI == (int)Epi::GateUp) wrow = (row >> 6) * args.up_offset + cb * 64 + (row & 63);
+            else wrow = cb * kTileM + row;
+            const float sw = __ldg(args.w_scale + (size_t)g * args.w_rows_per_group + wrow);
+            float* sa = row_scale_s + (tl & 1u) * BN;
+            int* fl = row_flag_s + (tl & 1u) * BN;
+            for (int jj = ew * 32 + lane; jj < BN; jj += 128) {
+                const bool in = jj < nvalid;
+                sa[jj] = in ? __ldg(args.act_scale + row0 + jj) : 0.f;
+                fl[jj] = in ? __ldg(args.flags + row0 + jj) : 1;
+            }
+            if (!epi_sync(epi_bar, eit, ctl)) break;
+            if (!warp_wait_cluster(&acc_full[d], (tl / kPairND) & 1u, ctl)) break;
+            tc_fence_after();
+            const uint32_t col0 = (uint32_t)C::kDCol0 + d * BN;
+            const int nch = (nvalid + 31) / 32;
+            for (int ch = 0; ch < nch; ++ch) {
+                uint32_t r[32];
+                tmem_ld_32(tmem + lane_addr + col0 + ch * 32, r);
+                tmem_wait_ld();
+                if (ch == nch - 1) {  // every column is in registers: release the accumulator
+                    tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) mbar_arrive_cluster(acc_empty_leader + d * 8);
+                }
+                const int j0 = ch * 32;
+                if (args.acc_out) {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j)
+                        if (fl[j0 + j] == 0)
+                            args.acc_out[(size_t)(row0 + j0 + j) * args.w_rows_per_group + wrow] =
+                                __float2int_rn(__uint_as_float(r[j]));
+                }
+                if (EPI == (int)Epi::GateUp) {
+                    float* xrow = xch + row * C::kXchStride;
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) xrow[j] = dequant(__uint_as_float(r[j]), sa[j0 + j], sw);
+                    if (!epi_sync(epi_bar, eit, ctl)) { ok = false; break; }
+                    // warp ew: tokens j0 + 8*ew .. +7; lanes: channels lane, lane + 32
+                    float* out = static_cast<float*>(args.out);
+#pragma unroll
+                    for (int t = 0; t < 8; ++t) {
+                        const int j = ew * 8 + t;
+                        const int rr = row0 + j0 + j;
+                        if (fl[j0 + j] == 0) {
+#pragma unroll
+                            for (int c2 = 0; c2 < 2; ++c2) {
+                                const int c = lane + 32 * c2;
+                                const float gv = xch[c * C::kXchStride + j];
+                                const float uv = xch[(64 + c) * C::kXchStride + j];
+                                out[(size_t)rr * args.ld_out + cb * 64 + c] = __fmul_rn(silu_f32(gv), uv);
+                            }
+                        }
+                    }
+                    if (!epi_sync(epi_bar, eit, ctl)) { ok = false; break; }
+                } else {
+#pragma unroll
+                    for (int j = 0; j < 32; ++j) {
+                        const int rr = row0 + j0 + j;
+                        if (fl[j0 + j] == 0) {
+                            const float v = dequant(__uint_as_float(r[j]), sa[j0 + j], sw);
+                            if (EPI == (int)Epi::ScaleF32)
+                                static_cast<float*>(args.out)[(size_t)rr * args.ld_out + wrow] = v;
+                            else
+                                static_cast<__nv_bfloat16*>(args.out)[(size_t)rr * args.ld_out + wrow] =
+                                    __float2bfloat16_rn(v);
+                        }
+                    }
+                }
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    cluster_sync_all();  // the pair's MMAs, TMA fills and remote arrivals are all done
+    if (warp == 1) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc_pair(tmem, 512);
+    }
+    if (!*abort_flag) fallback_rows<EPI>(args, row_start, n_groups);
+}
+
+int max_pair_clusters(const void* kern, int smem) {
+    cudaLaunchConfig_t cfg = {};
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.gridDim = dim3(2 * (unsigned)num_sms(), 1, 1);
+    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.dynamicSmemBytes = (size_t)smem;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    int n = 0;
+    if (cudaOccupancyMaxActiveClusters(&n, kern, &cfg) != cudaSuccess || n < 1) {
+        cudaGetLastError();
+        n = num_sms() / 2;
+    }
+    return n;
+}
+
+template <class C, int EPI>
+cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st) {
+    auto kern = grouped_gemm_pair_kernel<C, EPI>;
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    static int clusters = 0;
+    std::call_once(once, [&] {
+        attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
+        if (attr_err == cudaSuccess) clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), C::kSmem);
+    });
+    if (attr_err != cudaSuccess) return attr_err;
+
+    CUtensorMap tw, tb[4];
+    const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
+    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, 128, 64,
+                            CU_TENSOR_MAP_SWIZZLE_128B))
+        return cudaErrorInvalidValue;
+    for (int i = 0; i < 4; ++i)
+        if (!make_tensor_map_2d(&tb[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K,
+                                (uint64_t)args.total_rows, 64, pair_box_rows<C::kHalf>(i),
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+
+    const long max_tiles = ((long)(args.total_rows + C::BN - 1) / C::BN + args.n_groups) * (args.n_cb / 2);
+    long n = clusters;
+    if (max_tiles < n) n = max_tiles;
+    if (n < 1) n = 1;
+    kern<<<(unsigned)(2 * n), kThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], args);
+    return cudaGetLastError();
+}
+
+}  // namespace
+
+bool pair_gemm_supported(const GemmArgs& args) { return args.n_cb >= 2 && (args.n_cb & 1) == 0; }
+
+cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st) {
+    if (args.total_rows == 0) return cudaSuccess;
+    switch (epi) {
+        case Epi::GateUp: return launch_pair_impl<CfgPair, 0>(args, st);
+        case Epi::ScaleF32: return launch_pair_impl<CfgPair, 1>(args, st);
+        case Epi::ScaleBF16: return launch_pair_impl<CfgPair, 2>(args, st);
+    }
+    return cudaErrorInvalidValue;
+}
+
+}  // namespace moe

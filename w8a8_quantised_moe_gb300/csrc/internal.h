@@ -27,11 +27,12 @@ enum class Epi : int {
     ScaleBF16 = 2  // (acc * s_act) * s_w, bf16 out (linear layer)
 };
 
-// Tile shapes of the grouped GEMM (activation rows per tile / K per stage).
+// Tile shapes of the grouped GEMM.
 enum class GemmShape : int {
-    Wide = 0,    // 256 rows per tile: groups of a few hundred rows or more
-    Mid = 1,     // 128 rows per tile
-    Narrow = 2   // 32 rows per tile: a few rows per group (decode)
+    Wide = 0,    // one CTA per tile, 160 activation rows: groups of a few hundred rows
+    Mid = 1,     // one CTA per tile, 128 rows: about a hundred rows per group
+    Narrow = 2,  // one CTA per tile, 32 rows: a few rows per group (decode)
+    Pair = 3     // CTA pairs, 256 weight rows x 192 activation rows per tile
 };
 
 // Largest L1 norm of a quantised activation row for which the fp32
@@ -102,6 +103,9 @@ cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, in
                                   int row_stride_of, int8_t* q8, cudaStream_t st);
 GemmShape choose_gemm_shape(long rows, long groups, long K);
 cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st);
+// CTA-pair kernel (gemm_pair.cu): needs an even number of channel blocks.
+bool pair_gemm_supported(const GemmArgs& args);
+cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st);
 
 int num_sms();
 

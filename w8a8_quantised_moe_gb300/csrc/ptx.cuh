@@ -137,6 +137,47 @@ __device__ __forceinline__ void cluster_sync_all() {
     asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Address, in the cluster's shared-memory window, of the object at the same
+// offset as `p` in the shared memory of CTA `rank` of this cluster.
+__device__ __forceinline__ uint32_t cluster_addr(const void* p, uint32_t rank) {
+    uint32_t r;
+    asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(p)), "r"(rank));
+    return r;
+}
+
+// Arrive once on an mbarrier given by its cluster address (possibly in
+// another CTA of the cluster).  The arrival keeps the default (CTA-scope)
+// semantics: what it publishes to the other CTA is tensor-memory data,
+// ordered by tcgen05.wait::st and tcgen05.fence::before_thread_sync, and
+// TMA-written shared memory, whose completion the arriving thread observed.
+// A cluster-scope release here costs over a thousand cycles per arrival.
+__device__ __forceinline__ void mbar_arrive_cluster(uint32_t bar_cluster_addr) {
+    asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(bar_cluster_addr) : "memory");
+}
+
+// try_wait on a barrier that the other CTA of a pair (or the pair's tensor-
+// core commits) arrives on; same semantics as mbar_try_wait.
+__device__ __forceinline__ bool mbar_try_wait_cluster(uint64_t* bar, uint32_t parity) {
+    return mbar_try_wait(bar, parity);
+}
+
+// Bounded single-thread wait on such a barrier (see mbar_wait).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, const WaitCtl& ctl) {
+    if (mbar_try_wait_cluster(bar, parity)) return true;
+    const uint64_t t0 = global_timer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (mbar_try_wait_cluster(bar, parity)) return true;
+        if ((i & 31u) == 0u) {
+            if (*ctl.abort) return false;
+            if (global_timer_ns() - t0 > ctl.timeout_ns) {
+                *ctl.abort = 1;
+                atomicOr(ctl.error, kErrTimeout);
+                return false;
+            }
+        }
+    }
+}
+
 // ---------------------------------------------------------------- tcgen05
 
 __device__ __forceinline__ void tmem_alloc(uint32_t* dst_smem, uint32_t ncols) {
@@ -190,6 +231,49 @@ __device__ __forceinline__ void mma_commit(uint64_t* bar) {
     asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(
                      smem_u32(bar))
                  : "memory");
+}
+
+// ---- CTA pairs (cta_group::2): two CTAs of a cluster share one MMA ----
+// The allocator calls are collective: one warp of each CTA of the pair
+// executes them with the same column count, and both CTAs receive the same
+// TMEM address.
+__device__ __forceinline__ void tmem_alloc_pair(uint32_t* dst_smem, uint32_t ncols) {
+    asm volatile("tcgen05.alloc.cta_group::2.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(dst_smem)),
+                 "r"(ncols)
+                 : "memory");
+}
+
+__device__ __forceinline__ void tmem_relinquish_pair() {
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::2.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void tmem_dealloc_pair(uint32_t taddr, uint32_t ncols) {
+    asm volatile("tcgen05.dealloc.cta_group::2.sync.aligned.b32 %0, %1;" ::"r"(taddr), "r"(ncols) : "memory");
+}
+
+// D (+)= A * B^T for an M = 256 tile spread over the pair, issued by the even
+// CTA: rows 0-127 of A come from its tensor memory and rows 128-255 from the
+// odd CTA's at the same address; B's N rows are split in halves, rows
+// [0, N/2) in the even CTA's shared memory and [N/2, N) in the odd CTA's, at
+// the same offset; each CTA's tensor memory receives its 128 rows of D.
+__device__ __forceinline__ void mma_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc,
+                                                    uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc), "r"(idesc), "r"(accumulate)
+        : "memory");
+}
+
+// Arrive once on `bar` (same offset) in each CTA of `cta_mask` when every
+// pair MMA this thread issued so far has completed.
+__device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
+    asm volatile(
+        "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
+            smem_u32(bar)),
+        "h"(cta_mask)
+        : "memory");
 }
 
 // Like mma_commit, but the arrival goes to `bar` in every CTA of `cta_mask`.

@@ -46,6 +46,8 @@ CASES = {
     "pair_long_k": TINY.replace(T=800, H=1280, I=640, E=4, k=2, n_outlier=13),
     # CTA pairs under Zipf-skewed routing: experts from a few rows to several tiles
     "pair_skewed": TINY.replace(T=1200, H=256, I=256, E=8, k=2, bias="zipf", zipf_s=1.2),
+    # about 125 rows per expert: one partial CTA-pair tile per expert
+    "pair_one_tile": TINY.replace(T=500, H=512, I=256, E=8, k=2),
 }
 
 

@@ -509,7 +509,10 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes
 GemmShape choose_gemm_shape(long rows, long groups, long K) {
     (void)K;
     const long per_group = rows / (groups > 0 ? groups : 1);
-    if (per_group >= 160) return GemmShape::Pair;
+#ifndef MOE_PAIR_MIN_ROWS  // measured: CTA pairs win from about a hundred rows per group
+#define MOE_PAIR_MIN_ROWS 96
+#endif
+    if (per_group >= MOE_PAIR_MIN_ROWS) return GemmShape::Pair;
     if (per_group >= 48) return GemmShape::Mid;
     return GemmShape::Narrow;
 }

@@ -127,7 +127,8 @@ __device__ __forceinline__ float dequant(float acc, float s_act, float s_w) {
 }
 
 // Exact CUDA-core path for the rows the certificate rejected: one warp per
-// (row, output channel), int32 dot products over K.
+// (row, output channel), int32 dot products over K, spread over every warp of
+// the grid.
 template <int EPI>
 __device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_groups) {
     const int n_fb = *args.fb_count;
@@ -135,7 +136,7 @@ __device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_
     const int lane = threadIdx.x & 31;
     const int per_row = (EPI == (int)Epi::GateUp) ? args.up_offset : args.w_rows_per_group;
     const long n_items = (long)n_fb * per_row;
-    const int warps = kThreads / 32;
+    const int warps = (int)(blockDim.x >> 5);
     const int8_t* w = static_cast<const int8_t*>(args.w);
     const __half* act = static_cast<const __half*>(args.act16);
     for (long item = (long)blockIdx.x * warps + (threadIdx.x >> 5); item < n_items;

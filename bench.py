@@ -298,19 +298,29 @@ def layer_roofline_us(cfg, offsets, peaks):
     return max(t_b, t_f) * 1e6, ("hbm" if t_b >= t_f else "tensor"), b, f
 
 
+GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_common.cuh", "ptx.cuh")
+
+
+def gemm_source_sha():
+    """sha256 prefix of the GEMM kernels' sources (keys the committed traffic)."""
+    import hashlib
+    h = hashlib.sha256()
+    for name in GEMM_SOURCES:
+        with open(os.path.join(ROOT, "w8a8_quantised_moe_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def traffic_from_profiles(config_name, kernel):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if
-    it was taken on the current source of the GEMM kernel."""
-    import hashlib
+    it was taken on the current source of the GEMM kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         table = json.load(f)
-    src = os.path.join(ROOT, "w8a8_quantised_moe_gb300", "csrc", "gemm.cu")
-    sha = hashlib.sha256(open(src, "rb").read()).hexdigest()[:16]
     ent = table.get(config_name, {}).get(kernel)
-    if not ent or ent.get("gemm_cu_sha256_16") != sha:
+    if not ent or ent.get("gemm_src_sha256_16") != gemm_source_sha():
         return None
     return ent.get("dram_bytes_per_launch")
 

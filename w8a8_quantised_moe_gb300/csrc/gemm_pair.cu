@@ -18,16 +18,23 @@
 // matters because the issuing thread shares its SM sub-partition with a
 // converter and an epilogue warp.
 //
+// Roles per CTA (352 threads): warp 0 loads the int8 weight rows (ring of NQ
+// stages, deep: weights stream from HBM once), warp 10 loads this CTA's half of
+// the activation rows (ring of NB stages: they are re-read from L2 by every
+// channel-block pair), warp 1 allocates TMEM and in the even CTA issues the
+// MMAs, warps 2-5 convert, warps 6-9 run the epilogue.
 // Synchronisation (every wait bounded; see ptx.cuh):
-//   full[s]       per CTA: its TMA bytes of stage s landed
-//   a_ready[j]    even CTA, 8 arrivals (4 converter warps x 2 CTAs): tensor-
-//                 memory A slot j holds the stage's weights in both CTAs.  A
-//                 converter waited on its own full[s] first, so this also
-//                 covers both halves of B.
-//   empty[s]      per CTA, committed by the even CTA's MMAs to both CTAs:
-//                 stage s's shared memory and A slot (it % NA) are free again
-//   acc_full[d]   per CTA, committed to both: accumulator d complete
-//   acc_empty[d]  even CTA, 8 arrivals (4 epilogue warps x 2 CTAs)
+//   q_full/q_empty[NQ]  int8 stage landed / read by the 4 converter warps
+//   b_full[NB]          this CTA's activation half landed
+//   done[NB]            committed by the even CTA's MMAs of a stage to both
+//                       CTAs: its activation slot, and the A slot (it % NA) it
+//                       read, are free again
+//   a_ready[j]          even CTA, 8 arrivals (4 converter warps x 2 CTAs):
+//                       tensor-memory A slot j holds the stage's weights in both
+//                       CTAs.  A converter waited on its own b_full first, so
+//                       this also covers both halves of B.
+//   acc_full[d]         per CTA, committed to both: accumulator d complete
+//   acc_empty[d]        even CTA, 8 arrivals (4 epilogue warps x 2 CTAs)
 // Shared memory of the odd CTA is read by the even CTA's MMAs, and both CTAs
 // arrive on each other's barriers, so neither leaves before a final cluster
 // barrier that every thread of both CTAs reaches on every path.
@@ -47,49 +54,58 @@ namespace {
 constexpr int kPairBK = 128;  // K per stage
 constexpr int kPairND = 2;    // accumulator buffers
 
-template <int BN_, int NS_, int NA_>
+constexpr int kPairThreads = kThreads + 32;  // + warp 10, the activation producer
+constexpr int kPairBWarp = 10;
+
+template <int BN_, int NQ_, int NB_, int NA_>
 struct PairCfg {
     static constexpr int BN = BN_;        // activation rows per pair tile (MMA N, at most)
-    static constexpr int NS = NS_;        // shared-memory stages
-    static constexpr int NA = NA_;        // tensor-memory A slots (at most NS)
+    static constexpr int NQ = NQ_;        // int8 weight stages (deep: weights stream from HBM)
+    static constexpr int NB = NB_;        // activation stages
+    static constexpr int NA = NA_;        // tensor-memory A slots (at most NB)
     static constexpr int kHalf = BN / 2;  // activation rows per CTA
-    static constexpr int kStageA = kTileM * kPairBK;    // int8 weights, [128 x 128] 128-byte swizzle
+    static constexpr int kQStage = kTileM * kPairBK;    // int8 weights, [128 x 128] 128-byte swizzle
     static constexpr int kSubB = kHalf * 128;           // one 64-wide K half of the fp16 rows
-    static constexpr int kStageB = 2 * kSubB;
-    static constexpr int kStage = kStageA + kStageB;
+    static constexpr int kBStage = 2 * kSubB;
     static constexpr int kACols = kPairBK / 2;          // TMEM columns of one A slot
     static constexpr int kDCol0 = NA * kACols;          // first accumulator column
     static constexpr int kTmemCols = kDCol0 + kPairND * BN;
     static constexpr int kXchStride = 33;
     static constexpr int kXch = kTileM * kXchStride * 4;  // GateUp: gate/up exchange
     static constexpr int kStoreBuf = 32 * kTileM * 4;     // scale epilogues: [32 rows][128 channels] staging
-    static constexpr int kOffXch = NS * kStage;
+    static constexpr int kOffQ = 0;
+    static constexpr int kOffB = kOffQ + NQ * kQStage;
+    static constexpr int kOffXch = kOffB + NB * kBStage;
     static constexpr int kXchRegion = kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf;
     static constexpr int kOffBars = kOffXch + kXchRegion;
-    static constexpr int kNumBars = 2 * NS + NA + 2 * kPairND + 2;
+    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 2 * kPairND + 2;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
     static constexpr int kSmem = kOffMisc + 64 + 1024;
-    static_assert(kSubB % 1024 == 0 && kStageA % 1024 == 0, "stages keep 1024-byte alignment");
+    static_assert(kSubB % 1024 == 0 && kQStage % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
     static_assert(kTmemCols <= 512, "TMEM budget");
-    // a converter learns that A slot (it % NA) is free from empty[] of stage
-    // it - NA, whose barrier cannot have moved on to a later phase when NS >= NA
-    static_assert(NS >= NA, "stage ring and A slots");
+    // a converter learns that A slot (it % NA) is free from done[] of stage
+    // it - NA, whose barrier cannot have moved on to a later phase when NB >= NA
+    static_assert(NB >= NA, "activation ring and A slots");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
 // Tensor memory holds the A slots and two accumulators.  Measured on the
-// prefill and linear workloads: 192-wide tiles with two A slots and four
-// stages beat 160-wide tiles with three A slots (wider MMAs amortise the
-// issuing thread's per-stage cost) and a fifth stage gains nothing.
-#ifndef MOE_P_BN  // pair tile width, shared-memory stages, A slots
+// prefill and linear workloads: 192-wide tiles with two A slots beat 160-wide
+// tiles with three (wider MMAs amortise the issuing thread's per-stage cost).
+// Weights and activations have separate rings (weights stream from HBM once,
+// activations are re-read from L2 by every channel-block pair).  Measured:
+// four activation stages matter (two or three are clearly slower), a deeper
+// weight ring gains nothing.
+#ifndef MOE_P_BN  // pair tile width, int8 weight stages, activation stages, A slots
 #define MOE_P_BN 192
-#define MOE_P_NS 4
+#define MOE_P_NQ 4
+#define MOE_P_NB 4
 #define MOE_P_NA 2
 #endif
-using CfgPair = PairCfg<MOE_P_BN, MOE_P_NS, MOE_P_NA>;
+using CfgPair = PairCfg<MOE_P_BN, MOE_P_NQ, MOE_P_NB, MOE_P_NA>;
 
 // Box heights of the per-CTA activation tensor maps: a CTA of a tile with
 // half-width h loads the smallest box that covers h rows.
@@ -116,18 +132,20 @@ __device__ __forceinline__ void decode_pair_tile(const Tiles& t, int tile, int& 
 }
 
 template <class C, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b0,
                              const __grid_constant__ CUtensorMap tmap_b1, const __grid_constant__ CUtensorMap tmap_b2,
                              const __grid_constant__ CUtensorMap tmap_b3, const __grid_constant__ CUtensorMap tmap_out,
                              const GemmArgs args) {
-    constexpr int BN = C::BN, NS = C::NS;
+    constexpr int BN = C::BN, NQ = C::NQ, NB = C::NB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* bars = reinterpret_cast<uint64_t*>(smem + C::kOffBars);
-    uint64_t* full = bars;                     // [NS]
-    uint64_t* empty = bars + NS;               // [NS]
-    uint64_t* a_ready = bars + 2 * NS;         // [NA], used in the even CTA
+    uint64_t* q_full = bars;                   // [NQ] int8 weight stage landed
+    uint64_t* q_empty = q_full + NQ;           // [NQ] read by the 4 converter warps
+    uint64_t* b_full = q_empty + NQ;           // [NB] activation half landed
+    uint64_t* done = b_full + NB;              // [NB] MMAs of the stage done (both CTAs)
+    uint64_t* a_ready = done + NB;             // [NA], used in the even CTA
     uint64_t* acc_full = a_ready + C::NA;    // [ND]
     uint64_t* acc_empty = acc_full + kPairND;  // [ND], used in the even CTA
     uint64_t* teardown = acc_empty + kPairND;
@@ -148,9 +166,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const int nkb = (args.K + kPairBK - 1) / kPairBK;
 
     if (threadIdx.x == 0) {
-        for (int s = 0; s < NS; ++s) {
-            mbar_init(&full[s], 1);
-            mbar_init(&empty[s], 1);
+        for (int s = 0; s < NQ; ++s) {
+            mbar_init(&q_full[s], 1);
+            mbar_init(&q_empty[s], 4);
+        }
+        for (int s = 0; s < NB; ++s) {
+            mbar_init(&b_full[s], 1);
+            mbar_init(&done[s], 1);
         }
         for (int j = 0; j < C::NA; ++j) mbar_init(&a_ready[j], 8);
         for (int d = 0; d < kPairND; ++d) {
@@ -205,7 +227,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
     const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
 
     if (warp == 0) {
-        // ---------------------------------------------------------- producer
+        // ------------------------------------------------- int8 weight TMA
         if (lane == 0) {
             uint32_t it = 0;
             bool ok = true;
@@ -221,27 +243,47 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                     wrow0 = g * args.w_rows_per_group + cb * kTileM;
                     wrow1 = wrow0 + 64;
                 }
+                for (int kb = 0; kb < nkb; ++kb, ++it) {
+                    const uint32_t s = it % NQ, ph = (it / NQ) & 1u;
+                    if (!mbar_wait(&q_empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                    uint8_t* st = smem + C::kOffQ + s * C::kQStage;
+                    mbar_arrive_expect_tx(&q_full[s], (uint32_t)C::kQStage);
+                    tma_load_2d(st, &tmap_w, &q_full[s], kb * kPairBK, wrow0);
+                    tma_load_2d(st + C::kQStage / 2, &tmap_w, &q_full[s], kb * kPairBK, wrow1);
+                }
+            }
+            // drain: every fill issued must land before the CTA may exit
+            for (uint32_t s = 0; s < (uint32_t)NQ && s < it; ++s) {
+                const uint32_t last = it - 1 - ((it - 1 - s) % NQ);
+                mbar_wait_drain(&q_full[s], (last / NQ) & 1u);
+            }
+        }
+    } else if (warp == kPairBWarp) {
+        // ---------------------------------------------- activation-half TMA
+        if (lane == 0) {
+            uint32_t it = 0;
+            bool ok = true;
+            for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
+                int g, cp, row0, nvalid;
+                decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
                 const int half = ((nvalid + 15) & ~15) >> 1;  // activation rows per CTA
                 const int bi = pair_box_index(half);
                 const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
                 const int brow = row0 + (int)rank * half;
-                const uint32_t stage_bytes = (uint32_t)(C::kStageA + 2 * pair_box_rows<C::kHalf>(bi) * 128);
+                const uint32_t bytes = (uint32_t)(2 * pair_box_rows<C::kHalf>(bi) * 128);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % NS, ph = (it / NS) & 1u;
-                    if (!mbar_wait_cluster(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    const int kx = kb * kPairBK;
-                    tma_load_2d(st, &tmap_w, &full[s], kx, wrow0);
-                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kx, wrow1);
-                    tma_load_2d(st + C::kStageA, mb, &full[s], kx, brow);
-                    tma_load_2d(st + C::kStageA + C::kSubB, mb, &full[s], kx + 64, brow);
+                    const uint32_t s = it % NB, ph = (it / NB) & 1u;
+                    // slot s is free once the MMAs of stage it - NB completed
+                    if (!mbar_wait_cluster(&done[s], ph ^ 1u, ctl)) { ok = false; break; }
+                    uint8_t* st = smem + C::kOffB + s * C::kBStage;
+                    mbar_arrive_expect_tx(&b_full[s], bytes);
+                    tma_load_2d(st, mb, &b_full[s], kb * kPairBK, brow);
+                    tma_load_2d(st + C::kSubB, mb, &b_full[s], kb * kPairBK + 64, brow);
                 }
             }
-            // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
-                mbar_wait_drain(&full[s], (last / NS) & 1u);
+            for (uint32_t s = 0; s < (uint32_t)NB && s < it; ++s) {
+                const uint32_t last = it - 1 - ((it - 1 - s) % NB);
+                mbar_wait_drain(&b_full[s], (last / NB) & 1u);
             }
         }
     } else if (warp == 1) {
@@ -259,10 +301,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                 tc_fence_after();
                 const uint32_t d_col = (uint32_t)C::kDCol0 + d * BN;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % NS, j = it % C::NA;
+                    const uint32_t s = it % NB, j = it % C::NA;
                     if (!mbar_wait_cluster(&a_ready[j], (it / C::NA) & 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
-                    const uint32_t b_base = smem_u32(smem + s * C::kStage + C::kStageA);
+                    const uint32_t b_base = smem_u32(smem + C::kOffB + s * C::kBStage);
 #pragma unroll
                     for (int ks = 0; ks < kPairBK / 16; ++ks) {
                         const uint64_t bdesc =
@@ -270,7 +312,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         mma_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols + ks * 8, bdesc, idesc,
                                             (kb != 0 || ks != 0) ? 1u : 0u);
                     }
-                    mma_commit_pair(&empty[s], 3);
+                    mma_commit_pair(&done[s], 3);
                 }
                 if (!ok) break;
                 mma_commit_pair(&acc_full[d], 3);
@@ -278,7 +320,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
             mma_commit_pair(teardown, 1);
             mbar_wait_drain(teardown, 0);
         }
-    } else if (warp < kEpiWarp0) {
+    } else if (warp >= 2 && warp < kEpiWarp0) {
         // ------------------------------------------------------- converters
         const int q = warp & 3;
         const int row = q * 32 + lane;
@@ -287,15 +329,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
         bool ok = true;
         for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const uint32_t s = it % NS, ph = (it / NS) & 1u, j = it % C::NA;
-                // the even CTA's MMAs read this CTA's half of B once the
-                // arrival below is observed: it follows this wait
-                if (!warp_wait(&full[s], ph, ctl)) { ok = false; break; }
+                const uint32_t qs = it % NQ, bs = it % NB, j = it % C::NA;
+                if (!warp_wait(&q_full[qs], (it / NQ) & 1u, ctl)) { ok = false; break; }
                 if (it >= (uint32_t)C::NA) {  // A slot j is free once the MMAs of stage it - NA completed
                     const uint32_t p = it - C::NA;
-                    if (!warp_wait_cluster(&empty[p % NS], (p / NS) & 1u, ctl)) { ok = false; break; }
+                    if (!warp_wait_cluster(&done[p % NB], (p / NB) & 1u, ctl)) { ok = false; break; }
                 }
-                const uint8_t* src = smem + s * C::kStage + row * 128;
+                const uint8_t* src = smem + C::kOffQ + qs * C::kQStage + row * 128;
                 const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + j * C::kACols;
                 const uint32_t swz = (uint32_t)(row & 7);  // 128-byte swizzle: chunk c at c ^ (row & 7)
 #pragma unroll
@@ -306,13 +346,19 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kThreads, 1)
                         cvt_chunk(*reinterpret_cast<const uint4*>(src + (((hh * 4 + c) ^ swz) << 4)), v + c * 8);
                     tmem_st_32(taddr + hh * 32, v);
                 }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(&q_empty[qs]);  // the int8 stage has been read
+                // the even CTA's MMAs read this CTA's half of B once the
+                // arrival below is observed: it follows this wait (placed after
+                // the conversion, so that activation latency overlaps it)
+                if (!warp_wait(&b_full[bs], (it / NB) & 1u, ctl)) { ok = false; break; }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(a_ready_leader + j * 8);
             }
         }
-    } else {
+    } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {
         // --------------------------------------------------------- epilogue
         const int q = warp & 3;
         const int ew = warp - kEpiWarp0;  // 0..3
@@ -444,7 +490,7 @@ int max_pair_clusters(const void* kern, int smem) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (unsigned)num_sms(), 1, 1);
-    cfg.blockDim = dim3(kThreads, 1, 1);
+    cfg.blockDim = dim3(kPairThreads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -493,7 +539,7 @@ cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st) {
     long n = clusters;
     if (max_tiles < n) n = max_tiles;
     if (n < 1) n = 1;
-    kern<<<(unsigned)(2 * n), kThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], tout, args);
+    kern<<<(unsigned)(2 * n), kPairThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], tout, args);
     return cudaGetLastError();
 }
 

@@ -309,3 +309,52 @@ def test_exact_path_mixed_rows_on_cta_pairs():
     q_h = dev["q_h"].cpu().numpy()
     ref2 = q_h.astype(np.int64) @ w2[0].astype(np.int64).T
     np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)
+
+
+def _f32_to_bf16_bits(x):
+    """Round binary32 to bfloat16 bits, nearest-even (test-input construction)."""
+    u = np.asarray(x, np.float32).view(np.uint32).astype(np.uint64)
+    r = ((u + 0x7FFF + ((u >> 16) & 1)) >> 16).astype(np.uint16)
+    return r
+
+
+def test_quantiser_rounding_boundaries():
+    """Activation rows whose quotients x/s sit on or within a few ulp of the
+    half-integers where rint changes (ties to even included): the codes must
+    equal the oracle's, which divides exactly.  s = 1 and s = 2^-3 make
+    x/s = m + 0.5 exact; other scales land the bf16-rounded quotients just
+    either side of the boundaries."""
+    H = 256
+    rows = []
+    r = np.random.default_rng(21)
+    for amax in (127.0, 127.0 / 8, 3.0, 0.7, 1e-3, 5e4):
+        s = np.float32(np.float32(amax) / np.float32(127.0))
+        m = np.arange(-127, 127)  # (m + 0.5) * s stays within amax = 127 s
+        v = np.concatenate([(m + 0.5) * np.float64(s), [0.0]])
+        for jitter in (0.0, 1e-7, -1e-7, 1e-6, -1e-6):
+            row = np.empty(H, np.float64)
+            row[0] = amax  # fixes the row's amax
+            row[1:] = v * (1.0 + jitter)
+            r.shuffle(row[1:])
+            bits = _f32_to_bf16_bits(row.astype(np.float32))
+            # keep |x| <= amax after rounding: amax itself is exact in bf16 for the chosen values
+            rows.append(bits)
+    x = np.array(rows, np.uint16)
+    xf = bits_to_f32(x)
+    # amax of each row must stay the intended value after bf16 rounding
+    assert (np.abs(xf).max(axis=1) == xf[:, 0]).all()
+    T = x.shape[0]
+    q_ref, s_ref = oracle.quantize_rows_bf16(x)
+    # one expert, top-1: the codes of token t land in slot t
+    I = 128
+    w13 = np.zeros((1, 2 * I, H), np.int8)
+    w2 = np.zeros((1, H, I), np.int8)
+    args = (bf16_to_dev(x), torch.zeros((H, 1), device="cuda"), None, torch.from_numpy(w13).cuda(),
+            torch.full((1, 2 * I), 1e-3, device="cuda"), torch.from_numpy(w2).cuda(),
+            torch.full((1, H), 1e-3, device="cuda"), 1)
+    _, dev = moe.forward_debug(*args, fields=("s_x", "q_x"))
+    np.testing.assert_array_equal(dev["s_x"].cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(dev["q_x"].cpu().numpy(), q_ref)
+    # the construction does hit ties: some quotients are exact half-integers
+    ties = np.abs(xf[:, 1:] / s_ref[:, None] - np.round(xf[:, 1:] / s_ref[:, None])) == 0.5
+    assert ties.sum() > 100

@@ -305,13 +305,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     if (!mbar_wait_cluster(&a_ready[j], (it / C::NA) & 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_base = smem_u32(smem + C::kOffB + s * C::kBStage);
-#pragma unroll
-                    for (int ks = 0; ks < kPairBK / 16; ++ks) {
-                        const uint64_t bdesc =
-                            smem_desc_sw128(b_base + (ks / 4) * C::kSubB) + (uint64_t)((ks % 4) * 2);
-                        mma_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols + ks * 8, bdesc, idesc,
-                                            (kb != 0 || ks != 0) ? 1u : 0u);
-                    }
+                    mma8_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols, smem_desc_sw128(b_base),
+                                         (uint64_t)(C::kSubB >> 4), idesc, kb != 0 ? 1u : 0u);
                     mma_commit_pair(&done[s], 3);
                 }
                 if (!ok) break;

@@ -291,6 +291,49 @@ __device__ __forceinline__ void mma_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_
         : "memory");
 }
 
+// One stage of K = 128 as 8 pair MMAs (K = 16 each) in a single block: A in
+// tensor memory at a_tmem (8 columns per K step), B described by b_desc0 for
+// K steps 0-3 and by b_desc0 + b_sub16 for steps 4-7 (the second 64-wide K
+// half; both advance 32 bytes per step).  The first MMA overwrites D unless
+// accumulate != 0, the others accumulate.  Issuing them from one block keeps
+// the issuing thread's instruction count per stage small: that thread shares
+// its SM sub-partition with busy warps and waits for every issue slot.
+__device__ __forceinline__ void mma8_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a_tmem, uint64_t b_desc0,
+                                                     uint64_t b_sub16, uint32_t idesc, uint32_t accumulate) {
+    asm volatile(
+        "{\n\t"
+        ".reg .pred p0, p1;\n\t"
+        ".reg .b64 b1, b2, b3, b4, b5, b6, b7;\n\t"
+        ".reg .b32 a1, a2, a3, a4, a5, a6, a7;\n\t"
+        "setp.ne.b32 p0, %4, 0;\n\t"
+        "setp.eq.b32 p1, %4, %4;\n\t"
+        "add.s64 b1, %2, 2;\n\t"
+        "add.s64 b2, %2, 4;\n\t"
+        "add.s64 b3, %2, 6;\n\t"
+        "add.s64 b4, %2, %5;\n\t"
+        "add.s64 b5, b4, 2;\n\t"
+        "add.s64 b6, b4, 4;\n\t"
+        "add.s64 b7, b4, 6;\n\t"
+        "add.u32 a1, %1, 8;\n\t"
+        "add.u32 a2, %1, 16;\n\t"
+        "add.u32 a3, %1, 24;\n\t"
+        "add.u32 a4, %1, 32;\n\t"
+        "add.u32 a5, %1, 40;\n\t"
+        "add.u32 a6, %1, 48;\n\t"
+        "add.u32 a7, %1, 56;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [%1], %2, %3, p0;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a1], b1, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a2], b2, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a3], b3, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a4], b4, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a5], b5, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a6], b6, %3, p1;\n\t"
+        "tcgen05.mma.cta_group::2.kind::f16 [%0], [a7], b7, %3, p1;\n\t"
+        "}" ::"r"(d_tmem),
+        "r"(a_tmem), "l"(b_desc0), "r"(idesc), "r"(accumulate), "l"(b_sub16)
+        : "memory");
+}
+
 // Arrive once on `bar` (same offset) in each CTA of `cta_mask` when every
 // pair MMA this thread issued so far has completed.
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {

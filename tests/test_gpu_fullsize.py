@@ -1,0 +1,160 @@
+"""Parity at the benchmark's full sizes (decode, prefill and wide MoE layers,
+the 4096^3 linear layer), in the launch configuration bench.py times: inputs
+resident on the device, expert weights drawn in fp32 on the device and
+quantised by the library, one plain forward.
+
+The oracle cannot run these layers whole in a test's time, so it checks
+sampled tokens one by one, and the full-size results are checked against
+properties that hold at any size:
+
+* every routing array is consistent (expert offsets are the prefix sums of
+  the top-k counts, slots are a permutation, each slot lies in its expert's
+  range, a token's experts are distinct);
+* for the sampled tokens the router, the codes, both GEMMs' int32
+  accumulators, the requantisation and the output epilogue are bit-exact
+  against the oracle on the stage's input; h is within H_RTOL (expf);
+* the sampled rows of y agree with the oracle's own end-to-end computation
+  (from the oracle's h) within the layer's tolerance;
+* the library's int8 weights of every sampled expert equal the oracle's
+  quantisation of the same fp32 draws, so the oracle's weights are its own.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import w8a8_quantised_moe_gb300 as moe
+from w8a8_quantised_moe_gb300 import build as lib_build
+from w8a8_quantised_moe_gb300 import workloads as wl
+from gpu_helpers import H_RTOL, TOPK_W_ATOL, assert_y_close, bf16_from_dev, bf16_to_dev
+
+pytestmark = pytest.mark.gpu
+
+# sampled tokens per layer (each brings up to k experts the oracle quantises)
+SAMPLE = {"decode": 16, "prefill": 16, "wide": 4}
+
+
+@pytest.fixture(scope="module", autouse=True)
+def _built():
+    lib_build.build()
+    moe._lib.load()
+
+
+def _device_weights(cfg, seed):
+    w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=torch.int8, device="cuda")
+    w13_s = torch.empty((cfg.E, 2 * cfg.I), dtype=torch.float32, device="cuda")
+    w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=torch.int8, device="cuda")
+    w2_s = torch.empty((cfg.E, cfg.H), dtype=torch.float32, device="cuda")
+    for e in range(cfg.E):
+        q, s = moe.quantize_weights(wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda"))
+        w13_q[e].copy_(q)
+        w13_s[e].copy_(s)
+        q, s = moe.quantize_weights(wl.expert_weight_fp32(cfg, "w2", e, seed, device="cuda"))
+        w2_q[e].copy_(q)
+        w2_s[e].copy_(s)
+    return w13_q, w13_s, w2_q, w2_s
+
+
+def _oracle_expert(cfg, which, e, seed):
+    """The oracle's quantisation of the same fp32 draws (drawn where the
+    library's were, then copied to the host)."""
+    return oracle.quantize_rows(wl.expert_weight_fp32(cfg, which, e, seed, device="cuda").cpu().numpy())
+
+
+def _check_routing_arrays(cfg, ids, offsets, slot_of, slot_token):
+    T, k, E = cfg.T, cfg.k, cfg.E
+    S = T * k
+    counts = np.bincount(ids.ravel(), minlength=E)
+    assert offsets[0] == 0 and offsets[-1] == S
+    np.testing.assert_array_equal(np.diff(offsets), counts)
+    np.testing.assert_array_equal(np.sort(slot_of.ravel()), np.arange(S))
+    np.testing.assert_array_equal(slot_token[slot_of], np.repeat(np.arange(T)[:, None], k, axis=1))
+    expert_of_slot = np.searchsorted(offsets, slot_of, side="right") - 1
+    np.testing.assert_array_equal(expert_of_slot, ids)
+    assert (np.diff(np.sort(ids, axis=1), axis=1) > 0).all()  # distinct experts per token
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "wide"])
+def test_full_size_layer_sampled_against_oracle(name):
+    cfg = wl.CONFIGS[name]
+    seed = 0
+    inp = wl.make_moe_inputs(cfg, seed)
+    x = bf16_to_dev(inp.x)
+    Wr = torch.from_numpy(inp.Wr).cuda()
+    bias = None if inp.bias is None else torch.from_numpy(inp.bias).cuda()
+    w13_q, w13_s, w2_q, w2_s = _device_weights(cfg, seed)
+    args = (x, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k)
+
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    y_plain = moe.forward(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    y_dbg, dev = moe.forward_debug(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    assert torch.equal(y_plain.view(torch.int16), y_dbg.view(torch.int16))
+
+    ids = dev["topk_ids"].cpu().numpy()
+    topk_w = dev["topk_w"].cpu().numpy()
+    offsets = dev["offsets"].cpu().numpy()
+    slot_of = dev["slot_of"].cpu().numpy()
+    slot_token = dev["slot_token"].cpu().numpy()
+    _check_routing_arrays(cfg, ids, offsets, slot_of, slot_token)
+
+    tok = np.sort(np.random.default_rng(7).choice(cfg.T, SAMPLE[name], replace=False))
+    ids_ref, w_ref, _ = oracle.router(inp.x[tok], inp.Wr, inp.bias, cfg.k)
+    np.testing.assert_array_equal(ids[tok], ids_ref)
+    np.testing.assert_allclose(topk_w[tok], w_ref, rtol=0, atol=TOPK_W_ATOL)
+    q_ref, s_ref = oracle.quantize_rows_bf16(inp.x[tok])
+    np.testing.assert_array_equal(dev["q_x"][tok].cpu().numpy(), q_ref)
+    np.testing.assert_array_equal(dev["s_x"][tok].cpu().numpy(), s_ref)
+
+    ref_w = {}
+    for e in sorted(set(ids_ref.ravel().tolist())):
+        ref_w[e] = (_oracle_expert(cfg, "w13", e, seed), _oracle_expert(cfg, "w2", e, seed))
+        np.testing.assert_array_equal(w13_q[e].cpu().numpy(), ref_w[e][0][0])
+        np.testing.assert_array_equal(w13_s[e].cpu().numpy(), ref_w[e][0][1])
+        np.testing.assert_array_equal(w2_q[e].cpu().numpy(), ref_w[e][1][0])
+        np.testing.assert_array_equal(w2_s[e].cpu().numpy(), ref_w[e][1][1])
+
+    y_gpu = bf16_from_dev(y_dbg)[tok]
+    y_ref = np.empty_like(y_gpu)
+    for i, t in enumerate(tok):
+        slots = slot_of[t]
+        o_gpu = dev["o"][torch.from_numpy(slots).long().cuda()].cpu().numpy()
+        o_own = np.empty_like(o_gpu)
+        for j, s in enumerate(slots):
+            (w13r, s13r), (w2r, s2r) = ref_w[int(ids_ref[i, j])]
+            acc1 = oracle.gemm_s8(q_ref[i:i + 1], w13r)
+            np.testing.assert_array_equal(dev["acc1"][s].cpu().numpy(), acc1[0])
+            h_ref = oracle.epilogue_gate_up(acc1, s_ref[i:i + 1], s13r)
+            h_gpu = dev["h"][s].cpu().numpy()
+            np.testing.assert_allclose(h_gpu, h_ref[0], rtol=H_RTOL, atol=1e-30)
+            # requantisation, GEMM2 and its epilogue on the GPU's own h: exact
+            qh, sh = oracle.quantize_rows(h_gpu[None])
+            np.testing.assert_array_equal(dev["q_h"][s].cpu().numpy(), qh[0])
+            assert dev["s_h"][s].item() == sh[0]
+            acc2 = oracle.gemm_s8(qh, w2r)
+            np.testing.assert_array_equal(dev["acc2"][s].cpu().numpy(), acc2[0])
+            np.testing.assert_array_equal(o_gpu[j], oracle.epilogue_scale(acc2, sh, s2r)[0])
+            # the oracle's own path from its own h
+            qh_o, sh_o = oracle.quantize_rows(h_ref)
+            o_own[j] = oracle.epilogue_scale(oracle.gemm_s8(qh_o, w2r), sh_o, s2r)[0]
+        # combine of the GPU's own o rows: exact; of the oracle's: the layer tolerance
+        one = np.arange(cfg.k, dtype=np.int32)[None]
+        np.testing.assert_array_equal(y_gpu[i], oracle.combine(o_gpu, one, topk_w[t][None])[0])
+        y_ref[i] = oracle.combine(o_own, one, w_ref[i][None])[0]
+    assert_y_close(y_gpu, y_ref)
+
+
+def test_full_size_linear_sampled_against_oracle():
+    cfg = wl.LINEAR
+    seed = 0
+    x_bits = wl.linear_activations(cfg, seed)
+    w32 = wl.expert_weight_fp32(cfg, "linear", 0, seed, device="cuda")
+    w_q, w_s = moe.quantize_weights(w32)
+    y = moe.linear(bf16_to_dev(x_bits), w_q, w_s)
+    torch.cuda.synchronize()
+    wq_ref, ws_ref = oracle.quantize_rows(w32.cpu().numpy())
+    np.testing.assert_array_equal(w_q.cpu().numpy(), wq_ref)
+    np.testing.assert_array_equal(w_s.cpu().numpy(), ws_ref)
+    rows = np.sort(np.random.default_rng(8).choice(cfg.M, 16, replace=False))
+    np.testing.assert_array_equal(bf16_from_dev(y)[rows], oracle.linear(x_bits[rows], wq_ref, ws_ref))

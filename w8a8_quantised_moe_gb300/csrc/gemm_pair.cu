@@ -54,8 +54,18 @@ namespace {
 constexpr int kPairBK = 128;  // K per stage
 constexpr int kPairND = 2;    // accumulator buffers
 
-constexpr int kPairThreads = kThreads + 32;  // + warp 10, the activation producer
+// MMA-issuing threads in the even CTA.  Measured: two beat one by 8-10% on
+// the expert GEMMs.  Builds with three or four issuers (13-14 warps) failed
+// to run, with a launch failure whose cause is not known: they are not built.
+#ifndef MOE_P_ISSUERS
+#define MOE_P_ISSUERS 2
+#endif
+constexpr int kIssuers = MOE_P_ISSUERS;
+static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
+// + warp 10, the activation producer, and warp 11, the second MMA issuer
+constexpr int kPairThreads = kThreads + 32 * kIssuers;
 constexpr int kPairBWarp = 10;
+constexpr int kPairMma2Warp = 11;
 
 template <int BN_, int NQ_, int NB_, int NA_>
 struct PairCfg {
@@ -78,7 +88,7 @@ struct PairCfg {
     static constexpr int kOffXch = kOffB + NB * kBStage;
     static constexpr int kXchRegion = kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf;
     static constexpr int kOffBars = kOffXch + kXchRegion;
-    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 2 * kPairND + 2;
+    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 3 * kPairND + 3;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
@@ -148,8 +158,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint64_t* a_ready = done + NB;             // [NA], used in the even CTA
     uint64_t* acc_full = a_ready + C::NA;    // [ND]
     uint64_t* acc_empty = acc_full + kPairND;  // [ND], used in the even CTA
-    uint64_t* teardown = acc_empty + kPairND;
-    uint64_t* epi_bar = teardown + 1;
+    uint64_t* tile_go = acc_empty + kPairND;  // [ND], even CTA: the tile's overwriting MMAs are issued
+    uint64_t* teardown = tile_go + kPairND;   // [2], one per issuer
+    uint64_t* epi_bar = teardown + 2;
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -176,10 +187,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         for (int j = 0; j < C::NA; ++j) mbar_init(&a_ready[j], 8);
         for (int d = 0; d < kPairND; ++d) {
-            mbar_init(&acc_full[d], 1);
+            mbar_init(&acc_full[d], kIssuers);
+            mbar_init(&tile_go[d], 1);
             mbar_init(&acc_empty[d], 8);
         }
-        mbar_init(teardown, 1);
+        mbar_init(&teardown[0], 1);
+        mbar_init(&teardown[1], 1);
         mbar_init(epi_bar, 4);
         *abort_flag = 0;
         fence_barrier_init();
@@ -286,8 +299,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 mbar_wait_drain(&b_full[s], (last / NB) & 1u);
             }
         }
-    } else if (warp == 1) {
-        // ------------------------------------------- MMA issuer (even CTA)
+    } else if (warp == 1 || (kIssuers == 2 && warp == kPairMma2Warp)) {
+        // ------------------------------------------ MMA issuers (even CTA)
+        // With two issuers, warp 1 issues the even K stages of every tile and
+        // warp 11 (another SM sub-partition) the odd ones: each waits on its
+        // own stages, so one's waits overlap the other's issue.  MMAs into one
+        // accumulator may then run in either order (the sums are exact
+        // integers), except that the tile's first, overwriting MMAs must come
+        // first: warp 11 waits on tile_go[d], which warp 1 arrives on after
+        // issuing them (tcgen05 fences order the two threads' MMAs).  Each
+        // issuer commits its own stages and the tile (acc_full counts both).
+        const int role = warp == 1 ? 0 : 1;
         if (lane == 0 && rank == 0) {
             uint32_t it = 0, tl = 0;
             bool ok = true;
@@ -297,23 +319,34 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const uint32_t n_mma = (uint32_t)((nvalid + 15) & ~15);
                 const uint32_t idesc = idesc_f16_f32(2 * kTileM, n_mma);
                 const uint32_t d = tl % kPairND;
-                if (!mbar_wait_cluster(&acc_empty[d], ((tl / kPairND) & 1u) ^ 1u, ctl)) break;
-                tc_fence_after();
+                if (role == 0) {
+                    if (!mbar_wait_cluster(&acc_empty[d], ((tl / kPairND) & 1u) ^ 1u, ctl)) break;
+                    tc_fence_after();
+                } else if (nkb > role) {
+                    if (!mbar_wait(&tile_go[d], (tl / kPairND) & 1u, ctl)) break;
+                    tc_fence_after();
+                }
                 const uint32_t d_col = (uint32_t)C::kDCol0 + d * BN;
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % NB, j = it % C::NA;
-                    if (!mbar_wait_cluster(&a_ready[j], (it / C::NA) & 1u, ctl)) { ok = false; break; }
+                for (int kb = role; kb < nkb; kb += kIssuers) {
+                    const uint32_t itk = it + (uint32_t)kb;
+                    const uint32_t s = itk % NB, j = itk % C::NA;
+                    if (!mbar_wait_cluster(&a_ready[j], (itk / C::NA) & 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_base = smem_u32(smem + C::kOffB + s * C::kBStage);
                     mma8_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols, smem_desc_sw128(b_base),
                                          (uint64_t)(C::kSubB >> 4), idesc, kb != 0 ? 1u : 0u);
+                    if (kIssuers > 1 && kb == 0) {  // the overwriting MMAs are issued
+                        tc_fence_before();
+                        mbar_arrive(&tile_go[d]);
+                    }
                     mma_commit_pair(&done[s], 3);
                 }
+                it += (uint32_t)nkb;
                 if (!ok) break;
                 mma_commit_pair(&acc_full[d], 3);
             }
-            mma_commit_pair(teardown, 1);
-            mbar_wait_drain(teardown, 0);
+            mma_commit_pair(&teardown[role], 1);
+            mbar_wait_drain(&teardown[role], 0);
         }
     } else if (warp >= 2 && warp < kEpiWarp0) {
         // ------------------------------------------------------- converters

@@ -234,6 +234,20 @@ MOE_W8A8_API moe_status_t moe_w8a8_device_error(void* workspace, void* stream);
 MOE_W8A8_API uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns);
 
 /* ---------------------------------------------------------------------------
+ * moe_w8a8_set_gemm_path -- test hook: force the kernel of every expert GEMM
+ * and linear GEMM launched after this call (process-wide).  -1 (the default)
+ * chooses by the average rows per group; 0, 1, 2 force the one-CTA
+ * tensor-core kernel with 160-, 128- or 32-row tiles, 3 the CTA-pair
+ * tensor-core kernel (the 160-row kernel where the channel blocks do not
+ * pair up), 4 the CUDA-core dp4a kernel for groups of a few rows (the
+ * automatic choice where its shape rule fails: K a multiple of 128 and at
+ * most 28672, output channels a multiple of 32 for the gate/up GEMM and of
+ * 64 otherwise).  Every path computes the same bits.  Returns the previous
+ * setting, or -2 (and changes nothing) for a value outside [-1, 4].
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API int moe_w8a8_set_gemm_path(int path);
+
+/* ---------------------------------------------------------------------------
  * moe_w8a8_set_profile_events -- measurement hook.  While set (on the calling
  * host thread), every moe_w8a8_forward records events[i] on its stream right
  * before its i-th kernel launch (0 router/top-k, 1 scan, 2 permute+quantise,

@@ -1,5 +1,7 @@
 """Shared helpers of the GPU parity tests: moving seeded inputs to the device,
 running the oracle on the same inputs, and the float tolerances."""
+import contextlib
+
 import numpy as np
 import torch
 
@@ -18,6 +20,18 @@ H_RTOL = 2e-6
 # and rounds once.  At H = 4096-7168 the logits differ by up to ~1e-5, and a
 # softmax weight moves by at most a quarter of that.
 TOPK_W_ATOL = 1e-5
+
+
+@contextlib.contextmanager
+def gemm_path(name: str):
+    """Force the library's GEMM kernel ("auto", "skinny", "narrow", "mid",
+    "wide", "pair") inside the block; the automatic choice afterwards."""
+    import w8a8_quantised_moe_gb300 as moe
+    moe.set_gemm_path(name)
+    try:
+        yield
+    finally:
+        moe.set_gemm_path("auto")
 
 
 def bf16_to_dev(bits: np.ndarray) -> torch.Tensor:

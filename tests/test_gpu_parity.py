@@ -16,7 +16,7 @@ import w8a8_quantised_moe_gb300 as moe
 from w8a8_quantised_moe_gb300 import build as lib_build
 from w8a8_quantised_moe_gb300 import workloads as wl
 from gpu_helpers import (H_RTOL, Layer, assert_y_close, bf16_from_dev, bf16_to_dev, bits_to_f32,
-                         y_errors)
+                         gemm_path, y_errors)
 
 pytestmark = pytest.mark.gpu
 
@@ -106,6 +106,22 @@ def test_forward_matches_oracle_stage_by_stage(name):
     assert mismatch <= max(2, cfg.T * cfg.k * cfg.I // 10000)
 
 
+# every GEMM kernel on shapes from one row per expert to several tiles: the
+# CUDA-core dp4a kernel (its automatic range is a few rows per expert, here
+# also groups of hundreds of rows in chunks of 8), the one-CTA tensor-core
+# kernels with 32-, 128- and 160-row tiles and the CTA-pair kernel
+PATH_CASES = ("tiny", "one_token", "top4_bias", "long_k", "pair_skewed", "wide_tiles")
+
+
+@pytest.mark.parametrize("path", ["skinny", "narrow", "mid", "wide", "pair"])
+@pytest.mark.parametrize("name", PATH_CASES)
+def test_forward_stage_by_stage_on_each_gemm_path(name, path):
+    cfg = CASES[name]
+    with gemm_path(path):
+        mismatch, _ = _stagewise(Layer(cfg, seed=5))
+    assert mismatch <= max(2, cfg.T * cfg.k * cfg.I // 10000)
+
+
 def test_forward_all_tokens_to_one_expert():
     cfg = TINY.replace(T=150, H=256, I=256, E=6, k=1)
     layer = Layer(cfg, seed=2)
@@ -187,24 +203,31 @@ def test_linear_golden_example():
     assert (yf[:, 2:] == 0).all()
 
 
-@pytest.mark.parametrize("M,N,K", [(1, 128, 128), (37, 256, 384), (300, 384, 1280), (130, 128, 4096),
-                                   (500, 512, 1024)])
-def test_linear_bit_exact(M, N, K):
+@pytest.mark.parametrize("M,N,K,path", [(1, 128, 128, "auto"), (37, 256, 384, "auto"), (300, 384, 1280, "auto"),
+                                        (130, 128, 4096, "auto"), (500, 512, 1024, "auto"),
+                                        (3, 384, 640, "auto"), (8, 1024, 2048, "auto"), (37, 256, 384, "skinny"),
+                                        (9, 128, 1280, "narrow")])
+def test_linear_bit_exact(M, N, K, path):
+    """M <= 8 rows take the dp4a kernel by default; 37 rows forced onto it
+    pass through shared memory in five chunks, the last one ragged."""
     cfg = wl.LINEAR
     x = wl.draw_activations(7, cfg.cfg_id, M, K, max(1, K // 100))
     w32 = (np.random.default_rng(M + N + K).standard_normal((N, K)) * 0.02).astype(np.float32)
     w_q, s_w = oracle.quantize_rows(w32)
     y_ref = oracle.linear(x, w_q, s_w)
-    y = moe.linear(bf16_to_dev(x), torch.from_numpy(w_q).cuda(), torch.from_numpy(s_w).cuda())
+    with gemm_path(path):
+        y = moe.linear(bf16_to_dev(x), torch.from_numpy(w_q).cuda(), torch.from_numpy(s_w).cuda())
     np.testing.assert_array_equal(bf16_from_dev(y), y_ref)
 
 
 # --------------------------------------------------------------- exactness
 
-def test_int32_accumulators_exact_on_worst_case_inputs():
+@pytest.mark.parametrize("path", ["auto", "skinny"])
+def test_int32_accumulators_exact_on_worst_case_inputs(path):
     """x = +-1 (every code +-127) against int8 weights spanning [-128, 127],
     K = 7168: the exact sums run far beyond 2^24, so any fp32 rounding in the
-    tensor-core accumulation would show."""
+    tensor-core accumulation would show (and any int32 slip in the dp4a
+    kernel)."""
     T, H, I = 64, 7168, 128
     r = np.random.default_rng(5)
     x = np.where(r.random((T, H)) < 0.5, -1.0, 1.0).astype(np.float32)
@@ -220,7 +243,8 @@ def test_int32_accumulators_exact_on_worst_case_inputs():
     Wr = np.zeros((H, 1), np.float32)
     args = (xb.cuda(), torch.from_numpy(Wr).cuda(), None, torch.from_numpy(w13).cuda(),
             torch.from_numpy(s13).cuda(), torch.from_numpy(w2).cuda(), torch.from_numpy(s2).cuda(), 1)
-    _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
+    with gemm_path(path):
+        _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
     q_x = dev["q_x"].cpu().numpy()
     assert (np.abs(q_x) == 127).all()
     ref1 = q_x.astype(np.int64) @ w13[0].astype(np.int64).T
@@ -248,10 +272,12 @@ def _boundary_rows(H):
     return np.array(rows, np.float32)
 
 
-def test_exactness_certificate_boundary():
+@pytest.mark.parametrize("path", ["narrow", "skinny"])
+def test_exactness_certificate_boundary(path):
     """A positive row with L1 = 2^17 against weights -128 drives the partial
     sums down to exactly -2^24 on the tensor-core path; a row one above the
-    bound goes to the exact CUDA-core path.  Both must be exact."""
+    bound goes to the exact CUDA-core path.  Both must be exact, and so must
+    the dp4a kernel, which has no bound."""
     H, I = 2048, 128
     x = _boundary_rows(H)
     assert np.abs(x[0]).sum() == 2 ** 17 and np.abs(x[1]).sum() == 2 ** 17 + 1
@@ -263,7 +289,8 @@ def test_exactness_certificate_boundary():
     args = (torch.from_numpy(x).to(torch.bfloat16).cuda(), torch.zeros((H, 1), device="cuda"), None,
             torch.from_numpy(w13).cuda(), torch.full((1, 2 * I), 1e-7, device="cuda"),
             torch.from_numpy(w2).cuda(), torch.full((1, H), 1e-3, device="cuda"), 1)
-    _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
+    with gemm_path(path):
+        _, dev = moe.forward_debug(*args, fields=("q_x", "acc1", "q_h", "acc2"))
     q_x = dev["q_x"].cpu().numpy()
     np.testing.assert_array_equal(q_x, x.astype(np.int8))
     ref1 = q_x.astype(np.int64) @ w13[0].astype(np.int64).T
@@ -273,16 +300,19 @@ def test_exactness_certificate_boundary():
     np.testing.assert_array_equal(dev["acc2"].cpu().numpy(), ref2)
 
 
-def test_second_gemm_exact_path():
+@pytest.mark.parametrize("path", ["narrow", "skinny"])
+def test_second_gemm_exact_path(path):
     """Identical gate and up rows make h constant along I, so every q_h code
-    is +-127 and L1(q_h) = 127 * 2048 is far above the bound: GEMM2 runs on
-    the exact path for every row.  Compared with the oracle stage by stage."""
+    is +-127 and L1(q_h) = 127 * 2048 is far above the bound: on the
+    tensor-core kernel GEMM2 runs on the exact path for every row.  Compared
+    with the oracle stage by stage."""
     cfg = TINY.replace(T=8, H=256, I=2048, E=2, k=1)
     layer = Layer(cfg, seed=4)
     layer.w13_q[:] = 1
     layer.d_w13 = torch.from_numpy(layer.w13_q).cuda()
-    mismatch, _ = _stagewise(layer)
-    _, dev = moe.forward_debug(*layer.device_args(), fields=("q_h",))
+    with gemm_path(path):
+        mismatch, _ = _stagewise(layer)
+        _, dev = moe.forward_debug(*layer.device_args(), fields=("q_h",))
     q_h = dev["q_h"].cpu().numpy()
     assert (np.abs(q_h.astype(np.int64)).sum(axis=1) > 2 ** 17).all()
 

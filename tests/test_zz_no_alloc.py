@@ -59,7 +59,7 @@ def _static(lib, xb, w_q, s_w):
 def test_static_scratch_linear_matches_workspace_linear_twice(lib):
     # two calls in a row with different shapes and inputs: the second must
     # not see anything the first left in the shared scratch
-    for seed, (M, N, K) in ((1, (300, 384, 1280)), (2, (1000, 256, 4096))):
+    for seed, (M, N, K) in ((1, (300, 384, 1280)), (2, (1000, 256, 4096)), (3, (4, 512, 2048))):
         xb, w_q, s_w = _inputs(seed, M, N, K)
         y_static = _static(lib, xb, w_q, s_w)
         y_ws = _with_workspace(lib, xb, w_q, s_w)

@@ -20,7 +20,8 @@ from ._lib import MoeError, STATUS
 
 __all__ = [
     "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward",
-    "forward_debug", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns",
+    "forward_debug", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns", "set_gemm_path",
+    "GEMM_PATHS",
     "version",
 ]
 
@@ -56,6 +57,20 @@ def version() -> int:
 def set_wait_timeout_ns(ns: int) -> int:
     """Time limit of every in-kernel wait for later launches; returns the previous one."""
     return int(_lib.load().moe_w8a8_set_wait_timeout_ns(int(ns)))
+
+
+# kernel choices of moe_w8a8_set_gemm_path
+GEMM_PATHS = {"auto": -1, "wide": 0, "mid": 1, "narrow": 2, "pair": 3, "skinny": 4}
+
+
+def set_gemm_path(path: str) -> str:
+    """Force the GEMM kernel of later launches ("auto" restores the automatic
+    choice); returns the previous setting.  A test hook: every path computes
+    the same bits."""
+    prev = _lib.load().moe_w8a8_set_gemm_path(GEMM_PATHS[path])
+    if prev < -1:
+        raise ValueError(path)
+    return {v: k for k, v in GEMM_PATHS.items()}[prev]
 
 
 def quantize_weights(w, stream=None):

@@ -14,7 +14,8 @@ ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w8a8.so")
-SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu", "gemm_pair.cu", "static_linear.cu"]
+SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu", "gemm_pair.cu", "gemm_skinny.cu",
+           "static_linear.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh"]
 
 NVCC_FLAGS = [

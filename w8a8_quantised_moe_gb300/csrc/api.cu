@@ -28,6 +28,7 @@ int num_sms() {
 namespace {
 
 std::atomic<uint64_t> g_timeout_ns{kDefaultTimeoutNs};
+std::atomic<int> g_gemm_path{-1};  // -1: automatic choice of the GEMM kernel
 thread_local cudaEvent_t const* t_events = nullptr;  // measurement hook
 
 cudaError_t mark(int i, cudaStream_t st) {
@@ -50,6 +51,18 @@ bool moe_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
 }
 
 }  // namespace
+
+GemmShape pick_gemm_shape(long rows, long groups, long K, Epi epi, long w_rows_per_group, long up_offset) {
+    const int forced = g_gemm_path.load();
+    if (forced >= 0 && forced <= (int)GemmShape::Skinny) {
+        const GemmShape s = static_cast<GemmShape>(forced);
+        if (s != GemmShape::Skinny || skinny_shape_supported(epi, K, w_rows_per_group, up_offset)) return s;
+    }
+    GemmShape s = choose_gemm_shape(rows, groups, K);
+    if (s == GemmShape::Skinny && !skinny_shape_supported(epi, K, w_rows_per_group, up_offset))
+        s = GemmShape::Narrow;
+    return s;
+}
 
 FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     FwdLayout L{};
@@ -159,6 +172,12 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     uint16_t* q_h16 = at<uint16_t>(workspace, L.q_h16);
     float* o = at<float>(workspace, L.o);
     const uint64_t timeout = g_timeout_ns.load();
+    // GEMM kernels; the dp4a kernel reads int8 codes, which then take the
+    // place of the fp16 ones in the same workspace regions
+    const GemmShape shape1 = pick_gemm_shape(S, E, H, Epi::GateUp, 2 * I, I);
+    const GemmShape shape2 = pick_gemm_shape(S, E, I, Epi::ScaleF32, H, 0);
+    int8_t* q_x8 = shape1 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_x16) : nullptr;
+    int8_t* q_h8 = shape2 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_h16) : nullptr;
 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
@@ -170,12 +189,13 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                             s_x, s_slot, q_x16, flag1, list1, counts + 0, st);
+                             s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g1{};
     g1.w = w13_q;
     g1.act16 = q_x16;
+    g1.act8 = q_x8;
     g1.K = (int)H;
     g1.n_cb = (int)(I / 64);
     g1.n_groups = (int)E;
@@ -194,16 +214,20 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.error = err;
     g1.timeout_ns = timeout;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::GateUp, choose_gemm_shape(S, E, H), g1, st);
+    e = launch_grouped_gemm(Epi::GateUp, shape1, g1, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st);
+    if (q_h8)
+        e = launch_requant(h, S, (int)I, s_h, nullptr, q_h8, flag2, list2, counts + 1, st);
+    else
+        e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g2{};
     g2.w = w2_q;
     g2.act16 = q_h16;
+    g2.act8 = q_h8;
     g2.K = (int)I;
     g2.n_cb = (int)(H / 128);
     g2.n_groups = (int)E;
@@ -222,7 +246,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.error = err;
     g2.timeout_ns = timeout;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::ScaleF32, choose_gemm_shape(S, E, I), g2, st);
+    e = launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
@@ -245,9 +269,11 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
         if ((e = cp(dbg->h, h, (size_t)S * I * 4)) != cudaSuccess) return from_cuda(e);
         if ((e = cp(dbg->s_h, s_h, Sb)) != cudaSuccess) return from_cuda(e);
         if ((e = cp(dbg->o, o, (size_t)S * H * 4)) != cudaSuccess) return from_cuda(e);
+        if (q_h8 && (e = cp(dbg->q_h, q_h8, (size_t)S * I)) != cudaSuccess) return from_cuda(e);
         if (dbg->q_x) {
             // token t's quantised row sits in each of its slots; take the first
-            e = launch_f16_rows_to_s8(q_x16, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st);
+            e = q_x8 ? launch_s8_rows_gather(q_x8, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st)
+                     : launch_f16_rows_to_s8(q_x16, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st);
             if (e != cudaSuccess) return from_cuda(e);
         }
     }
@@ -276,6 +302,11 @@ int moe_w8a8_version(void) { return 100; }
 
 uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns) {
     return g_timeout_ns.exchange(ns == 0 ? kDefaultTimeoutNs : ns);
+}
+
+int moe_w8a8_set_gemm_path(int path) {
+    if (path < -1 || path > (int)GemmShape::Skinny) return -2;
+    return g_gemm_path.exchange(path);
 }
 
 moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows, int64_t K, int8_t* w_q,
@@ -336,16 +367,19 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     int32_t* flag = at<int32_t>(workspace, L.flag);
     int32_t* list = at<int32_t>(workspace, L.list);
     uint16_t* q16 = at<uint16_t>(workspace, L.q_x16);
+    const GemmShape shape = pick_gemm_shape(M, 1, K, Epi::ScaleBF16, N, 0);
+    int8_t* q8 = shape == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q16) : nullptr;
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
     if ((e = cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q16, flag, list, counts, st);
+                             q8 ? nullptr : q16, q8, flag, list, counts, st);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
     GemmArgs g{};
     g.w = w_q;
     g.act16 = q16;
+    g.act8 = q8;
     g.K = (int)K;
     g.n_cb = (int)(N / 128);
     g.n_groups = 1;
@@ -362,7 +396,7 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     g.fb_count = counts;
     g.error = at<int>(workspace, L.err);
     g.timeout_ns = g_timeout_ns.load();
-    if ((e = launch_grouped_gemm(Epi::ScaleBF16, choose_gemm_shape(M, 1, K), g, st)) != cudaSuccess)
+    if ((e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st)) != cudaSuccess)
         return from_cuda(e);
     return from_cuda(mark(2, st));
 }

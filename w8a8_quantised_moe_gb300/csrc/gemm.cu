@@ -469,7 +469,8 @@ cudaError_t launch_epi(GemmShape shape, const GemmArgs& args, cudaStream_t st) {
         case GemmShape::Wide: return launch_impl<CfgWide, EPI>(args, st);
         case GemmShape::Mid: return launch_impl<CfgMid, EPI>(args, st);
         case GemmShape::Narrow: return launch_impl<CfgNarrow, EPI>(args, st);
-        case GemmShape::Pair: break;  // dispatched by launch_grouped_gemm
+        case GemmShape::Pair: break;    // dispatched by launch_grouped_gemm
+        case GemmShape::Skinny: break;  // dispatched by launch_grouped_gemm
     }
     return cudaErrorInvalidValue;
 }
@@ -509,6 +510,10 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes
 GemmShape choose_gemm_shape(long rows, long groups, long K) {
     (void)K;
     const long per_group = rows / (groups > 0 ? groups : 1);
+#ifndef MOE_SKINNY_MAX_ROWS  // weight streaming: a few rows per group
+#define MOE_SKINNY_MAX_ROWS 8
+#endif
+    if (per_group <= MOE_SKINNY_MAX_ROWS) return GemmShape::Skinny;
 #ifndef MOE_PAIR_MIN_ROWS  // measured: CTA pairs win from about a hundred rows per group
 #define MOE_PAIR_MIN_ROWS 96
 #endif
@@ -519,6 +524,7 @@ GemmShape choose_gemm_shape(long rows, long groups, long K) {
 
 cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st) {
     if (args.total_rows == 0) return cudaSuccess;
+    if (shape == GemmShape::Skinny) return launch_grouped_gemm_skinny(epi, args, st);
     if (shape == GemmShape::Pair) {
         if (pair_gemm_supported(args)) return launch_grouped_gemm_pair(epi, args, st);
         shape = GemmShape::Wide;

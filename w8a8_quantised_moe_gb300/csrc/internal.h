@@ -32,7 +32,8 @@ enum class GemmShape : int {
     Wide = 0,    // one CTA per tile, 160 activation rows: groups of a few hundred rows
     Mid = 1,     // one CTA per tile, 128 rows: about a hundred rows per group
     Narrow = 2,  // one CTA per tile, 32 rows: a few rows per group (decode)
-    Pair = 3     // CTA pairs, 256 weight rows x 192 activation rows per tile
+    Pair = 3,    // CTA pairs, 256 weight rows x 192 activation rows per tile
+    Skinny = 4   // CUDA-core dp4a, weights streamed once: a few rows per group (decode)
 };
 
 // Largest L1 norm of a quantised activation row for which the fp32
@@ -43,6 +44,7 @@ constexpr int kExactL1 = 1 << 17;
 struct GemmArgs {
     const void* w;           // int8 weights [n_groups * w_rows_per_group][K]
     const void* act16;       // fp16 activation rows [total_rows][K] (exact int8 values)
+    const int8_t* act8;      // int8 activation rows [total_rows][K] (Skinny only; act16 unused there)
     int K;                   // reduction length (multiple of 128)
     int n_cb;                // channel blocks per group
     int n_groups;            // groups (experts); 1 for the linear layer
@@ -89,9 +91,11 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
                           int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st);
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
                         cudaStream_t st);
+// Codes go to q16 (fp16 values, the tensor-core operand) and/or q8 (int8,
+// the Skinny operand); either may be null.
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
-                                 int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16,
+                                 int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
                                  int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
                            int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
@@ -101,11 +105,22 @@ cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t*
                                     cudaStream_t st);
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
                                   int row_stride_of, int8_t* q8, cudaStream_t st);
+// out[r][:] = q8[row_of[r * stride]][:] (row_of == nullptr: identity).
+cudaError_t launch_s8_rows_gather(const int8_t* q8, const int32_t* row_of, int rows, int K, int row_stride_of,
+                                  int8_t* out, cudaStream_t st);
 GemmShape choose_gemm_shape(long rows, long groups, long K);
+// choose_gemm_shape unless a test forced a path (moe_w8a8_set_gemm_path);
+// a forced Skinny falls back to the automatic choice where unsupported.
+GemmShape pick_gemm_shape(long rows, long groups, long K, Epi epi, long w_rows_per_group, long up_offset);
 cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st);
 // CTA-pair kernel (gemm_pair.cu): needs an even number of channel blocks.
 bool pair_gemm_supported(const GemmArgs& args);
 cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st);
+// dp4a kernel (gemm_skinny.cu): needs act8, K a multiple of 128, and weight
+// rows (Scale) or channels (GateUp) per group a multiple of 64 / 32.
+bool skinny_gemm_supported(Epi epi, const GemmArgs& args);
+bool skinny_shape_supported(Epi epi, long K, long w_rows_per_group, long up_offset);
+cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st);
 
 int num_sms();
 

@@ -2,7 +2,8 @@
 //
 //   requant_kernel          per slot row of h: s_h = amax/127,
 //                           q_h = clamp(round(h/s_h)), written as exact fp16
-//                           values (the GEMM operand) and optionally int8.
+//                           values (the tensor-core operand) and/or int8.
+//   s8_rows_gather_kernel   copies int8 rows out by a row map (debug dumps).
 //   combine_kernel          y[t] = bf16_rne(sum_j w[t][j] * o[slot(t, j)]).
 //   quantize_weights_kernel per output channel: s = amax/127, q = round(w/s).
 //   f16_rows_to_s8_kernel   copies quantised rows out as int8 (debug dumps).
@@ -61,10 +62,14 @@ __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ 
         const int a = quant_code(v.x, s), b = quant_code(v.y, s), c = quant_code(v.z, s),
                   d = quant_code(v.w, s);
         l1 += abs(a) + abs(b) + abs(c) + abs(d);
-        uint2 o;
-        o.x = (uint32_t)__half_as_ushort(__int2half_rn(a)) | ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
-        o.y = (uint32_t)__half_as_ushort(__int2half_rn(c)) | ((uint32_t)__half_as_ushort(__int2half_rn(d)) << 16);
-        reinterpret_cast<uint2*>(q16 + (size_t)r * I)[i] = o;
+        if (q16 != nullptr) {
+            uint2 o;
+            o.x = (uint32_t)__half_as_ushort(__int2half_rn(a)) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+            o.y = (uint32_t)__half_as_ushort(__int2half_rn(c)) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(d)) << 16);
+            reinterpret_cast<uint2*>(q16 + (size_t)r * I)[i] = o;
+        }
         if (q8 != nullptr) {
             const uint32_t packed = (uint32_t)(uint8_t)a | ((uint32_t)(uint8_t)b << 8) |
                                     ((uint32_t)(uint8_t)c << 16) | ((uint32_t)(uint8_t)d << 24);
@@ -161,7 +166,24 @@ __global__ void f16_rows_to_s8_kernel(const uint16_t* __restrict__ q16, const in
         q8[(size_t)r * K + i] = (int8_t)__half2int_rn(__ushort_as_half(q16[(size_t)src * K + i]));
 }
 
+__global__ void s8_rows_gather_kernel(const int8_t* __restrict__ q8, const int32_t* __restrict__ row_of, int rows,
+                                      int K, int stride, int8_t* __restrict__ out) {
+    const int r = blockIdx.x;
+    if (r >= rows) return;
+    const int src = row_of ? row_of[(size_t)r * stride] : r;
+    const uint4* s = reinterpret_cast<const uint4*>(q8 + (size_t)src * K);
+    uint4* d = reinterpret_cast<uint4*>(out + (size_t)r * K);
+    for (int i = threadIdx.x; i < K / 16; i += blockDim.x) d[i] = s[i];
+}
+
 }  // namespace
+
+cudaError_t launch_s8_rows_gather(const int8_t* q8, const int32_t* row_of, int rows, int K, int row_stride_of,
+                                  int8_t* out, cudaStream_t st) {
+    if (rows == 0) return cudaSuccess;
+    s8_rows_gather_kernel<<<rows, 256, 0, st>>>(q8, row_of, rows, K, row_stride_of, out);
+    return cudaGetLastError();
+}
 
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
                            int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {

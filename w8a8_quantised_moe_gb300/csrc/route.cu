@@ -98,8 +98,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
-    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int32_t* __restrict__ flags,
-    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
+    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     if (t >= T) return;
@@ -135,7 +135,7 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     for (int i = lane; i < nv; i += 32) {
         const uint4 v = __ldg(row + i);
         const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4];
+        uint32_t out[4], out8[2] = {0u, 0u};
 #pragma unroll
         for (int j = 0; j < 4; ++j) {
             int q0 = 0, q1 = 0;
@@ -148,9 +148,16 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
             l1 += abs(q0) + abs(q1);
             out[j] = (uint32_t)__half_as_ushort(__int2half_rn(q0)) |
                      ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
+            out8[j >> 1] |= ((uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8)) << ((j & 1) * 16);
         }
-        const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
-        for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
+        if (q16 != nullptr) {
+            const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
+            for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
+        }
+        if (q8 != nullptr) {
+            const uint2 ov8 = make_uint2(out8[0], out8[1]);
+            for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = ov8;
+        }
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
@@ -181,11 +188,11 @@ cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int3
 
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
-                                 int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16,
+                                 int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
                                  int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {
     const int grid = (T + 7) / 8;
     permute_quant_kernel<<<grid, 256, 0, st>>>(x, topk_ids, rank, hist, T, H, E, k, slot_of, slot_token,
-                                               s_x, s_slot, q16, flags, fb_list, fb_count);
+                                               s_x, s_slot, q16, q8, flags, fb_list, fb_count);
     return cudaGetLastError();
 }
 

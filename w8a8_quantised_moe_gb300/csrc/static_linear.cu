@@ -71,17 +71,20 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     int32_t* flag = reinterpret_cast<int32_t*>(base + L.flag);
     int32_t* list = reinterpret_cast<int32_t*>(base + L.list);
     uint16_t* q16 = reinterpret_cast<uint16_t*>(base + L.q_x16);
+    const GemmShape shape = pick_gemm_shape(M, 1, K, Epi::ScaleBF16, N, 0);
+    int8_t* q8 = shape == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q16) : nullptr;
 
     // the scratch keeps the previous call's contents: clear the error word
     // and the exact-path counters, which must start at zero
     if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
-    e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x, q16,
-                             flag, list, counts, st);
+    e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
+                             q8 ? nullptr : q16, q8, flag, list, counts, st);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     GemmArgs g{};
     g.w = w_q;
     g.act16 = q16;
+    g.act8 = q8;
     g.K = (int)K;
     g.n_cb = (int)(N / 128);
     g.n_groups = 1;
@@ -98,6 +101,6 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     g.fb_count = counts;
     g.error = err;
     g.timeout_ns = kDefaultTimeoutNs;
-    e = launch_grouped_gemm(Epi::ScaleBF16, choose_gemm_shape(M, 1, K), g, st);
+    e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

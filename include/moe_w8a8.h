@@ -127,6 +127,11 @@ MOE_W8A8_API size_t moe_w8a8_workspace_size(int64_t T, int64_t H, int64_t I, int
  * Errors: MOE_ERR_INVALID_ARG (null/misaligned pointer), _UNSUPPORTED_SHAPE,
  * _WORKSPACE_TOO_SMALL, _CUDA (launch failure).  Device-side timeouts are
  * reported later through moe_w8a8_device_error.
+ * Launches: all on `stream`, no host synchronisation.  Every kernel after
+ * the first is launched with programmatic dependent launch (its set-up
+ * overlaps the previous kernel's tail; it reads nothing before that kernel
+ * has completed); the first serialises with earlier work on the stream as a
+ * plain launch does.  MOE_W8A8_NO_PDL=1 in the environment turns this off.
  * ------------------------------------------------------------------------- */
 MOE_W8A8_API moe_status_t moe_w8a8_forward(const uint16_t* x, const float* router_w, const float* router_bias,
                               const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
@@ -255,8 +260,18 @@ MOE_W8A8_API int moe_w8a8_set_gemm_path(int path);
  * and moe_w8a8_linear records events[0] (quantise), events[1] (GEMM) and
  * events[2] (end).  `events` holds `n` cudaEvent_t created by the caller
  * (n >= 8); NULL turns the hook off.  Returns MOE_ERR_INVALID_ARG if n < 8.
+ * While set, the kernels are launched without programmatic dependent launch,
+ * so that each event pair times one kernel alone.
  * ------------------------------------------------------------------------- */
 MOE_W8A8_API moe_status_t moe_w8a8_set_profile_events(void* const* events, int n);
+
+/* ---------------------------------------------------------------------------
+ * moe_w8a8_launch_count -- measurement hook: the number of CUDA kernels the
+ * library has launched (every entry point, every thread) since it was
+ * loaded.  A caller reads it before and after a region to count the kernels
+ * launched inside it.  Never fails.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API uint64_t moe_w8a8_launch_count(void);
 
 #ifdef __cplusplus
 }

@@ -206,10 +206,12 @@ def test_linear_golden_example():
 @pytest.mark.parametrize("M,N,K,path", [(1, 128, 128, "auto"), (37, 256, 384, "auto"), (300, 384, 1280, "auto"),
                                         (130, 128, 4096, "auto"), (500, 512, 1024, "auto"),
                                         (3, 384, 640, "auto"), (8, 1024, 2048, "auto"), (37, 256, 384, "skinny"),
-                                        (9, 128, 1280, "narrow")])
+                                        (9, 128, 1280, "narrow"), (5000, 128, 256, "auto")])
 def test_linear_bit_exact(M, N, K, path):
     """M <= 8 rows take the dp4a kernel by default; 37 rows forced onto it
-    pass through shared memory in five chunks, the last one ragged."""
+    pass in five chunks of up to 8 rows, the last one ragged; K = 384 and 640
+    end on a half-filled 256-byte weight stage.  5000
+    rows take the warp-per-token quantiser, fewer the CTA-per-token one."""
     cfg = wl.LINEAR
     x = wl.draw_activations(7, cfg.cfg_id, M, K, max(1, K // 100))
     w32 = (np.random.default_rng(M + N + K).standard_normal((N, K)) * 0.02).astype(np.float32)

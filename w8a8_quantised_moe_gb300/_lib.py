@@ -38,6 +38,7 @@ EXPORTS = (
     "moe_w8a8_set_wait_timeout_ns",
     "moe_w8a8_set_gemm_path",
     "moe_w8a8_set_profile_events",
+    "moe_w8a8_launch_count",
     "moe_w8a8_linear_static",
 )
 
@@ -82,6 +83,7 @@ def load(path: str = LIB_PATH):
             "moe_w8a8_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_uint64),
             "moe_w8a8_set_gemm_path": ([i32], i32),
             "moe_w8a8_set_profile_events": ([ctypes.c_void_p, i32], i32),
+            "moe_w8a8_launch_count": ([], ctypes.c_uint64),
             "moe_w8a8_linear_static": ([vp, vp, vp, i64, i64, i64, vp, vp], i32),
         }
         for name, (args, res) in decl.items():

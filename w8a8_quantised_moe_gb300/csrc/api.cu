@@ -11,6 +11,7 @@
 //   6 grouped GEMM 2   down GEMM + scale outer product -> o
 //   7 combine          weighted sum of each token's k slot rows -> y (bf16)
 #include <atomic>
+#include <cstdlib>
 #include <cstring>
 
 #include "moe_w8a8.h"
@@ -35,6 +36,14 @@ cudaError_t mark(int i, cudaStream_t st) {
     return t_events ? cudaEventRecord(t_events[i], st) : cudaSuccess;
 }
 
+bool pdl_env_off() {
+    static const bool off = [] {
+        const char* v = std::getenv("MOE_W8A8_NO_PDL");
+        return v != nullptr && v[0] != '\0' && v[0] != '0';
+    }();
+    return off;
+}
+
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
@@ -51,6 +60,13 @@ bool moe_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
 }
 
 }  // namespace
+
+bool pdl_default() { return t_events == nullptr && !pdl_env_off(); }
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+void count_launch() { g_launches.fetch_add(1, std::memory_order_relaxed); }
 
 GemmShape pick_gemm_shape(long rows, long groups, long K, Epi epi, long w_rows_per_group, long up_offset) {
     const int forced = g_gemm_path.load();
@@ -178,18 +194,19 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     const GemmShape shape2 = pick_gemm_shape(S, E, I, Epi::ScaleF32, H, 0);
     int8_t* q_x8 = shape1 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_x16) : nullptr;
     int8_t* q_h8 = shape2 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_h16) : nullptr;
+    const bool pdl = pdl_default();  // every launch after the first
 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
     e = launch_router(x, router_w, router_bias, (int)T, (int)H, (int)E, (int)k, wsplit, logits, topk_ids,
-                      topk_w, rank, hist, err, timeout, st);
+                      topk_w, rank, hist, err, timeout, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_scan(hist, nchunk, (int)E, offsets, counts, st);
+    e = launch_scan(hist, nchunk, (int)E, offsets, counts, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                             s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st);
+                             s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g1{};
@@ -214,14 +231,14 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.error = err;
     g1.timeout_ns = timeout;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::GateUp, shape1, g1, st);
+    e = launch_grouped_gemm(Epi::GateUp, shape1, g1, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
     if (q_h8)
-        e = launch_requant(h, S, (int)I, s_h, nullptr, q_h8, flag2, list2, counts + 1, st);
+        e = launch_requant(h, S, (int)I, s_h, nullptr, q_h8, flag2, list2, counts + 1, st, pdl);
     else
-        e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st);
+        e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g2{};
@@ -246,11 +263,11 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.error = err;
     g2.timeout_ns = timeout;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st);
+    e = launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_combine(o, slot_of, topk_w, (int)T, (int)H, (int)k, y, st);
+    e = launch_combine(o, slot_of, topk_w, (int)T, (int)H, (int)k, y, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(7, st)) != cudaSuccess) return from_cuda(e);
 
@@ -372,8 +389,9 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
     if ((e = cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return from_cuda(e);
+    // the quantiser follows a memset: a plain launch; the GEMM may overlap its tail
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q8 ? nullptr : q16, q8, flag, list, counts, st);
+                             q8 ? nullptr : q16, q8, flag, list, counts, st, false);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
     GemmArgs g{};
@@ -396,10 +414,12 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     g.fb_count = counts;
     g.error = at<int>(workspace, L.err);
     g.timeout_ns = g_timeout_ns.load();
-    if ((e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st)) != cudaSuccess)
+    if ((e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st, pdl_default())) != cudaSuccess)
         return from_cuda(e);
     return from_cuda(mark(2, st));
 }
+
+uint64_t moe_w8a8_launch_count(void) { return g_launches.load(std::memory_order_relaxed); }
 
 moe_status_t moe_w8a8_set_profile_events(void* const* events, int n) {
     if (events == nullptr) {

@@ -186,6 +186,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_alloc(tmem_slot, C::kTmemAlloc);
         tmem_relinquish();
     }
+    pdl_wait();  // the previous kernel's outputs (offsets, codes, scales) are visible from here
+    pdl_trigger();
     if (warp == 2) {  // tile table: tiles of group g = ceil(rows_g / BN) * n_cb
         int carry = 0;
         for (int base = 0; base < n_groups; base += 32) {
@@ -436,7 +438,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 // ------------------------------------------------------------------ host side
 
 template <class C, int EPI>
-cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st, bool pdl) {
     auto kern = grouped_gemm_kernel<C, EPI>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -459,16 +461,15 @@ cudaError_t launch_impl(const GemmArgs& args, cudaStream_t st) {
     int grid = num_sms();
     if (max_tiles < grid) grid = (int)max_tiles;
     if (grid < 1) grid = 1;
-    kern<<<grid, kThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3(grid), dim3(kThreads), C::kSmem, st, pdl, tw, tb[0], tb[1], tb[2], tb[3], args);
 }
 
 template <int EPI>
-cudaError_t launch_epi(GemmShape shape, const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_epi(GemmShape shape, const GemmArgs& args, cudaStream_t st, bool pdl) {
     switch (shape) {
-        case GemmShape::Wide: return launch_impl<CfgWide, EPI>(args, st);
-        case GemmShape::Mid: return launch_impl<CfgMid, EPI>(args, st);
-        case GemmShape::Narrow: return launch_impl<CfgNarrow, EPI>(args, st);
+        case GemmShape::Wide: return launch_impl<CfgWide, EPI>(args, st, pdl);
+        case GemmShape::Mid: return launch_impl<CfgMid, EPI>(args, st, pdl);
+        case GemmShape::Narrow: return launch_impl<CfgNarrow, EPI>(args, st, pdl);
         case GemmShape::Pair: break;    // dispatched by launch_grouped_gemm
         case GemmShape::Skinny: break;  // dispatched by launch_grouped_gemm
     }
@@ -522,17 +523,17 @@ GemmShape choose_gemm_shape(long rows, long groups, long K) {
     return GemmShape::Narrow;
 }
 
-cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (args.total_rows == 0) return cudaSuccess;
-    if (shape == GemmShape::Skinny) return launch_grouped_gemm_skinny(epi, args, st);
+    if (shape == GemmShape::Skinny) return launch_grouped_gemm_skinny(epi, args, st, pdl);
     if (shape == GemmShape::Pair) {
-        if (pair_gemm_supported(args)) return launch_grouped_gemm_pair(epi, args, st);
+        if (pair_gemm_supported(args)) return launch_grouped_gemm_pair(epi, args, st, pdl);
         shape = GemmShape::Wide;
     }
     switch (epi) {
-        case Epi::GateUp: return launch_epi<0>(shape, args, st);
-        case Epi::ScaleF32: return launch_epi<1>(shape, args, st);
-        case Epi::ScaleBF16: return launch_epi<2>(shape, args, st);
+        case Epi::GateUp: return launch_epi<0>(shape, args, st, pdl);
+        case Epi::ScaleF32: return launch_epi<1>(shape, args, st, pdl);
+        case Epi::ScaleBF16: return launch_epi<2>(shape, args, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -207,6 +207,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         tmem_alloc_pair(tmem_slot, 512);
         tmem_relinquish_pair();
     }
+    pdl_wait();  // the previous kernel's outputs (offsets, codes, scales) are visible from here
+    pdl_trigger();
     if (warp == 2) {  // tile table: pair tiles of group g = ceil(rows_g / BN) * n_cp
         int carry = 0;
         for (int base = 0; base < n_groups; base += 32) {
@@ -531,7 +533,7 @@ int max_pair_clusters(const void* kern, int smem) {
 }
 
 template <class C, int EPI>
-cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st, bool pdl) {
     auto kern = grouped_gemm_pair_kernel<C, EPI>;
     static std::once_flag once;
     static cudaError_t attr_err = cudaSuccess;
@@ -567,20 +569,20 @@ cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st) {
     long n = clusters;
     if (max_tiles < n) n = max_tiles;
     if (n < 1) n = 1;
-    kern<<<(unsigned)(2 * n), kPairThreads, C::kSmem, st>>>(tw, tb[0], tb[1], tb[2], tb[3], tout, args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3((unsigned)(2 * n)), dim3(kPairThreads), C::kSmem, st, pdl, tw, tb[0], tb[1],
+                         tb[2], tb[3], tout, args);
 }
 
 }  // namespace
 
 bool pair_gemm_supported(const GemmArgs& args) { return args.n_cb >= 2 && (args.n_cb & 1) == 0; }
 
-cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (args.total_rows == 0) return cudaSuccess;
     switch (epi) {
-        case Epi::GateUp: return launch_pair_impl<CfgPair, 0>(args, st);
-        case Epi::ScaleF32: return launch_pair_impl<CfgPair, 1>(args, st);
-        case Epi::ScaleBF16: return launch_pair_impl<CfgPair, 2>(args, st);
+        case Epi::GateUp: return launch_pair_impl<CfgPair, 0>(args, st, pdl);
+        case Epi::ScaleF32: return launch_pair_impl<CfgPair, 1>(args, st, pdl);
+        case Epi::ScaleBF16: return launch_pair_impl<CfgPair, 2>(args, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

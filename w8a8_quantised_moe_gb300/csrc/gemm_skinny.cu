@@ -48,32 +48,6 @@ __device__ __forceinline__ int dot16(const uint4 w, const uint4 a, int acc) {
     return __dp4a((int)w.w, (int)a.w, acc);
 }
 
-// Warp reduction of N per-lane values down to STOP values per lane: each
-// step exchanges half of the remaining values with the partner lane (lane ^ M)
-// and keeps the half selected by that lane bit, so that 32 values cost 31
-// shuffles instead of 160.  Afterwards lane l holds the sums of values
-// [b, b + STOP) with b = (l / (32 / (N / STOP))) * STOP.
-template <int N, int M, int STOP>
-struct Butterfly {
-    static __device__ __forceinline__ void run(int* v, int lane) {
-        if constexpr (N > STOP) {
-            const bool up = (lane & M) != 0;
-#pragma unroll
-            for (int i = 0; i < N / 2; ++i) {
-                const int send = up ? v[i] : v[i + N / 2];
-                const int keep = up ? v[i + N / 2] : v[i];
-                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
-            }
-            Butterfly<N / 2, M / 2, STOP>::run(v, lane);
-        } else {
-#pragma unroll
-            for (int m = M; m > 0; m >>= 1)
-#pragma unroll
-                for (int i = 0; i < STOP; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], m);
-        }
-    }
-};
-
 // One warp item: kSkRows weight rows x RC staged activation rows (rc valid),
 // dot products over K, then the epilogue of the valid (row, channel) pairs.
 // GateUp: rows are gate c, gate c+1, up c, up c+1 (c = first channel).
@@ -137,7 +111,7 @@ __device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* 
                 v[(c * RC + r) * 2 + 0] = acc[c][r];
                 v[(c * RC + r) * 2 + 1] = acc[2 + c][r];
             }
-        Butterfly<V, 16, 2>::run(v, lane);
+        WarpButterfly<int, V, 16, 2>::run(v, lane);
         constexpr int kDup = 32 / (V / 2);
         const int p = lane / kDup;  // (c, r)
         const int c = p / RC, r = p % RC;
@@ -160,7 +134,7 @@ __device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* 
         for (int j = 0; j < kSkRows; ++j)
 #pragma unroll
             for (int r = 0; r < RC; ++r) v[j * RC + r] = acc[j][r];
-        Butterfly<V, 16, 1>::run(v, lane);
+        WarpButterfly<int, V, 16, 1>::run(v, lane);
         constexpr int kDup = 32 / V;
         const int p = lane / kDup;
         const int j = p / RC, r = p % RC;
@@ -189,6 +163,8 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
     const int G = args.n_groups;
     const int unit_rows = EPI == (int)Epi::GateUp ? kSkUnitGateUp : kSkUnitScale;
     const int per_group = (EPI == (int)Epi::GateUp ? args.up_offset : args.w_rows_per_group) / unit_rows;
+    pdl_wait();  // the previous kernel's outputs (offsets, codes, scales) are visible from here
+    pdl_trigger();
 
     if (warp == 0) {  // unit table: exclusive prefix of per_group over the non-empty groups
         int carry = 0;
@@ -250,7 +226,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
 }
 
 template <int EPI>
-cudaError_t launch_skinny_impl(const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_skinny_impl(const GemmArgs& args, cudaStream_t st, bool pdl) {
     auto kern = grouped_gemm_skinny_kernel<EPI>;
     const int smem = kSkChunk * args.K;
     static std::mutex mu;
@@ -269,8 +245,7 @@ cudaError_t launch_skinny_impl(const GemmArgs& args, cudaStream_t st) {
     long grid = 2L * num_sms();
     if (max_units < grid) grid = max_units;
     if (grid < 1) grid = 1;
-    kern<<<(unsigned)grid, kSkThreads, smem, st>>>(args);
-    return cudaGetLastError();
+    return launch_kernel(kern, dim3((unsigned)grid), dim3(kSkThreads), (size_t)smem, st, pdl, args);
 }
 
 }  // namespace
@@ -286,12 +261,12 @@ bool skinny_gemm_supported(Epi epi, const GemmArgs& args) {
     return skinny_shape_supported(epi, args.K, args.w_rows_per_group, args.up_offset);
 }
 
-cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st) {
+cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (!skinny_gemm_supported(epi, args)) return cudaErrorInvalidValue;
     switch (epi) {
-        case Epi::GateUp: return launch_skinny_impl<0>(args, st);
-        case Epi::ScaleF32: return launch_skinny_impl<1>(args, st);
-        case Epi::ScaleBF16: return launch_skinny_impl<2>(args, st);
+        case Epi::GateUp: return launch_skinny_impl<0>(args, st, pdl);
+        case Epi::ScaleF32: return launch_skinny_impl<1>(args, st, pdl);
+        case Epi::ScaleBF16: return launch_skinny_impl<2>(args, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

@@ -12,6 +12,7 @@ namespace moe {
 constexpr int kRouterTokens = 32;  // tokens per top-k CTA = tokens per routing chunk
 constexpr int kRouterTargetCtas = 160;  // K slices of the router GEMM fill about this many CTAs
 constexpr int kRouterMaxSlices = 8;     // at most this many K slices (partial logits per token)
+constexpr int kRouterSmallT = 128;      // up to this many tokens the router runs on the CUDA cores
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
@@ -69,6 +70,7 @@ struct GemmArgs {
 // slices of kb_per_slice 64-wide steps.
 struct RouterPlan {
     int E_pad, NB, n_eb, KS, kb_per_slice;
+    bool small;  // CUDA-core router (T <= kRouterSmallT): no weight split, KS slices of kb_per_slice steps
 };
 RouterPlan router_plan(int64_t T, int64_t H, int64_t E);
 
@@ -84,23 +86,93 @@ struct LinLayout {
 };
 LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 
+// ---- programmatic dependent launch ----
+// A kernel launched with pdl = true may start while the previous kernel on
+// the stream is still running: it runs its set-up (barrier init, tensor
+// memory allocation) and then calls pdl_wait(), which returns once the
+// previous grid has completed and its memory is visible, before its first
+// global memory access.  Every kernel of the layer calls pdl_wait() first and
+// pdl_trigger() right after it, so at most two grids overlap: the one
+// finishing and the next one's set-up.  The first kernel of each entry point
+// is launched without it (it then serialises like a plain launch).
+#ifdef __CUDACC__
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Warp reduction of N per-lane values down to STOP values per lane: each
+// step exchanges half of the remaining values with the partner lane (lane ^ M)
+// and keeps the half selected by that lane bit, so that 32 values cost 31
+// shuffles instead of 160.  The order of the additions is fixed, so float
+// sums are deterministic.  Afterwards lane l holds the sums of values
+// [b, b + STOP) with b = (l / (32 / (N / STOP))) * STOP.
+template <typename V, int N, int M, int STOP>
+struct WarpButterfly {
+    static __device__ __forceinline__ void run(V* v, int lane) {
+        if constexpr (N > STOP) {
+            const bool up = (lane & M) != 0;
+#pragma unroll
+            for (int i = 0; i < N / 2; ++i) {
+                const V send = up ? v[i] : v[i + N / 2];
+                const V keep = up ? v[i + N / 2] : v[i];
+                v[i] = keep + __shfl_xor_sync(0xffffffffu, send, M);
+            }
+            WarpButterfly<V, N / 2, M / 2, STOP>::run(v, lane);
+        } else {
+#pragma unroll
+            for (int m = M; m > 0; m >>= 1)
+#pragma unroll
+                for (int i = 0; i < STOP; ++i) v[i] += __shfl_xor_sync(0xffffffffu, v[i], m);
+        }
+    }
+};
+#endif
+
+// Whether the layer's launches use programmatic dependent launch: on unless
+// MOE_W8A8_NO_PDL is set in the environment, and off while per-kernel
+// profiling events are set (events between kernels would time the overlap).
+bool pdl_default();
+
+// Kernels launched through launch_kernel since the library was loaded.
+void count_launch();
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
+                          Args... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = pdl ? 1 : 0;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
+    if (e == cudaSuccess) count_launch();
+    return e;
+}
+
 // ---- launchers (return cudaSuccess or the launch error) ----
+// pdl: launch with programmatic dependent launch (see above).
 // Router: weight split, tensor-core logits (partials per K slice), top-k.
+// The router's first kernel is launched without pdl; its later ones with pdl.
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                           uint16_t* wsplit, float* logits, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st);
+                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st, bool pdl);
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
-                        cudaStream_t st);
+                        cudaStream_t st, bool pdl);
 // Codes go to q16 (fp16 values, the tensor-core operand) and/or q8 (int8,
 // the Skinny operand); either may be null.
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
-                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
+                                 bool pdl);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
-                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st);
+                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st, bool pdl);
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
-                           int H, int k, uint16_t* y, cudaStream_t st);
+                           int H, int k, uint16_t* y, cudaStream_t st, bool pdl);
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
                                     cudaStream_t st);
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
@@ -112,15 +184,15 @@ GemmShape choose_gemm_shape(long rows, long groups, long K);
 // choose_gemm_shape unless a test forced a path (moe_w8a8_set_gemm_path);
 // a forced Skinny falls back to the automatic choice where unsupported.
 GemmShape pick_gemm_shape(long rows, long groups, long K, Epi epi, long w_rows_per_group, long up_offset);
-cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st);
+cudaError_t launch_grouped_gemm(Epi epi, GemmShape shape, const GemmArgs& args, cudaStream_t st, bool pdl);
 // CTA-pair kernel (gemm_pair.cu): needs an even number of channel blocks.
 bool pair_gemm_supported(const GemmArgs& args);
-cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st);
+cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
 // dp4a kernel (gemm_skinny.cu): needs act8, K a multiple of 128, and weight
 // rows (Scale) or channels (GateUp) per group a multiple of 64 / 32.
 bool skinny_gemm_supported(Epi epi, const GemmArgs& args);
 bool skinny_shape_supported(Epi epi, long K, long w_rows_per_group, long up_offset);
-cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st);
+cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
 
 int num_sms();
 

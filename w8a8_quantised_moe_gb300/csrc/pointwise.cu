@@ -45,6 +45,8 @@ __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ 
                                                       int32_t* __restrict__ fb_count) {
     const int lane = threadIdx.x & 31;
     const int r = blockIdx.x * 8 + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
     if (r >= S) return;
     const float4* row = reinterpret_cast<const float4*>(h + (size_t)r * I);
     const int nv = I / 4;
@@ -85,12 +87,90 @@ __global__ void __launch_bounds__(256) requant_kernel(const float* __restrict__ 
     }
 }
 
-// One CTA of 256 threads per token; each thread handles float4 columns.
+// One CTA of 256 threads per row of h, the row held in registers (I <= 256 *
+// 4 * kRqVec): for few rows (decode), where a warp per row leaves most of the
+// GPU idle.  The same outputs as requant_kernel.
+constexpr int kRqVec = 8;
+
+__global__ void __launch_bounds__(256) requant_cta_kernel(const float* __restrict__ h, int S, int I,
+                                                          float* __restrict__ s_h, uint16_t* __restrict__ q16,
+                                                          int8_t* __restrict__ q8, int32_t* __restrict__ flags,
+                                                          int32_t* __restrict__ fb_list,
+                                                          int32_t* __restrict__ fb_count) {
+    __shared__ float red_max[8];
+    __shared__ int red_l1[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int r = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (r >= S) return;
+    const float4* row = reinterpret_cast<const float4*>(h + (size_t)r * I);
+    const int nv = I / 4;
+    float4 v[kRqVec];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kRqVec; ++i) {
+        const int idx = tid + 256 * i;
+        v[i] = idx < nv ? row[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v[i].x)), fmaxf(fabsf(v[i].y), fabsf(v[i].z))), fabsf(v[i].w));
+    }
+    amax = warp_max(amax);
+    if (lane == 0) red_max[warp] = amax;
+    __syncthreads();
+    amax = red_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) s_h[r] = s;
+    int l1 = 0;
+#pragma unroll
+    for (int i = 0; i < kRqVec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        const int a = quant_code(v[i].x, s), b = quant_code(v[i].y, s), c = quant_code(v[i].z, s),
+                  d = quant_code(v[i].w, s);
+        l1 += abs(a) + abs(b) + abs(c) + abs(d);
+        if (q16 != nullptr) {
+            uint2 o;
+            o.x = (uint32_t)__half_as_ushort(__int2half_rn(a)) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(b)) << 16);
+            o.y = (uint32_t)__half_as_ushort(__int2half_rn(c)) |
+                  ((uint32_t)__half_as_ushort(__int2half_rn(d)) << 16);
+            reinterpret_cast<uint2*>(q16 + (size_t)r * I)[idx] = o;
+        }
+        if (q8 != nullptr) {
+            const uint32_t packed = (uint32_t)(uint8_t)a | ((uint32_t)(uint8_t)b << 8) |
+                                    ((uint32_t)(uint8_t)c << 16) | ((uint32_t)(uint8_t)d << 24);
+            reinterpret_cast<uint32_t*>(q8 + (size_t)r * I)[idx] = packed;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (lane == 0) red_l1[warp] = l1;
+    __syncthreads();
+    if (tid == 0) {
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += red_l1[i];
+        const int flagged = tot > kExactL1 ? 1 : 0;
+        flags[r] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = r;
+    }
+}
+
+// Grid (tokens, column splits): a CTA of 256 threads covers every
+// gridDim.y-th block of 256 float4 column groups of one token; each thread
+// reads its k slot rows with independent loads.  Few tokens (decode) split
+// each row over several CTAs to fill the GPU; many tokens use one CTA per
+// token (measured: splitting then costs more than it gains).
+template <int KMAX>  // k <= KMAX (register budget of the loads in flight)
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o,
                                                       const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ topk_w, int T,
                                                       int H, int k, uint16_t* __restrict__ y) {
     const int t = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
     if (t >= T) return;
     __shared__ int32_t slot[kMaxTopK];
     __shared__ float w[kMaxTopK];
@@ -100,15 +180,20 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
     __syncthreads();
     const int nv = H / 4;
-    for (int i = threadIdx.x; i < nv; i += 256) {
+    for (int i = blockIdx.y * 256 + threadIdx.x; i < nv; i += gridDim.y * 256) {
+        float4 v[KMAX];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j)  // independent loads first
+            if (j < k) v[j] = reinterpret_cast<const float4*>(o + (size_t)slot[j] * H)[i];
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
-        for (int j = 0; j < k; ++j) {
-            const float4 v = reinterpret_cast<const float4*>(o + (size_t)slot[j] * H)[i];
+#pragma unroll
+        for (int j = 0; j < KMAX; ++j) {  // then the sum in top-k order
+            if (j >= k) break;
             const float wj = w[j];
-            a0 = __fadd_rn(a0, __fmul_rn(wj, v.x));
-            a1 = __fadd_rn(a1, __fmul_rn(wj, v.y));
-            a2 = __fadd_rn(a2, __fmul_rn(wj, v.z));
-            a3 = __fadd_rn(a3, __fmul_rn(wj, v.w));
+            a0 = __fadd_rn(a0, __fmul_rn(wj, v[j].x));
+            a1 = __fadd_rn(a1, __fmul_rn(wj, v[j].y));
+            a2 = __fadd_rn(a2, __fmul_rn(wj, v[j].z));
+            a3 = __fadd_rn(a3, __fmul_rn(wj, v[j].w));
         }
         uint2 out;
         out.x = (uint32_t)__bfloat16_as_ushort(__float2bfloat16_rn(a0)) |
@@ -186,17 +271,27 @@ cudaError_t launch_s8_rows_gather(const int8_t* q8, const int32_t* row_of, int r
 }
 
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
-                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {
+                           int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st, bool pdl) {
     if (S == 0) return cudaSuccess;
-    requant_kernel<<<(S + 7) / 8, 256, 0, st>>>(h, S, I, s_h, q16, q8, flags, fb_list, fb_count);
-    return cudaGetLastError();
+    // a warp per row fills the GPU from about four CTAs of 8 rows per SM
+    if (S <= 32 * num_sms() && I <= 256 * 4 * kRqVec)
+        return launch_kernel(requant_cta_kernel, dim3(S), dim3(256), 0, st, pdl, h, S, I, s_h, q16, q8, flags,
+                             fb_list, fb_count);
+    return launch_kernel(requant_kernel, dim3((S + 7) / 8), dim3(256), 0, st, pdl, h, S, I, s_h, q16, q8, flags,
+                         fb_list, fb_count);
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
-                           int H, int k, uint16_t* y, cudaStream_t st) {
+                           int H, int k, uint16_t* y, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
-    combine_kernel<<<T, 256, 0, st>>>(o, slot_of, topk_w, T, H, k, y);
-    return cudaGetLastError();
+    const int blocks = (H / 4 + 255) / 256;
+    int split = (4 * num_sms() + T - 1) / T;
+    if (split > blocks) split = blocks;
+    if (split < 1) split = 1;
+    const dim3 grid(T, split), block(256);
+    if (k <= 2) return launch_kernel(combine_kernel<2>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
+    if (k <= 4) return launch_kernel(combine_kernel<4>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
+    return launch_kernel(combine_kernel<kMaxTopK>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
 }
 
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,

@@ -3,7 +3,11 @@
 //   scan_kernel          expert offsets (exclusive prefix over experts) and the
 //                        first slot of every (chunk, expert).
 //   permute_quant_kernel slot of every (token, choice); per-token dynamic INT8
-//                        quantisation of x, scattered into the token's slots.
+//                        quantisation of x, scattered into the token's slots
+//                        (one warp per token).
+//   permute_quant_cta_kernel  the same with one CTA per token, the row held in
+//                        registers: for few tokens (decode), where a warp per
+//                        token leaves most of the GPU idle.
 //
 // Routing pre-processing that reserves a contiguous slot range per expert:
 // "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section 1.3.  Per-token dynamic quantisation q = clamp(round(x/s)),
@@ -36,6 +40,8 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
     const int tid = threadIdx.x;
     const int n = nchunk * E;
     int32_t* tab = use_smem ? tab_s : hist;
+    pdl_wait();
+    pdl_trigger();
     if (tid < 2) counts[tid] = 0;  // rows listed for the exact GEMM path (GEMM1, GEMM2)
     if (use_smem) {
         for (int i = tid; i < n; i += kScanThreads) tab[i] = hist[i];
@@ -102,6 +108,8 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    pdl_wait();
+    pdl_trigger();
     if (t >= T) return;
     int my_slot = t;
     if (topk_ids != nullptr && lane < k) {
@@ -168,10 +176,108 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     }
 }
 
+// One CTA of 256 threads per token; the same outputs as permute_quant_kernel.
+// H <= 16384, so a thread holds at most kPqVec 16-byte vectors of the row.
+constexpr int kPqVec = 8;
+
+__global__ void __launch_bounds__(256) permute_quant_cta_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
+    const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
+    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
+    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    __shared__ float red_max[8];
+    __shared__ int red_l1[8];
+    __shared__ int slots_s[kMaxTopK];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int t = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= T) return;
+    const int nk = (topk_ids != nullptr) ? k : 1;
+    if (tid < nk) {
+        int my_slot = t;
+        if (topk_ids != nullptr) {
+            const int e = topk_ids[(size_t)t * k + tid];
+            my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid];
+            slot_of[(size_t)t * k + tid] = my_slot;
+            slot_token[my_slot] = t;
+        }
+        slots_s[tid] = my_slot;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int nv = H / 8;  // 8 bf16 per 16-byte vector
+    uint4 v[kPqVec];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kPqVec; ++i) {
+        const int idx = tid + 256 * i;
+        v[i] = idx < nv ? __ldg(row + idx) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[j] & 0xffffu)));
+            amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[j] >> 16)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red_max[warp] = amax;
+    __syncthreads();  // also publishes slots_s
+    amax = red_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) s_x[t] = s;
+    if (tid < nk) s_slot[slots_s[tid]] = s;
+    int l1 = 0;
+#pragma unroll
+    for (int i = 0; i < kPqVec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        uint32_t out[4], out8[2] = {0u, 0u};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            int q0 = 0, q1 = 0;
+            if (s != 0.f) {
+                q0 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] & 0xffffu), s));
+                q1 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] >> 16), s));
+                q0 = min(127, max(-128, q0));
+                q1 = min(127, max(-128, q1));
+            }
+            l1 += abs(q0) + abs(q1);
+            out[j] = (uint32_t)__half_as_ushort(__int2half_rn(q0)) |
+                     ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
+            out8[j >> 1] |= ((uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8)) << ((j & 1) * 16);
+        }
+        if (q16 != nullptr) {
+            const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
+            for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots_s[j] * H)[idx] = ov;
+        }
+        if (q8 != nullptr) {
+            const uint2 ov8 = make_uint2(out8[0], out8[1]);
+            for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = ov8;
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (lane == 0) red_l1[warp] = l1;
+    __syncthreads();
+    if (tid < nk) {
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += red_l1[i];
+        const int flagged = tot > kExactL1 ? 1 : 0;
+        flags[slots_s[tid]] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = slots_s[tid];
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
-                        cudaStream_t st) {
+                        cudaStream_t st, bool pdl) {
     const long n = (long)nchunk * E;
     const int use_smem = n <= kScanSmemInts ? 1 : 0;
     const size_t smem = use_smem ? (size_t)n * sizeof(int32_t) : 0;
@@ -182,18 +288,22 @@ cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int3
         if (err != cudaSuccess) return err;
         attr_set = true;
     }
-    scan_kernel<<<1, kScanThreads, smem, st>>>(hist, nchunk, E, offsets, counts, use_smem);
-    return cudaGetLastError();
+    return launch_kernel(scan_kernel, dim3(1), dim3(kScanThreads), smem, st, pdl, hist, nchunk, E, offsets, counts,
+                         use_smem);
 }
 
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
-                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st) {
-    const int grid = (T + 7) / 8;
-    permute_quant_kernel<<<grid, 256, 0, st>>>(x, topk_ids, rank, hist, T, H, E, k, slot_of, slot_token,
-                                               s_x, s_slot, q16, q8, flags, fb_list, fb_count);
-    return cudaGetLastError();
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
+                                 bool pdl) {
+    if (T == 0) return cudaSuccess;
+    // a warp per token fills the GPU from about four CTAs of 8 tokens per SM
+    if (T <= 32 * num_sms() && H <= 256 * 8 * kPqVec)
+        return launch_kernel(permute_quant_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist, T,
+                             H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+    return launch_kernel(permute_quant_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
+                         T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
 }
 
 }  // namespace moe

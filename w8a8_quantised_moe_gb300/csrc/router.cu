@@ -9,6 +9,9 @@
 //                        per K step into one fp32 accumulator.  x is bf16, so
 //                        every product is exact in fp32 and the result is an
 //                        fp32-accumulated dot product, like an FP32 GEMM.
+//   router_small_kernel  whole logits for a few tokens (decode), fp32 FMAs on
+//                        the CUDA cores straight from the fp32 weights: no
+//                        split, and many CTAs for a tiny GEMM.
 //   topk_kernel          logits = sum_ks P[ks] (+ bias) in a fixed order, top-k
 //                        with ties to the lower expert index, softmax over the
 //                        selected logits, and per 32-token chunk the count of
@@ -44,6 +47,8 @@ __global__ void __launch_bounds__(256) router_split_kernel(const float* __restri
     __shared__ float tile[32][33];
     const int h0 = blockIdx.x * 32, e0 = blockIdx.y * 32;
     const int tx = threadIdx.x & 31, ty = threadIdx.x >> 5;  // 8 rows per pass
+    pdl_wait();
+    pdl_trigger();
     for (int r = ty; r < 32; r += 8) {
         const int h = h0 + r, e = e0 + tx;
         tile[r][tx] = (h < H && e < E) ? Wr[(size_t)h * E + e] : 0.f;
@@ -114,6 +119,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
         tmem_alloc(tmem_slot, C::kTmemAlloc);
         tmem_relinquish();
     }
+    pdl_wait();  // the split weights of the previous kernel are visible from here
+    pdl_trigger();
     tc_fence_before();
     __syncthreads();
     tc_fence_after();
@@ -195,6 +202,73 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
 }
 
+// Few tokens (T <= kRouterSmallT): the router GEMM is far too small for the
+// tensor cores to pay (one 128-token tile, a handful of CTAs, a weight split
+// per call), so the CUDA cores compute whole logits directly from the fp32
+// weights.  Grid (expert blocks of 8, token blocks of 8); thread tid owns the
+// 8-wide h chunks tid, tid + 256, ... and accumulates the CTA's 8 x 8
+// (token, expert) dot products over them with fp32 FMAs, loading straight
+// from global memory (one load phase per chunk, no staging).  The 256 partial
+// sums of each logit are then reduced in a fixed order (warp butterfly, then
+// the 8 warps in order), so the logits are deterministic.
+constexpr int kRSmallEB = 8;  // experts per CTA
+constexpr int kRSmallTB = 8;  // tokens per CTA
+
+__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
+                                                           const float* __restrict__ Wr, int T, int H, int E,
+                                                           int E_pad, float* __restrict__ L) {
+    constexpr int NV = kRSmallTB * kRSmallEB;
+    __shared__ float red[8][NV];
+    const int e0 = blockIdx.x * kRSmallEB, t0 = blockIdx.y * kRSmallTB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool vec_w = (E % 4 == 0) && (e0 + kRSmallEB <= E);  // Wr rows 16-byte aligned, 8 experts present
+    pdl_wait();
+    pdl_trigger();
+    float acc[NV];  // [token][expert]
+#pragma unroll
+    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+    for (int c = tid; c < H / 8; c += 256) {
+        const int h = c * 8;
+        uint4 xv[kRSmallTB];
+#pragma unroll
+        for (int t = 0; t < kRSmallTB; ++t)
+            xv[t] = (t0 + t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + h))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            float w[kRSmallEB];
+            const float* wrow = Wr + (size_t)(h + hh) * E + e0;
+            if (vec_w) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(wrow));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(wrow) + 1);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < kRSmallEB; ++e) w[e] = (e0 + e < E) ? __ldg(wrow + e) : 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < kRSmallTB; ++t) {
+                const uint32_t word = (&xv[t].x)[hh >> 1];
+                const float xf = __uint_as_float((hh & 1) ? (word & 0xffff0000u) : (word << 16));
+#pragma unroll
+                for (int e = 0; e < kRSmallEB; ++e) acc[t * kRSmallEB + e] = fmaf(xf, w[e], acc[t * kRSmallEB + e]);
+            }
+        }
+    }
+    WarpButterfly<float, NV, 16, NV / 32>::run(acc, lane);  // lane l: values 2l, 2l + 1
+#pragma unroll
+    for (int i = 0; i < NV / 32; ++i) red[warp][lane * (NV / 32) + i] = acc[i];
+    __syncthreads();
+    if (tid < NV) {
+        float v = red[0][tid];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[w][tid]);
+        const int t = t0 + tid / kRSmallEB, e = e0 + tid % kRSmallEB;
+        if (t < T && e < E_pad) L[(size_t)t * E_pad + e] = v;
+    }
+}
+
 // Thread layout: warp w owns tokens 4w..4w+3 of a 32-token chunk; lane l owns
 // experts l + 32*i for i < EPT.
 template <int EPT>
@@ -206,8 +280,38 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
     __shared__ uint32_t mask[EP];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = blockIdx.x * kRouterTokens;
+    pdl_wait();
+    pdl_trigger();
     for (int i = tid; i < EP; i += 256) mask[i] = 0u;
     __syncthreads();
+    // the logits of the warp's 4 tokens, loaded before any selection so that
+    // the loads of all tokens are in flight together
+    float vv[4][EPT];
+    if (KS == 1) {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int t = t0 + warp * 4 + r, e = lane + 32 * i;
+                vv[r][i] = (t < T && e < E) ? P[(size_t)t * E_pad + e] : -INFINITY;
+            }
+    } else {
+#pragma unroll
+        for (int r = 0; r < 4; ++r)
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int t = t0 + warp * 4 + r, e = lane + 32 * i;
+                float part[kRouterMaxSlices];
+#pragma unroll
+                for (int ks = 0; ks < kRouterMaxSlices; ++ks)  // independent loads first
+                    part[ks] = (ks < KS && t < T && e < E) ? P[((size_t)ks * T + t) * E_pad + e] : 0.f;
+                float acc = part[0];
+#pragma unroll
+                for (int ks = 1; ks < kRouterMaxSlices; ++ks)  // then the sum in slice order
+                    if (ks < KS) acc = __fadd_rn(acc, part[ks]);
+                vv[r][i] = (t < T && e < E) ? acc : -INFINITY;
+            }
+    }
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int t = t0 + warp * 4 + r;
@@ -216,19 +320,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
             const int e = lane + 32 * i;
-            if (e < E) {
-                float part[kRouterMaxSlices];
-#pragma unroll
-                for (int ks = 0; ks < kRouterMaxSlices; ++ks)  // independent loads first
-                    part[ks] = ks < KS ? P[((size_t)ks * T + t) * E_pad + e] : 0.f;
-                float acc = part[0];
-#pragma unroll
-                for (int ks = 1; ks < kRouterMaxSlices; ++ks)  // then the sum in slice order
-                    if (ks < KS) acc = __fadd_rn(acc, part[ks]);
-                v[i] = bias ? __fadd_rn(acc, bias[e]) : acc;
-            } else {
-                v[i] = -INFINITY;
-            }
+            v[i] = (bias && e < E) ? __fadd_rn(vv[r][i], bias[e]) : vv[r][i];
         }
         bool taken[EPT];
 #pragma unroll
@@ -287,7 +379,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
 template <int NB, int NS>
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* wsplit, int T, int H, int E, int E_pad,
                                int n_eb, int KS, int kb_per_slice, float* P, int* error, uint64_t timeout_ns,
-                               cudaStream_t st) {
+                               cudaStream_t st, bool pdl) {
     using C = RCfg<NB, NS>;
     auto kern = router_gemm_kernel<NB, NS>;
     static std::once_flag once;
@@ -304,8 +396,25 @@ cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* wsplit, int T,
                             CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     const dim3 grid((T + kRTM - 1) / kRTM, n_eb, KS);
-    kern<<<grid, kRThreads, C::kSmem, st>>>(tx, tw, T, H, E, E_pad, kb_per_slice, P, error, timeout_ns);
-    return cudaGetLastError();
+    return launch_kernel(kern, grid, dim3(kRThreads), C::kSmem, st, pdl, tx, tw, T, H, E, E_pad, kb_per_slice, P,
+                         error, timeout_ns);
+}
+
+cudaError_t launch_topk(const float* P, const RouterPlan& p, int T, int E, const float* bias, int k,
+                        int32_t* topk_ids, float* topk_w, int32_t* rank, int32_t* hist, cudaStream_t st,
+                        bool pdl) {
+    const dim3 grid((T + kRouterTokens - 1) / kRouterTokens), block(256);
+    if (E <= 32)
+        return launch_kernel(topk_kernel<1>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
+                             topk_w, rank, hist);
+    if (E <= 64)
+        return launch_kernel(topk_kernel<2>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
+                             topk_w, rank, hist);
+    if (E <= 128)
+        return launch_kernel(topk_kernel<4>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
+                             topk_w, rank, hist);
+    return launch_kernel(topk_kernel<8>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
+                         topk_w, rank, hist);
 }
 
 }  // namespace
@@ -315,6 +424,12 @@ RouterPlan router_plan(int64_t T, int64_t H, int64_t E) {
     p.E_pad = E <= 128 ? (int)((E + 15) / 16 * 16) : (int)((E + 127) / 128 * 128);
     p.NB = p.E_pad <= 128 ? p.E_pad : 128;
     p.n_eb = (p.E_pad + p.NB - 1) / p.NB;
+    p.small = T <= kRouterSmallT;
+    if (p.small) {  // CUDA-core router: whole logits, one "slice"
+        p.kb_per_slice = (int)(H / kRBK);
+        p.KS = 1;
+        return p;
+    }
     const int nkb = (int)(H / kRBK);
     const long tiles = (long)((T + kRTM - 1) / kRTM) * p.n_eb;
     int ks = (int)(kRouterTargetCtas / (tiles > 0 ? tiles : 1));
@@ -328,32 +443,31 @@ RouterPlan router_plan(int64_t T, int64_t H, int64_t E) {
 
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                           uint16_t* wsplit, float* P, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st) {
+                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st, bool pdl) {
     const RouterPlan p = router_plan(T, H, E);
-    router_split_kernel<<<dim3((H + 31) / 32, (p.E_pad + 31) / 32), 256, 0, st>>>(Wr, H, E, p.E_pad, wsplit);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e;
+    if (p.small) {
+        e = launch_kernel(router_small_kernel,
+                          dim3((E + kRSmallEB - 1) / kRSmallEB, (T + kRSmallTB - 1) / kRSmallTB), dim3(256), 0,
+                          st, false, x, Wr, T, H, E, p.E_pad, P);
+        if (e != cudaSuccess) return e;
+        return launch_topk(P, p, T, E, bias, k, topk_ids, topk_w, rank, hist, st, pdl);
+    }
+    e = launch_kernel(router_split_kernel, dim3((H + 31) / 32, (p.E_pad + 31) / 32), dim3(256), 0, st, false, Wr, H,
+                      E, p.E_pad, wsplit);
     if (e != cudaSuccess) return e;
     switch (p.NB) {
-        case 16: e = launch_router_gemm<16, 6>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 32: e = launch_router_gemm<32, 6>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 48: e = launch_router_gemm<48, 5>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 64: e = launch_router_gemm<64, 5>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 80: e = launch_router_gemm<80, 4>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 96: e = launch_router_gemm<96, 4>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        case 112: e = launch_router_gemm<112, 3>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
-        default: e = launch_router_gemm<128, 3>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st); break;
+        case 16: e = launch_router_gemm<16, 6>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 32: e = launch_router_gemm<32, 6>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 48: e = launch_router_gemm<48, 5>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 64: e = launch_router_gemm<64, 5>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 80: e = launch_router_gemm<80, 4>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 96: e = launch_router_gemm<96, 4>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        case 112: e = launch_router_gemm<112, 3>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
+        default: e = launch_router_gemm<128, 3>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
     }
     if (e != cudaSuccess) return e;
-    const int grid = (T + kRouterTokens - 1) / kRouterTokens;
-    if (E <= 32)
-        topk_kernel<1><<<grid, 256, 0, st>>>(P, p.KS, T, E, p.E_pad, bias, k, topk_ids, topk_w, rank, hist);
-    else if (E <= 64)
-        topk_kernel<2><<<grid, 256, 0, st>>>(P, p.KS, T, E, p.E_pad, bias, k, topk_ids, topk_w, rank, hist);
-    else if (E <= 128)
-        topk_kernel<4><<<grid, 256, 0, st>>>(P, p.KS, T, E, p.E_pad, bias, k, topk_ids, topk_w, rank, hist);
-    else
-        topk_kernel<8><<<grid, 256, 0, st>>>(P, p.KS, T, E, p.E_pad, bias, k, topk_ids, topk_w, rank, hist);
-    return cudaGetLastError();
+    return launch_topk(P, p, T, E, bias, k, topk_ids, topk_w, rank, hist, st, pdl);
 }
 
 }  // namespace moe

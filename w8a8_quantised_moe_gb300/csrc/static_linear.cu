@@ -79,7 +79,7 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
     if (cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q8 ? nullptr : q16, q8, flag, list, counts, st);
+                             q8 ? nullptr : q16, q8, flag, list, counts, st, false);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     GemmArgs g{};
     g.w = w_q;
@@ -101,6 +101,6 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     g.fb_count = counts;
     g.error = err;
     g.timeout_ns = kDefaultTimeoutNs;
-    e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st);
+    e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st, false);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
 }

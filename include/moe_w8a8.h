@@ -101,8 +101,10 @@ MOE_W8A8_API moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows
  * caller-owned device memory (256-byte aligned) that the forward uses for
  * its intermediates (routing tables, quantised activations, the FP32 gate/up
  * output, its requantised form and the per-slot expert outputs).  Its first
- * 256 bytes hold the sticky device error word read by moe_w8a8_device_error;
- * zero them once before the first call on a new workspace.
+ * 256 bytes hold the sticky device error word read by moe_w8a8_device_error
+ * and a routing counter that every call leaves at zero; zero them once before
+ * the first call on a new workspace.  Calls that share a workspace must not
+ * overlap on the GPU.
  * ------------------------------------------------------------------------- */
 MOE_W8A8_API size_t moe_w8a8_workspace_size(int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k);
 
@@ -246,7 +248,7 @@ MOE_W8A8_API uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns);
  * tensor-core kernel (the 160-row kernel where the channel blocks do not
  * pair up), 4 the CUDA-core dp4a kernel for groups of a few rows (the
  * automatic choice where its shape rule fails: K a multiple of 128 and at
- * most 28672, output channels a multiple of 32 for the gate/up GEMM and of
+ * most 28672, output channels a multiple of 16 for the gate/up GEMM and of
  * 64 otherwise).  Every path computes the same bits.  Returns the previous
  * setting, or -2 (and changes nothing) for a value outside [-1, 4].
  * ------------------------------------------------------------------------- */

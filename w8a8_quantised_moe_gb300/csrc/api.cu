@@ -46,6 +46,10 @@ bool pdl_env_off() {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Byte offset, within the first 256 bytes of the workspace (the error
+// region, zeroed once by the caller), of the small-batch router's ticket.
+constexpr size_t kTicketOffset = 128;
+
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
@@ -198,12 +202,16 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
 
     cudaError_t e;
     if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
+    // the routing ticket of the small-batch router sits in the error region
+    unsigned int* ticket = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(err) + kTicketOffset);
     e = launch_router(x, router_w, router_bias, (int)T, (int)H, (int)E, (int)k, wsplit, logits, topk_ids,
-                      topk_w, rank, hist, err, timeout, st, pdl);
+                      topk_w, rank, hist, offsets, counts, ticket, err, timeout, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_scan(hist, nchunk, (int)E, offsets, counts, st, pdl);
-    if (e != cudaSuccess) return from_cuda(e);
+    if (!router_plan(T, H, E).small) {  // else the router computed the prefix sums
+        e = launch_scan(hist, nchunk, (int)E, offsets, counts, st, pdl);
+        if (e != cudaSuccess) return from_cuda(e);
+    }
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
     e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
                              s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);

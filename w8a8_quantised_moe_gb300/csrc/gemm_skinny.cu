@@ -7,8 +7,11 @@
 // rows, so the tensor cores would idle while the converters of the
 // tensor-core kernels sit on the critical path.  Here every warp streams four
 // weight rows with coalesced 16-byte loads (512 contiguous bytes per row and
-// step), multiplies them against the group's activation rows staged once per
-// work unit in shared memory, and reduces across the warp.  int8 x int8
+// step, several steps per row in flight), multiplies them against the
+// group's activation rows staged once per work unit in shared memory, and
+// reduces across the warp.  (Tried and measured slower: staging the weights
+// through shared memory with TMA tensor boxes or 1-D bulk copies fed by one
+// producer thread; that path delivered 10-16 bytes per clock per SM here.)  int8 x int8
 // products summed in int32 are exact for any K the library accepts
 // (K * 127 * 128 < 2^31), so no row needs the exact path of the tensor-core
 // kernels.
@@ -27,11 +30,16 @@ namespace {
 constexpr int kSkThreads = 256;
 constexpr int kSkWarps = kSkThreads / 32;
 constexpr int kSkRows = 4;   // weight rows per warp item (GateUp: gate and up of two channels)
-constexpr int kSkItems = 2;  // items per warp per work unit
+// Items per warp per work unit: measured on the decode layer, the gate/up
+// GEMM (K = 4096) is fastest with one (117 against 121 us with two: finer
+// units leave less of a tail), the down GEMM (K = 1536) with two (69.6 against
+// 76.7 us: fewer units, less per-unit overhead).
+constexpr int kSkItemsGateUp = 1;
+constexpr int kSkItemsScale = 2;
 constexpr int kSkChunk = 8;  // activation rows staged per pass
 // weight rows (Scale) or channels (GateUp) of one work unit
-constexpr int kSkUnitScale = kSkWarps * kSkItems * kSkRows;       // 64
-constexpr int kSkUnitGateUp = kSkWarps * kSkItems * kSkRows / 2;  // 32
+constexpr int kSkUnitScale = kSkWarps * kSkItemsScale * kSkRows;        // weight rows per unit (64)
+constexpr int kSkUnitGateUp = kSkWarps * kSkItemsGateUp * kSkRows / 2;  // gate/up channel pairs per unit (16)
 
 __device__ __forceinline__ uint4 ld_stream16(const void* p) {
     uint4 v;
@@ -51,7 +59,10 @@ __device__ __forceinline__ int dot16(const uint4 w, const uint4 a, int acc) {
 // One warp item: kSkRows weight rows x RC staged activation rows (rc valid),
 // dot products over K, then the epilogue of the valid (row, channel) pairs.
 // GateUp: rows are gate c, gate c+1, up c, up c+1 (c = first channel).
-template <int EPI, int RC>
+// Each batch issues NB 512-byte steps of every row before using any (NB * 2
+// KB in flight per warp): measured on the down GEMM of the decode layer
+// (K = 1536), 69.6 us against 76 us with two steps per batch.
+template <int EPI, int RC, int NB = (RC <= 4 ? 4 : 2)>
 __device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* __restrict__ act_s, int rc,
                                             int row0, int g, int first, int lane) {
     const int K = args.K;
@@ -70,31 +81,25 @@ __device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* 
 #pragma unroll
         for (int r = 0; r < RC; ++r) acc[j][r] = 0;
 
-    int k = lane * 16;
-    for (; k + 512 < K; k += 1024) {  // two 16-byte steps per row in flight
-        uint4 w0[kSkRows], w1[kSkRows];
+    for (int k0 = lane * 16; k0 < K; k0 += NB * 512) {
+        uint4 wv[NB][kSkRows];
 #pragma unroll
-        for (int j = 0; j < kSkRows; ++j) {
-            w0[j] = ld_stream16(wr[j] + k);
-            w1[j] = ld_stream16(wr[j] + k + 512);
+        for (int b = 0; b < NB; ++b) {  // every load of the batch first
+            const int k = k0 + b * 512;
+#pragma unroll
+            for (int j = 0; j < kSkRows; ++j) wv[b][j] = k < K ? ld_stream16(wr[j] + k) : make_uint4(0u, 0u, 0u, 0u);
         }
 #pragma unroll
-        for (int r = 0; r < RC; ++r) {
-            const uint4 a0 = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k);
-            const uint4 a1 = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k + 512);
+        for (int b = 0; b < NB; ++b) {
+            const int k = k0 + b * 512;
+            if (k < K) {
 #pragma unroll
-            for (int j = 0; j < kSkRows; ++j) acc[j][r] = dot16(w1[j], a1, dot16(w0[j], a0, acc[j][r]));
-        }
-    }
-    if (k < K) {
-        uint4 w0[kSkRows];
+                for (int r = 0; r < RC; ++r) {
+                    const uint4 a = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k);
 #pragma unroll
-        for (int j = 0; j < kSkRows; ++j) w0[j] = ld_stream16(wr[j] + k);
-#pragma unroll
-        for (int r = 0; r < RC; ++r) {
-            const uint4 a0 = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k);
-#pragma unroll
-            for (int j = 0; j < kSkRows; ++j) acc[j][r] = dot16(w0[j], a0, acc[j][r]);
+                    for (int j = 0; j < kSkRows; ++j) acc[j][r] = dot16(wv[b][j], a, acc[j][r]);
+                }
+            }
         }
     }
 
@@ -196,6 +201,10 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
     const int K = args.K;
     const int8_t* act = args.act8;
 
+    // units dealt round-robin: the CTAs running at one time stream one window
+    // of consecutive weight rows (measured faster than a contiguous range of
+    // units per CTA)
+    int staged_row0 = -1;  // first activation row in act_s (row ranges of groups are disjoint)
     for (int u = blockIdx.x; u < total_units; u += gridDim.x) {
         const int g = last_le(unit_start, G, u);
         const int unit = u - unit_start[g];
@@ -203,24 +212,28 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
         for (int row0 = r_begin; row0 < r_end; row0 += kSkChunk) {
             const int rc = min(kSkChunk, r_end - row0);
             const int RC = rc <= 2 ? 2 : rc <= 4 ? 4 : 8;
-            // stage rows row0 .. row0 + rc, zeros up to RC
-            const int n16 = RC * K / 16;
-            const int valid16 = rc * K / 16;
-            const uint4* src = reinterpret_cast<const uint4*>(act + (size_t)row0 * K);
-            uint4* dst = reinterpret_cast<uint4*>(act_s);
-            for (int i = threadIdx.x; i < n16; i += kSkThreads)
-                dst[i] = i < valid16 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
-            __syncthreads();
+            if (row0 != staged_row0) {
+                // stage rows row0 .. row0 + rc, zeros up to RC
+                __syncthreads();  // every warp is done with the previous rows
+                const int n16 = RC * K / 16;
+                const int valid16 = rc * K / 16;
+                const uint4* src = reinterpret_cast<const uint4*>(act + (size_t)row0 * K);
+                uint4* dst = reinterpret_cast<uint4*>(act_s);
+                for (int i = threadIdx.x; i < n16; i += kSkThreads)
+                    dst[i] = i < valid16 ? __ldg(src + i) : make_uint4(0, 0, 0, 0);
+                __syncthreads();
+                staged_row0 = row0;
+            }
 #pragma unroll 1
-            for (int it = 0; it < kSkItems; ++it) {
-                const int item = warp * kSkItems + it;
+            constexpr int kItems = EPI == (int)Epi::GateUp ? kSkItemsGateUp : kSkItemsScale;
+            for (int it = 0; it < kItems; ++it) {
+                const int item = warp * kItems + it;
                 const int first = EPI == (int)Epi::GateUp ? unit * kSkUnitGateUp + item * (kSkRows / 2)
                                                            : unit * kSkUnitScale + item * kSkRows;
                 if (RC == 2) skinny_item<EPI, 2>(args, act_s, rc, row0, g, first, lane);
                 else if (RC == 4) skinny_item<EPI, 4>(args, act_s, rc, row0, g, first, lane);
                 else skinny_item<EPI, 8>(args, act_s, rc, row0, g, first, lane);
             }
-            __syncthreads();
         }
     }
 }

@@ -157,9 +157,13 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // pdl: launch with programmatic dependent launch (see above).
 // Router: weight split, tensor-core logits (partials per K slice), top-k.
 // The router's first kernel is launched without pdl; its later ones with pdl.
+// For T <= kRouterSmallT (RouterPlan::small) one kernel also computes the
+// prefix sums of launch_scan (offsets, chunk bases in hist) and clears
+// counts[0..1]; `ticket` is a zeroed workspace word that it leaves zeroed.
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                           uint16_t* wsplit, float* logits, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st, bool pdl);
+                          int32_t* hist, int32_t* offsets, int32_t* counts, unsigned int* ticket, int* error,
+                          uint64_t timeout_ns, cudaStream_t st, bool pdl);
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
                         cudaStream_t st, bool pdl);
 // Codes go to q16 (fp16 values, the tensor-core operand) and/or q8 (int8,

@@ -202,86 +202,17 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
 }
 
-// Few tokens (T <= kRouterSmallT): the router GEMM is far too small for the
-// tensor cores to pay (one 128-token tile, a handful of CTAs, a weight split
-// per call), so the CUDA cores compute whole logits directly from the fp32
-// weights.  Grid (expert blocks of 8, token blocks of 8); thread tid owns the
-// 8-wide h chunks tid, tid + 256, ... and accumulates the CTA's 8 x 8
-// (token, expert) dot products over them with fp32 FMAs, loading straight
-// from global memory (one load phase per chunk, no staging).  The 256 partial
-// sums of each logit are then reduced in a fixed order (warp butterfly, then
-// the 8 warps in order), so the logits are deterministic.
-constexpr int kRSmallEB = 8;  // experts per CTA
-constexpr int kRSmallTB = 8;  // tokens per CTA
-
-__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
-                                                           const float* __restrict__ Wr, int T, int H, int E,
-                                                           int E_pad, float* __restrict__ L) {
-    constexpr int NV = kRSmallTB * kRSmallEB;
-    __shared__ float red[8][NV];
-    const int e0 = blockIdx.x * kRSmallEB, t0 = blockIdx.y * kRSmallTB;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool vec_w = (E % 4 == 0) && (e0 + kRSmallEB <= E);  // Wr rows 16-byte aligned, 8 experts present
-    pdl_wait();
-    pdl_trigger();
-    float acc[NV];  // [token][expert]
-#pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-    for (int c = tid; c < H / 8; c += 256) {
-        const int h = c * 8;
-        uint4 xv[kRSmallTB];
-#pragma unroll
-        for (int t = 0; t < kRSmallTB; ++t)
-            xv[t] = (t0 + t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + h))
-                                 : make_uint4(0u, 0u, 0u, 0u);
-#pragma unroll
-        for (int hh = 0; hh < 8; ++hh) {
-            float w[kRSmallEB];
-            const float* wrow = Wr + (size_t)(h + hh) * E + e0;
-            if (vec_w) {
-                const float4 a = __ldg(reinterpret_cast<const float4*>(wrow));
-                const float4 b = __ldg(reinterpret_cast<const float4*>(wrow) + 1);
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < kRSmallEB; ++e) w[e] = (e0 + e < E) ? __ldg(wrow + e) : 0.f;
-            }
-#pragma unroll
-            for (int t = 0; t < kRSmallTB; ++t) {
-                const uint32_t word = (&xv[t].x)[hh >> 1];
-                const float xf = __uint_as_float((hh & 1) ? (word & 0xffff0000u) : (word << 16));
-#pragma unroll
-                for (int e = 0; e < kRSmallEB; ++e) acc[t * kRSmallEB + e] = fmaf(xf, w[e], acc[t * kRSmallEB + e]);
-            }
-        }
-    }
-    WarpButterfly<float, NV, 16, NV / 32>::run(acc, lane);  // lane l: values 2l, 2l + 1
-#pragma unroll
-    for (int i = 0; i < NV / 32; ++i) red[warp][lane * (NV / 32) + i] = acc[i];
-    __syncthreads();
-    if (tid < NV) {
-        float v = red[0][tid];
-#pragma unroll
-        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[w][tid]);
-        const int t = t0 + tid / kRSmallEB, e = e0 + tid % kRSmallEB;
-        if (t < T && e < E_pad) L[(size_t)t * E_pad + e] = v;
-    }
-}
-
-// Thread layout: warp w owns tokens 4w..4w+3 of a 32-token chunk; lane l owns
-// experts l + 32*i for i < EPT.
+// One 32-token chunk, by a whole CTA of 256 threads; `mask` is shared memory
+// of 32 * EPT words.  The logits are read with ld.global.cg (from L2): when
+// another CTA of this grid wrote them, no stale L1 line can be hit.
 template <int EPT>
-__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, int KS, int T, int E, int E_pad,
-                                                   const float* __restrict__ bias, int k,
-                                                   int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                   int32_t* __restrict__ rank, int32_t* __restrict__ hist) {
+__device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, int T, int E, int E_pad,
+                                           const float* __restrict__ bias, int k, int chunk,
+                                           int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                           int32_t* __restrict__ rank, int32_t* __restrict__ hist, uint32_t* mask) {
     constexpr int EP = 32 * EPT;
-    __shared__ uint32_t mask[EP];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int t0 = blockIdx.x * kRouterTokens;
-    pdl_wait();
-    pdl_trigger();
+    const int t0 = chunk * kRouterTokens;
     for (int i = tid; i < EP; i += 256) mask[i] = 0u;
     __syncthreads();
     // the logits of the warp's 4 tokens, loaded before any selection so that
@@ -293,7 +224,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
 #pragma unroll
             for (int i = 0; i < EPT; ++i) {
                 const int t = t0 + warp * 4 + r, e = lane + 32 * i;
-                vv[r][i] = (t < T && e < E) ? P[(size_t)t * E_pad + e] : -INFINITY;
+                vv[r][i] = (t < T && e < E) ? __ldcg(P + (size_t)t * E_pad + e) : -INFINITY;
             }
     } else {
 #pragma unroll
@@ -304,7 +235,7 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
                 float part[kRouterMaxSlices];
 #pragma unroll
                 for (int ks = 0; ks < kRouterMaxSlices; ++ks)  // independent loads first
-                    part[ks] = (ks < KS && t < T && e < E) ? P[((size_t)ks * T + t) * E_pad + e] : 0.f;
+                    part[ks] = (ks < KS && t < T && e < E) ? __ldcg(P + ((size_t)ks * T + t) * E_pad + e) : 0.f;
                 float acc = part[0];
 #pragma unroll
                 for (int ks = 1; ks < kRouterMaxSlices; ++ks)  // then the sum in slice order
@@ -373,8 +304,155 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
             rank[(size_t)t * k + (i % k)] = __popc(mask[e] & ((1u << r) - 1u));
         }
     }
-    for (int e = tid; e < E; e += 256) hist[(size_t)blockIdx.x * E + e] = __popc(mask[e]);
+    for (int e = tid; e < E; e += 256) hist[(size_t)chunk * E + e] = __popc(mask[e]);
 }
+
+template <int EPT>
+__global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, int KS, int T, int E, int E_pad,
+                                                   const float* __restrict__ bias, int k,
+                                                   int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                   int32_t* __restrict__ rank, int32_t* __restrict__ hist) {
+    __shared__ uint32_t mask[32 * EPT];
+    pdl_wait();
+    pdl_trigger();
+    topk_chunk<EPT>(P, KS, T, E, E_pad, bias, k, blockIdx.x, topk_ids, topk_w, rank, hist, mask);
+}
+
+// Few tokens (T <= kRouterSmallT): the router GEMM is far too small for the
+// tensor cores to pay (one 128-token tile, a handful of CTAs, a weight split
+// per call), so the CUDA cores compute whole logits directly from the fp32
+// weights.  Grid (expert blocks of 8, token blocks of 8); thread tid owns the
+// 8-wide h chunks tid, tid + 256, ... and accumulates the CTA's 8 x 8
+// (token, expert) dot products over them with fp32 FMAs, loading straight
+// from global memory (one load phase per chunk, no staging).  The 256 partial
+// sums of each logit are then reduced in a fixed order (warp butterfly, then
+// the 8 warps in order), so the logits are deterministic.
+//
+// The CTA that finishes last (an atomic ticket in the workspace, which it
+// resets to zero for the next call) then runs the top-k of every 32-token
+// chunk and the prefix sums that the scan kernel computes for larger T
+// (expert offsets and the first slot of every (chunk, expert)), and clears
+// the exact-path counters: for few tokens these are a few microseconds of
+// work, less than the two launches they replace.  Every CTA publishes its
+// logits with a device-scope fence before taking its ticket, as in the
+// classic threadfence reduction; nothing waits on another CTA.
+constexpr int kRSmallEB = 8;  // experts per CTA
+constexpr int kRSmallTB = 8;  // tokens per CTA
+
+template <int EPT>
+__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
+                                                           const float* __restrict__ Wr, int T, int H, int E,
+                                                           int E_pad, float* __restrict__ L,
+                                                           const float* __restrict__ bias, int k,
+                                                           int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
+                                                           int32_t* __restrict__ rank, int32_t* __restrict__ hist,
+                                                           int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
+                                                           unsigned int* __restrict__ ticket) {
+    constexpr int NV = kRSmallTB * kRSmallEB;
+    __shared__ float red[8][NV];
+    __shared__ uint32_t mask[32 * EPT];
+    __shared__ int32_t wsum[8];
+    __shared__ int is_last;
+    const int e0 = blockIdx.x * kRSmallEB, t0 = blockIdx.y * kRSmallTB;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const bool vec_w = (E % 4 == 0) && (e0 + kRSmallEB <= E);  // Wr rows 16-byte aligned, 8 experts present
+    pdl_wait();
+    pdl_trigger();
+    float acc[NV];  // [token][expert]
+#pragma unroll
+    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
+    for (int c = tid; c < H / 8; c += 256) {
+        const int h = c * 8;
+        uint4 xv[kRSmallTB];
+#pragma unroll
+        for (int t = 0; t < kRSmallTB; ++t)
+            xv[t] = (t0 + t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + h))
+                                 : make_uint4(0u, 0u, 0u, 0u);
+#pragma unroll
+        for (int hh = 0; hh < 8; ++hh) {
+            float w[kRSmallEB];
+            const float* wrow = Wr + (size_t)(h + hh) * E + e0;
+            if (vec_w) {
+                const float4 a = __ldg(reinterpret_cast<const float4*>(wrow));
+                const float4 b = __ldg(reinterpret_cast<const float4*>(wrow) + 1);
+                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
+                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
+            } else {
+#pragma unroll
+                for (int e = 0; e < kRSmallEB; ++e) w[e] = (e0 + e < E) ? __ldg(wrow + e) : 0.f;
+            }
+#pragma unroll
+            for (int t = 0; t < kRSmallTB; ++t) {
+                const uint32_t word = (&xv[t].x)[hh >> 1];
+                const float xf = __uint_as_float((hh & 1) ? (word & 0xffff0000u) : (word << 16));
+#pragma unroll
+                for (int e = 0; e < kRSmallEB; ++e) acc[t * kRSmallEB + e] = fmaf(xf, w[e], acc[t * kRSmallEB + e]);
+            }
+        }
+    }
+    WarpButterfly<float, NV, 16, NV / 32>::run(acc, lane);  // lane l: values 2l, 2l + 1
+#pragma unroll
+    for (int i = 0; i < NV / 32; ++i) red[warp][lane * (NV / 32) + i] = acc[i];
+    __syncthreads();
+    if (tid < NV) {
+        float v = red[0][tid];
+#pragma unroll
+        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[w][tid]);
+        const int t = t0 + tid / kRSmallEB, e = e0 + tid % kRSmallEB;
+        if (t < T && e < E_pad) L[(size_t)t * E_pad + e] = v;
+    }
+
+    // ---- the last CTA: top-k of every chunk, then the prefix sums
+    __threadfence();  // this thread's logits are visible device-wide before the ticket
+    __syncthreads();
+    if (tid == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x * gridDim.y - 1u;
+    __syncthreads();
+    if (!is_last) return;
+    __threadfence();
+    const int nchunk = (T + kRouterTokens - 1) / kRouterTokens;
+    for (int c = 0; c < nchunk; ++c) {
+        topk_chunk<EPT>(L, 1, T, E, E_pad, bias, k, c, topk_ids, topk_w, rank, hist, mask);
+        __syncthreads();  // hist and mask are complete before the next chunk reuses mask
+    }
+    // per expert: first slot of each chunk relative to the expert, and its total
+    int32_t tot = 0;
+    if (tid < E) {
+        for (int c = 0; c < nchunk; ++c) {
+            const int32_t v = hist[(size_t)c * E + tid];
+            hist[(size_t)c * E + tid] = tot;
+            tot += v;
+        }
+    }
+    // exclusive prefix of the totals over the experts (E <= 256 = blockDim)
+    int32_t incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) before += wsum[w];
+        all += wsum[w];
+    }
+    const int32_t excl = before + incl - tot;
+    if (tid < E) {
+        for (int c = 0; c < nchunk; ++c) hist[(size_t)c * E + tid] += excl;
+        offsets[tid] = excl;
+    }
+    if (tid == 0) {
+        offsets[E] = all;
+        counts[0] = 0;  // rows listed for the exact GEMM paths (GEMM1, GEMM2)
+        counts[1] = 0;
+        *ticket = 0u;   // ready for the next call
+    }
+}
+
+// Thread layout: warp w owns tokens 4w..4w+3 of a 32-token chunk; lane l owns
+// experts l + 32*i for i < EPT.
 
 template <int NB, int NS>
 cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* wsplit, int T, int H, int E, int E_pad,
@@ -443,15 +521,23 @@ RouterPlan router_plan(int64_t T, int64_t H, int64_t E) {
 
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                           uint16_t* wsplit, float* P, int32_t* topk_ids, float* topk_w, int32_t* rank,
-                          int32_t* hist, int* error, uint64_t timeout_ns, cudaStream_t st, bool pdl) {
+                          int32_t* hist, int32_t* offsets, int32_t* counts, unsigned int* ticket, int* error,
+                          uint64_t timeout_ns, cudaStream_t st, bool pdl) {
     const RouterPlan p = router_plan(T, H, E);
     cudaError_t e;
-    if (p.small) {
-        e = launch_kernel(router_small_kernel,
-                          dim3((E + kRSmallEB - 1) / kRSmallEB, (T + kRSmallTB - 1) / kRSmallTB), dim3(256), 0,
-                          st, false, x, Wr, T, H, E, p.E_pad, P);
-        if (e != cudaSuccess) return e;
-        return launch_topk(P, p, T, E, bias, k, topk_ids, topk_w, rank, hist, st, pdl);
+    if (p.small) {  // one kernel: logits, top-k and the prefix sums
+        const dim3 grid((E + kRSmallEB - 1) / kRSmallEB, (T + kRSmallTB - 1) / kRSmallTB), block(256);
+        if (E <= 32)
+            return launch_kernel(router_small_kernel<1>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
+                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+        if (E <= 64)
+            return launch_kernel(router_small_kernel<2>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
+                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+        if (E <= 128)
+            return launch_kernel(router_small_kernel<4>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
+                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+        return launch_kernel(router_small_kernel<8>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias, k,
+                             topk_ids, topk_w, rank, hist, offsets, counts, ticket);
     }
     e = launch_kernel(router_split_kernel, dim3((H + 31) / 32, (p.E_pad + 31) / 32), dim3(256), 0, st, false, Wr, H,
                       E, p.E_pad, wsplit);

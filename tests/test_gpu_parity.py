@@ -350,6 +350,40 @@ def _f32_to_bf16_bits(x):
     return r
 
 
+def test_quantiser_every_bf16_value():
+    """Every finite bf16 value v with |v| <= amax, quantised with the scale
+    s = amax / 127 of ten row maxima: about 350 thousand quotients, dense near
+    every half-integer where rint changes (the fast reciprocal path of the
+    kernels decides those more than 2^-14 away, the division the rest).  The
+    codes must equal the oracle's, which divides every element."""
+    H = 4096
+    allbits = np.arange(1 << 16, dtype=np.uint32).astype(np.uint16)
+    allf = bits_to_f32(allbits)
+    finite = np.isfinite(allf)
+    rows = []
+    for amax in (1.0, 0.7, 1.3, 3.1, 100.0, 2e-3, 7e4, 0.0371, 5.9, 117.0):
+        a_bits = _f32_to_bf16_bits(np.array([amax], np.float32))[0]
+        a = bits_to_f32(np.array([a_bits], np.uint16))[0]
+        vals = allbits[finite & (np.abs(allf) <= a)]
+        n = H - 1
+        pad = (-len(vals)) % n
+        vals = np.concatenate([vals, np.zeros(pad, np.uint16)]).reshape(-1, n)
+        rows.append(np.concatenate([np.full((vals.shape[0], 1), a_bits, np.uint16), vals], axis=1))
+    x = np.concatenate(rows)
+    T = x.shape[0]
+    q_ref, s_ref = oracle.quantize_rows_bf16(x)
+    I = 128
+    w13 = np.zeros((1, 2 * I, H), np.int8)
+    w2 = np.zeros((1, H, I), np.int8)
+    args = (bf16_to_dev(x), torch.zeros((H, 1), device="cuda"), None, torch.from_numpy(w13).cuda(),
+            torch.full((1, 2 * I), 1e-3, device="cuda"), torch.from_numpy(w2).cuda(),
+            torch.full((1, H), 1e-3, device="cuda"), 1)
+    _, dev = moe.forward_debug(*args, fields=("s_x", "q_x"))
+    np.testing.assert_array_equal(dev["s_x"].cpu().numpy(), s_ref)
+    np.testing.assert_array_equal(dev["q_x"].cpu().numpy(), q_ref)
+    assert T * H > 300_000
+
+
 def test_quantiser_rounding_boundaries():
     """Activation rows whose quotients x/s sit on or within a few ulp of the
     half-integers where rint changes (ties to even included): the codes must

@@ -6,6 +6,9 @@
 #include <cstdint>
 #include <cuda.h>
 #include <cuda_runtime.h>
+#ifdef __CUDACC__
+#include <cuda_fp16.h>
+#endif
 
 namespace moe {
 
@@ -98,6 +101,47 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 #ifdef __CUDACC__
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+// Asynchronous 16-byte copy global -> shared (the LSU path, no registers),
+// and the wait for every such copy this thread issued.
+__device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_wait_all() {
+    asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+
+// Quantisation code of v for the scale s = amax / 127 of its row:
+// clamp(round_half_even(v / s), -128, 127) with v / s the correctly rounded
+// binary32 quotient; s == 0 gives 0.  (Measured: replacing the division by a
+// product with 1/s plus an exact fallback near the half-integers was slower
+// in the quantisation kernels.)
+__device__ __forceinline__ int quant_code_div(float v, float s) {
+    if (s == 0.f) return 0;
+    return min(127, max(-128, __float2int_rn(__fdiv_rn(v, s))));
+}
+
+// Eight codes (|q| <= 128) as exact fp16 values (four words, element 0 in the
+// low half of word 0) or as int8 (two words, element 0 in the low byte).
+__device__ __forceinline__ uint4 pack_codes_f16(const int (&q)[8]) {
+    uint32_t w[4];
+#pragma unroll
+    for (int j = 0; j < 4; ++j)
+        w[j] = (uint32_t)__half_as_ushort(__int2half_rn(q[2 * j])) |
+               ((uint32_t)__half_as_ushort(__int2half_rn(q[2 * j + 1])) << 16);
+    return make_uint4(w[0], w[1], w[2], w[3]);
+}
+__device__ __forceinline__ uint2 pack_codes_s8(const int (&q)[8]) {
+    uint32_t w[2];
+#pragma unroll
+    for (int j = 0; j < 2; ++j)
+        w[j] = (uint32_t)(uint8_t)q[4 * j] | ((uint32_t)(uint8_t)q[4 * j + 1] << 8) |
+               ((uint32_t)(uint8_t)q[4 * j + 2] << 16) | ((uint32_t)(uint8_t)q[4 * j + 3] << 24);
+    return make_uint2(w[0], w[1]);
+}
 
 // Warp reduction of N per-lane values down to STOP values per lane: each
 // step exchanges half of the remaining values with the partner lane (lane ^ M)

@@ -23,6 +23,30 @@ namespace {
 
 __device__ __forceinline__ float bf16_bits_to_float(uint32_t b) { return __uint_as_float(b << 16); }
 
+// max |v| over 8 bf16 values (one 16-byte vector).
+__device__ __forceinline__ float absmax8(const uint4 v) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        m = fmaxf(m, fabsf(bf16_bits_to_float(w[j] & 0xffffu)));
+        m = fmaxf(m, fabsf(bf16_bits_to_float(w[j] >> 16)));
+    }
+    return m;
+}
+
+// Codes of 8 bf16 values (one 16-byte vector) and their L1 norm, added to l1.
+__device__ __forceinline__ void quant8(const uint4 v, float s, int (&q)[8], int& l1) {
+    const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        q[2 * j] = quant_code_div(bf16_bits_to_float(w[j] & 0xffffu), s);
+        q[2 * j + 1] = quant_code_div(bf16_bits_to_float(w[j] >> 16), s);
+    }
+#pragma unroll
+    for (int j = 0; j < 8; ++j) l1 += abs(q[j]);
+}
+
 // One CTA.  hist [nchunk][E] holds per-chunk counts on entry and the first
 // slot of every (chunk, expert) on exit; offsets[E+1] receives the exclusive
 // prefix of the expert totals.  Thread (e, p) scans rows p*L..p*L+L-1 of
@@ -100,14 +124,20 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
 // the token itself (the dense linear layer).  Besides the codes, every token
 // gets the L1 norm of its code row; rows above kExactL1 are flagged in each
 // of their slots and listed for the exact path of the GEMM.
-__global__ void __launch_bounds__(256) permute_quant_kernel(
+// A warp per token, 8 per CTA: the amax pass and the code pass each read the
+// row (the second mostly from cache).  (Measured at T = 8192: staging rows
+// through shared memory with cp.async, 4 tokens per CTA, was slower: 53
+// against 52 us.)
+constexpr int kPqWarps = 8;
+
+__global__ void __launch_bounds__(32 * kPqWarps) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
     int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
-    const int lane = threadIdx.x & 31;
-    const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    const int t = blockIdx.x * kPqWarps + warp;
     pdl_wait();
     pdl_trigger();
     if (t >= T) return;
@@ -122,48 +152,25 @@ __global__ void __launch_bounds__(256) permute_quant_kernel(
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     const int nv = H / 8;  // 8 bf16 per 16-byte vector
     float amax = 0.f;
-    for (int i = lane; i < nv; i += 32) {
-        const uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[j] & 0xffffu)));
-            amax = fmaxf(amax, fabsf(bf16_bits_to_float(w[j] >> 16)));
-        }
-    }
+    for (int i = lane; i < nv; i += 32) amax = fmaxf(amax, absmax8(__ldg(row + i)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
     const float s = __fdiv_rn(amax, 127.0f);
     if (lane == 0) s_x[t] = s;
-    int slots[kMaxTopK];
+    if (lane < nk) s_slot[my_slot] = s;
+    int slots[kMaxTopK];  // slot j of the token is lane j's my_slot (taken before the lanes diverge)
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
-    if (lane < nk) s_slot[my_slot] = s;
     int l1 = 0;
     for (int i = lane; i < nv; i += 32) {
-        const uint4 v = __ldg(row + i);
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        uint32_t out[4], out8[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int q0 = 0, q1 = 0;
-            if (s != 0.f) {
-                q0 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] & 0xffffu), s));
-                q1 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] >> 16), s));
-                q0 = min(127, max(-128, q0));
-                q1 = min(127, max(-128, q1));
-            }
-            l1 += abs(q0) + abs(q1);
-            out[j] = (uint32_t)__half_as_ushort(__int2half_rn(q0)) |
-                     ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
-            out8[j >> 1] |= ((uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8)) << ((j & 1) * 16);
-        }
+        int q[8];
+        quant8(__ldg(row + i), s, q, l1);
         if (q16 != nullptr) {
-            const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
+            const uint4 ov = pack_codes_f16(q);
             for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
         }
         if (q8 != nullptr) {
-            const uint2 ov8 = make_uint2(out8[0], out8[1]);
+            const uint2 ov8 = pack_codes_s8(q);
             for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = ov8;
         }
     }
@@ -235,28 +242,14 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
     for (int i = 0; i < kPqVec; ++i) {
         const int idx = tid + 256 * i;
         if (idx >= nv) break;
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        uint32_t out[4], out8[2] = {0u, 0u};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            int q0 = 0, q1 = 0;
-            if (s != 0.f) {
-                q0 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] & 0xffffu), s));
-                q1 = __float2int_rn(__fdiv_rn(bf16_bits_to_float(w[j] >> 16), s));
-                q0 = min(127, max(-128, q0));
-                q1 = min(127, max(-128, q1));
-            }
-            l1 += abs(q0) + abs(q1);
-            out[j] = (uint32_t)__half_as_ushort(__int2half_rn(q0)) |
-                     ((uint32_t)__half_as_ushort(__int2half_rn(q1)) << 16);
-            out8[j >> 1] |= ((uint32_t)(uint8_t)q0 | ((uint32_t)(uint8_t)q1 << 8)) << ((j & 1) * 16);
-        }
+        int q[8];
+        quant8(v[i], s, q, l1);
         if (q16 != nullptr) {
-            const uint4 ov = make_uint4(out[0], out[1], out[2], out[3]);
+            const uint4 ov = pack_codes_f16(q);
             for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots_s[j] * H)[idx] = ov;
         }
         if (q8 != nullptr) {
-            const uint2 ov8 = make_uint2(out8[0], out8[1]);
+            const uint2 ov8 = pack_codes_s8(q);
             for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = ov8;
         }
     }
@@ -298,12 +291,17 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
                                  int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
                                  bool pdl) {
     if (T == 0) return cudaSuccess;
-    // a warp per token fills the GPU from about four CTAs of 8 tokens per SM
-    if (T <= 32 * num_sms() && H <= 256 * 8 * kPqVec)
+    // few tokens: one CTA per token (measured at T = 8192: a warp per token
+    // takes 52 us, a CTA per token 96 us; at T = 64, 8 us against 17 us)
+#ifndef MOE_PQ_CTA_TOKENS_PER_SM
+#define MOE_PQ_CTA_TOKENS_PER_SM 8
+#endif
+    if ((long)T <= (long)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kPqVec)
         return launch_kernel(permute_quant_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist, T,
                              H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
-    return launch_kernel(permute_quant_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
-                         T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+    return launch_kernel(permute_quant_kernel, dim3((T + kPqWarps - 1) / kPqWarps), dim3(32 * kPqWarps), 0, st, pdl,
+                         x, topk_ids, rank, hist, T, H, E, k,
+                         slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
 }
 
 }  // namespace moe

@@ -298,7 +298,7 @@ def layer_roofline_us(cfg, offsets, peaks):
     return max(t_b, t_f) * 1e6, ("hbm" if t_b >= t_f else "tensor"), b, f
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_common.cuh", "ptx.cuh")
+GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_common.cuh", "ptx.cuh", "internal.h")
 
 
 def gemm_source_sha():

@@ -52,7 +52,10 @@ namespace moe {
 namespace {
 
 constexpr int kPairBK = 128;  // K per stage
-constexpr int kPairND = 2;    // accumulator buffers
+#ifndef MOE_P_ND
+#define MOE_P_ND 2
+#endif
+constexpr int kPairND = MOE_P_ND;  // accumulator buffers
 
 // MMA-issuing threads in the even CTA.  Measured: two beat one by 8-10% on
 // the expert GEMMs.  Builds with three or four issuers (13-14 warps) failed

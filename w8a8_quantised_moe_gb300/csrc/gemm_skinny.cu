@@ -11,8 +11,8 @@
 // group's activation rows staged once per work unit in shared memory, and
 // reduces across the warp.  (Tried and measured slower: staging the weights
 // through shared memory with TMA tensor boxes or 1-D bulk copies fed by one
-// producer thread; that path delivered 10-16 bytes per clock per SM here.)  int8 x int8
-// products summed in int32 are exact for any K the library accepts
+// producer thread; that path delivered 10-16 bytes per clock per SM here.)
+// int8 x int8 products summed in int32 are exact for any K the library accepts
 // (K * 127 * 128 < 2^31), so no row needs the exact path of the tensor-core
 // kernels.
 //

@@ -554,3 +554,239 @@ done:
     free(q_x); free(s_x); free(acc);
     return rc;
 }
+
+/* ==== FP8 (E4M3) variant of the layer =====================================
+ * "DeepSeek V4 950 FP8 inference on H100" (lpnh.cn): weights and activations
+ * of the forward pass in E4M3 (4 exponent bits, 3 mantissa bits, largest
+ * finite magnitude 448; section 2.1), FP8 operands with an FP32 accumulator
+ * whose result is re-quantised to FP8 for the next operator (section 2.3),
+ * one scale per weight output channel and per token for the activations,
+ * computed dynamically (section 2.4), weight scales from the absolute
+ * maximum (section 3.1).  The rest of the layer (router, slots, SiLU gate,
+ * combine) is the INT8 layer's.
+ *
+ * Readings where the page is silent (each is listed in the design notes):
+ *   scale        -> s = amax / 448.0f, one correctly rounded binary32 division
+ *   code         -> the E4M3 value nearest to the binary32 quotient x / s,
+ *                   ties to the code with an even mantissa, magnitudes above
+ *                   448 saturated to 448 (the quotient exceeds 448 only through
+ *                   its own rounding); the sign of a zero quotient is kept
+ *   amax == 0    -> s = 0 and every code +0
+ *   accumulator  -> the exact sum of the exact E4M3 products, rounded once to
+ *                   binary32 (the best binary32 value of the FP32 accumulator's
+ *                   dot product).  Every E4M3 value is an integer multiple of
+ *                   2^-9 below 2^18 * 2^-9 in magnitude, so every product is an
+ *                   integer multiple of 2^-18 below 2^18 in magnitude and the
+ *                   binary64 sum of K < 2^17 of them is exact.
+ */
+
+/* Value of an E4M3 code: sign bit 7, exponent bits 6..3 (bias 7), mantissa
+ * bits 2..0; exponent 0 is subnormal (m * 2^-9); S.1111.111 is NaN and there
+ * is no infinity. */
+static float e4m3_value(uint8_t b) {
+    const int e = (b >> 3) & 15, m = b & 7;
+    float v;
+    if (e == 15 && m == 7) return NAN;
+    if (e == 0) v = ldexpf((float)m, -9);
+    else v = ldexpf((float)(8 + m), e - 10);
+    return (b & 0x80) ? -v : v;
+}
+
+/* Nearest E4M3 code (see the readings above).  The non-negative finite
+ * codes 0x00..0x7E are increasing in value, so the nearest one is found by
+ * bisection and a comparison with its two neighbours. */
+static uint8_t e4m3_code(float v) {
+    const uint8_t sign = signbit(v) ? 0x80 : 0x00;
+    const float a = fabsf(v);
+    if (a >= 448.0f) return (uint8_t)(sign | 0x7E);
+    int lo = 0, hi = 0x7E;  /* invariant: value(lo) <= a < value(hi) */
+    while (hi - lo > 1) {
+        const int mid = (lo + hi) / 2;
+        if (e4m3_value((uint8_t)mid) <= a) lo = mid; else hi = mid;
+    }
+    const double dlo = (double)a - (double)e4m3_value((uint8_t)lo);
+    const double dhi = (double)e4m3_value((uint8_t)hi) - (double)a;
+    int c;
+    if (dlo < dhi) c = lo;
+    else if (dhi < dlo) c = hi;
+    else c = (lo % 2 == 0) ? lo : hi;  /* tie: the even mantissa */
+    return (uint8_t)(sign | c);
+}
+
+int oracle_e4m3_encode(const float* in, int64_t n, uint8_t* out) {
+    if (n < 0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_code(in[i]);
+    return ORACLE_OK;
+}
+
+int oracle_e4m3_decode(const uint8_t* in, int64_t n, float* out) {
+    if (n < 0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) out[i] = e4m3_value(in[i]);
+    return ORACLE_OK;
+}
+
+/* One scale per row: amax = max_k |x[k]|, s = amax / 448, q[k] = code(x[k] / s). */
+static void quantize_row_fp8(const float* x, int64_t K, uint8_t* q, float* s_out) {
+    float amax = 0.0f;
+    for (int64_t k = 0; k < K; ++k) {
+        float a = fabsf(x[k]);
+        if (a > amax) amax = a;
+    }
+    float s = amax / 448.0f;
+    *s_out = s;
+    for (int64_t k = 0; k < K; ++k) q[k] = (s == 0.0f) ? 0 : e4m3_code(x[k] / s);
+}
+
+int oracle_quantize_rows_fp8(const float* x, int64_t rows, int64_t K, uint8_t* q, float* s) {
+    if (rows < 0 || K <= 0) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) quantize_row_fp8(x + r * K, K, q + r * K, s + r);
+    return ORACLE_OK;
+}
+
+int oracle_quantize_rows_bf16_fp8(const uint16_t* x, int64_t rows, int64_t K, uint8_t* q, float* s) {
+    if (rows < 0 || K <= 0) return ORACLE_ERR_ARG;
+    int err = 0;
+#pragma omp parallel
+    {
+        float* row = (float*)malloc((size_t)K * sizeof(float));
+        if (!row) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!row) continue;
+            for (int64_t k = 0; k < K; ++k) row[k] = bf16_to_f32(x[r * K + k]);
+            quantize_row_fp8(row, K, q + r * K, s + r);
+        }
+        free(row);
+    }
+    return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* acc[m][n] = binary32( sum_k value(a[m][k]) * value(b[n][k]) ), the sum exact
+ * in binary64 (K < 2^17); a [M][K], b [N][K] (both K-contiguous). */
+int oracle_gemm_fp8(const uint8_t* a, const uint8_t* b, int64_t M, int64_t N, int64_t K, float* acc) {
+    if (M < 0 || N < 0 || K <= 0 || K >= (1 << 17)) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t m = 0; m < M; ++m) {
+        for (int64_t n = 0; n < N; ++n) {
+            double sum = 0.0;
+            for (int64_t k = 0; k < K; ++k)
+                sum += (double)e4m3_value(a[m * K + k]) * (double)e4m3_value(b[n * K + k]);
+            acc[m * N + n] = (float)sum;
+        }
+    }
+    return ORACLE_OK;
+}
+
+/* The epilogues of the FP8 layer: those of the INT8 layer on a binary32
+ * accumulator, value = (acc * s_act) * s_w. */
+static float dequant_f(float acc, float s_act, float s_w) {
+    float v = acc * s_act;
+    v = v * s_w;
+    return v;
+}
+
+int oracle_epilogue_gate_up_f32(const float* acc1, const float* s_act, const float* s_w13, int64_t S,
+                                int64_t I, float* h) {
+    if (S < 0 || I <= 0) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < S; ++s) {
+        for (int64_t n = 0; n < I; ++n) {
+            float g = dequant_f(acc1[s * 2 * I + n], s_act[s], s_w13[n]);
+            float u = dequant_f(acc1[s * 2 * I + I + n], s_act[s], s_w13[I + n]);
+            h[s * I + n] = silu(g) * u;
+        }
+    }
+    return ORACLE_OK;
+}
+
+int oracle_epilogue_scale_f32(const float* acc, const float* s_act, const float* s_w, int64_t S, int64_t N,
+                              float* out) {
+    if (S < 0 || N <= 0) return ORACLE_ERR_ARG;
+#pragma omp parallel for schedule(static)
+    for (int64_t s = 0; s < S; ++s)
+        for (int64_t c = 0; c < N; ++c) out[s * N + c] = dequant_f(acc[s * N + c], s_act[s], s_w[c]);
+    return ORACLE_OK;
+}
+
+/* The whole FP8 layer, sparse path: the INT8 layer's steps with the E4M3
+ * quantisers and GEMMs.  w13_q E4M3 [E][2I][H], w2_q E4M3 [E][H][I]; the dump
+ * fields q_x and q_h receive E4M3 codes, acc1 and acc2 binary32 values (as
+ * their bit patterns in the int32 fields). */
+int oracle_moe_forward_fp8(const uint16_t* x, const float* Wr, const float* bias, const uint8_t* w13_q,
+                           const float* s_w13, const uint8_t* w2_q, const float* s_w2, int64_t T, int64_t H,
+                           int64_t I, int64_t E, int64_t k, uint16_t* y, const oracle_dump_t* dump) {
+    if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORACLE_ERR_ARG;
+    const int64_t S = T * k;
+    int rc = ORACLE_OK;
+    int32_t* topk_ids = (int32_t*)xmalloc((size_t)S * 4);
+    float* topk_w = (float*)xmalloc((size_t)S * 4);
+    int32_t* counts = (int32_t*)xmalloc((size_t)E * 4);
+    int32_t* offsets = (int32_t*)xmalloc((size_t)(E + 1) * 4);
+    int32_t* slot_of = (int32_t*)xmalloc((size_t)S * 4);
+    int32_t* slot_token = (int32_t*)xmalloc((size_t)S * 4);
+    float* s_x = (float*)xmalloc((size_t)T * 4);
+    uint8_t* q_x = (uint8_t*)xmalloc((size_t)(T * H));
+    float* s_slot = (float*)xmalloc((size_t)S * 4);
+    uint8_t* q_slot = (uint8_t*)xmalloc((size_t)(S * H));
+    float* acc1 = (float*)xmalloc((size_t)(S * 2 * I) * 4);
+    float* h = (float*)xmalloc((size_t)(S * I) * 4);
+    float* s_h = (float*)xmalloc((size_t)S * 4);
+    uint8_t* q_h = (uint8_t*)xmalloc((size_t)(S * I));
+    float* acc2 = (float*)xmalloc((size_t)(S * H) * 4);
+    float* o = (float*)xmalloc((size_t)(S * H) * 4);
+    if (!topk_ids || !topk_w || !counts || !offsets || !slot_of || !slot_token || !s_x || !q_x ||
+        !s_slot || !q_slot || !acc1 || !h || !s_h || !q_h || !acc2 || !o) {
+        rc = ORACLE_ERR_NOMEM;
+        goto done;
+    }
+    rc = oracle_router(x, Wr, bias, T, H, E, k, topk_ids, topk_w, NULL);
+    if (rc) goto done;
+    rc = oracle_permute(topk_ids, T, E, k, counts, offsets, slot_of, slot_token);
+    if (rc) goto done;
+    rc = oracle_quantize_rows_bf16_fp8(x, T, H, q_x, s_x);
+    if (rc) goto done;
+    for (int64_t s = 0; s < S; ++s) {  /* each slot holds its token's codes and scale */
+        memcpy(q_slot + s * H, q_x + (int64_t)slot_token[s] * H, (size_t)H);
+        s_slot[s] = s_x[slot_token[s]];
+    }
+    for (int64_t e = 0; e < E; ++e) {
+        int64_t s0 = offsets[e], n = offsets[e + 1] - offsets[e];
+        if (n == 0) continue;
+        rc = oracle_gemm_fp8(q_slot + s0 * H, w13_q + e * 2 * I * H, n, 2 * I, H, acc1 + s0 * 2 * I);
+        if (rc) goto done;
+        rc = oracle_epilogue_gate_up_f32(acc1 + s0 * 2 * I, s_slot + s0, s_w13 + e * 2 * I, n, I, h + s0 * I);
+        if (rc) goto done;
+        rc = oracle_quantize_rows_fp8(h + s0 * I, n, I, q_h + s0 * I, s_h + s0);
+        if (rc) goto done;
+        rc = oracle_gemm_fp8(q_h + s0 * I, w2_q + e * H * I, n, H, I, acc2 + s0 * H);
+        if (rc) goto done;
+        rc = oracle_epilogue_scale_f32(acc2 + s0 * H, s_h + s0, s_w2 + e * H, n, H, o + s0 * H);
+        if (rc) goto done;
+    }
+    rc = oracle_combine(o, slot_of, topk_w, T, k, H, y);
+    if (rc) goto done;
+    if (dump) {
+        if (dump->topk_ids) memcpy(dump->topk_ids, topk_ids, (size_t)S * 4);
+        if (dump->topk_w) memcpy(dump->topk_w, topk_w, (size_t)S * 4);
+        if (dump->offsets) memcpy(dump->offsets, offsets, (size_t)(E + 1) * 4);
+        if (dump->slot_of) memcpy(dump->slot_of, slot_of, (size_t)S * 4);
+        if (dump->slot_token) memcpy(dump->slot_token, slot_token, (size_t)S * 4);
+        if (dump->s_x) memcpy(dump->s_x, s_x, (size_t)T * 4);
+        if (dump->q_x) memcpy(dump->q_x, q_x, (size_t)(T * H));
+        if (dump->acc1) memcpy(dump->acc1, acc1, (size_t)(S * 2 * I) * 4);
+        if (dump->h) memcpy(dump->h, h, (size_t)(S * I) * 4);
+        if (dump->s_h) memcpy(dump->s_h, s_h, (size_t)S * 4);
+        if (dump->q_h) memcpy(dump->q_h, q_h, (size_t)(S * I));
+        if (dump->acc2) memcpy(dump->acc2, acc2, (size_t)(S * H) * 4);
+        if (dump->o) memcpy(dump->o, o, (size_t)(S * H) * 4);
+    }
+done:
+    free(topk_ids); free(topk_w); free(counts); free(offsets); free(slot_of); free(slot_token);
+    free(s_x); free(q_x); free(s_slot); free(q_slot); free(acc1); free(h); free(s_h); free(q_h);
+    free(acc2); free(o);
+    return rc;
+}

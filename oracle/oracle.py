@@ -71,6 +71,15 @@ def open_library(path: str):
         "oracle_linear": [vp, vp, vp, i64, i64, i64, vp, vp, vp, vp],
         "oracle_bf16_to_f32": [vp, i64, vp],
         "oracle_f32_to_bf16": [vp, i64, vp],
+        "oracle_e4m3_encode": [vp, i64, vp],
+        "oracle_e4m3_decode": [vp, i64, vp],
+        "oracle_quantize_rows_fp8": [vp, i64, i64, vp, vp],
+        "oracle_quantize_rows_bf16_fp8": [vp, i64, i64, vp, vp],
+        "oracle_gemm_fp8": [vp, vp, i64, i64, i64, vp],
+        "oracle_epilogue_gate_up_f32": [vp, vp, vp, i64, i64, vp],
+        "oracle_epilogue_scale_f32": [vp, vp, vp, i64, i64, vp],
+        "oracle_moe_forward_fp8": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp,
+                                   ctypes.POINTER(_Dump)],
         "oracle_num_threads": [],
         "oracle_set_num_threads": [ctypes.c_int],
     }
@@ -311,3 +320,99 @@ def linear(x_bits, w_q, s_w, want_intermediates=False):
     if want_intermediates:
         return y, {"q_x": q_x, "s_x": s_x, "acc": acc}
     return y
+
+
+# ---- FP8 (E4M3) variant (oracle.c, "FP8 (E4M3) variant of the layer") ----
+
+def e4m3_encode(x: np.ndarray) -> np.ndarray:
+    """Nearest E4M3 code of each binary32 value (ties to even, saturating)."""
+    x = _c(x, np.float32)
+    out = np.empty(x.shape, np.uint8)
+    _check(_load().oracle_e4m3_encode(_p(x), x.size, _p(out)), "e4m3_encode")
+    return out
+
+
+def e4m3_decode(codes: np.ndarray) -> np.ndarray:
+    codes = _c(codes, np.uint8)
+    out = np.empty(codes.shape, np.float32)
+    _check(_load().oracle_e4m3_decode(_p(codes), codes.size, _p(out)), "e4m3_decode")
+    return out
+
+
+def quantize_rows_fp8(x: np.ndarray):
+    """Per-row E4M3 quantisation of a 2-D fp32 array -> (codes uint8, s fp32)."""
+    x = _c(x, np.float32)
+    rows, K = x.shape
+    q = np.empty((rows, K), np.uint8)
+    s = np.empty(rows, np.float32)
+    _check(_load().oracle_quantize_rows_fp8(_p(x), rows, K, _p(q), _p(s)), "quantize_rows_fp8")
+    return q, s
+
+
+def quantize_rows_bf16_fp8(x_bits: np.ndarray):
+    x_bits = _c(x_bits, np.uint16)
+    rows, K = x_bits.shape
+    q = np.empty((rows, K), np.uint8)
+    s = np.empty(rows, np.float32)
+    _check(_load().oracle_quantize_rows_bf16_fp8(_p(x_bits), rows, K, _p(q), _p(s)), "quantize_rows_bf16_fp8")
+    return q, s
+
+
+def gemm_fp8(a, b):
+    """acc[m][n] = binary32(exact sum_k value(a[m][k]) * value(b[n][k]))."""
+    a = _c(a, np.uint8)
+    b = _c(b, np.uint8)
+    M, K = a.shape
+    N = b.shape[0]
+    assert b.shape[1] == K
+    acc = np.empty((M, N), np.float32)
+    _check(_load().oracle_gemm_fp8(_p(a), _p(b), M, N, K, _p(acc)), "gemm_fp8")
+    return acc
+
+
+def epilogue_gate_up_f32(acc1, s_act, s_w13):
+    acc1 = _c(acc1, np.float32)
+    S, two_i = acc1.shape
+    I = two_i // 2
+    h = np.empty((S, I), np.float32)
+    _check(_load().oracle_epilogue_gate_up_f32(_p(acc1), _p(_c(s_act, np.float32)), _p(_c(s_w13, np.float32)),
+                                               S, I, _p(h)), "epilogue_gate_up_f32")
+    return h
+
+
+def epilogue_scale_f32(acc, s_act, s_w):
+    acc = _c(acc, np.float32)
+    S, N = acc.shape
+    out = np.empty((S, N), np.float32)
+    _check(_load().oracle_epilogue_scale_f32(_p(acc), _p(_c(s_act, np.float32)), _p(_c(s_w, np.float32)),
+                                             S, N, _p(out)), "epilogue_scale_f32")
+    return out
+
+
+_DUMP_SPEC_FP8 = dict(_DUMP_SPEC, q_x=(np.uint8, _DUMP_SPEC["q_x"][1]), q_h=(np.uint8, _DUMP_SPEC["q_h"][1]),
+                      acc1=(np.float32, _DUMP_SPEC["acc1"][1]), acc2=(np.float32, _DUMP_SPEC["acc2"][1]))
+
+
+def moe_forward_fp8(x_bits, Wr, bias, w13_q, s_w13, w2_q, s_w2, k, dump=()):
+    """FP8 layer forward (E4M3 codes as uint8).  Returns y (bf16 bits) and,
+    if ``dump`` names intermediates, a dict of them (q_x, q_h: E4M3 codes;
+    acc1, acc2: binary32)."""
+    x_bits = _c(x_bits, np.uint16)
+    T, H = x_bits.shape
+    w13_q = _c(w13_q, np.uint8)
+    E, two_i, _ = w13_q.shape
+    I = two_i // 2
+    Wr = _c(Wr, np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    y = np.empty((T, H), np.uint16)
+    out = {}
+    d = _Dump()
+    for name in dump:
+        dt, shape = _DUMP_SPEC_FP8[name]
+        arr = np.empty(shape(T, H, I, E, k), dt)
+        out[name] = arr
+        setattr(d, name, arr.ctypes.data)
+    _check(_load().oracle_moe_forward_fp8(_p(x_bits), _p(Wr), _p(b), _p(w13_q), _p(_c(s_w13, np.float32)),
+                                          _p(_c(w2_q, np.uint8)), _p(_c(s_w2, np.float32)), T, H, I, E, k,
+                                          _p(y), ctypes.byref(d)), "moe_forward_fp8")
+    return (y, out) if dump else y

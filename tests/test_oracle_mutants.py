@@ -6,6 +6,7 @@ import pytest
 
 import oracle
 import test_oracle as pins
+import test_oracle_fp8 as pins8
 from w8a8_quantised_moe_gb300 import workloads as wl
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
@@ -32,12 +33,26 @@ MUTANTS = [
     ("combine_weights_reversed", "float term = topk_w[t * k + j] * o[(int64_t)slot_of[t * k + j] * H + c];",
      "float term = topk_w[t * k + (k - 1 - j)] * o[(int64_t)slot_of[t * k + j] * H + c];",
      [pins.test_combine_golden]),
-    ("dequant_drops_weight_scale", "    v = v * s_w;\n", "",
+    ("dequant_drops_weight_scale", "    v = v * s_act;\n    v = v * s_w;\n", "    v = v * s_act;\n",
      [pins.test_linear_golden_2x4]),
-    ("moe_wrong_expert_w2", "w2_q + e * H * I, n, H, I, acc2 + s0 * H", "w2_q, n, H, I, acc2 + s0 * H",
+    ("moe_wrong_expert_w2", "oracle_gemm_s8(q_h + s0 * I, w2_q + e * H * I", "oracle_gemm_s8(q_h + s0 * I, w2_q",
      [lambda: pins.test_sparse_equals_brute_force_dense(wl.CONFIGS["tiny"])]),
     ("moe_wrong_slot_scale", "s_slot[s] = s_x[t];", "s_slot[s] = s_x[s % T];",
      [lambda: pins.test_sparse_equals_brute_force_dense(wl.CONFIGS["tiny"])]),
+    # the FP8 (E4M3) layer
+    ("fp8_scale_over_447", "float s = amax / 448.0f;", "float s = amax / 447.0f;",
+     [pins8.test_quantize_rows_fp8_invariants]),
+    ("fp8_ties_to_odd", "else c = (lo % 2 == 0) ? lo : hi;", "else c = (lo % 2 == 1) ? lo : hi;",
+     [pins8.test_e4m3_golden_table, pins8.test_e4m3_encode_against_torch]),
+    ("fp8_no_saturation", "if (a >= 448.0f) return (uint8_t)(sign | 0x7E);",
+     "if (a >= 464.0f) return (uint8_t)(sign | 0x7F);", [pins8.test_e4m3_golden_table]),
+    ("fp8_gemm_binary32_running_sum", "double sum = 0.0;", "float sum = 0.0f;",
+     [pins8.test_gemm_fp8_cancellation, pins8.test_gemm_fp8_exact_against_integer_arithmetic]),
+    ("fp8_subnormal_exponent", "if (e == 0) v = ldexpf((float)m, -9);", "if (e == 0) v = ldexpf((float)m, -10);",
+     [pins8.test_e4m3_decode_every_code_against_torch]),
+    ("fp8_moe_wrong_w13_expert", "oracle_gemm_fp8(q_slot + s0 * H, w13_q + e * 2 * I * H",
+     "oracle_gemm_fp8(q_slot + s0 * H, w13_q",
+     [lambda: pins8.test_moe_forward_fp8_equals_dense_brute_force(16, 256, 128, 8, 2)]),
 ]
 
 

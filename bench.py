@@ -46,6 +46,8 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="prefill", choices=["prefill", "decode", "wide", "tiny", "linear"])
+    p.add_argument("--format", default="int8", choices=["int8", "fp8"],
+                   help="int8: the W8A8 INT8 layer; fp8: its E4M3 variant (MoE configs only)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -165,13 +167,24 @@ def measured_peaks():
     return {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "source": "fallback"}
 
 
-def describe(cfg) -> str:
+# fp8 tensor peak = the measured bf16 peak x the nominal fp8 : bf16 ratio (4.5 : 2.25 PFLOP/s dense)
+FP8_TO_BF16 = 2.0
+
+
+def tensor_peak(peaks, fmt):
+    """Dense tensor peak (TFLOP/s) of the format's contraction: the exact int8
+    path runs on f16 tensor cores (the bf16 rate), E4M3 on the fp8 rate."""
+    return peaks["bf16_tflops"] * (FP8_TO_BF16 if fmt == "fp8" else 1.0)
+
+
+def describe(cfg, fmt="int8") -> str:
     from w8a8_quantised_moe_gb300 import workloads as wl
     if isinstance(cfg, wl.LinearConfig):
         return f"w8a8_linear M={cfg.M} K={cfg.K} N={cfg.N}"
     route = {"none": "uniform routing", "zipf": f"Zipf({cfg.zipf_s}) expert popularity",
              "normal": f"router bias N(0,{cfg.bias_std}^2)"}[cfg.bias]
-    return (f"moe_{cfg.name} T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}, {route}")
+    tail = ", E4M3 weights and activations" if fmt == "fp8" else ""
+    return (f"moe_{cfg.name} T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}, {route}{tail}")
 
 
 def get_config(name):
@@ -179,7 +192,7 @@ def get_config(name):
     return wl.LINEAR if name == "linear" else wl.CONFIGS[name]
 
 
-def device_weights(cfg, seed, dev):
+def device_weights(cfg, seed, dev, fmt="int8"):
     """Expert weights drawn in fp32 on the device, quantised by the library."""
     import torch
     import w8a8_quantised_moe_gb300 as moe
@@ -187,33 +200,37 @@ def device_weights(cfg, seed, dev):
     if isinstance(cfg, wl.LinearConfig):
         w = wl.expert_weight_fp32(cfg, "linear", 0, seed, device=dev)
         return moe.quantize_weights(w)
-    w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=torch.int8, device=dev)
+    quant = moe.fp8_quantize_weights if fmt == "fp8" else moe.quantize_weights
+    code = torch.uint8 if fmt == "fp8" else torch.int8
+    w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=code, device=dev)
     w13_s = torch.empty((cfg.E, 2 * cfg.I), dtype=torch.float32, device=dev)
-    w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=torch.int8, device=dev)
+    w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=code, device=dev)
     w2_s = torch.empty((cfg.E, cfg.H), dtype=torch.float32, device=dev)
     for e in range(cfg.E):
-        q, s = moe.quantize_weights(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev))
+        q, s = quant(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev))
         w13_q[e].copy_(q)
         w13_s[e].copy_(s)
-        q, s = moe.quantize_weights(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev))
+        q, s = quant(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev))
         w2_q[e].copy_(q)
         w2_s[e].copy_(s)
     return w13_q, w13_s, w2_q, w2_s
 
 
-def oracle_weights(cfg, seed, dev):
+def oracle_weights(cfg, seed, dev, fmt="int8"):
     """The same fp32 draws, quantised by the CPU oracle (for the oracle's timing)."""
     import oracle
     from w8a8_quantised_moe_gb300 import workloads as wl
     if isinstance(cfg, wl.LinearConfig):
         return oracle.quantize_rows(wl.expert_weight_fp32(cfg, "linear", 0, seed, device=dev).cpu().numpy())
-    w13_q = np.empty((cfg.E, 2 * cfg.I, cfg.H), np.int8)
+    quant = oracle.quantize_rows_fp8 if fmt == "fp8" else oracle.quantize_rows
+    code = np.uint8 if fmt == "fp8" else np.int8
+    w13_q = np.empty((cfg.E, 2 * cfg.I, cfg.H), code)
     w13_s = np.empty((cfg.E, 2 * cfg.I), np.float32)
-    w2_q = np.empty((cfg.E, cfg.H, cfg.I), np.int8)
+    w2_q = np.empty((cfg.E, cfg.H, cfg.I), code)
     w2_s = np.empty((cfg.E, cfg.H), np.float32)
     for e in range(cfg.E):
-        w13_q[e], w13_s[e] = oracle.quantize_rows(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev).cpu().numpy())
-        w2_q[e], w2_s[e] = oracle.quantize_rows(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev).cpu().numpy())
+        w13_q[e], w13_s[e] = quant(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev).cpu().numpy())
+        w2_q[e], w2_s[e] = quant(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev).cpu().numpy())
     return w13_q, w13_s, w2_q, w2_s
 
 
@@ -232,7 +249,7 @@ def tokens_of(cfg):
 
 # ------------------------------------------------------------ CPU oracle
 
-def oracle_sample_rate(cfg, inputs, oweights, target_s, max_tokens=None):
+def oracle_sample_rate(cfg, inputs, oweights, target_s, max_tokens=None, fmt="int8"):
     """Tokens/s of the oracle forward on a sample of the workload's first
     tokens, sized to take about ``target_s`` seconds.  -> (rate, tokens, seconds)."""
     import oracle
@@ -246,7 +263,8 @@ def oracle_sample_rate(cfg, inputs, oweights, target_s, max_tokens=None):
         if isinstance(cfg, wl.LinearConfig):
             oracle.linear(x, *oweights)
         else:
-            oracle.moe_forward(x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
+            fwd = oracle.moe_forward_fp8 if fmt == "fp8" else oracle.moe_forward
+            fwd(x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
         return time.perf_counter() - t0
 
     n = min(lim, 8)
@@ -281,7 +299,7 @@ def algorithmic_work(cfg, offsets, peaks):
     }
 
 
-def layer_roofline_us(cfg, offsets, peaks):
+def layer_roofline_us(cfg, offsets, peaks, fmt="int8"):
     """Roofline time of the whole layer: max(weight+activation bytes at HBM
     peak, routed int8 MACs at the tensor peak)."""
     from w8a8_quantised_moe_gb300 import workloads as wl
@@ -294,7 +312,7 @@ def layer_roofline_us(cfg, offsets, peaks):
              + 4 * cfg.H * cfg.E)
         f = 2.0 * cfg.T * cfg.k * 3 * cfg.H * cfg.I
     t_b = b / (peaks["hbm_gbs"] * 1e9)
-    t_f = f / (peaks["bf16_tflops"] * 1e12)
+    t_f = f / (tensor_peak(peaks, fmt) * 1e12)
     return max(t_b, t_f) * 1e6, ("hbm" if t_b >= t_f else "tensor"), b, f
 
 
@@ -335,10 +353,15 @@ def run_ours(args, ranks: Ranks):
     stream = torch.cuda.current_stream()
     cfg = get_config(args.config)
     linear = isinstance(cfg, wl.LinearConfig)
+    fmt = args.format
+    if linear and fmt != "int8":
+        raise SystemExit("--format fp8 applies to the MoE configs")
+    fwd = moe.fp8_forward if fmt == "fp8" else moe.forward
+    fwd_debug = moe.fp8_forward_debug if fmt == "fp8" else moe.forward_debug
     peaks = measured_peaks()
     seed = args.seed + ranks.rank
     inputs = host_inputs(cfg, seed)
-    weights = device_weights(cfg, seed, dev)
+    weights = device_weights(cfg, seed, dev, fmt)
     x_host = torch.from_numpy(inputs["x"].view(np.int16)).view(torch.bfloat16)
     x = x_host.to(dev)
     T = tokens_of(cfg)
@@ -358,7 +381,7 @@ def run_ours(args, ranks: Ranks):
         y = torch.empty((cfg.T, cfg.H), dtype=torch.bfloat16, device=dev)
 
         def step(xin, out):
-            return moe.forward(xin, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k, workspace=ws, out=out)
+            return fwd(xin, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k, workspace=ws, out=out)
         stage_names = STAGES
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lib = moe._lib.load()
@@ -367,7 +390,7 @@ def run_ours(args, ranks: Ranks):
     if linear:
         offsets = None
     else:
-        _, d = moe.forward_debug(x, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k, fields=("offsets", "topk_ids"))
+        _, d = fwd_debug(x, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k, fields=("offsets", "topk_ids"))
         offsets = d["offsets"].cpu().numpy()
         shares = wl.realised_shares(d["topk_ids"].cpu().numpy(), cfg.E)
 
@@ -437,23 +460,25 @@ def run_ours(args, ranks: Ranks):
     work = algorithmic_work(cfg, offsets, peaks)
     dom = max(work, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom]
-    _, bound, _, _ = layer_roofline_us(cfg, offsets, peaks)
     w = work[dom]
-    t_f = w["flops"] / (peaks["bf16_tflops"] * 1e12)
+    peak_t = tensor_peak(peaks, fmt)
+    t_f = w["flops"] / (peak_t * 1e12)
     t_b = w["bytes"] / (peaks["hbm_gbs"] * 1e9)
     if t_f >= t_b:
         achieved = w["flops"] / (dom_ms * 1e-3) / 1e12
-        roof = {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"], "unit": "TFLOP/s"}
+        roof = {"bound": "tensor", "achieved": achieved, "peak": peak_t, "unit": "TFLOP/s"}
     else:
         achieved = w["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_from_profiles(args.config, dom)
+    roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom)
     roof["kernel"] = dom
     roof["kernel_ms"] = dom_ms
     roof["algorithmic"] = {"flops": w["flops"], "bytes": w["bytes"]}
-    roof["peak_source"] = peaks["source"] + " (bf16 burst; f16 tensor rate carries the exact int8 products)"
-    layer_us, layer_bound, layer_bytes, layer_flops = layer_roofline_us(cfg, offsets, peaks)
+    roof["peak_source"] = peaks["source"] + (
+        " (bf16 burst x 2, the nominal fp8 : bf16 ratio)" if fmt == "fp8"
+        else " (bf16 burst; f16 tensor rate carries the exact int8 products)")
+    layer_us, layer_bound, layer_bytes, layer_flops = layer_roofline_us(cfg, offsets, peaks, fmt)
 
     # end to end through the public API with host buffers
     x_pin = x_host.pin_memory()
@@ -491,13 +516,15 @@ def run_ours(args, ranks: Ranks):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8",
+        "dtype": "e4m3" if fmt == "fp8" else "int8",
         "data": "synthetic (seeded; random-init expert weights quantised per channel)",
         "config": {
-            "workload": describe(cfg),
+            "workload": describe(cfg, fmt),
             "parallelism": f"replicas x{ranks.world}" if ranks.world > 1 else "single GPU",
             "l2": "flushed between timed steps (256 MB write, untimed)",
-            "arithmetic": "int8 x int8 -> exact int32 on f16 tensor cores (tcgen05 kind::f16), fp32 epilogues",
+            "arithmetic": ("E4M3 x E4M3 -> fp32 on the fp8 tensor cores (tcgen05 kind::f8f6f4), fp32 epilogues"
+                           if fmt == "fp8" else
+                           "int8 x int8 -> exact int32 on f16 tensor cores (tcgen05 kind::f16), fp32 epilogues"),
             "stage_ms": stage_ms,
             "stage_ms_note": "per-kernel pass with an event between launches (serialised), "
                              f"{serial_step_ms:.4f} ms per step there",
@@ -519,8 +546,8 @@ def run_ours(args, ranks: Ranks):
 
     if ranks.rank == 0 and ranks.world == 1 and not args.no_cpu_baseline:
         import oracle
-        oweights = oracle_weights(cfg, seed, dev)
-        rate, n, dt = oracle_sample_rate(cfg, inputs, oweights, args.cpu_seconds)
+        oweights = oracle_weights(cfg, seed, dev, fmt)
+        rate, n, dt = oracle_sample_rate(cfg, inputs, oweights, args.cpu_seconds, fmt=fmt)
         out["cpu_baseline"] = {"value": rate, "unit": "tokens/s", "cores": oracle.num_threads(),
                                "kind": "oracle",
                                "sample": f"first {n} tokens of the same workload, one oracle forward "
@@ -541,11 +568,12 @@ def run_reference(args):
     import oracle
     cfg = get_config(args.config)
     dev = "cuda" if torch.cuda.is_available() else "cpu"
+    fmt = args.format
     inputs = host_inputs(cfg, args.seed)
-    oweights = oracle_weights(cfg, args.seed, dev)
+    oweights = oracle_weights(cfg, args.seed, dev, fmt)
     total = args.steps + args.warmup
     per_step_s = min(8.0, 150.0 / max(total, 1))
-    _, n, _ = oracle_sample_rate(cfg, inputs, oweights, per_step_s)
+    _, n, _ = oracle_sample_rate(cfg, inputs, oweights, per_step_s, fmt=fmt)
     import w8a8_quantised_moe_gb300.workloads as wl
     x = inputs["x"][:n]
 
@@ -553,7 +581,8 @@ def run_reference(args):
         if isinstance(cfg, wl.LinearConfig):
             oracle.linear(x, *oweights)
         else:
-            oracle.moe_forward(x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
+            (oracle.moe_forward_fp8 if fmt == "fp8" else oracle.moe_forward)(
+                x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
 
     for _ in range(args.warmup):
         step()
@@ -574,9 +603,9 @@ def run_reference(args):
         "higher_is_better": True,
         "scaling": "weak",
         "vs_baseline": None,
-        "dtype": "int8",
+        "dtype": "e4m3" if fmt == "fp8" else "int8",
         "data": "synthetic (seeded)",
-        "config": {"workload": describe(cfg), "parallelism": "host cores (OpenMP)",
+        "config": {"workload": describe(cfg, fmt), "parallelism": "host cores (OpenMP)",
                    "sample_tokens_per_step": n},
         "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
                          "sample": f"first {n} of {tokens_of(cfg)} tokens per step"},

@@ -222,6 +222,48 @@ MOE_W8A8_API moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t
                                                  int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream);
 
 /* ---------------------------------------------------------------------------
+ * The FP8 (E4M3) layer.  "DeepSeek V4 950 FP8 inference on H100" (lpnh.cn):
+ * weights and activations in E4M3 (section 2.1), FP8 operands with an FP32
+ * accumulator whose result is re-quantised to FP8 for the next operator
+ * (2.3), per-channel weight scales and per-token dynamic activation scales
+ * (2.4), weight scales from the absolute maximum (3.1).  A row's scale is
+ * s = amax / 448 (binary32 division) and its codes are the E4M3 values
+ * nearest to the binary32 quotients x / s, ties to even, saturated at +-448;
+ * a row of zeros gives s = 0 and codes 0.  E4M3 codes are bytes (sign bit 7,
+ * exponent bits 6..3 with bias 7, mantissa bits 2..0).
+ *
+ * moe_w8a8_fp8_quantize_weights: the weight quantiser.  w fp32 [rows][K]
+ * (K a multiple of 4), w_q E4M3 [rows][K], w_scale fp32 [rows]; call it once
+ * per expert tensor as moe_w8a8_quantize_weights.  Errors as that function.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_fp8_quantize_weights(const float* w, int64_t rows, int64_t K, uint8_t* w_q,
+                                                        float* w_scale, void* stream);
+
+/* moe_w8a8_fp8_forward: the whole FP8 layer.  Arguments, shapes, workspace
+ * (moe_w8a8_workspace_size), launches and errors as moe_w8a8_forward, with
+ * w13_q and w2_q holding E4M3 codes.  Router, top-k, slots, SiLU gate and
+ * combine are those of the INT8 layer; the expert GEMMs run on the
+ * tcgen05.mma kind::f8f6f4 tensor cores.  The E4M3 products are exact and
+ * their sum is an fp32 accumulation, so the GEMM results agree with the
+ * exact dot product within fp32 accumulation error (not bit for bit). */
+MOE_W8A8_API moe_status_t moe_w8a8_fp8_forward(const uint16_t* x, const float* router_w, const float* router_bias,
+                                               const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                                               const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                                               int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                               void* stream);
+
+/* moe_w8a8_fp8_forward plus copies of the intermediates into `dbg`, as
+ * moe_w8a8_forward_debug; q_x and q_h receive E4M3 codes and acc1, acc2 the
+ * fp32 accumulators (their bit patterns in the int32 fields). */
+MOE_W8A8_API moe_status_t moe_w8a8_fp8_forward_debug(const uint16_t* x, const float* router_w,
+                                                     const float* router_bias, const uint8_t* w13_q,
+                                                     const float* w13_scale, const uint8_t* w2_q,
+                                                     const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                                     int64_t E, int64_t top_k, uint16_t* y, void* workspace,
+                                                     size_t workspace_bytes, void* stream,
+                                                     const moe_w8a8_debug_t* dbg);
+
+/* ---------------------------------------------------------------------------
  * moe_w8a8_device_error -- synchronise `stream`, then read and clear the
  * sticky device error word in the first bytes of `workspace`.  Returns
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a pipeline wait inside a kernel gave up;

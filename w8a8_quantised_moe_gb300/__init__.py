@@ -98,8 +98,9 @@ def new_workspace(nbytes: int, device="cuda"):
     return torch.zeros(nbytes, dtype=torch.uint8, device=device)
 
 
-def _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k):
+def _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, code_dtype=None):
     torch = _torch()
+    code_dtype = torch.int8 if code_dtype is None else code_dtype
     T, H = x.shape
     E = router_w.shape[1]
     I = w2_q.shape[2] if w2_q.dim() == 3 else 0
@@ -107,9 +108,9 @@ def _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, to
     _need(router_w, torch.float32, (H, E), "router_w")
     if router_bias is not None:
         _need(router_bias, torch.float32, (E,), "router_bias")
-    _need(w13_q, torch.int8, (E, 2 * I, H), "w13_q")
+    _need(w13_q, code_dtype, (E, 2 * I, H), "w13_q")
     _need(w13_scale, torch.float32, (E, 2 * I), "w13_scale")
-    _need(w2_q, torch.int8, (E, H, I), "w2_q")
+    _need(w2_q, code_dtype, (E, H, I), "w2_q")
     _need(w2_scale, torch.float32, (E, H), "w2_scale")
     return T, H, I, E
 
@@ -203,3 +204,65 @@ def linear(x, w_q, w_scale, workspace=None, out=None, stream=None):
 def device_error(workspace, stream=None) -> int:
     """Synchronise the stream, read and clear the workspace's device error word (a status code)."""
     return int(_lib.load().moe_w8a8_device_error(_ptr(workspace), _stream(stream)))
+
+
+# ---- FP8 (E4M3) variant: E4M3 codes travel as uint8 tensors ----------------
+
+def fp8_quantize_weights(w, stream=None):
+    """Per-output-channel E4M3 quantisation of fp32 ``w [rows, K]`` ->
+    (E4M3 codes as uint8 [rows, K], fp32 scales [rows]); s = amax / 448."""
+    torch = _torch()
+    rows, K = w.shape
+    _need(w, torch.float32, (rows, K), "w")
+    q = torch.empty((rows, K), dtype=torch.uint8, device=w.device)
+    s = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    _lib.check(_lib.load().moe_w8a8_fp8_quantize_weights(_ptr(w), rows, K, _ptr(q), _ptr(s), _stream(stream)),
+               "moe_w8a8_fp8_quantize_weights")
+    return q, s
+
+
+def fp8_forward(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, workspace=None, out=None,
+                stream=None):
+    """The FP8 MoE layer: bf16 x [T, H] -> bf16 y [T, H]; w13_q, w2_q E4M3 (uint8)."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, torch.uint8)
+    need = workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (T, H), "out")
+    _lib.check(_lib.load().moe_w8a8_fp8_forward(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream)), "moe_w8a8_fp8_forward")
+    return y
+
+
+_DEBUG_FIELDS_FP8 = dict(_DEBUG_FIELDS, q_x=("uint8", _DEBUG_FIELDS["q_x"][1]),
+                         q_h=("uint8", _DEBUG_FIELDS["q_h"][1]), acc1=("float32", _DEBUG_FIELDS["acc1"][1]),
+                         acc2=("float32", _DEBUG_FIELDS["acc2"][1]))
+
+
+def fp8_forward_debug(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, fields=None,
+                      workspace=None, stream=None):
+    """``fp8_forward`` plus the intermediates named in ``fields`` (q_x, q_h:
+    E4M3 codes; acc1, acc2: fp32 accumulators).  Returns (y, dict)."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, torch.uint8)
+    need = workspace_size(T, H, I, E, top_k)
+    if workspace is None:
+        workspace = new_workspace(need, x.device)
+    fields = tuple(_DEBUG_FIELDS_FP8) if fields is None else tuple(fields)
+    bufs = _lib.DebugBuffers()
+    out = {}
+    for name in fields:
+        dt, shape = _DEBUG_FIELDS_FP8[name]
+        t = torch.zeros(shape(T, H, I, E, top_k), dtype=getattr(torch, dt), device=x.device)
+        out[name] = t
+        setattr(bufs, name, t.data_ptr())
+    y = torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _lib.check(_lib.load().moe_w8a8_fp8_forward_debug(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), ctypes.byref(bufs)), "moe_w8a8_fp8_forward_debug")
+    return y, out

@@ -155,7 +155,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
                           const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
                           const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
                           int64_t k, uint16_t* y, void* workspace, size_t workspace_bytes,
-                          void* stream, const moe_w8a8_debug_t* dbg) {
+                          void* stream, const moe_w8a8_debug_t* dbg, bool fp8 = false) {
     if (!moe_shape_ok(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;  // nothing is read or written
     const void* ptrs[] = {x, router_w, w13_q, w13_scale, w2_q, w2_scale, y, workspace};
@@ -196,8 +196,10 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     // place of the fp16 ones in the same workspace regions
     const GemmShape shape1 = pick_gemm_shape(S, E, H, Epi::GateUp, 2 * I, I);
     const GemmShape shape2 = pick_gemm_shape(S, E, I, Epi::ScaleF32, H, 0);
-    int8_t* q_x8 = shape1 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_x16) : nullptr;
-    int8_t* q_h8 = shape2 == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q_h16) : nullptr;
+    // 8-bit codes (int8 for the dp4a kernel, E4M3 for the FP8 layer) take the
+    // place of the fp16 ones in the same workspace regions
+    int8_t* q_x8 = (fp8 || shape1 == GemmShape::Skinny) ? reinterpret_cast<int8_t*>(q_x16) : nullptr;
+    int8_t* q_h8 = (fp8 || shape2 == GemmShape::Skinny) ? reinterpret_cast<int8_t*>(q_h16) : nullptr;
     const bool pdl = pdl_default();  // every launch after the first
 
     cudaError_t e;
@@ -213,8 +215,12 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
         if (e != cudaSuccess) return from_cuda(e);
     }
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                             s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
+    if (fp8)
+        e = launch_permute_quant_fp8(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
+                                     s_x, s_slot, reinterpret_cast<uint8_t*>(q_x8), st, pdl);
+    else
+        e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
+                                 s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     GemmArgs g1{};
@@ -239,11 +245,13 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.error = err;
     g1.timeout_ns = timeout;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::GateUp, shape1, g1, st, pdl);
+    e = fp8 ? launch_grouped_gemm_fp8(Epi::GateUp, g1, st, pdl) : launch_grouped_gemm(Epi::GateUp, shape1, g1, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(4, st)) != cudaSuccess) return from_cuda(e);
-    if (q_h8)
+    if (fp8)
+        e = launch_requant_fp8(h, S, (int)I, s_h, reinterpret_cast<uint8_t*>(q_h8), st, pdl);
+    else if (q_h8)
         e = launch_requant(h, S, (int)I, s_h, nullptr, q_h8, flag2, list2, counts + 1, st, pdl);
     else
         e = launch_requant(h, S, (int)I, s_h, q_h16, dbg ? dbg->q_h : nullptr, flag2, list2, counts + 1, st, pdl);
@@ -271,7 +279,8 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.error = err;
     g2.timeout_ns = timeout;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st, pdl);
+    e = fp8 ? launch_grouped_gemm_fp8(Epi::ScaleF32, g2, st, pdl)
+            : launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
@@ -332,6 +341,35 @@ uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns) {
 int moe_w8a8_set_gemm_path(int path) {
     if (path < -1 || path > (int)GemmShape::Skinny) return -2;
     return g_gemm_path.exchange(path);
+}
+
+moe_status_t moe_w8a8_fp8_quantize_weights(const float* w, int64_t rows, int64_t K, uint8_t* w_q, float* w_scale,
+                                           void* stream) {
+    if (rows < 0 || K < 4 || K > (int64_t(1) << 20) || K % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(
+        launch_quantize_weights_fp8(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream)));
+}
+
+moe_status_t moe_w8a8_fp8_forward(const uint16_t* x, const float* router_w, const float* router_bias,
+                                  const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                                  const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
+                                  uint16_t* y, void* workspace, size_t workspace_bytes, void* stream) {
+    return forward_impl(x, router_w, router_bias, reinterpret_cast<const int8_t*>(w13_q), w13_scale,
+                        reinterpret_cast<const int8_t*>(w2_q), w2_scale, T, H, I, E, top_k, y, workspace,
+                        workspace_bytes, stream, nullptr, true);
+}
+
+moe_status_t moe_w8a8_fp8_forward_debug(const uint16_t* x, const float* router_w, const float* router_bias,
+                                        const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                                        const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                                        int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                        void* stream, const moe_w8a8_debug_t* dbg) {
+    return forward_impl(x, router_w, router_bias, reinterpret_cast<const int8_t*>(w13_q), w13_scale,
+                        reinterpret_cast<const int8_t*>(w2_q), w2_scale, T, H, I, E, top_k, y, workspace,
+                        workspace_bytes, stream, dbg, true);
 }
 
 moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows, int64_t K, int8_t* w_q,

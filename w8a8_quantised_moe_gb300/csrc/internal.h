@@ -242,6 +242,16 @@ bool skinny_gemm_supported(Epi epi, const GemmArgs& args);
 bool skinny_shape_supported(Epi epi, long K, long w_rows_per_group, long up_offset);
 cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
 
+// FP8 (E4M3) variant (fp8.cu).  Codes are bytes; args.act8 carries the E4M3
+// activation rows and args.w the E4M3 weights; GateUp and ScaleF32 only.
+cudaError_t launch_quantize_weights_fp8(const float* w, int64_t rows, int K, uint8_t* q, float* s, cudaStream_t st);
+cudaError_t launch_permute_quant_fp8(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
+                                     const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
+                                     int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, cudaStream_t st,
+                                     bool pdl);
+cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t* q8, cudaStream_t st, bool pdl);
+cudaError_t launch_grouped_gemm_fp8(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
+
 int num_sms();
 
 // 2-D tiled tensor map (row-major, inner dimension contiguous).

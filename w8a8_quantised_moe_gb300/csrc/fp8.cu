@@ -196,7 +196,11 @@ struct F8Cfg {
     static_assert(kTmemCols <= 512, "TMEM budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
+// Wide tiles for groups of many rows; narrow tiles with a deep ring for a
+// few rows per group (decode), where each stage is mostly a weight tile
+// streamed from HBM and the depth of the ring sets the bytes in flight.
 using F8Wide = F8Cfg<256, 4>;
+using F8Narrow = F8Cfg<32, 10>;
 
 template <int BN>
 __device__ __forceinline__ void f8_decode_tile(const Tiles& t, int tile, int& g, int& cb, int& row0, int& nvalid) {
@@ -507,9 +511,12 @@ cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t
 cudaError_t launch_grouped_gemm_fp8(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (args.total_rows == 0) return cudaSuccess;
     if (args.act8 == nullptr || args.K % kF8BK != 0) return cudaErrorInvalidValue;
+    const bool narrow = (long)args.total_rows <= 32L * (args.n_groups > 0 ? args.n_groups : 1);
     switch (epi) {
-        case Epi::GateUp: return launch_fp8_impl<F8Wide, 0>(args, st, pdl);
-        case Epi::ScaleF32: return launch_fp8_impl<F8Wide, 1>(args, st, pdl);
+        case Epi::GateUp:
+            return narrow ? launch_fp8_impl<F8Narrow, 0>(args, st, pdl) : launch_fp8_impl<F8Wide, 0>(args, st, pdl);
+        case Epi::ScaleF32:
+            return narrow ? launch_fp8_impl<F8Narrow, 1>(args, st, pdl) : launch_fp8_impl<F8Wide, 1>(args, st, pdl);
         default: return cudaErrorInvalidValue;
     }
 }

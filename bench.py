@@ -316,29 +316,32 @@ def layer_roofline_us(cfg, offsets, peaks, fmt="int8"):
     return max(t_b, t_f) * 1e6, ("hbm" if t_b >= t_f else "tensor"), b, f
 
 
-GEMM_SOURCES = ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_common.cuh", "ptx.cuh", "internal.h")
+GEMM_SOURCES = {
+    "int8": ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
+    "fp8": ("fp8.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
+}
 
 
-def gemm_source_sha():
-    """sha256 prefix of the GEMM kernels' sources (keys the committed traffic)."""
+def gemm_source_sha(fmt="int8"):
+    """sha256 prefix of the format's GEMM kernel sources (keys the committed traffic)."""
     import hashlib
     h = hashlib.sha256()
-    for name in GEMM_SOURCES:
+    for name in GEMM_SOURCES[fmt]:
         with open(os.path.join(ROOT, "w8a8_quantised_moe_gb300", "csrc", name), "rb") as f:
             h.update(f.read())
     return h.hexdigest()[:16]
 
 
-def traffic_from_profiles(config_name, kernel):
+def traffic_from_profiles(config_name, kernel, fmt="int8"):
     """dram bytes per launch of ``kernel`` from the committed ncu summary, if
-    it was taken on the current source of the GEMM kernels."""
+    it was taken on the current source of the format's GEMM kernels."""
     path = os.path.join(ROOT, "profiles", "traffic.json")
     if not os.path.exists(path):
         return None
     with open(path) as f:
         table = json.load(f)
     ent = table.get(config_name, {}).get(kernel)
-    if not ent or ent.get("gemm_src_sha256_16") != gemm_source_sha():
+    if not ent or ent.get("gemm_src_sha256_16") != gemm_source_sha(fmt):
         return None
     return ent.get("dram_bytes_per_launch")
 
@@ -471,7 +474,7 @@ def run_ours(args, ranks: Ranks):
         achieved = w["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom)
+    roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom, fmt)
     roof["kernel"] = dom
     roof["kernel_ms"] = dom_ms
     roof["algorithmic"] = {"flops": w["flops"], "bytes": w["bytes"]}

@@ -1,5 +1,6 @@
 """Parity at the benchmark's full sizes (decode, prefill and wide MoE layers,
-the 4096^3 linear layer), in the launch configuration bench.py times: inputs
+the 4096^3 linear layer, and the FP8 (E4M3) variant of the decode and prefill
+layers), in the launch configuration bench.py times: inputs
 resident on the device, expert weights drawn in fp32 on the device and
 quantised by the library, one plain forward.
 
@@ -17,6 +18,10 @@ properties that hold at any size:
   (from the oracle's h) within the layer's tolerance;
 * the library's int8 weights of every sampled expert equal the oracle's
   quantisation of the same fp32 draws, so the oracle's weights are its own.
+
+The FP8 layer is checked the same way, except that its fp32 accumulators
+are bounded against the exact dot products of the E4M3 codes instead of
+compared bit for bit.
 """
 import numpy as np
 import pytest
@@ -158,3 +163,111 @@ def test_full_size_linear_sampled_against_oracle():
     np.testing.assert_array_equal(w_s.cpu().numpy(), ws_ref)
     rows = np.sort(np.random.default_rng(8).choice(cfg.M, 16, replace=False))
     np.testing.assert_array_equal(bf16_from_dev(y)[rows], oracle.linear(x_bits[rows], wq_ref, ws_ref))
+
+
+# ---- the FP8 (E4M3) layer at the benchmark's sizes -------------------------
+
+# fp32 accumulation of exact E4M3 products (the bound of the FP8 parity tests)
+FP8_ACC_REL = 2.0 ** -16
+
+
+def _fp8_device_weights(cfg, seed):
+    code = torch.uint8
+    w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=code, device="cuda")
+    w13_s = torch.empty((cfg.E, 2 * cfg.I), dtype=torch.float32, device="cuda")
+    w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=code, device="cuda")
+    w2_s = torch.empty((cfg.E, cfg.H), dtype=torch.float32, device="cuda")
+    for e in range(cfg.E):
+        q, s = moe.fp8_quantize_weights(wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda"))
+        w13_q[e].copy_(q)
+        w13_s[e].copy_(s)
+        q, s = moe.fp8_quantize_weights(wl.expert_weight_fp32(cfg, "w2", e, seed, device="cuda"))
+        w2_q[e].copy_(q)
+        w2_s[e].copy_(s)
+    return w13_q, w13_s, w2_q, w2_s
+
+
+def _assert_fp8_acc_close(acc, a_codes, w_codes):
+    """acc within FP8_ACC_REL * sum |a_k w_k| of the exact dot products."""
+    A = oracle.e4m3_decode(a_codes).astype(np.float64)
+    W = oracle.e4m3_decode(w_codes).astype(np.float64)
+    exact = A @ W.T  # exact: products are multiples of 2^-18 below 2^18
+    mag = np.abs(A) @ np.abs(W).T
+    err = np.abs(acc.astype(np.float64) - exact)
+    assert (err <= FP8_ACC_REL * mag).all(), float((err / np.maximum(mag, 1e-300)).max())
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_full_size_fp8_layer_sampled_against_oracle(name):
+    cfg = wl.CONFIGS[name]
+    seed = 0
+    inp = wl.make_moe_inputs(cfg, seed)
+    x = bf16_to_dev(inp.x)
+    Wr = torch.from_numpy(inp.Wr).cuda()
+    bias = None if inp.bias is None else torch.from_numpy(inp.bias).cuda()
+    w13_q, w13_s, w2_q, w2_s = _fp8_device_weights(cfg, seed)
+    args = (x, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k)
+
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    y_plain = moe.fp8_forward(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    y_dbg, dev = moe.fp8_forward_debug(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    assert torch.equal(y_plain.view(torch.int16), y_dbg.view(torch.int16))
+
+    ids = dev["topk_ids"].cpu().numpy()
+    topk_w = dev["topk_w"].cpu().numpy()
+    offsets = dev["offsets"].cpu().numpy()
+    slot_of = dev["slot_of"].cpu().numpy()
+    slot_token = dev["slot_token"].cpu().numpy()
+    _check_routing_arrays(cfg, ids, offsets, slot_of, slot_token)
+
+    tok = np.sort(np.random.default_rng(9).choice(cfg.T, SAMPLE[name], replace=False))
+    ids_ref, w_ref, _ = oracle.router(inp.x[tok], inp.Wr, inp.bias, cfg.k)
+    np.testing.assert_array_equal(ids[tok], ids_ref)
+    np.testing.assert_allclose(topk_w[tok], w_ref, rtol=0, atol=TOPK_W_ATOL)
+    q_ref, s_ref = oracle.quantize_rows_bf16_fp8(inp.x[tok])
+    np.testing.assert_array_equal(dev["q_x"][tok].cpu().numpy(), q_ref)
+    np.testing.assert_array_equal(dev["s_x"][tok].cpu().numpy(), s_ref)
+
+    ref_w = {}
+    for e in sorted(set(ids_ref.ravel().tolist())):
+        w13 = wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda").cpu().numpy()
+        w2 = wl.expert_weight_fp32(cfg, "w2", e, seed, device="cuda").cpu().numpy()
+        ref_w[e] = (oracle.quantize_rows_fp8(w13), oracle.quantize_rows_fp8(w2))
+        np.testing.assert_array_equal(w13_q[e].cpu().numpy(), ref_w[e][0][0])
+        np.testing.assert_array_equal(w13_s[e].cpu().numpy(), ref_w[e][0][1])
+        np.testing.assert_array_equal(w2_q[e].cpu().numpy(), ref_w[e][1][0])
+        np.testing.assert_array_equal(w2_s[e].cpu().numpy(), ref_w[e][1][1])
+
+    y_gpu = bf16_from_dev(y_dbg)[tok]
+    y_ref = np.empty_like(y_gpu)
+    for i, t in enumerate(tok):
+        slots = slot_of[t]
+        o_gpu = dev["o"][torch.from_numpy(slots).long().cuda()].cpu().numpy()
+        o_own = np.empty_like(o_gpu)
+        for j, s in enumerate(slots):
+            (w13r, s13r), (w2r, s2r) = ref_w[int(ids_ref[i, j])]
+            # GEMM1: within the fp32 accumulation bound of the exact dot products
+            acc1 = dev["acc1"][s].cpu().numpy()[None]
+            _assert_fp8_acc_close(acc1, q_ref[i:i + 1], w13r)
+            # gate/up epilogue of the GPU's own accumulators: differs only through expf
+            h_gpu = dev["h"][s].cpu().numpy()
+            np.testing.assert_allclose(h_gpu, oracle.epilogue_gate_up_f32(acc1, s_ref[i:i + 1], s13r)[0],
+                                       rtol=H_RTOL, atol=1e-30)
+            # requantisation of the GPU's own h: exact; GEMM2 within the bound; its epilogue exact
+            qh, sh = oracle.quantize_rows_fp8(h_gpu[None])
+            np.testing.assert_array_equal(dev["q_h"][s].cpu().numpy(), qh[0])
+            assert dev["s_h"][s].item() == sh[0]
+            acc2 = dev["acc2"][s].cpu().numpy()[None]
+            _assert_fp8_acc_close(acc2, qh, w2r)
+            np.testing.assert_array_equal(o_gpu[j], oracle.epilogue_scale_f32(acc2, sh, s2r)[0])
+            # the oracle's own path: exact sums, its own h
+            h_own = oracle.epilogue_gate_up_f32(oracle.gemm_fp8(q_ref[i:i + 1], w13r), s_ref[i:i + 1], s13r)
+            qh_o, sh_o = oracle.quantize_rows_fp8(h_own)
+            o_own[j] = oracle.epilogue_scale_f32(oracle.gemm_fp8(qh_o, w2r), sh_o, s2r)[0]
+        # combine of the GPU's own o rows: exact; of the oracle's: the layer tolerance
+        one = np.arange(cfg.k, dtype=np.int32)[None]
+        np.testing.assert_array_equal(y_gpu[i], oracle.combine(o_gpu, one, topk_w[t][None])[0])
+        y_ref[i] = oracle.combine(o_own, one, w_ref[i][None])[0]
+    assert_y_close(y_gpu, y_ref)

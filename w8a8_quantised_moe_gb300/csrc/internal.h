@@ -73,7 +73,8 @@ struct GemmArgs {
 // slices of kb_per_slice 64-wide steps.
 struct RouterPlan {
     int E_pad, NB, n_eb, KS, kb_per_slice;
-    bool small;  // CUDA-core router (T <= kRouterSmallT): no weight split, KS slices of kb_per_slice steps
+    int hs;      // small router: rows of Wr per slice (KS slices)
+    bool small;  // CUDA-core router (T <= kRouterSmallT): no weight split
 };
 RouterPlan router_plan(int64_t T, int64_t H, int64_t E);
 
@@ -201,8 +202,8 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
 // pdl: launch with programmatic dependent launch (see above).
 // Router: weight split, tensor-core logits (partials per K slice), top-k.
 // The router's first kernel is launched without pdl; its later ones with pdl.
-// For T <= kRouterSmallT (RouterPlan::small) one kernel also computes the
-// prefix sums of launch_scan (offsets, chunk bases in hist) and clears
+// For T <= kRouterSmallT (RouterPlan::small) the router's last kernel also
+// computes the prefix sums of launch_scan (offsets, chunk bases in hist) and clears
 // counts[0..1]; `ticket` is a zeroed workspace word that it leaves zeroed.
 cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias, int T, int H, int E, int k,
                           uint16_t* wsplit, float* logits, int32_t* topk_ids, float* topk_w, int32_t* rank,

@@ -9,9 +9,11 @@
 //                        per K step into one fp32 accumulator.  x is bf16, so
 //                        every product is exact in fp32 and the result is an
 //                        fp32-accumulated dot product, like an FP32 GEMM.
-//   router_small_kernel  whole logits for a few tokens (decode), fp32 FMAs on
-//                        the CUDA cores straight from the fp32 weights: no
-//                        split, and many CTAs for a tiny GEMM.
+//   router_partial_kernel  few tokens (decode): partial logits of every token
+//                        over one slice of rows of the fp32 weights, fp32 FMAs
+//                        on the CUDA cores (no split; ~128 CTAs for a tiny GEMM).
+//   router_finish_kernel per token the slice sums, bias and top-k; the last
+//                        CTA ranks the choices and computes the prefix sums.
 //   topk_kernel          logits = sum_ks P[ks] (+ bias) in a fixed order, top-k
 //                        with ties to the lower expert index, softmax over the
 //                        selected logits, and per 32-token chunk the count of
@@ -202,6 +204,51 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
 }
 
+// Top-k of one token's logits, one warp: lane l holds the logits of experts
+// l + 32 i (experts >= E are never taken).  Ties go to the lower expert
+// index; choice j ends in lane j as its expert and its softmax weight over
+// the selected logits.
+template <int EPT>
+__device__ __forceinline__ void warp_topk(const float (&v)[EPT], int E, int k, int lane, int& my_e, float& my_w) {
+    bool taken[EPT];
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) taken[i] = (lane + 32 * i) >= E;
+    float sel0 = 0.f, den = 0.f, my_v = 0.f;
+    my_e = 0;
+    for (int j = 0; j < k; ++j) {
+        float bv = -INFINITY;
+        int be = 0x7fffffff;
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const int e = lane + 32 * i;
+            if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
+                bv = v[i];
+                be = e;
+            }
+        }
+#pragma unroll
+        for (int off = 16; off > 0; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
+            if (ov > bv || (ov == bv && oe < be)) {
+                bv = ov;
+                be = oe;
+            }
+        }
+#pragma unroll
+        for (int i = 0; i < EPT; ++i)
+            if (lane + 32 * i == be) taken[i] = true;
+        if (j == 0) sel0 = bv;
+        const float ex = expf(__fsub_rn(bv, sel0));
+        den = __fadd_rn(den, ex);
+        if (lane == j) {  // lane j keeps choice j
+            my_v = ex;
+            my_e = be;
+        }
+    }
+    my_w = __fdiv_rn(my_v, den);
+}
+
 // One 32-token chunk, by a whole CTA of 256 threads; `mask` is shared memory
 // of 32 * EPT words.  The logits are read with ld.global.cg (from L2): when
 // another CTA of this grid wrote them, no stale L1 line can be hit.
@@ -253,45 +300,12 @@ __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, 
             const int e = lane + 32 * i;
             v[i] = (bias && e < E) ? __fadd_rn(vv[r][i], bias[e]) : vv[r][i];
         }
-        bool taken[EPT];
-#pragma unroll
-        for (int i = 0; i < EPT; ++i) taken[i] = (lane + 32 * i) >= E;
-        float sel0 = 0.f, den = 0.f, my_v = 0.f;
-        int my_e = 0;
-        for (int j = 0; j < k; ++j) {
-            float bv = -INFINITY;
-            int be = 0x7fffffff;
-#pragma unroll
-            for (int i = 0; i < EPT; ++i) {
-                const int e = lane + 32 * i;
-                if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
-                    bv = v[i];
-                    be = e;
-                }
-            }
-#pragma unroll
-            for (int off = 16; off > 0; off >>= 1) {
-                const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-                const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-                if (ov > bv || (ov == bv && oe < be)) {
-                    bv = ov;
-                    be = oe;
-                }
-            }
-#pragma unroll
-            for (int i = 0; i < EPT; ++i)
-                if (lane + 32 * i == be) taken[i] = true;
-            if (j == 0) sel0 = bv;
-            const float ex = expf(__fsub_rn(bv, sel0));
-            den = __fadd_rn(den, ex);
-            if (lane == j) {  // lane j keeps choice j
-                my_v = ex;
-                my_e = be;
-            }
-        }
+        int my_e;
+        float my_w;
+        warp_topk<EPT>(v, E, k, lane, my_e, my_w);
         if (lane < k) {
             topk_ids[(size_t)t * k + lane] = my_e;
-            topk_w[(size_t)t * k + lane] = __fdiv_rn(my_v, den);
+            topk_w[(size_t)t * k + lane] = my_w;
             atomicOr(&mask[my_e], 1u << (warp * 4 + r));
         }
     }
@@ -320,107 +334,220 @@ __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, 
 
 // Few tokens (T <= kRouterSmallT): the router GEMM is far too small for the
 // tensor cores to pay (one 128-token tile, a handful of CTAs, a weight split
-// per call), so the CUDA cores compute whole logits directly from the fp32
-// weights.  Grid (expert blocks of 8, token blocks of 8); thread tid owns the
-// 8-wide h chunks tid, tid + 256, ... and accumulates the CTA's 8 x 8
-// (token, expert) dot products over them with fp32 FMAs, loading straight
-// from global memory (one load phase per chunk, no staging).  The 256 partial
-// sums of each logit are then reduced in a fixed order (warp butterfly, then
-// the 8 warps in order), so the logits are deterministic.
+// per call), so the CUDA cores compute the logits straight from the fp32
+// weights, in two kernels.
 //
-// The CTA that finishes last (an atomic ticket in the workspace, which it
-// resets to zero for the next call) then runs the top-k of every 32-token
-// chunk and the prefix sums that the scan kernel computes for larger T
-// (expert offsets and the first slot of every (chunk, expert)), and clears
-// the exact-path counters: for few tokens these are a few microseconds of
-// work, less than the two launches they replace.  Every CTA publishes its
-// logits with a device-scope fence before taking its ticket, as in the
-// classic threadfence reduction; nothing waits on another CTA.
-constexpr int kRSmallEB = 8;  // experts per CTA
-constexpr int kRSmallTB = 8;  // tokens per CTA
+// router_partial_kernel: CTA s owns rows [s*hs, (s+1)*hs) of Wr, about 128
+// slices in all, and computes the partial logits of every token over them:
+// P[s][t][e] = sum over its rows of x[t][h] * Wr[h][e], fp32 FMAs in row
+// order.  Each SM thus reads only its own few KB of Wr and x, once (reading
+// all of Wr for a block of tokens, as one kernel per token block must, made
+// the loads the critical path: 192 KB per SM at one load round trip per 4 KB
+// or so).  The slice is staged in shared memory (Wr rows with cp.async, x
+// rows transposed to [h][t] fp32), then each thread accumulates a 4 x 4 block
+// of (token, expert) sums per 64 x 64 output tile.
+//
+// router_finish_kernel: one CTA per token sums the slices in a fixed order
+// (warp w sums its run of slices in order, then the 8 warp sums in order),
+// adds the bias, and selects the top-k with its softmax weights.  The CTA that
+// finishes last (an atomic ticket in the workspace, which it resets to zero
+// for the next call) then builds the per-chunk expert masks of all tokens'
+// choices, the ranks of each choice in its 32-token chunk, and the prefix
+// sums that the scan kernel computes for larger T (expert offsets and the
+// first slot of every (chunk, expert)), and clears the exact-path counters.
+// Every CTA publishes its choices with a device-scope fence before taking its
+// ticket, as in the classic threadfence reduction; nothing waits on another CTA.
+constexpr int kRPTile = 64;         // output tile: 64 tokens x 64 experts, 4 x 4 per thread
+constexpr int kRPTargetSlices = 128;
+constexpr int kRPMaxLoads = 8;      // x vectors staged per thread (T <= 128, hs <= 128)
+constexpr int kRFMaxChunks = kRouterSmallT / kRouterTokens;
 
-template <int EPT>
-__global__ void __launch_bounds__(256) router_small_kernel(const uint16_t* __restrict__ x,
-                                                           const float* __restrict__ Wr, int T, int H, int E,
-                                                           int E_pad, float* __restrict__ L,
-                                                           const float* __restrict__ bias, int k,
-                                                           int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                           int32_t* __restrict__ rank, int32_t* __restrict__ hist,
-                                                           int32_t* __restrict__ offsets, int32_t* __restrict__ counts,
-                                                           unsigned int* __restrict__ ticket) {
-    constexpr int NV = kRSmallTB * kRSmallEB;
-    __shared__ float red[8][NV];
-    __shared__ uint32_t mask[32 * EPT];
-    __shared__ int32_t wsum[8];
-    __shared__ int is_last;
-    const int e0 = blockIdx.x * kRSmallEB, t0 = blockIdx.y * kRSmallTB;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const bool vec_w = (E % 4 == 0) && (e0 + kRSmallEB <= E);  // Wr rows 16-byte aligned, 8 experts present
+__device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) {
+    asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src)
+                 : "memory");
+}
+
+__global__ void __launch_bounds__(256) router_partial_kernel(const uint16_t* __restrict__ x,
+                                                             const float* __restrict__ Wr, int T, int H, int E,
+                                                             int E_pad, int hs_max, float* __restrict__ P) {
+    extern __shared__ float4 rp_smem[];
+    const int T64 = (T + kRPTile - 1) / kRPTile * kRPTile;
+    const int E64 = (E + kRPTile - 1) / kRPTile * kRPTile;
+    float* xs = reinterpret_cast<float*>(rp_smem);  // [hs_max][T64]
+    float* ws = xs + (size_t)hs_max * T64;           // [hs_max][E64]
+    const int tid = threadIdx.x;
+    const int s = blockIdx.x, h0 = s * hs_max, hs = min(hs_max, H - h0);
     pdl_wait();
     pdl_trigger();
-    float acc[NV];  // [token][expert]
+    // Wr rows h0 .. h0 + hs (one contiguous block), columns padded with zeros to E64
+    if (E % 4 == 0) {
+        const int q = E / 4;
+        for (int i = tid; i < hs * q; i += 256) {
+            const int r = i / q, c = i - r * q;
+            cp_async16(ws + (size_t)r * E64 + 4 * c, Wr + (size_t)(h0 + r) * E + 4 * c);
+        }
+    } else {
+        for (int i = tid; i < hs * E; i += 256) {
+            const int r = i / E, c = i - r * E;
+            cp_async4(ws + (size_t)r * E64 + c, Wr + (size_t)(h0 + r) * E + c);
+        }
+    }
+    for (int i = tid; i < hs * (E64 - E); i += 256) {
+        const int r = i / (E64 - E);
+        ws[(size_t)r * E64 + E + (i - r * (E64 - E))] = 0.f;
+    }
+    // x[t][h0 .. h0 + hs]: 8 bf16 per 16-byte load, every load in flight
+    // before any store; stored transposed as fp32, tokens past T are zero
+    const int hv = hs / 8;  // 16-byte vectors per token row
+    uint4 v[kRPMaxLoads];
 #pragma unroll
-    for (int i = 0; i < NV; ++i) acc[i] = 0.f;
-    for (int c = tid; c < H / 8; c += 256) {
-        const int h = c * 8;
-        uint4 xv[kRSmallTB];
+    for (int j = 0; j < kRPMaxLoads; ++j) {
+        const int i = tid + 256 * j;
+        const int t = i / hv, c = i - t * hv;
+        v[j] = (t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * H + h0) + c)
+                       : make_uint4(0u, 0u, 0u, 0u);
+    }
 #pragma unroll
-        for (int t = 0; t < kRSmallTB; ++t)
-            xv[t] = (t0 + t < T) ? __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + t) * H + h))
-                                 : make_uint4(0u, 0u, 0u, 0u);
+    for (int j = 0; j < kRPMaxLoads; ++j) {
+        const int i = tid + 256 * j;
+        const int t = i / hv, c = i - t * hv;
+        if (t < T64) {
+            const uint32_t w4[4] = {v[j].x, v[j].y, v[j].z, v[j].w};
 #pragma unroll
-        for (int hh = 0; hh < 8; ++hh) {
-            float w[kRSmallEB];
-            const float* wrow = Wr + (size_t)(h + hh) * E + e0;
-            if (vec_w) {
-                const float4 a = __ldg(reinterpret_cast<const float4*>(wrow));
-                const float4 b = __ldg(reinterpret_cast<const float4*>(wrow) + 1);
-                w[0] = a.x; w[1] = a.y; w[2] = a.z; w[3] = a.w;
-                w[4] = b.x; w[5] = b.y; w[6] = b.z; w[7] = b.w;
-            } else {
-#pragma unroll
-                for (int e = 0; e < kRSmallEB; ++e) w[e] = (e0 + e < E) ? __ldg(wrow + e) : 0.f;
-            }
-#pragma unroll
-            for (int t = 0; t < kRSmallTB; ++t) {
-                const uint32_t word = (&xv[t].x)[hh >> 1];
-                const float xf = __uint_as_float((hh & 1) ? (word & 0xffff0000u) : (word << 16));
-#pragma unroll
-                for (int e = 0; e < kRSmallEB; ++e) acc[t * kRSmallEB + e] = fmaf(xf, w[e], acc[t * kRSmallEB + e]);
+            for (int m = 0; m < 4; ++m) {
+                xs[(size_t)(8 * c + 2 * m) * T64 + t] = __uint_as_float(w4[m] << 16);
+                xs[(size_t)(8 * c + 2 * m + 1) * T64 + t] = __uint_as_float(w4[m] & 0xffff0000u);
             }
         }
     }
-    WarpButterfly<float, NV, 16, NV / 32>::run(acc, lane);  // lane l: values 2l, 2l + 1
-#pragma unroll
-    for (int i = 0; i < NV / 32; ++i) red[warp][lane * (NV / 32) + i] = acc[i];
+    cp_async_wait_all();
     __syncthreads();
-    if (tid < NV) {
-        float v = red[0][tid];
+
+    const int tx = tid & 15, ty = tid >> 4;
+    float* out = P + (size_t)s * T * E_pad;
+    for (int tt0 = 0; tt0 < T; tt0 += kRPTile)
+        for (int te0 = 0; te0 < E; te0 += kRPTile) {
+            float acc[4][4];
 #pragma unroll
-        for (int w = 1; w < 8; ++w) v = __fadd_rn(v, red[w][tid]);
-        const int t = t0 + tid / kRSmallEB, e = e0 + tid % kRSmallEB;
-        if (t < T && e < E_pad) L[(size_t)t * E_pad + e] = v;
+            for (int a = 0; a < 4; ++a)
+#pragma unroll
+                for (int b = 0; b < 4; ++b) acc[a][b] = 0.f;
+            const float* xp = xs + tt0 + 4 * ty;
+            const float* wp = ws + te0 + 4 * tx;
+#pragma unroll 8
+            for (int h = 0; h < hs; ++h) {
+                const float4 xv = *reinterpret_cast<const float4*>(xp + (size_t)h * T64);
+                const float4 wv = *reinterpret_cast<const float4*>(wp + (size_t)h * E64);
+                const float xa[4] = {xv.x, xv.y, xv.z, xv.w}, wa[4] = {wv.x, wv.y, wv.z, wv.w};
+#pragma unroll
+                for (int a = 0; a < 4; ++a)
+#pragma unroll
+                    for (int b = 0; b < 4; ++b) acc[a][b] = fmaf(xa[a], wa[b], acc[a][b]);
+            }
+#pragma unroll
+            for (int a = 0; a < 4; ++a) {
+                const int t = tt0 + 4 * ty + a;
+                if (t >= T) continue;
+#pragma unroll
+                for (int b = 0; b < 4; ++b) {
+                    const int e = te0 + 4 * tx + b;
+                    if (e < E_pad) out[(size_t)t * E_pad + e] = acc[a][b];
+                }
+            }
+        }
+}
+
+template <int EPT>
+__global__ void __launch_bounds__(256) router_finish_kernel(const float* __restrict__ P, int KS, int T, int E,
+                                                            int E_pad, const float* __restrict__ bias, int k,
+                                                            int32_t* __restrict__ topk_ids,
+                                                            float* __restrict__ topk_w, int32_t* __restrict__ rank,
+                                                            int32_t* __restrict__ hist,
+                                                            int32_t* __restrict__ offsets,
+                                                            int32_t* __restrict__ counts,
+                                                            unsigned int* __restrict__ ticket) {
+    constexpr int EP = 32 * EPT;
+    __shared__ float part[8][EP];
+    __shared__ uint32_t mask[kRFMaxChunks * kMaxExperts];
+    __shared__ int32_t wsum[8];
+    __shared__ int is_last;
+    const int t = blockIdx.x;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    pdl_wait();
+    pdl_trigger();
+    // warp w: slices [w * per, (w + 1) * per) in order, kB slices' loads at a time
+    constexpr int kB = EPT <= 2 ? 16 : 32 / EPT;
+    const int per = (KS + 7) / 8;
+    const int s0 = warp * per, s1 = min(KS, s0 + per);
+    float acc[EPT];
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) acc[i] = 0.f;
+    for (int sb = s0; sb < s1; sb += kB) {
+        float pv[kB][EPT];
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int s = sb + u, e = lane + 32 * i;
+                pv[u][i] = (s < s1 && e < E) ? __ldcg(P + ((size_t)s * T + t) * E_pad + e) : 0.f;
+            }
+#pragma unroll
+        for (int u = 0; u < kB; ++u)
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) acc[i] = __fadd_rn(acc[i], pv[u][i]);
+    }
+#pragma unroll
+    for (int i = 0; i < EPT; ++i) part[warp][lane + 32 * i] = acc[i];
+    __syncthreads();
+    if (warp == 0) {
+        float v[EPT];
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const int e = lane + 32 * i;
+            float l = part[0][e];
+#pragma unroll
+            for (int w = 1; w < 8; ++w) l = __fadd_rn(l, part[w][e]);
+            if (bias && e < E) l = __fadd_rn(l, bias[e]);
+            v[i] = e < E ? l : -INFINITY;
+        }
+        int my_e;
+        float my_w;
+        warp_topk<EPT>(v, E, k, lane, my_e, my_w);
+        if (lane < k) {
+            topk_ids[(size_t)t * k + lane] = my_e;
+            topk_w[(size_t)t * k + lane] = my_w;
+        }
     }
 
-    // ---- the last CTA: top-k of every chunk, then the prefix sums
-    __threadfence();  // this thread's logits are visible device-wide before the ticket
+    // ---- the last CTA: chunk masks, ranks, then the prefix sums
+    __threadfence();  // this CTA's choices are visible device-wide before the ticket
     __syncthreads();
-    if (tid == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x * gridDim.y - 1u;
+    if (tid == 0) is_last = atomicAdd(ticket, 1u) == gridDim.x - 1u;
     __syncthreads();
     if (!is_last) return;
     __threadfence();
     const int nchunk = (T + kRouterTokens - 1) / kRouterTokens;
-    for (int c = 0; c < nchunk; ++c) {
-        topk_chunk<EPT>(L, 1, T, E, E_pad, bias, k, c, topk_ids, topk_w, rank, hist, mask);
-        __syncthreads();  // hist and mask are complete before the next chunk reuses mask
+    for (int i = tid; i < nchunk * E; i += 256) mask[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < T * k; i += 256) {
+        const int tk = i / k;
+        const int e = __ldcg(topk_ids + i);
+        atomicOr(&mask[(tk / kRouterTokens) * E + e], 1u << (tk % kRouterTokens));
+    }
+    __syncthreads();
+    for (int i = tid; i < T * k; i += 256) {
+        const int tk = i / k;
+        const int e = __ldcg(topk_ids + i);
+        rank[i] = __popc(mask[(tk / kRouterTokens) * E + e] & ((1u << (tk % kRouterTokens)) - 1u));
     }
     // per expert: first slot of each chunk relative to the expert, and its total
     int32_t tot = 0;
     if (tid < E) {
         for (int c = 0; c < nchunk; ++c) {
-            const int32_t v = hist[(size_t)c * E + tid];
             hist[(size_t)c * E + tid] = tot;
-            tot += v;
+            tot += __popc(mask[c * E + tid]);
         }
     }
     // exclusive prefix of the totals over the experts (E <= 256 = blockDim)
@@ -503,9 +630,11 @@ RouterPlan router_plan(int64_t T, int64_t H, int64_t E) {
     p.NB = p.E_pad <= 128 ? p.E_pad : 128;
     p.n_eb = (p.E_pad + p.NB - 1) / p.NB;
     p.small = T <= kRouterSmallT;
-    if (p.small) {  // CUDA-core router: whole logits, one "slice"
-        p.kb_per_slice = (int)(H / kRBK);
-        p.KS = 1;
+    if (p.small) {  // CUDA-core router: KS slices of hs rows of Wr (about kRPTargetSlices)
+        const int64_t rows = (H + kRPTargetSlices - 1) / kRPTargetSlices;
+        p.hs = (int)((rows + 7) / 8 * 8);
+        p.KS = (int)((H + p.hs - 1) / p.hs);
+        p.kb_per_slice = 0;
         return p;
     }
     const int nkb = (int)(H / kRBK);
@@ -525,18 +654,33 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
                           uint64_t timeout_ns, cudaStream_t st, bool pdl) {
     const RouterPlan p = router_plan(T, H, E);
     cudaError_t e;
-    if (p.small) {  // one kernel: logits, top-k and the prefix sums
-        const dim3 grid((E + kRSmallEB - 1) / kRSmallEB, (T + kRSmallTB - 1) / kRSmallTB), block(256);
+    if (p.small) {  // partial logits per slice of Wr; per token the sums and top-k; prefix sums
+        const int T64 = (T + kRPTile - 1) / kRPTile * kRPTile, E64 = (E + kRPTile - 1) / kRPTile * kRPTile;
+        const int smem = p.hs * (T64 + E64) * (int)sizeof(float);
+        {
+            static std::mutex mu;
+            static int smem_set = 0;
+            std::lock_guard<std::mutex> lock(mu);
+            if (smem > smem_set) {
+                e = cudaFuncSetAttribute(router_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, smem);
+                if (e != cudaSuccess) return e;
+                smem_set = smem;
+            }
+        }
+        e = launch_kernel(router_partial_kernel, dim3(p.KS), dim3(256), (size_t)smem, st, false, x, Wr, T, H, E,
+                          p.E_pad, p.hs, P);
+        if (e != cudaSuccess) return e;
+        const dim3 grid(T), block(256);
         if (E <= 32)
-            return launch_kernel(router_small_kernel<1>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
-                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+            return launch_kernel(router_finish_kernel<1>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
         if (E <= 64)
-            return launch_kernel(router_small_kernel<2>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
-                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+            return launch_kernel(router_finish_kernel<2>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
         if (E <= 128)
-            return launch_kernel(router_small_kernel<4>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias,
-                                 k, topk_ids, topk_w, rank, hist, offsets, counts, ticket);
-        return launch_kernel(router_small_kernel<8>, grid, block, 0, st, false, x, Wr, T, H, E, p.E_pad, P, bias, k,
+            return launch_kernel(router_finish_kernel<4>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+        return launch_kernel(router_finish_kernel<8>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
                              topk_ids, topk_w, rank, hist, offsets, counts, ticket);
     }
     e = launch_kernel(router_split_kernel, dim3((H + 31) / 32, (p.E_pad + 31) / 32), dim3(256), 0, st, false, Wr, H,

@@ -147,6 +147,98 @@ __global__ void __launch_bounds__(256) requant_fp8_kernel(const float* __restric
     }
 }
 
+// Few rows (decode): one CTA of 256 threads per token (or per row of h), the
+// row held in registers, so that the whole GPU works on the few rows; the
+// same outputs as the warp-per-row kernels above.  H <= 256 * 8 * kF8Vec
+// (bf16 x) and I <= 256 * 4 * kF8Vec (fp32 h).
+constexpr int kF8Vec = 8;
+
+__device__ __forceinline__ float cta_max_f(float v, float* red) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+    v = warp_max_f(v);
+    if (lane == 0) red[warp] = v;
+    __syncthreads();
+    v = red[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) v = fmaxf(v, red[i]);
+    return v;
+}
+
+__global__ void __launch_bounds__(256) permute_quant_fp8_cta_kernel(
+    const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ rank,
+    const int32_t* __restrict__ base, int T, int H, int E, int k, int32_t* __restrict__ slot_of,
+    int32_t* __restrict__ slot_token, float* __restrict__ s_x, float* __restrict__ s_slot,
+    uint8_t* __restrict__ q8) {
+    __shared__ float red[8];
+    __shared__ int slots_s[kMaxTopK];
+    const int tid = threadIdx.x;
+    const int t = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (t >= T) return;
+    if (tid < k) {
+        const int e = topk_ids[(size_t)t * k + tid];
+        const int my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid];
+        slot_of[(size_t)t * k + tid] = my_slot;
+        slot_token[my_slot] = t;
+        slots_s[tid] = my_slot;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int nv = H / 8;  // 8 bf16 per 16-byte vector
+    uint4 v[kF8Vec];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kF8Vec; ++i) {
+        const int idx = tid + 256 * i;
+        v[i] = idx < nv ? __ldg(row + idx) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) amax = fmaxf(amax, fmaxf(fabsf(bf16_lo(w[j])), fabsf(bf16_hi(w[j]))));
+    }
+    amax = cta_max_f(amax, red);  // its barrier also publishes slots_s
+    const float s = __fdiv_rn(amax, kE4m3Max);
+    if (tid == 0) s_x[t] = s;
+    if (tid < k) s_slot[slots_s[tid]] = s;
+#pragma unroll
+    for (int i = 0; i < kF8Vec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        const uint2 c = make_uint2(e4m3_codes4(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y), s),
+                                   e4m3_codes4(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w), bf16_hi(v[i].w), s));
+        for (int j = 0; j < k; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = c;
+    }
+}
+
+__global__ void __launch_bounds__(256) requant_fp8_cta_kernel(const float* __restrict__ h, int S, int I,
+                                                              float* __restrict__ s_h, uint8_t* __restrict__ q8) {
+    __shared__ float red[8];
+    const int tid = threadIdx.x;
+    const int r = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (r >= S) return;
+    const float4* row = reinterpret_cast<const float4*>(h + (size_t)r * I);
+    const int nv = I / 4;
+    float4 v[kF8Vec];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kF8Vec; ++i) {
+        const int idx = tid + 256 * i;
+        v[i] = idx < nv ? row[idx] : make_float4(0.f, 0.f, 0.f, 0.f);
+        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v[i].x)), fmaxf(fabsf(v[i].y), fabsf(v[i].z))), fabsf(v[i].w));
+    }
+    amax = cta_max_f(amax, red);
+    const float s = __fdiv_rn(amax, kE4m3Max);
+    if (tid == 0) s_h[r] = s;
+    uint32_t* qr = reinterpret_cast<uint32_t*>(q8 + (size_t)r * I);
+#pragma unroll
+    for (int i = 0; i < kF8Vec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        qr[idx] = e4m3_codes4(v[i].x, v[i].y, v[i].z, v[i].w, s);
+    }
+}
+
 // One tcgen05 MMA, kind::f8f6f4, both operands from shared memory: D[M x N]
 // (+)= A[M x 32] * B[N x 32]^T.  The instruction descriptor's operand format
 // fields are 0 = E4M3 for this kind.
@@ -499,12 +591,17 @@ cudaError_t launch_permute_quant_fp8(const uint16_t* x, const int32_t* topk_ids,
                                      int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, cudaStream_t st,
                                      bool pdl) {
     if (T == 0) return cudaSuccess;
+    if ((long)T <= 8L * num_sms() && H <= 256 * 8 * kF8Vec)  // few tokens: a CTA per token
+        return launch_kernel(permute_quant_fp8_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
+                             T, H, E, k, slot_of, slot_token, s_x, s_slot, q8);
     return launch_kernel(permute_quant_fp8_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
                          T, H, E, k, slot_of, slot_token, s_x, s_slot, q8);
 }
 
 cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t* q8, cudaStream_t st, bool pdl) {
     if (S == 0) return cudaSuccess;
+    if ((long)S <= 8L * num_sms() && I <= 256 * 4 * kF8Vec)  // few rows: a CTA per row
+        return launch_kernel(requant_fp8_cta_kernel, dim3(S), dim3(256), 0, st, pdl, h, S, I, s_h, q8);
     return launch_kernel(requant_fp8_kernel, dim3((S + 7) / 8), dim3(256), 0, st, pdl, h, S, I, s_h, q8);
 }
 

@@ -127,10 +127,12 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
 // A warp per token, 8 per CTA: the amax pass and the code pass each read the
 // row (the second mostly from cache).  (Measured at T = 8192: staging rows
 // through shared memory with cp.async, 4 tokens per CTA, was slower: 53
-// against 52 us.)
+// against 52 us.)  Registers are capped for 8 CTAs per SM, so that the 1024
+// CTAs of T = 8192 run in one wave instead of 6 per SM and a tail of 112
+// (measured: 54 -> 51 us; the kernel is issue-bound, 55 % issue-active).
 constexpr int kPqWarps = 8;
 
-__global__ void __launch_bounds__(32 * kPqWarps) permute_quant_kernel(
+__global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,

@@ -48,6 +48,15 @@ CASES = {
     "pair_skewed": TINY.replace(T=1200, H=256, I=256, E=8, k=2, bias="zipf", zipf_s=1.2),
     # about 125 rows per expert: one partial CTA-pair tile per expert
     "pair_one_tile": TINY.replace(T=500, H=512, I=256, E=8, k=2),
+    # few-token router: an expert count that is not a multiple of 4 (router
+    # weights staged 4 bytes at a time), top-3
+    "odd_experts": TINY.replace(T=90, H=384, I=256, E=7, k=3),
+    # few-token router at its largest T, 40 experts (padded logit tiles)
+    "few_token_max": TINY.replace(T=128, H=512, I=256, E=40, k=3),
+    # one token past it: the tensor-core router
+    "tensor_router_min": TINY.replace(T=129, H=512, I=256, E=12, k=2),
+    # the most experts and choices the library takes, few tokens
+    "experts_256_top8": TINY.replace(T=100, H=256, I=128, E=256, k=8),
 }
 
 

@@ -264,6 +264,73 @@ MOE_W8A8_API moe_status_t moe_w8a8_fp8_forward_debug(const uint16_t* x, const fl
                                                      const moe_w8a8_debug_t* dbg);
 
 /* ---------------------------------------------------------------------------
+ * moe_w8a8_forward_host -- moe_w8a8_forward for activations that live in
+ * host memory: x is copied in and y copied out inside the call, in token
+ * chunks, so that the copies of one chunk overlap the layer's compute on
+ * another.  The method's pages have no counterpart to it: it is the layer of
+ * moe_w8a8_forward ("Tencent Hunyuan AI Infra on Hopper", section 1.3, and
+ * "W8A8 quantisation of MiniMax-M3 on K100AI", section 2.1) applied to each
+ * chunk of tokens, tokens being independent in the layer.
+ *
+ *   x_host      bf16 [T][H]  host memory, page-locked (cudaHostAlloc or
+ *                            cudaHostRegister) for the copies to overlap
+ *   y_host      bf16 [T][H]  host memory (output), page-locked likewise
+ *   x_dev       bf16 [T][H]  device staging for x (caller-owned)
+ *   y_dev       bf16 [T][H]  device staging for y (caller-owned)
+ *   other arguments as moe_w8a8_forward; the workspace is sized for T
+ *   copy_stream a second stream for the copies, or NULL (copies then go on
+ *               `stream`, in order with the compute: nothing overlaps); with
+ *               one chunk the copies go on `stream` in any case
+ *   chunks      0: the library chooses (moe_w8a8_host_chunks); 1..16: that
+ *               many chunks of near-equal token counts
+ *
+ * Measured on GB300 (prefill layer, T = 8192, H = 4096, 64 experts): the host
+ * link moves ~200 GB/s each way, so x in and y out take about as long as the
+ * layer; two chunks overlap them but make the two half-size layers cost 1.4x
+ * the whole one, a net gain of 3 % (INT8) to 7 % (FP8); more chunks lose.
+ *
+ * Each chunk is a complete forward of its tokens: its result equals
+ * moe_w8a8_forward on those tokens bit for bit, and with one chunk it equals
+ * moe_w8a8_forward on the batch.  Over several chunks, the router's binary32
+ * sums may associate differently than for the whole batch (the router's
+ * partition of the hidden dimension depends on the token count), so a token
+ * can differ from the whole-batch call only as two evaluations of the layer
+ * within its stated accuracy can.  Every chunk re-reads the weights of the
+ * experts its tokens touch.
+ * Ordering: the copies wait for work queued on `stream` before the call (the
+ * staging buffers are free), and work queued on `stream` after the call waits
+ * for the last copy of y: synchronising `stream` makes y_host complete.
+ * No host synchronisation.  Creates a few CUDA events once per host thread
+ * (kept for the life of the process); allocates no memory.
+ * Errors: as moe_w8a8_forward, checked before anything is queued, plus
+ * MOE_ERR_INVALID_ARG for chunks outside 0..16 or a null/misaligned staging
+ * or host pointer; MOE_ERR_CUDA for a failed copy, event or launch.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_forward_host(const uint16_t* x_host, const float* router_w,
+                                                const float* router_bias, const int8_t* w13_q,
+                                                const float* w13_scale, const int8_t* w2_q, const float* w2_scale,
+                                                int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
+                                                uint16_t* y_host, uint16_t* x_dev, uint16_t* y_dev,
+                                                void* workspace, size_t workspace_bytes, void* stream,
+                                                void* copy_stream, int chunks);
+
+/* moe_w8a8_forward_host for the FP8 (E4M3) layer of moe_w8a8_fp8_forward. */
+MOE_W8A8_API moe_status_t moe_w8a8_fp8_forward_host(const uint16_t* x_host, const float* router_w,
+                                                    const float* router_bias, const uint8_t* w13_q,
+                                                    const float* w13_scale, const uint8_t* w2_q,
+                                                    const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                                    int64_t E, int64_t top_k, uint16_t* y_host, uint16_t* x_dev,
+                                                    uint16_t* y_dev, void* workspace, size_t workspace_bytes,
+                                                    void* stream, void* copy_stream, int chunks);
+
+/* The number of chunks moe_w8a8_forward_host takes for chunks == 0: two when
+ * T >= 2048 and one direction of the host link (about 200 GB/s on GB300)
+ * moves x more slowly than HBM (about 6.6 TB/s) streams every expert's
+ * weights once, i.e. when T * H * 2 * 32 > E * 3 * H * I bytes; else one.
+ * 0 for T < 0. */
+MOE_W8A8_API int moe_w8a8_host_chunks(int64_t T, int64_t H, int64_t I, int64_t E);
+
+/* ---------------------------------------------------------------------------
  * moe_w8a8_device_error -- synchronise `stream`, then read and clear the
  * sticky device error word in the first bytes of `workspace`.  Returns
  * MOE_OK, MOE_ERR_DEVICE_TIMEOUT (a pipeline wait inside a kernel gave up;

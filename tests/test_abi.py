@@ -93,6 +93,37 @@ def test_forward_with_no_tokens_is_a_no_op(lib):
     assert _fwd(lib, T=0) == OK
 
 
+
+def _fwd_host(lib, T=16, H=256, I=512, E=8, k=2, ptrs=None, ws_bytes=None, chunks=0, fn="moe_w8a8_forward_host"):
+    p = dict(xh=FAKE, rw=FAKE, w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, yh=FAKE, xd=FAKE, yd=FAKE, ws=FAKE)
+    p.update(ptrs or {})
+    need = lib.moe_w8a8_workspace_size(T, H, I, E, k)
+    return getattr(lib, fn)(p["xh"], p["rw"], None, p["w13"], p["s13"], p["w2"], p["s2"], T, H, I, E, k, p["yh"],
+                            p["xd"], p["yd"], p["ws"], need if ws_bytes is None else ws_bytes, None, None, chunks)
+
+
+@pytest.mark.parametrize("fn", ["moe_w8a8_forward_host", "moe_w8a8_fp8_forward_host"])
+def test_forward_host_rejects_bad_arguments_without_copying(lib, fn):
+    assert _fwd_host(lib, H=100, fn=fn) == SHAPE
+    for name in ("xh", "rw", "w13", "s13", "w2", "s2", "yh", "xd", "yd", "ws"):
+        assert _fwd_host(lib, ptrs={name: None}, fn=fn) == INVALID, name
+        assert _fwd_host(lib, ptrs={name: FAKE + 4}, fn=fn) == INVALID, name
+    assert _fwd_host(lib, chunks=-1, fn=fn) == INVALID
+    assert _fwd_host(lib, chunks=17, fn=fn) == INVALID
+    assert _fwd_host(lib, ws_bytes=1024, fn=fn) == WS_SMALL
+    assert _fwd_host(lib, T=0, fn=fn) == OK  # no tokens: nothing is copied or launched
+
+
+def test_host_chunk_rule(lib):
+    # prefill-shaped: x moves over the host link more slowly than HBM streams the weights -> 2
+    assert lib.moe_w8a8_host_chunks(8192, 4096, 1536, 64) == 2
+    # weights dominate (256 experts) or few tokens -> 1
+    assert lib.moe_w8a8_host_chunks(4096, 7168, 2048, 256) == 1
+    assert lib.moe_w8a8_host_chunks(64, 4096, 1536, 64) == 1
+    assert lib.moe_w8a8_host_chunks(2047, 4096, 128, 1) == 1
+    assert lib.moe_w8a8_host_chunks(0, 4096, 1536, 64) == 1
+    assert lib.moe_w8a8_host_chunks(-1, 4096, 1536, 64) == 0
+
 def test_linear_rejects_bad_arguments(lib):
     need = lib.moe_w8a8_linear_workspace_size(64, 256, 256)
     assert need > 0

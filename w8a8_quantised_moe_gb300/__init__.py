@@ -20,7 +20,7 @@ from ._lib import MoeError, STATUS
 
 __all__ = [
     "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward",
-    "forward_debug", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns", "set_gemm_path",
+    "forward_debug", "forward_host", "host_chunks", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns", "set_gemm_path",
     "GEMM_PATHS",
     "version",
 ]
@@ -131,6 +131,66 @@ def forward(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, w
         _stream(stream)), "moe_w8a8_forward")
     return y
 
+
+
+
+def _need_host(t, dtype, shape, name):
+    torch = _torch()
+    if not isinstance(t, torch.Tensor):
+        raise TypeError(f"{name} must be a torch.Tensor")
+    if t.is_cuda or t.dtype != dtype or tuple(t.shape) != tuple(shape) or not t.is_contiguous():
+        raise ValueError(f"{name}: expected contiguous host {dtype} {tuple(shape)} (page-locked for the copies "
+                         f"to overlap), got {t.dtype} {tuple(t.shape)} on {t.device}")
+
+def host_chunks(T, H, I, E) -> int:
+    """Token chunks ``forward_host`` takes when ``chunks`` is 0."""
+    return int(_lib.load().moe_w8a8_host_chunks(T, H, I, E))
+
+
+def _forward_host(fn, name, code_dtype, x_host, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k,
+                  y_host, x_dev, y_dev, workspace, stream, copy_stream, chunks):
+    torch = _torch()
+    T, H = x_host.shape
+    E = router_w.shape[1]
+    I = w2_q.shape[2] if w2_q.dim() == 3 else 0
+    _need_host(x_host, torch.bfloat16, (T, H), "x_host")
+    _need(router_w, torch.float32, (H, E), "router_w")
+    if router_bias is not None:
+        _need(router_bias, torch.float32, (E,), "router_bias")
+    _need(w13_q, code_dtype, (E, 2 * I, H), "w13_q")
+    _need(w13_scale, torch.float32, (E, 2 * I), "w13_scale")
+    _need(w2_q, code_dtype, (E, H, I), "w2_q")
+    _need(w2_scale, torch.float32, (E, H), "w2_scale")
+    dev = router_w.device
+    if y_host is None:
+        y_host = torch.empty((T, H), dtype=torch.bfloat16).pin_memory()
+    _need_host(y_host, torch.bfloat16, (T, H), "y_host")
+    if x_dev is None:
+        x_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    if y_dev is None:
+        y_dev = torch.empty((T, H), dtype=torch.bfloat16, device=dev)
+    _need(x_dev, torch.bfloat16, (T, H), "x_dev")
+    _need(y_dev, torch.bfloat16, (T, H), "y_dev")
+    if workspace is None:
+        workspace = new_workspace(workspace_size(T, H, I, E, top_k), dev)
+    cs = None if copy_stream is None else copy_stream.cuda_stream
+    _lib.check(fn(
+        _ptr(x_host), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y_host), _ptr(x_dev), _ptr(y_dev), _ptr(workspace),
+        workspace.numel() * workspace.element_size(), _stream(stream), cs, int(chunks)), name)
+    return y_host
+
+
+def forward_host(x_host, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, y_host=None, x_dev=None,
+                 y_dev=None, workspace=None, stream=None, copy_stream=None, chunks=0):
+    """The MoE layer on host-resident bf16 x [T, H] -> host bf16 y [T, H]:
+    copies in and out inside the call, overlapped with compute on
+    ``copy_stream`` (see include/moe_w8a8.h).  y_host is complete once
+    ``stream`` is synchronised."""
+    torch = _torch()
+    return _forward_host(_lib.load().moe_w8a8_forward_host, "moe_w8a8_forward_host", torch.int8, x_host, router_w,
+                         router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, y_host, x_dev, y_dev, workspace,
+                         stream, copy_stream, chunks)
 
 _DEBUG_FIELDS = {
     # name: (dtype, shape(T, H, I, E, k))
@@ -266,3 +326,12 @@ def fp8_forward_debug(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale
         T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
         _stream(stream), ctypes.byref(bufs)), "moe_w8a8_fp8_forward_debug")
     return y, out
+
+
+def fp8_forward_host(x_host, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, y_host=None,
+                     x_dev=None, y_dev=None, workspace=None, stream=None, copy_stream=None, chunks=0):
+    """``forward_host`` for the FP8 layer (w13_q, w2_q E4M3 as uint8)."""
+    torch = _torch()
+    return _forward_host(_lib.load().moe_w8a8_fp8_forward_host, "moe_w8a8_fp8_forward_host", torch.uint8, x_host,
+                         router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, y_host, x_dev, y_dev,
+                         workspace, stream, copy_stream, chunks)

@@ -43,6 +43,9 @@ EXPORTS = (
     "moe_w8a8_fp8_quantize_weights",
     "moe_w8a8_fp8_forward",
     "moe_w8a8_fp8_forward_debug",
+    "moe_w8a8_forward_host",
+    "moe_w8a8_fp8_forward_host",
+    "moe_w8a8_host_chunks",
 )
 
 
@@ -92,6 +95,11 @@ def load(path: str = LIB_PATH):
             "moe_w8a8_fp8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
             "moe_w8a8_fp8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
                                             ctypes.POINTER(DebugBuffers)], i32),
+            "moe_w8a8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz, vp,
+                                       vp, i32], i32),
+            "moe_w8a8_fp8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz,
+                                           vp, vp, i32], i32),
+            "moe_w8a8_host_chunks": ([i64, i64, i64, i64], i32),
         }
         for name, (args, res) in decl.items():
             fn = getattr(lib, name)

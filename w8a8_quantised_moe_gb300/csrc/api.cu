@@ -13,6 +13,7 @@
 #include <atomic>
 #include <cstdlib>
 #include <cstring>
+#include <vector>
 
 #include "moe_w8a8.h"
 #include "internal.h"
@@ -314,6 +315,98 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     return MOE_OK;
 }
 
+// Host-resident activations: x copied in and y copied out in token chunks on
+// a copy stream, overlapping the layer's compute on another chunk.  Tokens
+// are independent in the layer, so each chunk is a whole forward of its own
+// tokens (routing, expert GEMMs and combine over just those tokens).
+// Splitting re-reads the touched experts' weights once per chunk, so two
+// chunks are taken only where one direction of the host link moves x more
+// slowly than HBM streams all the expert weights once (kLinkHbmRatio: about
+// 200 GB/s per direction of the host link against about 6.6 TB/s of HBM).
+constexpr double kLinkHbmRatio = 32.0;
+constexpr int64_t kMinChunkTokens = 1024;
+constexpr int kMaxChunks = 16;
+
+int auto_chunks(int64_t T, int64_t H, int64_t I, int64_t E) {
+    const double x_bytes = (double)T * (double)H * 2.0;
+    const double w_bytes = (double)E * 3.0 * (double)H * (double)I;
+    return (T >= 2 * kMinChunkTokens && x_bytes * kLinkHbmRatio > w_bytes) ? 2 : 1;
+}
+
+// One event pool per host thread, created on first use and kept for the
+// life of the process (the only CUDA objects the library creates).
+cudaEvent_t* event_pool(int n) {
+    thread_local std::vector<cudaEvent_t> pool;
+    while ((int)pool.size() < n) {
+        cudaEvent_t ev;
+        if (cudaEventCreateWithFlags(&ev, cudaEventDisableTiming) != cudaSuccess) return nullptr;
+        pool.push_back(ev);
+    }
+    return pool.data();
+}
+
+moe_status_t forward_host_impl(const uint16_t* x_host, const float* router_w, const float* router_bias,
+                               const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                               const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                               uint16_t* y_host, uint16_t* x_dev, uint16_t* y_dev, void* workspace,
+                               size_t workspace_bytes, void* stream, void* copy_stream, int chunks, bool fp8) {
+    if (!moe_shape_ok(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    const void* ptrs[] = {x_host, y_host, x_dev, y_dev, router_w, w13_q, w13_scale, w2_q, w2_scale, workspace};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+    if (router_bias != nullptr && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (chunks < 0 || chunks > kMaxChunks) return MOE_ERR_INVALID_ARG;
+    if (workspace_bytes < fwd_layout(T, H, I, E, k).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    int n = chunks == 0 ? auto_chunks(T, H, I, E) : chunks;
+    if (n > T) n = (int)T;
+    cudaStream_t cs = static_cast<cudaStream_t>(stream);
+    cudaStream_t ps = copy_stream ? static_cast<cudaStream_t>(copy_stream) : cs;
+    const bool two = ps != cs && n > 1;
+    if (!two) ps = cs;  // one chunk (or one stream): nothing to overlap, everything in order on `stream`
+    cudaEvent_t* ev = two ? event_pool(2 * n + 2) : nullptr;  // start, in[n], out[n], done
+    if (two && ev == nullptr) return MOE_ERR_CUDA;
+    cudaError_t e;
+    auto chunk = [&](int c, int64_t& t0, int64_t& tc) {
+        t0 = T * c / n;
+        tc = T * (c + 1) / n - t0;
+    };
+    if (two) {  // the staging buffers are free of earlier work on the compute stream
+        if ((e = cudaEventRecord(ev[0], cs)) != cudaSuccess) return from_cuda(e);
+        if ((e = cudaStreamWaitEvent(ps, ev[0], 0)) != cudaSuccess) return from_cuda(e);
+    }
+    for (int c = 0; c < n; ++c) {  // every input copy first: they run while earlier chunks compute
+        int64_t t0, tc;
+        chunk(c, t0, tc);
+        const size_t off = (size_t)t0 * H, bytes = (size_t)tc * H * 2;
+        if ((e = cudaMemcpyAsync(x_dev + off, x_host + off, bytes, cudaMemcpyHostToDevice, ps)) != cudaSuccess)
+            return from_cuda(e);
+        if (two && (e = cudaEventRecord(ev[1 + c], ps)) != cudaSuccess) return from_cuda(e);
+    }
+    for (int c = 0; c < n; ++c) {
+        int64_t t0, tc;
+        chunk(c, t0, tc);
+        const size_t off = (size_t)t0 * H, bytes = (size_t)tc * H * 2;
+        if (two && (e = cudaStreamWaitEvent(cs, ev[1 + c], 0)) != cudaSuccess) return from_cuda(e);
+        const moe_status_t r = forward_impl(x_dev + off, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale,
+                                            tc, H, I, E, k, y_dev + off, workspace, workspace_bytes, stream,
+                                            nullptr, fp8);
+        if (r != MOE_OK) return r;
+        if (two) {
+            if ((e = cudaEventRecord(ev[1 + n + c], cs)) != cudaSuccess) return from_cuda(e);
+            if ((e = cudaStreamWaitEvent(ps, ev[1 + n + c], 0)) != cudaSuccess) return from_cuda(e);
+        }
+        if ((e = cudaMemcpyAsync(y_host + off, y_dev + off, bytes, cudaMemcpyDeviceToHost, ps)) != cudaSuccess)
+            return from_cuda(e);
+    }
+    if (two) {  // work queued on the compute stream after this call sees y complete
+        if ((e = cudaEventRecord(ev[1 + 2 * n], ps)) != cudaSuccess) return from_cuda(e);
+        if ((e = cudaStreamWaitEvent(cs, ev[1 + 2 * n], 0)) != cudaSuccess) return from_cuda(e);
+    }
+    return MOE_OK;
+}
+
 }  // namespace
 
 extern "C" {
@@ -393,6 +486,31 @@ moe_status_t moe_w8a8_forward(const uint16_t* x, const float* router_w, const fl
                               void* stream) {
     return forward_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
                         workspace, workspace_bytes, stream, nullptr);
+}
+
+moe_status_t moe_w8a8_forward_host(const uint16_t* x_host, const float* router_w, const float* router_bias,
+                                   const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                                   const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k,
+                                   uint16_t* y_host, uint16_t* x_dev, uint16_t* y_dev, void* workspace,
+                                   size_t workspace_bytes, void* stream, void* copy_stream, int chunks) {
+    return forward_host_impl(x_host, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k,
+                             y_host, x_dev, y_dev, workspace, workspace_bytes, stream, copy_stream, chunks, false);
+}
+
+moe_status_t moe_w8a8_fp8_forward_host(const uint16_t* x_host, const float* router_w, const float* router_bias,
+                                       const uint8_t* w13_q, const float* w13_scale, const uint8_t* w2_q,
+                                       const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                                       int64_t top_k, uint16_t* y_host, uint16_t* x_dev, uint16_t* y_dev,
+                                       void* workspace, size_t workspace_bytes, void* stream, void* copy_stream,
+                                       int chunks) {
+    return forward_host_impl(x_host, router_w, router_bias, reinterpret_cast<const int8_t*>(w13_q), w13_scale,
+                             reinterpret_cast<const int8_t*>(w2_q), w2_scale, T, H, I, E, top_k, y_host, x_dev,
+                             y_dev, workspace, workspace_bytes, stream, copy_stream, chunks, true);
+}
+
+int moe_w8a8_host_chunks(int64_t T, int64_t H, int64_t I, int64_t E) {
+    if (T < 0) return 0;
+    return T == 0 ? 1 : auto_chunks(T, H, I, E);
 }
 
 moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float* router_w,

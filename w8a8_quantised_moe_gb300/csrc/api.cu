@@ -4,12 +4,17 @@
 // Forward launch sequence on the caller's stream (no host synchronisation):
 //   1 router           split of the router weights into three bf16 parts,
 //                      tensor-core logits, top-k, weights, chunk counts/ranks
+//                      (T <= 128: partial logits per slice of the fp32 weights
+//                      on the CUDA cores, then per-token sums and top-k, whose
+//                      last CTA also does step 2)
 //   2 scan             expert offsets, first slot of every (chunk, expert)
 //   3 permute_quant    slots; per-token quantisation scattered into slots
 //   4 grouped GEMM 1   gate/up GEMM + scale outer product + SiLU(gate)*up -> h
 //   5 requant          per-slot requantisation of h
 //   6 grouped GEMM 2   down GEMM + scale outer product -> o
 //   7 combine          weighted sum of each token's k slot rows -> y (bf16)
+// The host-resident entry point runs this sequence once per token chunk,
+// with the copies of x and y on a second stream.
 #include <atomic>
 #include <cstdlib>
 #include <cstring>

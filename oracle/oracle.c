@@ -23,6 +23,8 @@
  *   gate -> top-k -> per-expert contiguous slots -> expert GEMMs -> weighted
  *   combine back to token order
  *     -- "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section 1.3
+ *   SmoothQuant-folded activations with per-expert factors (last section)
+ *     -- "W8A8 quantisation of MiniMax-M3 on K100AI", section 2.2
  *
  * Precision.  Wherever a floating-point value decides an integer (a
  * quantised code) the oracle works in IEEE binary32 with the operation order
@@ -377,10 +379,16 @@ typedef struct {
 
 static void* xmalloc(size_t n) { return malloc(n ? n : 1); }
 
-int oracle_moe_forward(const uint16_t* x, const float* Wr, const float* bias, const int8_t* w13_q,
-                       const float* s_w13, const int8_t* w2_q, const float* s_w2, int64_t T,
-                       int64_t H, int64_t I, int64_t E, int64_t k, uint16_t* y,
-                       const oracle_dump_t* dump) {
+static void quantize_row_bf16_smoothed(const uint16_t* x, const float* sm, int64_t H, float* tmp, int8_t* q,
+                                       float* s_out);
+
+/* smooth: NULL, or the per-expert smoothing factors [E][H] of the section on
+ * SmoothQuant below (each slot's row is then its token's row times the
+ * reciprocal factors of the slot's expert, quantised per slot). */
+static int moe_forward_impl(const uint16_t* x, const float* Wr, const float* bias, const float* smooth,
+                            const int8_t* w13_q, const float* s_w13, const int8_t* w2_q, const float* s_w2,
+                            int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, uint16_t* y,
+                            const oracle_dump_t* dump, float* s_slot_dump, int8_t* q_slot_dump) {
     if (T < 0 || H <= 0 || I <= 0 || E <= 0 || k <= 0 || k > E) return ORACLE_ERR_ARG;
     const int64_t S = T * k;
     int rc = ORACLE_OK;
@@ -415,11 +423,30 @@ int oracle_moe_forward(const uint16_t* x, const float* Wr, const float* bias, co
     /* per-token dynamic activation quantisation */
     rc = oracle_quantize_rows_bf16(x, T, H, q_x, s_x);
     if (rc) goto done;
-    /* every slot holds a copy of its token's quantised row and scale */
-    for (int64_t s = 0; s < S; ++s) {
-        int64_t t = slot_token[s];
-        memcpy(q_slot + s * H, q_x + t * H, (size_t)H);
-        s_slot[s] = s_x[t];
+    if (!smooth) {
+        /* every slot holds a copy of its token's quantised row and scale */
+        for (int64_t s = 0; s < S; ++s) {
+            int64_t t = slot_token[s];
+            memcpy(q_slot + s * H, q_x + t * H, (size_t)H);
+            s_slot[s] = s_x[t];
+        }
+    } else {
+        /* every slot quantises its token's row smoothed by its expert's factors */
+        float* tmp = (float*)xmalloc((size_t)H * 4);
+        if (!tmp) {
+            rc = ORACLE_ERR_NOMEM;
+            goto done;
+        }
+        for (int64_t e = 0; e < E; ++e)
+            for (int64_t s = offsets[e]; s < offsets[e + 1]; ++s)
+                quantize_row_bf16_smoothed(x + (int64_t)slot_token[s] * H, smooth + e * H, H, tmp,
+                                           q_slot + s * H, s_slot + s);
+        free(tmp);
+        /* a token's own scale and row are those of its first choice */
+        for (int64_t t = 0; t < T; ++t) {
+            s_x[t] = s_slot[slot_of[t * k]];
+            memcpy(q_x + t * H, q_slot + (int64_t)slot_of[t * k] * H, (size_t)H);
+        }
     }
     /* per expert: GEMM1, gate/up epilogue, requant, GEMM2, output epilogue */
     for (int64_t e = 0; e < E; ++e) {
@@ -455,11 +482,20 @@ int oracle_moe_forward(const uint16_t* x, const float* Wr, const float* bias, co
         if (dump->acc2) memcpy(dump->acc2, acc2, (size_t)(S * H) * 4);
         if (dump->o) memcpy(dump->o, o, (size_t)(S * H) * 4);
     }
+    if (s_slot_dump) memcpy(s_slot_dump, s_slot, (size_t)S * 4);
+    if (q_slot_dump) memcpy(q_slot_dump, q_slot, (size_t)(S * H));
 done:
     free(topk_ids); free(topk_w); free(counts); free(offsets); free(slot_of); free(slot_token);
     free(s_x); free(q_x); free(s_slot); free(q_slot); free(acc1); free(h); free(s_h); free(q_h);
     free(acc2); free(o);
     return rc;
+}
+
+int oracle_moe_forward(const uint16_t* x, const float* Wr, const float* bias, const int8_t* w13_q,
+                       const float* s_w13, const int8_t* w2_q, const float* s_w2, int64_t T,
+                       int64_t H, int64_t I, int64_t E, int64_t k, uint16_t* y,
+                       const oracle_dump_t* dump) {
+    return moe_forward_impl(x, Wr, bias, NULL, w13_q, s_w13, w2_q, s_w2, T, H, I, E, k, y, dump, NULL, NULL);
 }
 
 /* ---- the whole layer, brute force -----------------------------------------
@@ -789,4 +825,77 @@ done:
     free(s_x); free(q_x); free(s_slot); free(q_slot); free(acc1); free(h); free(s_h); free(q_h);
     free(acc2); free(o);
     return rc;
+}
+
+/* ==== SmoothQuant-folded activations, calibrated per expert ================
+ * "W8A8 quantisation of MiniMax-M3 on K100AI" (mhpn.cn), section 2.2: the
+ * activations are hard to quantise because a few channels hold large values;
+ * a per-channel factor moves part of that difficulty onto the weights (the
+ * activation channel is scaled down, the weights' input channel up by the
+ * same factor, which leaves x W^T unchanged in exact arithmetic), with alpha
+ * setting the balance and the statistics gathered per expert (each expert's
+ * calibration tokens are those the router sends to it).
+ * Readings (listed in the design notes): the factor s_e[h] of expert e and
+ * channel h follows SmoothQuant's balance
+ *     s = max|X_e[:,h]|^alpha / max|W_e[:,h]|^(1 - alpha)
+ * (binary64 powers, rounded once to binary32; a channel whose activation or
+ * weight statistic is 0 gets s = 1); the folded weight is w[n][h] * s[h] (one
+ * binary32 multiply) before the per-channel quantiser; the activation of a
+ * slot of expert e is x[t][h] * (1 / s_e[h]) with 1 / s the correctly
+ * rounded binary32 reciprocal (one multiply), quantised per slot.  The page's
+ * alpha sweep on calibration data and its percentile statistics need data
+ * this project does not have.
+ */
+int oracle_smooth_factors(const float* x_absmax, const float* w_absmax, int64_t n, double alpha, float* s) {
+    if (n < 0 || alpha < 0.0 || alpha > 1.0) return ORACLE_ERR_ARG;
+    for (int64_t i = 0; i < n; ++i) {
+        double a = x_absmax[i], b = w_absmax[i];
+        s[i] = (a > 0.0 && b > 0.0) ? (float)(pow(a, alpha) / pow(b, 1.0 - alpha)) : 1.0f;
+    }
+    return ORACLE_OK;
+}
+
+/* Per-output-channel quantisation of the folded weights w[r][k] * s[k]. */
+int oracle_quantize_rows_smoothed(const float* w, const float* s, int64_t rows, int64_t K, int8_t* q,
+                                  float* scale) {
+    if (rows < 0 || K <= 0) return ORACLE_ERR_ARG;
+    int err = 0;
+#pragma omp parallel
+    {
+        float* row = (float*)malloc((size_t)K * sizeof(float));
+        if (!row) {
+#pragma omp atomic write
+            err = 1;
+        }
+#pragma omp for schedule(static)
+        for (int64_t r = 0; r < rows; ++r) {
+            if (!row) continue;
+            for (int64_t k = 0; k < K; ++k) row[k] = w[r * K + k] * s[k];
+            quantize_row(row, K, q + r * K, scale + r);
+        }
+        free(row);
+    }
+    return err ? ORACLE_ERR_NOMEM : ORACLE_OK;
+}
+
+/* One activation row smoothed by one expert's factors, then quantised. */
+static void quantize_row_bf16_smoothed(const uint16_t* x, const float* sm, int64_t H, float* tmp, int8_t* q,
+                                       float* s_out) {
+    for (int64_t h = 0; h < H; ++h) {
+        float r = 1.0f / sm[h];
+        tmp[h] = bf16_to_f32(x[h]) * r;
+    }
+    quantize_row(tmp, H, q, s_out);
+}
+
+/* The layer with per-expert smoothing factors smooth [E][H] and w13_q folded
+ * with them; s_slot [S] and q_slot [S][H] (optional) receive each slot's
+ * scale and codes.  Everything else is the sparse layer above. */
+int oracle_moe_forward_smooth(const uint16_t* x, const float* Wr, const float* bias, const float* smooth,
+                              const int8_t* w13_q, const float* s_w13, const int8_t* w2_q, const float* s_w2,
+                              int64_t T, int64_t H, int64_t I, int64_t E, int64_t k, uint16_t* y,
+                              const oracle_dump_t* dump, float* s_slot, int8_t* q_slot) {
+    if (!smooth) return ORACLE_ERR_ARG;
+    return moe_forward_impl(x, Wr, bias, smooth, w13_q, s_w13, w2_q, s_w2, T, H, I, E, k, y, dump, s_slot,
+                            q_slot);
 }

@@ -80,6 +80,10 @@ def open_library(path: str):
         "oracle_epilogue_scale_f32": [vp, vp, vp, i64, i64, vp],
         "oracle_moe_forward_fp8": [vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp,
                                    ctypes.POINTER(_Dump)],
+        "oracle_smooth_factors": [vp, vp, i64, ctypes.c_double, vp],
+        "oracle_quantize_rows_smoothed": [vp, vp, i64, i64, vp, vp],
+        "oracle_moe_forward_smooth": [vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp,
+                                      ctypes.POINTER(_Dump), vp, vp],
         "oracle_num_threads": [],
         "oracle_set_num_threads": [ctypes.c_int],
     }
@@ -415,4 +419,69 @@ def moe_forward_fp8(x_bits, Wr, bias, w13_q, s_w13, w2_q, s_w2, k, dump=()):
     _check(_load().oracle_moe_forward_fp8(_p(x_bits), _p(Wr), _p(b), _p(w13_q), _p(_c(s_w13, np.float32)),
                                           _p(_c(w2_q, np.uint8)), _p(_c(s_w2, np.float32)), T, H, I, E, k,
                                           _p(y), ctypes.byref(d)), "moe_forward_fp8")
+    return (y, out) if dump else y
+
+
+# ---- SmoothQuant-folded activations, calibrated per expert -------------------
+
+def smooth_factors(x_absmax, w_absmax, alpha=0.5):
+    """Per-channel factors max|X|^alpha / max|W|^(1 - alpha) (1 where a
+    statistic is 0), computed in binary64 and rounded once to binary32."""
+    a = _c(x_absmax, np.float32)
+    b = _c(w_absmax, np.float32)
+    if a.shape != b.shape:
+        raise ValueError("x_absmax and w_absmax differ in shape")
+    out = np.empty(a.shape, np.float32)
+    _check(_load().oracle_smooth_factors(_p(a), _p(b), a.size, float(alpha), _p(out)), "smooth_factors")
+    return out
+
+
+def quantize_rows_smoothed(w, s):
+    """Per-row INT8 quantisation of the folded rows w[r][k] * s[k]."""
+    w = _c(w, np.float32)
+    s = _c(s, np.float32)
+    rows, K = w.shape
+    if s.shape != (K,):
+        raise ValueError("s must hold one factor per column")
+    q = np.empty((rows, K), np.int8)
+    sc = np.empty(rows, np.float32)
+    _check(_load().oracle_quantize_rows_smoothed(_p(w), _p(s), rows, K, _p(q), _p(sc)), "quantize_rows_smoothed")
+    return q, sc
+
+
+def moe_forward_smooth(x_bits, Wr, bias, smooth, w13_q, s_w13, w2_q, s_w2, k, dump=()):
+    """The layer with per-expert smoothing factors ``smooth [E, H]`` (w13_q
+    folded with them).  ``dump`` may also name "s_slot" and "q_slot"."""
+    x_bits = _c(x_bits, np.uint16)
+    T, H = x_bits.shape
+    w13_q = _c(w13_q, np.int8)
+    E, two_i, _ = w13_q.shape
+    I = two_i // 2
+    smooth = _c(smooth, np.float32)
+    if smooth.shape != (E, H):
+        raise ValueError("smooth must be [E, H]")
+    Wr = _c(Wr, np.float32)
+    b = None if bias is None else _c(bias, np.float32)
+    s_w13 = _c(s_w13, np.float32)
+    w2_q = _c(w2_q, np.int8)
+    s_w2 = _c(s_w2, np.float32)
+    y = np.empty((T, H), np.uint16)
+    out = {}
+    d = _Dump()
+    for name in dump:
+        if name in ("s_slot", "q_slot"):
+            continue
+        dt, shape = _DUMP_SPEC[name]
+        arr = np.empty(shape(T, H, I, E, k), dt)
+        out[name] = arr
+        setattr(d, name, arr.ctypes.data)
+    s_slot = np.empty(T * k, np.float32) if "s_slot" in dump else None
+    q_slot = np.empty((T * k, H), np.int8) if "q_slot" in dump else None
+    if s_slot is not None:
+        out["s_slot"] = s_slot
+    if q_slot is not None:
+        out["q_slot"] = q_slot
+    _check(_load().oracle_moe_forward_smooth(_p(x_bits), _p(Wr), _p(b), _p(smooth), _p(w13_q), _p(s_w13), _p(w2_q),
+                                             _p(s_w2), T, H, I, E, k, _p(y), ctypes.byref(d), _p(s_slot), _p(q_slot)),
+           "moe_forward_smooth")
     return (y, out) if dump else y

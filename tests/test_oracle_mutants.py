@@ -7,6 +7,7 @@ import pytest
 import oracle
 import test_oracle as pins
 import test_oracle_fp8 as pins8
+import test_oracle_smooth as pins_sm
 from w8a8_quantised_moe_gb300 import workloads as wl
 
 SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "oracle.c")
@@ -53,6 +54,15 @@ MUTANTS = [
     ("fp8_moe_wrong_w13_expert", "oracle_gemm_fp8(q_slot + s0 * H, w13_q + e * 2 * I * H",
      "oracle_gemm_fp8(q_slot + s0 * H, w13_q",
      [lambda: pins8.test_moe_forward_fp8_equals_dense_brute_force(16, 256, 128, 8, 2)]),
+    # SmoothQuant-folded activations
+    ("smooth_multiplies_activation", "float r = 1.0f / sm[h];", "float r = sm[h];",
+     [pins_sm.test_power_of_two_factors_leave_the_layer_unchanged, pins_sm.test_smoothing_worked_by_hand]),
+    ("smooth_expert0_for_every_slot", "smooth + e * H, H, tmp,", "smooth, H, tmp,",
+     [lambda: pins_sm.test_sparse_smoothed_layer_equals_dense_brute_force(16, 128, 64, 6, 2)]),
+    ("smooth_fold_divides_weights", "row[k] = w[r * K + k] * s[k];", "row[k] = w[r * K + k] / s[k];",
+     [pins_sm.test_quantize_rows_smoothed_unit_and_power_of_two_factors]),
+    ("smooth_alpha_swapped", "pow(a, alpha) / pow(b, 1.0 - alpha)", "pow(a, 1.0 - alpha) / pow(b, alpha)",
+     [pins_sm.test_smooth_factors_worked_by_hand]),
 ]
 
 

@@ -46,8 +46,9 @@ def parse_args(argv=None):
     p.add_argument("--warmup", type=int, default=5)
     p.add_argument("--impl", choices=["ours", "reference"], default="ours")
     p.add_argument("--config", default="prefill", choices=["prefill", "decode", "wide", "tiny", "linear"])
-    p.add_argument("--format", default="int8", choices=["int8", "fp8"],
-                   help="int8: the W8A8 INT8 layer; fp8: its E4M3 variant (MoE configs only)")
+    p.add_argument("--format", default="int8", choices=["int8", "fp8", "int8-smooth"],
+                   help="int8: the W8A8 INT8 layer; fp8: its E4M3 variant; int8-smooth: the INT8 layer with "
+                        "SmoothQuant-folded activations, per-expert factors (MoE configs only)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -183,7 +184,8 @@ def describe(cfg, fmt="int8") -> str:
         return f"w8a8_linear M={cfg.M} K={cfg.K} N={cfg.N}"
     route = {"none": "uniform routing", "zipf": f"Zipf({cfg.zipf_s}) expert popularity",
              "normal": f"router bias N(0,{cfg.bias_std}^2)"}[cfg.bias]
-    tail = ", E4M3 weights and activations" if fmt == "fp8" else ""
+    tail = {"fp8": ", E4M3 weights and activations",
+            "int8-smooth": ", SmoothQuant-folded activations (per-expert factors)"}.get(fmt, "")
     return (f"moe_{cfg.name} T={cfg.T} H={cfg.H} I={cfg.I} E={cfg.E} top-{cfg.k}, {route}{tail}")
 
 
@@ -202,12 +204,14 @@ def device_weights(cfg, seed, dev, fmt="int8"):
         return moe.quantize_weights(w)
     quant = moe.fp8_quantize_weights if fmt == "fp8" else moe.quantize_weights
     code = torch.uint8 if fmt == "fp8" else torch.int8
+    smooth = torch.from_numpy(wl.smoothing_factors(cfg, seed)).to(dev) if fmt == "int8-smooth" else None
     w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=code, device=dev)
     w13_s = torch.empty((cfg.E, 2 * cfg.I), dtype=torch.float32, device=dev)
     w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=code, device=dev)
     w2_s = torch.empty((cfg.E, cfg.H), dtype=torch.float32, device=dev)
     for e in range(cfg.E):
-        q, s = quant(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev))
+        w13 = wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev)
+        q, s = quant(w13) if smooth is None else moe.quantize_weights_smoothed(w13, smooth[e])
         w13_q[e].copy_(q)
         w13_s[e].copy_(s)
         q, s = quant(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev))
@@ -224,12 +228,14 @@ def oracle_weights(cfg, seed, dev, fmt="int8"):
         return oracle.quantize_rows(wl.expert_weight_fp32(cfg, "linear", 0, seed, device=dev).cpu().numpy())
     quant = oracle.quantize_rows_fp8 if fmt == "fp8" else oracle.quantize_rows
     code = np.uint8 if fmt == "fp8" else np.int8
+    smooth = wl.smoothing_factors(cfg, seed) if fmt == "int8-smooth" else None
     w13_q = np.empty((cfg.E, 2 * cfg.I, cfg.H), code)
     w13_s = np.empty((cfg.E, 2 * cfg.I), np.float32)
     w2_q = np.empty((cfg.E, cfg.H, cfg.I), code)
     w2_s = np.empty((cfg.E, cfg.H), np.float32)
     for e in range(cfg.E):
-        w13_q[e], w13_s[e] = quant(wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev).cpu().numpy())
+        w13 = wl.expert_weight_fp32(cfg, "w13", e, seed, device=dev).cpu().numpy()
+        w13_q[e], w13_s[e] = quant(w13) if smooth is None else oracle.quantize_rows_smoothed(w13, smooth[e])
         w2_q[e], w2_s[e] = quant(wl.expert_weight_fp32(cfg, "w2", e, seed, device=dev).cpu().numpy())
     return w13_q, w13_s, w2_q, w2_s
 
@@ -239,7 +245,7 @@ def host_inputs(cfg, seed):
     if isinstance(cfg, wl.LinearConfig):
         return {"x": wl.linear_activations(cfg, seed)}
     inp = wl.make_moe_inputs(cfg, seed)
-    return {"x": inp.x, "Wr": inp.Wr, "bias": inp.bias, "redrawn": inp.redrawn_rows}
+    return {"x": inp.x, "Wr": inp.Wr, "bias": inp.bias, "redrawn": inp.redrawn_rows, "seed": seed}
 
 
 def tokens_of(cfg):
@@ -263,8 +269,12 @@ def oracle_sample_rate(cfg, inputs, oweights, target_s, max_tokens=None, fmt="in
         if isinstance(cfg, wl.LinearConfig):
             oracle.linear(x, *oweights)
         else:
-            fwd = oracle.moe_forward_fp8 if fmt == "fp8" else oracle.moe_forward
-            fwd(x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
+            if fmt == "int8-smooth":
+                oracle.moe_forward_smooth(x, inputs["Wr"], inputs["bias"], wl.smoothing_factors(cfg, inputs["seed"]),
+                                          *oweights, cfg.k)
+            else:
+                fwd = oracle.moe_forward_fp8 if fmt == "fp8" else oracle.moe_forward
+                fwd(x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)
         return time.perf_counter() - t0
 
     n = min(lim, 8)
@@ -358,9 +368,18 @@ def run_ours(args, ranks: Ranks):
     linear = isinstance(cfg, wl.LinearConfig)
     fmt = args.format
     if linear and fmt != "int8":
-        raise SystemExit("--format fp8 applies to the MoE configs")
-    fwd = moe.fp8_forward if fmt == "fp8" else moe.forward
-    fwd_debug = moe.fp8_forward_debug if fmt == "fp8" else moe.forward_debug
+        raise SystemExit(f"--format {fmt} applies to the MoE configs")
+    if fmt == "int8-smooth":
+        smooth_dev = torch.from_numpy(wl.smoothing_factors(cfg, args.seed + ranks.rank)).to(dev)
+
+        def fwd(*a, **kw):
+            return moe.forward_smooth(*a[:3], smooth_dev, *a[3:], **kw)
+
+        def fwd_debug(*a, fields=None, **kw):
+            return moe.forward_smooth(*a[:3], smooth_dev, *a[3:], fields=fields, **kw)
+    else:
+        fwd = moe.fp8_forward if fmt == "fp8" else moe.forward
+        fwd_debug = moe.fp8_forward_debug if fmt == "fp8" else moe.forward_debug
     peaks = measured_peaks()
     seed = args.seed + ranks.rank
     inputs = host_inputs(cfg, seed)
@@ -474,7 +493,8 @@ def run_ours(args, ranks: Ranks):
         achieved = w["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
-    roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom, fmt)
+    gemm_fmt = "fp8" if fmt == "fp8" else "int8"  # the smoothed layer runs the INT8 GEMM kernels
+    roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom, gemm_fmt)
     roof["kernel"] = dom
     roof["kernel_ms"] = dom_ms
     roof["algorithmic"] = {"flops": w["flops"], "bytes": w["bytes"]}
@@ -491,7 +511,7 @@ def run_ours(args, ranks: Ranks):
     y_pin = torch.empty(y.shape, dtype=torch.bfloat16).pin_memory()
     x_dev2 = torch.empty_like(x)
     copy_stream = torch.cuda.Stream(device=dev)
-    if linear:
+    if linear or fmt == "int8-smooth":  # no host-resident entry point: copies around the device one
         def step_host():
             x_dev2.copy_(x_pin, non_blocking=True)
             step(x_dev2, y)
@@ -597,6 +617,9 @@ def run_reference(args):
     def step():
         if isinstance(cfg, wl.LinearConfig):
             oracle.linear(x, *oweights)
+        elif fmt == "int8-smooth":
+            oracle.moe_forward_smooth(x, inputs["Wr"], inputs["bias"], wl.smoothing_factors(cfg, inputs["seed"]),
+                                      *oweights, cfg.k)
         else:
             (oracle.moe_forward_fp8 if fmt == "fp8" else oracle.moe_forward)(
                 x, inputs["Wr"], inputs["bias"], *oweights, cfg.k)

@@ -158,6 +158,8 @@ typedef struct {
     int8_t* q_h;          /* [S][I]      requantised h */
     int32_t* acc2;        /* [S][H]      GEMM2 accumulators */
     float* o;             /* [S][H]      per-slot expert outputs */
+    float* s_slot;        /* [S]         activation scale of each slot */
+    int8_t* q_slot;       /* [S][H]      quantised activation row of each slot */
 } moe_w8a8_debug_t;
 
 /* moe_w8a8_forward plus copies of the intermediates into `dbg` (same
@@ -262,6 +264,43 @@ MOE_W8A8_API moe_status_t moe_w8a8_fp8_forward_debug(const uint16_t* x, const fl
                                                      int64_t E, int64_t top_k, uint16_t* y, void* workspace,
                                                      size_t workspace_bytes, void* stream,
                                                      const moe_w8a8_debug_t* dbg);
+
+/* ---------------------------------------------------------------------------
+ * SmoothQuant-folded activations, calibrated per expert ("W8A8 quantisation
+ * of MiniMax-M3 on K100AI", section 2.2: part of the activations'
+ * quantisation difficulty is moved onto the weights by a per-channel factor,
+ * with statistics gathered per expert).  A factor s_e[h] > 0 per expert e and
+ * hidden channel h multiplies the weights' input channel h and divides the
+ * activation's channel h; the two cancel in exact arithmetic.
+ *
+ * moe_w8a8_quantize_weights_smoothed -- moe_w8a8_quantize_weights of the
+ * rows w[r][k] * col_scale[k] (one binary32 multiply per element): call it
+ * once per expert on its w13 rows [2I][H] with col_scale = s_e [H].  (w2 is
+ * quantised as before: the factors act on GEMM1's input only.)
+ *   col_scale  fp32 [K], device, 16-byte aligned
+ * Errors: as moe_w8a8_quantize_weights; col_scale NULL -> INVALID_ARG.
+ *
+ * moe_w8a8_forward_smooth -- moe_w8a8_forward with the activation of each
+ * (token, expert) slot taken as x[t][h] * rcp(s_e[h]) (rcp: the correctly
+ * rounded binary32 reciprocal; one binary32 multiply) and quantised per slot
+ * (amax over the slot's row, s = amax / 127), since the row now depends on the
+ * expert.  The weights must have been folded with the same factors.
+ *   smooth     fp32 [E][H], device, 16-byte aligned, every factor > 0 and
+ *              finite (not checked)
+ *   dbg        may be NULL; as moe_w8a8_forward_debug, with s_x[t] the scale
+ *              of the token's first choice and q_x[t] its first slot's row
+ * Errors: as moe_w8a8_forward; smooth NULL (T > 0) or misaligned ->
+ * MOE_ERR_INVALID_ARG.  INT8 layer only.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_quantize_weights_smoothed(const float* w, int64_t rows, int64_t K,
+                                                             const float* col_scale, int8_t* w_q, float* w_scale,
+                                                             void* stream);
+MOE_W8A8_API moe_status_t moe_w8a8_forward_smooth(const uint16_t* x, const float* router_w,
+                                                  const float* router_bias, const float* smooth,
+                                                  const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                                                  const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                                                  int64_t top_k, uint16_t* y, void* workspace,
+                                                  size_t workspace_bytes, void* stream, const moe_w8a8_debug_t* dbg);
 
 /* ---------------------------------------------------------------------------
  * moe_w8a8_forward_host -- moe_w8a8_forward for activations that live in

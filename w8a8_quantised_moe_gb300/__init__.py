@@ -207,6 +207,8 @@ _DEBUG_FIELDS = {
     "q_h": ("int8", lambda T, H, I, E, k: (T * k, I)),
     "acc2": ("int32", lambda T, H, I, E, k: (T * k, H)),
     "o": ("float32", lambda T, H, I, E, k: (T * k, H)),
+    "s_slot": ("float32", lambda T, H, I, E, k: (T * k,)),
+    "q_slot": ("int8", lambda T, H, I, E, k: (T * k, H)),
 }
 
 
@@ -234,6 +236,50 @@ def forward_debug(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, to
         _stream(stream), ctypes.byref(bufs)), "moe_w8a8_forward_debug")
     return y, out
 
+
+
+# ---- SmoothQuant-folded activations, calibrated per expert ------------------
+
+def quantize_weights_smoothed(w, col_scale, stream=None):
+    """Per-output-channel INT8 quantisation of fp32 ``w [rows, K]`` times the
+    column factors ``col_scale [K]`` -> (int8 [rows, K], fp32 scales [rows])."""
+    torch = _torch()
+    rows, K = w.shape
+    _need(w, torch.float32, (rows, K), "w")
+    _need(col_scale, torch.float32, (K,), "col_scale")
+    q = torch.empty((rows, K), dtype=torch.int8, device=w.device)
+    s = torch.empty((rows,), dtype=torch.float32, device=w.device)
+    _lib.check(_lib.load().moe_w8a8_quantize_weights_smoothed(_ptr(w), rows, K, _ptr(col_scale), _ptr(q), _ptr(s),
+                                                              _stream(stream)), "moe_w8a8_quantize_weights_smoothed")
+    return q, s
+
+
+def forward_smooth(x, router_w, router_bias, smooth, w13_q, w13_scale, w2_q, w2_scale, top_k, fields=(),
+                   workspace=None, out=None, stream=None):
+    """The MoE layer with per-expert smoothing factors ``smooth [E, H]``
+    (weights folded by ``quantize_weights_smoothed``).  Returns y, or (y,
+    dict of the intermediates named in ``fields``) when ``fields`` is given."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k)
+    _need(smooth, torch.float32, (E, H), "smooth")
+    if workspace is None:
+        workspace = new_workspace(workspace_size(T, H, I, E, top_k), x.device)
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (T, H), "out")
+    fields = tuple(_DEBUG_FIELDS) if fields is None else tuple(fields)
+    bufs, dumps = None, {}
+    if fields:
+        bufs = _lib.DebugBuffers()
+        for name in fields:
+            dt, shape = _DEBUG_FIELDS[name]
+            t = torch.zeros(shape(T, H, I, E, top_k), dtype=getattr(torch, dt), device=x.device)
+            dumps[name] = t
+            setattr(bufs, name, t.data_ptr())
+    _lib.check(_lib.load().moe_w8a8_forward_smooth(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(smooth), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q),
+        _ptr(w2_scale), T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), ctypes.byref(bufs) if bufs is not None else None), "moe_w8a8_forward_smooth")
+    return (y, dumps) if fields else y
 
 def linear_workspace_size(M, N, K) -> int:
     n = _lib.load().moe_w8a8_linear_workspace_size(M, N, K)
@@ -299,6 +345,7 @@ def fp8_forward(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_
 
 
 _DEBUG_FIELDS_FP8 = dict(_DEBUG_FIELDS, q_x=("uint8", _DEBUG_FIELDS["q_x"][1]),
+                         q_slot=("uint8", _DEBUG_FIELDS["q_slot"][1]),
                          q_h=("uint8", _DEBUG_FIELDS["q_h"][1]), acc1=("float32", _DEBUG_FIELDS["acc1"][1]),
                          acc2=("float32", _DEBUG_FIELDS["acc2"][1]))
 

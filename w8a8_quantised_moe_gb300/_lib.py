@@ -46,6 +46,8 @@ EXPORTS = (
     "moe_w8a8_forward_host",
     "moe_w8a8_fp8_forward_host",
     "moe_w8a8_host_chunks",
+    "moe_w8a8_quantize_weights_smoothed",
+    "moe_w8a8_forward_smooth",
 )
 
 
@@ -58,7 +60,7 @@ class MoeError(RuntimeError):
 class DebugBuffers(ctypes.Structure):
     _fields_ = [(name, ctypes.c_void_p) for name in (
         "topk_ids", "topk_w", "offsets", "slot_of", "slot_token", "s_x", "q_x", "acc1", "h",
-        "s_h", "q_h", "acc2", "o")]
+        "s_h", "q_h", "acc2", "o", "s_slot", "q_slot")]
 
 
 _lock = threading.Lock()
@@ -100,6 +102,9 @@ def load(path: str = LIB_PATH):
             "moe_w8a8_fp8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz,
                                            vp, vp, i32], i32),
             "moe_w8a8_host_chunks": ([i64, i64, i64, i64], i32),
+            "moe_w8a8_quantize_weights_smoothed": ([vp, i64, i64, vp, vp, vp, vp], i32),
+            "moe_w8a8_forward_smooth": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
+                                         ctypes.POINTER(DebugBuffers)], i32),
         }
         for name, (args, res) in decl.items():
             fn = getattr(lib, name)

@@ -161,9 +161,11 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
                           const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
                           const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
                           int64_t k, uint16_t* y, void* workspace, size_t workspace_bytes,
-                          void* stream, const moe_w8a8_debug_t* dbg, bool fp8 = false) {
+                          void* stream, const moe_w8a8_debug_t* dbg, bool fp8 = false,
+                          const float* smooth = nullptr) {
     if (!moe_shape_ok(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (T == 0) return MOE_OK;  // nothing is read or written
+    if (smooth != nullptr && !aligned16(smooth)) return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {x, router_w, w13_q, w13_scale, w2_q, w2_scale, y, workspace};
     for (const void* p : ptrs)
         if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
@@ -224,6 +226,10 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     if (fp8)
         e = launch_permute_quant_fp8(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
                                      s_x, s_slot, reinterpret_cast<uint8_t*>(q_x8), st, pdl);
+    else if (smooth)
+        e = launch_permute_quant_smooth(x, smooth, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of,
+                                        slot_token, s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1,
+                                        counts + 0, st, pdl);
     else
         e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
                                  s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
@@ -310,6 +316,12 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
         if ((e = cp(dbg->s_h, s_h, Sb)) != cudaSuccess) return from_cuda(e);
         if ((e = cp(dbg->o, o, (size_t)S * H * 4)) != cudaSuccess) return from_cuda(e);
         if (q_h8 && (e = cp(dbg->q_h, q_h8, (size_t)S * I)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_slot, s_slot, Sb)) != cudaSuccess) return from_cuda(e);
+        if (dbg->q_slot) {  // every slot's row, in slot order
+            e = q_x8 ? launch_s8_rows_gather(q_x8, nullptr, S, (int)H, 1, dbg->q_slot, st)
+                     : launch_f16_rows_to_s8(q_x16, nullptr, S, (int)H, 1, dbg->q_slot, st);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
         if (dbg->q_x) {
             // token t's quantised row sits in each of its slots; take the first
             e = q_x8 ? launch_s8_rows_gather(q_x8, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st)
@@ -516,6 +528,27 @@ moe_status_t moe_w8a8_fp8_forward_host(const uint16_t* x_host, const float* rout
 int moe_w8a8_host_chunks(int64_t T, int64_t H, int64_t I, int64_t E) {
     if (T < 0) return 0;
     return T == 0 ? 1 : auto_chunks(T, H, I, E);
+}
+
+moe_status_t moe_w8a8_quantize_weights_smoothed(const float* w, int64_t rows, int64_t K, const float* col_scale,
+                                                int8_t* w_q, float* w_scale, void* stream) {
+    if (rows < 0 || K < 1 || K > (int64_t(1) << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (rows == 0) return MOE_OK;
+    if (!w || !col_scale || !w_q || !w_scale || !aligned16(w) || !aligned16(col_scale) || !aligned16(w_q) ||
+        !aligned16(w_scale))
+        return MOE_ERR_INVALID_ARG;
+    return from_cuda(
+        launch_quantize_weights(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream), col_scale));
+}
+
+moe_status_t moe_w8a8_forward_smooth(const uint16_t* x, const float* router_w, const float* router_bias,
+                                     const float* smooth, const int8_t* w13_q, const float* w13_scale,
+                                     const int8_t* w2_q, const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                     int64_t E, int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                     void* stream, const moe_w8a8_debug_t* dbg) {
+    if (T > 0 && smooth == nullptr) return MOE_ERR_INVALID_ARG;
+    return forward_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
+                        workspace, workspace_bytes, stream, dbg, false, smooth);
 }
 
 moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float* router_w,

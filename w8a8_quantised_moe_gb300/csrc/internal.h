@@ -218,12 +218,21 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
                                  int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
                                  bool pdl);
+// The same with SmoothQuant-folded activations per expert: each (token,
+// choice) row is x[t] times the reciprocals of smooth[e] ([E][H]), quantised
+// per slot; s_x[t] receives the scale of the token's first choice.
+cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, const int32_t* topk_ids,
+                                        const int32_t* rank, const int32_t* hist, int T, int H, int E, int k,
+                                        int32_t* slot_of, int32_t* slot_token, float* s_x, float* s_slot,
+                                        uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
+                                        int32_t* fb_count, cudaStream_t st, bool pdl);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
                            int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st, bool pdl);
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
                            int H, int k, uint16_t* y, cudaStream_t st, bool pdl);
+// col_scale (optional, [K]): the row quantised is w[r][k] * col_scale[k].
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
-                                    cudaStream_t st);
+                                    cudaStream_t st, const float* col_scale = nullptr);
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
                                   int row_stride_of, int8_t* q8, cudaStream_t st);
 // out[r][:] = q8[row_of[r * stride]][:] (row_of == nullptr: identity).

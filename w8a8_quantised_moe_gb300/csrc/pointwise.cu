@@ -5,7 +5,8 @@
 //                           values (the tensor-core operand) and/or int8.
 //   s8_rows_gather_kernel   copies int8 rows out by a row map (debug dumps).
 //   combine_kernel          y[t] = bf16_rne(sum_j w[t][j] * o[slot(t, j)]).
-//   quantize_weights_kernel per output channel: s = amax/127, q = round(w/s).
+//   quantize_weights_kernel per output channel: s = amax/127, q = round(w/s)
+//                           (optionally of w times per-column smoothing factors).
 //   f16_rows_to_s8_kernel   copies quantised rows out as int8 (debug dumps).
 //
 // Quantisation: "W8A8 quantisation of MiniMax-M3 on K100AI" (mhpn.cn),
@@ -215,23 +216,35 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     }
 }
 
-// One warp per weight row; grid-stride over rows.
+// One warp per weight row; grid-stride over rows.  With column factors cs
+// (smoothing folded into the weights) the row quantised is w[r][k] * cs[k],
+// one binary32 multiply per element.
+template <bool CS>
 __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __restrict__ w,
-                                                               int64_t rows, int K,
-                                                               int8_t* __restrict__ q,
+                                                               const float* __restrict__ cs, int64_t rows,
+                                                               int K, int8_t* __restrict__ q,
                                                                float* __restrict__ s_out) {
     const int lane = threadIdx.x & 31;
     const int64_t nwarps = (int64_t)gridDim.x * 8;
+    auto ld4 = [&](const float* row, int i) {
+        float4 v = reinterpret_cast<const float4*>(row)[i];
+        if (CS) {
+            const float4 c = reinterpret_cast<const float4*>(cs)[i];
+            v = make_float4(__fmul_rn(v.x, c.x), __fmul_rn(v.y, c.y), __fmul_rn(v.z, c.z), __fmul_rn(v.w, c.w));
+        }
+        return v;
+    };
+    auto ld1 = [&](const float* row, int i) { return CS ? __fmul_rn(row[i], cs[i]) : row[i]; };
     for (int64_t r = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5); r < rows; r += nwarps) {
         const float* row = w + r * K;
         float amax = 0.f;
         if ((K & 3) == 0) {
             for (int i = lane; i < K / 4; i += 32) {
-                const float4 v = reinterpret_cast<const float4*>(row)[i];
+                const float4 v = ld4(row, i);
                 amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
             }
         } else {
-            for (int i = lane; i < K; i += 32) amax = fmaxf(amax, fabsf(row[i]));
+            for (int i = lane; i < K; i += 32) amax = fmaxf(amax, fabsf(ld1(row, i)));
         }
         amax = warp_max(amax);
         const float s = __fdiv_rn(amax, 127.0f);
@@ -239,7 +252,7 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __re
         int8_t* qr = q + r * K;
         if ((K & 3) == 0) {
             for (int i = lane; i < K / 4; i += 32) {
-                const float4 v = reinterpret_cast<const float4*>(row)[i];
+                const float4 v = ld4(row, i);
                 const uint32_t packed = (uint32_t)(uint8_t)quant_code(v.x, s) |
                                         ((uint32_t)(uint8_t)quant_code(v.y, s) << 8) |
                                         ((uint32_t)(uint8_t)quant_code(v.z, s) << 16) |
@@ -247,7 +260,7 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __re
                 reinterpret_cast<uint32_t*>(qr)[i] = packed;
             }
         } else {
-            for (int i = lane; i < K; i += 32) qr[i] = (int8_t)quant_code(row[i], s);
+            for (int i = lane; i < K; i += 32) qr[i] = (int8_t)quant_code(ld1(row, i), s);
         }
     }
 }
@@ -314,12 +327,15 @@ cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* 
 }
 
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
-                                    cudaStream_t st) {
+                                    cudaStream_t st, const float* col_scale) {
     if (rows == 0) return cudaSuccess;
     int64_t blocks = (rows + 7) / 8;
     const int64_t cap = (int64_t)num_sms() * 16;
     if (blocks > cap) blocks = cap;
-    quantize_weights_kernel<<<(unsigned)blocks, 256, 0, st>>>(w, rows, K, q, s);
+    if (col_scale)
+        quantize_weights_kernel<true><<<(unsigned)blocks, 256, 0, st>>>(w, col_scale, rows, K, q, s);
+    else
+        quantize_weights_kernel<false><<<(unsigned)blocks, 256, 0, st>>>(w, nullptr, rows, K, q, s);
     return cudaGetLastError();
 }
 

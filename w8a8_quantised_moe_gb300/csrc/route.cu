@@ -8,6 +8,8 @@
 //   permute_quant_cta_kernel  the same with one CTA per token, the row held in
 //                        registers: for few tokens (decode), where a warp per
 //                        token leaves most of the GPU idle.
+//   permute_quant_smooth_kernel  the same with SmoothQuant-folded activations
+//                        per expert: one warp per (token, choice), a scale per slot.
 //
 // Routing pre-processing that reserves a contiguous slot range per expert:
 // "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section 1.3.  Per-token dynamic quantisation q = clamp(round(x/s)),
@@ -269,6 +271,80 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
     }
 }
 
+// SmoothQuant-folded activations, per expert ("W8A8 quantisation of
+// MiniMax-M3 on K100AI" (mhpn.cn), section 2.2: part of the activations'
+// quantisation difficulty moves onto the weights through a per-channel
+// factor, calibrated per expert).  The factor s_e[h] multiplies the weights'
+// input channel h offline; here the activation is multiplied by its correctly
+// rounded reciprocal.  A slot's row then depends on its expert, so one warp
+// per (token, choice) quantises its own row with its own scale.
+__device__ __forceinline__ void smooth8(const uint4 xv, const float4 f0, const float4 f1, float (&v)[8]) {
+    const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
+    const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+        v[2 * j] = __fmul_rn(bf16_bits_to_float(w[j] & 0xffffu), __frcp_rn(f[2 * j]));
+        v[2 * j + 1] = __fmul_rn(bf16_bits_to_float(w[j] >> 16), __frcp_rn(f[2 * j + 1]));
+    }
+}
+
+__global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ smooth, const int32_t* __restrict__ topk_ids,
+    const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
+    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
+    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    const int lane = threadIdx.x & 31;
+    const int64_t c = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // choice t * k + j
+    pdl_wait();
+    pdl_trigger();
+    if (c >= (int64_t)T * k) return;
+    const int t = (int)(c / k);
+    const int e = topk_ids[c];
+    const int slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[c];
+    if (lane == 0) {
+        slot_of[c] = slot;
+        slot_token[slot] = t;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const float4* fr = reinterpret_cast<const float4*>(smooth + (size_t)e * H);
+    const int nv = H / 8;  // 8 bf16 per 16-byte vector
+    float amax = 0.f;
+    for (int i = lane; i < nv; i += 32) {
+        float v[8];
+        smooth8(__ldg(row + i), __ldg(fr + 2 * i), __ldg(fr + 2 * i + 1), v);
+#pragma unroll
+        for (int m = 0; m < 8; ++m) amax = fmaxf(amax, fabsf(v[m]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (lane == 0) {
+        s_slot[slot] = s;
+        if (c - (int64_t)t * k == 0) s_x[t] = s;
+    }
+    int l1 = 0;
+    for (int i = lane; i < nv; i += 32) {
+        float v[8];
+        smooth8(__ldg(row + i), __ldg(fr + 2 * i), __ldg(fr + 2 * i + 1), v);
+        int q[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            q[m] = quant_code_div(v[m], s);
+            l1 += abs(q[m]);
+        }
+        if (q16 != nullptr) reinterpret_cast<uint4*>(q16 + (size_t)slot * H)[i] = pack_codes_f16(q);
+        if (q8 != nullptr) reinterpret_cast<uint2*>(q8 + (size_t)slot * H)[i] = pack_codes_s8(q);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (lane == 0) {
+        const int flagged = l1 > kExactL1 ? 1 : 0;
+        flags[slot] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = slot;
+    }
+}
+
 }  // namespace
 
 cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int32_t* counts,
@@ -304,6 +380,18 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
     return launch_kernel(permute_quant_kernel, dim3((T + kPqWarps - 1) / kPqWarps), dim3(32 * kPqWarps), 0, st, pdl,
                          x, topk_ids, rank, hist, T, H, E, k,
                          slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+}
+
+cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, const int32_t* topk_ids,
+                                        const int32_t* rank, const int32_t* hist, int T, int H, int E, int k,
+                                        int32_t* slot_of, int32_t* slot_token, float* s_x, float* s_slot,
+                                        uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
+                                        int32_t* fb_count, cudaStream_t st, bool pdl) {
+    if (T == 0) return cudaSuccess;
+    const int64_t n = (int64_t)T * k;
+    return launch_kernel(permute_quant_smooth_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, pdl, x,
+                         smooth, topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
+                         fb_list, fb_count);
 }
 
 }  // namespace moe

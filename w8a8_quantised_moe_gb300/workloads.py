@@ -40,7 +40,7 @@ OUTLIER_GAIN = 20.0
 EXPERT_W_STD = 0.02
 
 # tensor ids of the random streams
-_T_X, _T_OUTL, _T_WR, _T_BIAS, _T_W13, _T_W2, _T_REDRAW, _T_ZIPF, _T_LIN_W = range(9)
+_T_X, _T_OUTL, _T_WR, _T_BIAS, _T_W13, _T_W2, _T_REDRAW, _T_ZIPF, _T_LIN_W, _T_SMOOTH = range(10)
 
 
 @dataclasses.dataclass(frozen=True)
@@ -222,6 +222,15 @@ def expert_weight_fp32(cfg, which: str, e: int, seed: int = 0, device="cpu"):
     g.manual_seed(expert_weight_seed(seed, cfg.cfg_id, which, e))
     w = torch.randn(shape, generator=g, device=device, dtype=torch.float32)
     return w.mul_(EXPERT_W_STD)
+
+
+def smoothing_factors(cfg: MoEConfig, seed: int = 0) -> np.ndarray:
+    """Per-expert, per-channel smoothing factors [E, H] for the layer with
+    SmoothQuant-folded activations: log-uniform on [e^-1.5, e^1.5], seeded.
+    (Calibrated factors need activation statistics of a trained model; these
+    stand in for them.)"""
+    r = rng(seed, cfg.cfg_id, _T_SMOOTH)
+    return np.exp(r.uniform(-1.5, 1.5, (cfg.E, cfg.H))).astype(np.float32)
 
 
 def linear_activations(cfg: LinearConfig, seed: int = 0) -> np.ndarray:

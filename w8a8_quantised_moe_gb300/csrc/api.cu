@@ -227,9 +227,11 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
         e = launch_permute_quant_fp8(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
                                      s_x, s_slot, reinterpret_cast<uint8_t*>(q_x8), st, pdl);
     else if (smooth)
-        e = launch_permute_quant_smooth(x, smooth, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of,
-                                        slot_token, s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1,
-                                        counts + 0, st, pdl);
+        // the router's weight split is dead once the router has run: its region
+        // (6 * E_pad * H >= 4 * E * H bytes) holds the smoothing reciprocals
+        e = launch_permute_quant_smooth(x, smooth, reinterpret_cast<float*>(wsplit), topk_ids, rank, hist, (int)T,
+                                        (int)H, (int)E, (int)k, slot_of, slot_token, s_x, s_slot,
+                                        q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
     else
         e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
                                  s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);

@@ -220,11 +220,12 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
                                  bool pdl);
 // The same with SmoothQuant-folded activations per expert: each (token,
 // choice) row is x[t] times the reciprocals of smooth[e] ([E][H]), quantised
-// per slot; s_x[t] receives the scale of the token's first choice.
-cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, const int32_t* topk_ids,
-                                        const int32_t* rank, const int32_t* hist, int T, int H, int E, int k,
-                                        int32_t* slot_of, int32_t* slot_token, float* s_x, float* s_slot,
-                                        uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
+// per slot; s_x[t] receives the scale of the token's first choice.  rcp:
+// scratch of E * H floats for the reciprocals (two launches).
+cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, float* rcp,
+                                        const int32_t* topk_ids, const int32_t* rank, const int32_t* hist, int T,
+                                        int H, int E, int k, int32_t* slot_of, int32_t* slot_token, float* s_x,
+                                        float* s_slot, uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
                                         int32_t* fb_count, cudaStream_t st, bool pdl);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
                            int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st, bool pdl);

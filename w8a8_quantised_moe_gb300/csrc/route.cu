@@ -278,18 +278,30 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
 // input channel h offline; here the activation is multiplied by its correctly
 // rounded reciprocal.  A slot's row then depends on its expert, so one warp
 // per (token, choice) quantises its own row with its own scale.
-__device__ __forceinline__ void smooth8(const uint4 xv, const float4 f0, const float4 f1, float (&v)[8]) {
+__device__ __forceinline__ void smooth8(const uint4 xv, const float4 r0, const float4 r1, float (&v)[8]) {
     const uint32_t w[4] = {xv.x, xv.y, xv.z, xv.w};
-    const float f[8] = {f0.x, f0.y, f0.z, f0.w, f1.x, f1.y, f1.z, f1.w};
+    const float r[8] = {r0.x, r0.y, r0.z, r0.w, r1.x, r1.y, r1.z, r1.w};
 #pragma unroll
     for (int j = 0; j < 4; ++j) {
-        v[2 * j] = __fmul_rn(bf16_bits_to_float(w[j] & 0xffffu), __frcp_rn(f[2 * j]));
-        v[2 * j + 1] = __fmul_rn(bf16_bits_to_float(w[j] >> 16), __frcp_rn(f[2 * j + 1]));
+        v[2 * j] = __fmul_rn(bf16_bits_to_float(w[j] & 0xffffu), r[2 * j]);
+        v[2 * j + 1] = __fmul_rn(bf16_bits_to_float(w[j] >> 16), r[2 * j + 1]);
+    }
+}
+
+// rcp[i] = the correctly rounded reciprocal of smooth[i] (once per call,
+// before the quantisers; n a multiple of 4).
+__global__ void __launch_bounds__(256) smooth_rcp_kernel(const float* __restrict__ smooth, int64_t n4,
+                                                         float* __restrict__ rcp) {
+    pdl_wait();
+    pdl_trigger();
+    for (int64_t i = (int64_t)blockIdx.x * 256 + threadIdx.x; i < n4; i += (int64_t)gridDim.x * 256) {
+        const float4 f = reinterpret_cast<const float4*>(smooth)[i];
+        reinterpret_cast<float4*>(rcp)[i] = make_float4(__frcp_rn(f.x), __frcp_rn(f.y), __frcp_rn(f.z), __frcp_rn(f.w));
     }
 }
 
 __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ smooth, const int32_t* __restrict__ topk_ids,
+    const uint16_t* __restrict__ x, const float* __restrict__ rcp, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
@@ -307,7 +319,7 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
         slot_token[slot] = t;
     }
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    const float4* fr = reinterpret_cast<const float4*>(smooth + (size_t)e * H);
+    const float4* fr = reinterpret_cast<const float4*>(rcp + (size_t)e * H);
     const int nv = H / 8;  // 8 bf16 per 16-byte vector
     float amax = 0.f;
     for (int i = lane; i < nv; i += 32) {
@@ -340,6 +352,87 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
     for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
     if (lane == 0) {
         const int flagged = l1 > kExactL1 ? 1 : 0;
+        flags[slot] = flagged;
+        if (flagged) fb_list[atomicAdd(fb_count, 1)] = slot;
+    }
+}
+
+// The same with one CTA of 256 threads per (token, choice) and the smoothed
+// row in registers (H <= 256 * 8 * kSmVec): for few slots (decode).
+constexpr int kSmVec = 8;
+
+__global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
+    const uint16_t* __restrict__ x, const float* __restrict__ rcp, const int32_t* __restrict__ topk_ids,
+    const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
+    int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
+    float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
+    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    __shared__ float red_max[8];
+    __shared__ int red_l1[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int64_t c = blockIdx.x;
+    pdl_wait();
+    pdl_trigger();
+    if (c >= (int64_t)T * k) return;
+    const int t = (int)(c / k);
+    const int e = topk_ids[c];
+    const int slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[c];
+    if (tid == 0) {
+        slot_of[c] = slot;
+        slot_token[slot] = t;
+    }
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const float4* fr = reinterpret_cast<const float4*>(rcp + (size_t)e * H);
+    const int nv = H / 8;
+    float v[kSmVec][8];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kSmVec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx < nv) {
+            smooth8(__ldg(row + idx), __ldg(fr + 2 * idx), __ldg(fr + 2 * idx + 1), v[i]);
+        } else {
+#pragma unroll
+            for (int m = 0; m < 8; ++m) v[i][m] = 0.f;
+        }
+#pragma unroll
+        for (int m = 0; m < 8; ++m) amax = fmaxf(amax, fabsf(v[i][m]));
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red_max[warp] = amax;
+    __syncthreads();
+    amax = red_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) {
+        s_slot[slot] = s;
+        if (c - (int64_t)t * k == 0) s_x[t] = s;
+    }
+    int l1 = 0;
+#pragma unroll
+    for (int i = 0; i < kSmVec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        int q[8];
+#pragma unroll
+        for (int m = 0; m < 8; ++m) {
+            q[m] = quant_code_div(v[i][m], s);
+            l1 += abs(q[m]);
+        }
+        if (q16 != nullptr) reinterpret_cast<uint4*>(q16 + (size_t)slot * H)[idx] = pack_codes_f16(q);
+        if (q8 != nullptr) reinterpret_cast<uint2*>(q8 + (size_t)slot * H)[idx] = pack_codes_s8(q);
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (lane == 0) red_l1[warp] = l1;
+    __syncthreads();
+    if (tid == 0) {
+        int tot = 0;
+#pragma unroll
+        for (int i = 0; i < 8; ++i) tot += red_l1[i];
+        const int flagged = tot > kExactL1 ? 1 : 0;
         flags[slot] = flagged;
         if (flagged) fb_list[atomicAdd(fb_count, 1)] = slot;
     }
@@ -382,15 +475,25 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
                          slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
 }
 
-cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, const int32_t* topk_ids,
-                                        const int32_t* rank, const int32_t* hist, int T, int H, int E, int k,
-                                        int32_t* slot_of, int32_t* slot_token, float* s_x, float* s_slot,
-                                        uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
+cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, float* rcp,
+                                        const int32_t* topk_ids, const int32_t* rank, const int32_t* hist, int T,
+                                        int H, int E, int k, int32_t* slot_of, int32_t* slot_token, float* s_x,
+                                        float* s_slot, uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
                                         int32_t* fb_count, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
+    const int64_t n4 = (int64_t)E * H / 4;
+    int64_t blocks = (n4 + 255) / 256;
+    if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
+    cudaError_t e = launch_kernel(smooth_rcp_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, smooth, n4, rcp);
+    if (e != cudaSuccess) return e;
     const int64_t n = (int64_t)T * k;
-    return launch_kernel(permute_quant_smooth_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, pdl, x,
-                         smooth, topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
+    // few slots: a CTA per slot (as the plain quantiser's threshold)
+    if (n <= (int64_t)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kSmVec)
+        return launch_kernel(permute_quant_smooth_cta_kernel, dim3((unsigned)n), dim3(256), 0, st, pdl, x, rcp,
+                             topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
+                             fb_list, fb_count);
+    return launch_kernel(permute_quant_smooth_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, pdl, x, rcp,
+                         topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
                          fb_list, fb_count);
 }
 

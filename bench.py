@@ -328,7 +328,7 @@ def layer_roofline_us(cfg, offsets, peaks, fmt="int8"):
 
 GEMM_SOURCES = {
     "int8": ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
-    "fp8": ("fp8.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
+    "fp8": ("fp8.cu", "gemm_fp8_pair.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
 }
 
 

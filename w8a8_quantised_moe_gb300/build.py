@@ -15,7 +15,7 @@ CSRC = os.path.join(PKG, "csrc")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmoe_w8a8.so")
 SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu", "gemm_pair.cu", "gemm_skinny.cu",
-           "static_linear.cu", "fp8.cu"]
+           "static_linear.cu", "fp8.cu", "gemm_fp8_pair.cu"]
 HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh"]
 
 NVCC_FLAGS = [

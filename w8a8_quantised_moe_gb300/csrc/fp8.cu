@@ -605,10 +605,17 @@ cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t
     return launch_kernel(requant_fp8_kernel, dim3((S + 7) / 8), dim3(256), 0, st, pdl, h, S, I, s_h, q8);
 }
 
+// The CTA-pair kernel (gemm_fp8_pair.cu).
+bool fp8_pair_gemm_supported(const GemmArgs& args);
+cudaError_t launch_grouped_gemm_fp8_pair(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
+
 cudaError_t launch_grouped_gemm_fp8(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (args.total_rows == 0) return cudaSuccess;
     if (args.act8 == nullptr || args.K % kF8BK != 0) return cudaErrorInvalidValue;
     const bool narrow = (long)args.total_rows <= 32L * (args.n_groups > 0 ? args.n_groups : 1);
+    // wide groups on CTA pairs when the channel blocks pair up (measured on the
+    // prefill layer: see the pair kernel's notes)
+    if (!narrow && fp8_pair_gemm_supported(args)) return launch_grouped_gemm_fp8_pair(epi, args, st, pdl);
     switch (epi) {
         case Epi::GateUp:
             return narrow ? launch_fp8_impl<F8Narrow, 0>(args, st, pdl) : launch_fp8_impl<F8Wide, 0>(args, st, pdl);

@@ -50,6 +50,7 @@ struct P8Cfg {
     static constexpr int kStageB = kHalf * kP8BK;   // [BN/2 x 128] E4M3
     static constexpr int kStage = kStageA + kStageB;
     static constexpr int kTmemCols = kP8ND * BN;
+    static constexpr int kTmemAlloc = 512;  // a power of two; the pair takes all of it
     static constexpr int kXchStride = 33;
     static constexpr int kXch = kTileM * kXchStride * 4;  // GateUp: gate/up exchange
     static constexpr int kStoreBuf = 32 * kTileM * 4;     // ScaleF32: [32 rows][128 channels] staging
@@ -63,10 +64,19 @@ struct P8Cfg {
     static constexpr int kSmem = kOffMisc + 64 + 1024;
     static_assert(kStageA % 1024 == 0 && kStageB % 1024 == 0, "stages keep 1024-byte alignment");
     static_assert(BN % 32 == 0 && BN <= 256, "pair tile width");
-    static_assert(kTmemCols == 512, "the pair allocates all of tensor memory");
+    static_assert(kTmemCols <= kTmemAlloc, "TMEM budget");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
-using P8Wide = P8Cfg<256, 5>;
+// Measured on the prefill layer (GEMM1 / GEMM2 us): 256-row tiles with 5
+// stages 271 / 143; 4 stages 277 / 150; 192-row tiles with 6 stages 261 / 148;
+// 128-row tiles with 7 stages 313 / 179.
+#ifndef MOE_P8_NS
+#define MOE_P8_NS 5
+#endif
+#ifndef MOE_P8_BN
+#define MOE_P8_BN 256
+#endif
+using P8Wide = P8Cfg<MOE_P8_BN, MOE_P8_NS>;
 
 // One tcgen05 MMA on the CTA pair, kind::f8f6f4, both operands from shared
 // memory (each CTA's half at the same offset): D[256 x N] (+)= A * B^T, K = 32.
@@ -166,7 +176,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
         if (EPI != (int)Epi::GateUp) tma_prefetch_desc(&tmap_out);
     }
     if (warp == 1) {
-        tmem_alloc_pair(tmem_slot, C::kTmemCols);
+        tmem_alloc_pair(tmem_slot, C::kTmemAlloc);
         tmem_relinquish_pair();
     }
     pdl_wait();  // the previous kernel's outputs (offsets, codes, scales) are visible from here
@@ -391,7 +401,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
     if (warp == 1) {
         __syncwarp();
         tc_fence_after();
-        tmem_dealloc_pair(tmem, C::kTmemCols);
+        tmem_dealloc_pair(tmem, C::kTmemAlloc);
     }
 }
 

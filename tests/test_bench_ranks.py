@@ -9,6 +9,7 @@ import pytest
 import torch.multiprocessing as mp
 
 import bench
+from conftest import ROOT
 
 
 def _free_port():
@@ -62,3 +63,23 @@ def test_reference_arm_other_ranks_exit_without_work(monkeypatch, capsys):
     monkeypatch.setenv("RANK", "1")
     assert bench.main(["--impl", "reference", "--config", "tiny", "--steps", "1", "--warmup", "0"]) == 0
     assert capsys.readouterr().out == ""
+
+
+@pytest.mark.parametrize("fmt", ["int8", "fp8", "int8-smooth"])
+def test_reference_arm_line_on_the_host(fmt):
+    """The reference arm (the oracle on the host cores) prints one JSON line
+    with the contract's keys, for every format, on the tiny layer."""
+    import json
+    import subprocess
+    import sys
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference", "--config", "tiny",
+                        "--steps", "1", "--warmup", "1", "--format", fmt],
+                       capture_output=True, text=True, cwd=ROOT, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]
+    line = json.loads(r.stdout.strip().splitlines()[-1])
+    assert line["impl"] == "reference" and line["value"] > 0 and line["unit"] == "tokens/s"
+    for key in ("metric", "n_gpus", "steps", "warmup", "ms_per_step", "higher_is_better", "cpu_baseline", "e2e",
+                "config", "dtype"):
+        assert key in line, key
+    assert line["cpu_baseline"]["kind"] == "oracle"
+    assert line["e2e"]["h2d_bytes_per_step"] == 0

@@ -103,6 +103,8 @@ FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     L.err = take(256);
     L.counts = take(2 * 4);
     const RouterPlan rp = router_plan(T, H, E);
+    // the router's three-part bf16 weight split; once the router has run, the
+    // smoothed layer keeps its reciprocal factors here (4 * E * H <= 6 * E_pad * H)
     L.wsplit = take((size_t)3 * rp.E_pad * H * 2);
     L.logits = take((size_t)rp.KS * T * rp.E_pad * 4);
     L.topk_ids = take(S * 4);

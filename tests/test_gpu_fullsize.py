@@ -1,6 +1,6 @@
 """Parity at the benchmark's full sizes (decode, prefill and wide MoE layers,
-the 4096^3 linear layer, and the FP8 (E4M3) variant of the decode and prefill
-layers), in the launch configuration bench.py times: inputs
+the 4096^3 linear layer, and the FP8 (E4M3) and SmoothQuant-folded variants
+of the decode and prefill layers), in the launch configuration bench.py times: inputs
 resident on the device, expert weights drawn in fp32 on the device and
 quantised by the library, one plain forward.
 
@@ -267,6 +267,87 @@ def test_full_size_fp8_layer_sampled_against_oracle(name):
             qh_o, sh_o = oracle.quantize_rows_fp8(h_own)
             o_own[j] = oracle.epilogue_scale_f32(oracle.gemm_fp8(qh_o, w2r), sh_o, s2r)[0]
         # combine of the GPU's own o rows: exact; of the oracle's: the layer tolerance
+        one = np.arange(cfg.k, dtype=np.int32)[None]
+        np.testing.assert_array_equal(y_gpu[i], oracle.combine(o_gpu, one, topk_w[t][None])[0])
+        y_ref[i] = oracle.combine(o_own, one, w_ref[i][None])[0]
+    assert_y_close(y_gpu, y_ref)
+
+
+# ---- the SmoothQuant-folded layer at the benchmark's sizes ------------------
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_full_size_smoothed_layer_sampled_against_oracle(name):
+    cfg = wl.CONFIGS[name]
+    seed = 0
+    inp = wl.make_moe_inputs(cfg, seed)
+    smooth = wl.smoothing_factors(cfg, seed)
+    sm_dev = torch.from_numpy(smooth).cuda()
+    w13_q = torch.empty((cfg.E, 2 * cfg.I, cfg.H), dtype=torch.int8, device="cuda")
+    w13_s = torch.empty((cfg.E, 2 * cfg.I), dtype=torch.float32, device="cuda")
+    w2_q = torch.empty((cfg.E, cfg.H, cfg.I), dtype=torch.int8, device="cuda")
+    w2_s = torch.empty((cfg.E, cfg.H), dtype=torch.float32, device="cuda")
+    for e in range(cfg.E):
+        q, s = moe.quantize_weights_smoothed(wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda"), sm_dev[e])
+        w13_q[e].copy_(q)
+        w13_s[e].copy_(s)
+        q, s = moe.quantize_weights(wl.expert_weight_fp32(cfg, "w2", e, seed, device="cuda"))
+        w2_q[e].copy_(q)
+        w2_s[e].copy_(s)
+    x = bf16_to_dev(inp.x)
+    Wr = torch.from_numpy(inp.Wr).cuda()
+    bias = None if inp.bias is None else torch.from_numpy(inp.bias).cuda()
+    args = (x, Wr, bias, sm_dev, w13_q, w13_s, w2_q, w2_s, cfg.k)
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    y_plain = moe.forward_smooth(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    names = ("topk_ids", "topk_w", "offsets", "slot_of", "slot_token", "s_slot", "q_slot", "acc1", "h", "s_h", "q_h",
+             "acc2", "o")
+    y_dbg, dev = moe.forward_smooth(*args, fields=names, workspace=ws)
+    assert moe.device_error(ws) == 0
+    assert torch.equal(y_plain.view(torch.int16), y_dbg.view(torch.int16))
+
+    ids = dev["topk_ids"].cpu().numpy()
+    topk_w = dev["topk_w"].cpu().numpy()
+    slot_of = dev["slot_of"].cpu().numpy()
+    _check_routing_arrays(cfg, ids, dev["offsets"].cpu().numpy(), slot_of, dev["slot_token"].cpu().numpy())
+
+    tok = np.sort(np.random.default_rng(10).choice(cfg.T, SAMPLE[name], replace=False))
+    ids_ref, w_ref, _ = oracle.router(inp.x[tok], inp.Wr, inp.bias, cfg.k)
+    np.testing.assert_array_equal(ids[tok], ids_ref)
+    np.testing.assert_allclose(topk_w[tok], w_ref, rtol=0, atol=TOPK_W_ATOL)
+    ref_w = {}
+    for e in sorted(set(ids_ref.ravel().tolist())):
+        w13 = wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda").cpu().numpy()
+        ref_w[e] = (oracle.quantize_rows_smoothed(w13, smooth[e]), _oracle_expert(cfg, "w2", e, seed))
+        np.testing.assert_array_equal(w13_q[e].cpu().numpy(), ref_w[e][0][0])
+        np.testing.assert_array_equal(w13_s[e].cpu().numpy(), ref_w[e][0][1])
+
+    xf = oracle.bf16_to_f32(inp.x[tok])
+    y_gpu = bf16_from_dev(y_dbg)[tok]
+    y_ref = np.empty_like(y_gpu)
+    for i, t in enumerate(tok):
+        slots = slot_of[t]
+        o_gpu = dev["o"][torch.from_numpy(slots).long().cuda()].cpu().numpy()
+        o_own = np.empty_like(o_gpu)
+        for j, s in enumerate(slots):
+            e = int(ids_ref[i, j])
+            (w13r, s13r), (w2r, s2r) = ref_w[e]
+            # the slot's row: x times the binary32 reciprocals of its expert's factors, quantised per slot
+            qx, sx = oracle.quantize_rows((xf[i] * (np.float32(1) / smooth[e]))[None])
+            np.testing.assert_array_equal(dev["q_slot"][s].cpu().numpy(), qx[0])
+            assert dev["s_slot"][s].item() == sx[0]
+            acc1 = oracle.gemm_s8(qx, w13r)
+            np.testing.assert_array_equal(dev["acc1"][s].cpu().numpy(), acc1[0])
+            h_ref = oracle.epilogue_gate_up(acc1, sx, s13r)
+            h_gpu = dev["h"][s].cpu().numpy()
+            np.testing.assert_allclose(h_gpu, h_ref[0], rtol=H_RTOL, atol=1e-30)
+            qh, sh = oracle.quantize_rows(h_gpu[None])
+            np.testing.assert_array_equal(dev["q_h"][s].cpu().numpy(), qh[0])
+            acc2 = oracle.gemm_s8(qh, w2r)
+            np.testing.assert_array_equal(dev["acc2"][s].cpu().numpy(), acc2[0])
+            np.testing.assert_array_equal(o_gpu[j], oracle.epilogue_scale(acc2, sh, s2r)[0])
+            qh_o, sh_o = oracle.quantize_rows(h_ref)
+            o_own[j] = oracle.epilogue_scale(oracle.gemm_s8(qh_o, w2r), sh_o, s2r)[0]
         one = np.arange(cfg.k, dtype=np.int32)[None]
         np.testing.assert_array_equal(y_gpu[i], oracle.combine(o_gpu, one, topk_w[t][None])[0])
         y_ref[i] = oracle.combine(o_own, one, w_ref[i][None])[0]

@@ -19,10 +19,10 @@ from . import _lib
 from ._lib import MoeError, STATUS
 
 __all__ = [
-    "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward",
-    "forward_debug", "forward_host", "host_chunks", "linear_workspace_size", "linear", "device_error", "set_wait_timeout_ns", "set_gemm_path",
-    "GEMM_PATHS",
-    "version",
+    "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward", "forward_debug",
+    "forward_host", "host_chunks", "quantize_weights_smoothed", "forward_smooth", "linear_workspace_size", "linear",
+    "device_error", "set_wait_timeout_ns", "set_gemm_path", "GEMM_PATHS", "version",
+    "fp8_quantize_weights", "fp8_forward", "fp8_forward_debug", "fp8_forward_host",
 ]
 
 

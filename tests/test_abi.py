@@ -161,3 +161,21 @@ def test_python_front_end_fails_loudly_without_library(tmp_path, monkeypatch):
     with pytest.raises(ImportError):
         _lib.load(str(tmp_path / "missing.so"))
     assert moe.__name__  # the package itself imports without the library
+
+
+def test_smoothed_entry_points_reject_bad_arguments(lib):
+    T, H, I, E, k = 16, 256, 512, 8, 2
+    need = lib.moe_w8a8_workspace_size(T, H, I, E, k)
+
+    def fwd(smooth=FAKE, T=T, x=FAKE):
+        return lib.moe_w8a8_forward_smooth(x, FAKE, None, smooth, FAKE, FAKE, FAKE, FAKE, T, H, I, E, k, FAKE, FAKE,
+                                           need, None, None)
+    assert fwd(smooth=None) == INVALID
+    assert fwd(smooth=FAKE + 4) == INVALID
+    assert fwd(x=None) == INVALID
+    assert fwd(T=0, smooth=None) == OK  # no tokens: nothing is read
+    q = lib.moe_w8a8_quantize_weights_smoothed
+    assert q(FAKE, 4, 128, None, FAKE, FAKE, None) == INVALID
+    assert q(FAKE, 4, 128, FAKE + 4, FAKE, FAKE, None) == INVALID
+    assert q(FAKE, 4, 0, FAKE, FAKE, FAKE, None) == SHAPE
+    assert q(FAKE, 0, 128, FAKE, FAKE, FAKE, None) == OK

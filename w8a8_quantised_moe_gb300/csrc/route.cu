@@ -358,11 +358,17 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
 }
 
 // The same with one CTA of 256 threads per (token, choice) and the smoothed
-// row in registers (H <= 256 * 8 * kSmVec): for few slots (decode).
+// row in registers (H <= 256 * 8 * kSmVec): for few slots (decode).  It takes
+// the factors themselves and forms each reciprocal where it is used, so that
+// no table (and no extra launch) is needed for a few rows.
 constexpr int kSmVec = 8;
 
+__device__ __forceinline__ float4 rcp4(const float4 f) {
+    return make_float4(__frcp_rn(f.x), __frcp_rn(f.y), __frcp_rn(f.z), __frcp_rn(f.w));
+}
+
 __global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
-    const uint16_t* __restrict__ x, const float* __restrict__ rcp, const int32_t* __restrict__ topk_ids,
+    const uint16_t* __restrict__ x, const float* __restrict__ smooth, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
@@ -382,7 +388,7 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
         slot_token[slot] = t;
     }
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    const float4* fr = reinterpret_cast<const float4*>(rcp + (size_t)e * H);
+    const float4* fr = reinterpret_cast<const float4*>(smooth + (size_t)e * H);
     const int nv = H / 8;
     float v[kSmVec][8];
     float amax = 0.f;
@@ -390,7 +396,7 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
     for (int i = 0; i < kSmVec; ++i) {
         const int idx = tid + 256 * i;
         if (idx < nv) {
-            smooth8(__ldg(row + idx), __ldg(fr + 2 * idx), __ldg(fr + 2 * idx + 1), v[i]);
+            smooth8(__ldg(row + idx), rcp4(__ldg(fr + 2 * idx)), rcp4(__ldg(fr + 2 * idx + 1)), v[i]);
         } else {
 #pragma unroll
             for (int m = 0; m < 8; ++m) v[i][m] = 0.f;
@@ -481,17 +487,18 @@ cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, 
                                         float* s_slot, uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
                                         int32_t* fb_count, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
+    const int64_t n = (int64_t)T * k;
+    // few slots: a CTA per slot (as the plain quantiser's threshold), reciprocals formed in place
+    if (n <= (int64_t)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kSmVec)
+        return launch_kernel(permute_quant_smooth_cta_kernel, dim3((unsigned)n), dim3(256), 0, st, pdl, x, smooth,
+                             topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
+                             fb_list, fb_count);
+    // many slots: the reciprocal table once, then a warp per slot
     const int64_t n4 = (int64_t)E * H / 4;
     int64_t blocks = (n4 + 255) / 256;
     if (blocks > 4L * num_sms()) blocks = 4L * num_sms();
     cudaError_t e = launch_kernel(smooth_rcp_kernel, dim3((unsigned)blocks), dim3(256), 0, st, pdl, smooth, n4, rcp);
     if (e != cudaSuccess) return e;
-    const int64_t n = (int64_t)T * k;
-    // few slots: a CTA per slot (as the plain quantiser's threshold)
-    if (n <= (int64_t)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kSmVec)
-        return launch_kernel(permute_quant_smooth_cta_kernel, dim3((unsigned)n), dim3(256), 0, st, pdl, x, rcp,
-                             topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
-                             fb_list, fb_count);
     return launch_kernel(permute_quant_smooth_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, pdl, x, rcp,
                          topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
                          fb_list, fb_count);

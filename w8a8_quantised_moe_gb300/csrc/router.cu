@@ -204,49 +204,67 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
 }
 
-// Top-k of one token's logits, one warp: lane l holds the logits of experts
-// l + 32 i (experts >= E are never taken).  Ties go to the lower expert
-// index; choice j ends in lane j as its expert and its softmax weight over
-// the selected logits.
-template <int EPT>
-__device__ __forceinline__ void warp_topk(const float (&v)[EPT], int E, int k, int lane, int& my_e, float& my_w) {
-    bool taken[EPT];
+// Top-k of NT tokens' logits, one warp, the tokens' reductions interleaved:
+// lane l holds the logits of experts l + 32 i (experts >= E are never taken).
+// Ties go to the lower expert index; choice j of token r ends in lane j as
+// my_e[r] and its softmax weight over the selected logits, my_w[r].
+template <int EPT, int NT>
+__device__ __forceinline__ void warp_topk(const float (&v)[NT][EPT], int E, int k, int lane, int (&my_e)[NT],
+                                          float (&my_w)[NT]) {
+    bool taken[NT][EPT];
+    float sel0[NT], den[NT], my_v[NT];
 #pragma unroll
-    for (int i = 0; i < EPT; ++i) taken[i] = (lane + 32 * i) >= E;
-    float sel0 = 0.f, den = 0.f, my_v = 0.f;
-    my_e = 0;
+    for (int r = 0; r < NT; ++r) {
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) taken[r][i] = (lane + 32 * i) >= E;
+        sel0[r] = 0.f;
+        den[r] = 0.f;
+        my_v[r] = 0.f;
+        my_e[r] = 0;
+    }
     for (int j = 0; j < k; ++j) {
-        float bv = -INFINITY;
-        int be = 0x7fffffff;
+        float bv[NT];
+        int be[NT];
 #pragma unroll
-        for (int i = 0; i < EPT; ++i) {
-            const int e = lane + 32 * i;
-            if (!taken[i] && (v[i] > bv || (v[i] == bv && e < be))) {
-                bv = v[i];
-                be = e;
+        for (int r = 0; r < NT; ++r) {
+            bv[r] = -INFINITY;
+            be[r] = 0x7fffffff;
+#pragma unroll
+            for (int i = 0; i < EPT; ++i) {
+                const int e = lane + 32 * i;
+                if (!taken[r][i] && (v[r][i] > bv[r] || (v[r][i] == bv[r] && e < be[r]))) {
+                    bv[r] = v[r][i];
+                    be[r] = e;
+                }
             }
         }
 #pragma unroll
-        for (int off = 16; off > 0; off >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
-            const int oe = __shfl_xor_sync(0xffffffffu, be, off);
-            if (ov > bv || (ov == bv && oe < be)) {
-                bv = ov;
-                be = oe;
-            }
-        }
+        for (int off = 16; off > 0; off >>= 1)
 #pragma unroll
-        for (int i = 0; i < EPT; ++i)
-            if (lane + 32 * i == be) taken[i] = true;
-        if (j == 0) sel0 = bv;
-        const float ex = expf(__fsub_rn(bv, sel0));
-        den = __fadd_rn(den, ex);
-        if (lane == j) {  // lane j keeps choice j
-            my_v = ex;
-            my_e = be;
+            for (int r = 0; r < NT; ++r) {
+                const float ov = __shfl_xor_sync(0xffffffffu, bv[r], off);
+                const int oe = __shfl_xor_sync(0xffffffffu, be[r], off);
+                if (ov > bv[r] || (ov == bv[r] && oe < be[r])) {
+                    bv[r] = ov;
+                    be[r] = oe;
+                }
+            }
+#pragma unroll
+        for (int r = 0; r < NT; ++r) {
+#pragma unroll
+            for (int i = 0; i < EPT; ++i)
+                if (lane + 32 * i == be[r]) taken[r][i] = true;
+            if (j == 0) sel0[r] = bv[r];
+            const float ex = expf(__fsub_rn(bv[r], sel0[r]));
+            den[r] = __fadd_rn(den[r], ex);
+            if (lane == j) {  // lane j keeps choice j
+                my_v[r] = ex;
+                my_e[r] = be[r];
+            }
         }
     }
-    my_w = __fdiv_rn(my_v, den);
+#pragma unroll
+    for (int r = 0; r < NT; ++r) my_w[r] = __fdiv_rn(my_v[r], den[r]);
 }
 
 // One 32-token chunk, by a whole CTA of 256 threads; `mask` is shared memory
@@ -290,23 +308,24 @@ __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, 
                 vv[r][i] = (t < T && e < E) ? acc : -INFINITY;
             }
     }
+    // the warp's 4 tokens selected together (their shuffle chains interleave)
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-        const int t = t0 + warp * 4 + r;
-        if (t >= T) continue;
-        float v[EPT];
+    for (int r = 0; r < 4; ++r)
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
             const int e = lane + 32 * i;
-            v[i] = (bias && e < E) ? __fadd_rn(vv[r][i], bias[e]) : vv[r][i];
+            if (bias && e < E) vv[r][i] = __fadd_rn(vv[r][i], bias[e]);
         }
-        int my_e;
-        float my_w;
-        warp_topk<EPT>(v, E, k, lane, my_e, my_w);
-        if (lane < k) {
-            topk_ids[(size_t)t * k + lane] = my_e;
-            topk_w[(size_t)t * k + lane] = my_w;
-            atomicOr(&mask[my_e], 1u << (warp * 4 + r));
+    int my_e[4];
+    float my_w[4];
+    warp_topk<EPT, 4>(vv, E, k, lane, my_e, my_w);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+        const int t = t0 + warp * 4 + r;
+        if (t < T && lane < k) {
+            topk_ids[(size_t)t * k + lane] = my_e[r];
+            topk_w[(size_t)t * k + lane] = my_w[r];
+            atomicOr(&mask[my_e[r]], 1u << (warp * 4 + r));
         }
     }
     __syncthreads();
@@ -502,7 +521,7 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float* __restr
     for (int i = 0; i < EPT; ++i) part[warp][lane + 32 * i] = acc[i];
     __syncthreads();
     if (warp == 0) {
-        float v[EPT];
+        float v[1][EPT];
 #pragma unroll
         for (int i = 0; i < EPT; ++i) {
             const int e = lane + 32 * i;
@@ -510,14 +529,14 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float* __restr
 #pragma unroll
             for (int w = 1; w < 8; ++w) l = __fadd_rn(l, part[w][e]);
             if (bias && e < E) l = __fadd_rn(l, bias[e]);
-            v[i] = e < E ? l : -INFINITY;
+            v[0][i] = e < E ? l : -INFINITY;
         }
-        int my_e;
-        float my_w;
-        warp_topk<EPT>(v, E, k, lane, my_e, my_w);
+        int my_e[1];
+        float my_w[1];
+        warp_topk<EPT, 1>(v, E, k, lane, my_e, my_w);
         if (lane < k) {
-            topk_ids[(size_t)t * k + lane] = my_e;
-            topk_w[(size_t)t * k + lane] = my_w;
+            topk_ids[(size_t)t * k + lane] = my_e[0];
+            topk_w[(size_t)t * k + lane] = my_w[0];
         }
     }
 

@@ -217,7 +217,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const int total_tiles = tile_start[n_groups];
     const Tiles tiles{tile_start, row_start, n_groups};
-    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
+    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns, 0u};
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer

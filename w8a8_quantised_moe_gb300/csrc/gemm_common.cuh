@@ -52,8 +52,7 @@ __device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, const 
                 if (*ctl.abort) {
                     give_up = 1;
                 } else if (now - t0 > ctl.timeout_ns) {
-                    *ctl.abort = 1;
-                    atomicOr(ctl.error, kErrTimeout);
+                    give_up_timeout(ctl);
                     give_up = 1;
                 }
             }
@@ -78,8 +77,7 @@ __device__ __forceinline__ bool warp_wait_cluster(uint64_t* bar, uint32_t parity
                 if (*ctl.abort) {
                     give_up = 1;
                 } else if (now - t0 > ctl.timeout_ns) {
-                    *ctl.abort = 1;
-                    atomicOr(ctl.error, kErrTimeout);
+                    give_up_timeout(ctl);
                     give_up = 1;
                 }
             }

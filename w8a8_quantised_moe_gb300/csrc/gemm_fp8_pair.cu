@@ -211,7 +211,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
     const uint32_t tmem = *tmem_slot;
     const int total_tiles = tile_start[n_groups];
     const Tiles tiles{tile_start, row_start, n_groups};
-    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
+    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns,
+                      cluster_addr(const_cast<const int*>(abort_flag), rank ^ 1u)};
 
     if (warp == 0) {
         // ------------------------------------------------ stage TMA (both CTAs)

@@ -58,8 +58,13 @@ constexpr int kPairBK = 128;  // K per stage
 constexpr int kPairND = MOE_P_ND;  // accumulator buffers
 
 // MMA-issuing threads in the even CTA.  Measured: two beat one by 8-10% on
-// the expert GEMMs.  Builds with three or four issuers (13-14 warps) failed
-// to run, with a launch failure whose cause is not known: they are not built.
+// the expert GEMMs.  At most two: an issuer may wait on a_ready[j] for stage
+// i only while the phase of stage i - NA is complete (a parity wait cannot
+// tell phases two apart).  With two issuers that holds for NA >= 2: an issuer
+// has passed the wait of its previous stage, at most two stages back, or, on a
+// tile's first stage, the tile_go barrier, which follows the other issuer's
+// wait on stage i - 1.  A third issuer can be three stages past its previous
+// wait, where two A slots no longer order it.
 #ifndef MOE_P_ISSUERS
 #define MOE_P_ISSUERS 2
 #endif
@@ -91,7 +96,9 @@ struct PairCfg {
     static constexpr int kOffXch = kOffB + NB * kBStage;
     static constexpr int kXchRegion = kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf;
     static constexpr int kOffBars = kOffXch + kXchRegion;
-    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 3 * kPairND + 3;
+    // q_full, q_empty, b_full, done, a_ready, acc_full, acc_empty, tile_go,
+    // one teardown barrier per issuer, epi_bar
+    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 3 * kPairND + kIssuers + 1;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
@@ -102,6 +109,7 @@ struct PairCfg {
     // a converter learns that A slot (it % NA) is free from done[] of stage
     // it - NA, whose barrier cannot have moved on to a later phase when NB >= NA
     static_assert(NB >= NA, "activation ring and A slots");
+    static_assert(NA >= kIssuers, "two issuers need two A slots");
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
@@ -162,8 +170,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint64_t* acc_full = a_ready + C::NA;    // [ND]
     uint64_t* acc_empty = acc_full + kPairND;  // [ND], used in the even CTA
     uint64_t* tile_go = acc_empty + kPairND;  // [ND], even CTA: the tile's overwriting MMAs are issued
-    uint64_t* teardown = tile_go + kPairND;   // [2], one per issuer
-    uint64_t* epi_bar = teardown + 2;
+    uint64_t* teardown = tile_go + kPairND;   // [kIssuers], one per issuer
+    uint64_t* epi_bar = teardown + kIssuers;  // the last barrier of the block (kNumBars)
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -194,8 +202,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mbar_init(&tile_go[d], 1);
             mbar_init(&acc_empty[d], 8);
         }
-        mbar_init(&teardown[0], 1);
-        mbar_init(&teardown[1], 1);
+        for (int r = 0; r < kIssuers; ++r) mbar_init(&teardown[r], 1);
         mbar_init(epi_bar, 4);
         *abort_flag = 0;
         fence_barrier_init();
@@ -242,7 +249,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const uint32_t tmem = *tmem_slot;
     const int total_tiles = tile_start[n_groups];
     const Tiles tiles{tile_start, row_start, n_groups};
-    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns};
+    const WaitCtl ctl{abort_flag, args.error, args.timeout_ns,
+                      cluster_addr(const_cast<const int*>(abort_flag), rank ^ 1u)};
 
     if (warp == 0) {
         // ------------------------------------------------- int8 weight TMA

@@ -58,12 +58,26 @@ __device__ __forceinline__ bool mbar_try_wait(uint64_t* bar, uint32_t parity) {
 }
 
 // Shared control block of one CTA's pipeline: an abort flag that every
-// waiting role polls, the wait limit, and the device error word.
+// waiting role polls, the wait limit, and the device error word.  In a CTA
+// pair, peer_abort is the cluster address of the other CTA's abort flag (0
+// for a lone CTA): a CTA that gives up aborts its peer as well, so the pair's
+// roles stop together instead of each waiting out its own limit.
 struct WaitCtl {
     volatile int* abort;  // shared memory
     int* error;           // global memory (sticky error word)
     uint64_t timeout_ns;
+    uint32_t peer_abort;  // shared::cluster address, or 0
 };
+
+// Records a timed-out wait: aborts this CTA (and its pair peer) and sets the
+// timeout bit of the device error word.  The remote store reaches the peer
+// before either CTA passes the pair's final cluster barrier.
+__device__ __forceinline__ void give_up_timeout(const WaitCtl& ctl) {
+    *ctl.abort = 1;
+    if (ctl.peer_abort != 0u)
+        asm volatile("st.shared::cluster.u32 [%0], %1;" ::"r"(ctl.peer_abort), "r"(1) : "memory");
+    atomicOr(ctl.error, kErrTimeout);
+}
 
 // Wait until the phase of `bar` with parity `parity` has completed.  Gives
 // up when another role has aborted the CTA, or after ctl.timeout_ns, in
@@ -77,8 +91,7 @@ __device__ __forceinline__ bool mbar_wait(uint64_t* bar, uint32_t parity, const 
         if ((i & 31u) == 0u) {
             if (*ctl.abort) return false;
             if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                *ctl.abort = 1;
-                atomicOr(ctl.error, kErrTimeout);
+                give_up_timeout(ctl);
                 return false;
             }
         }
@@ -138,17 +151,6 @@ __device__ __forceinline__ void fence_proxy_async_smem() {
     asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
 }
 
-// Multicast form: the box lands at the same shared-memory offset in every CTA
-// of the cluster named in `cta_mask`, and each signals its own `bar` there.
-__device__ __forceinline__ void tma_load_2d_multicast(void* dst, const CUtensorMap* map, uint64_t* bar, int c0,
-                                                      int c1, uint16_t cta_mask) {
-    asm volatile(
-        "cp.async.bulk.tensor.2d.shared::cluster.global.tile.mbarrier::complete_tx::bytes.multicast::cluster"
-        " [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(smem_u32(dst)),
-        "l"(reinterpret_cast<uint64_t>(map)), "r"(smem_u32(bar)), "r"(c0), "r"(c1), "h"(cta_mask)
-        : "memory");
-}
-
 // ---------------------------------------------------------------- clusters
 
 __device__ __forceinline__ uint32_t cluster_ctarank() {
@@ -195,8 +197,7 @@ __device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity
         if ((i & 31u) == 0u) {
             if (*ctl.abort) return false;
             if (global_timer_ns() - t0 > ctl.timeout_ns) {
-                *ctl.abort = 1;
-                atomicOr(ctl.error, kErrTimeout);
+                give_up_timeout(ctl);
                 return false;
             }
         }
@@ -339,15 +340,6 @@ __device__ __forceinline__ void mma8_f16_tmem_a_pair(uint32_t d_tmem, uint32_t a
 __device__ __forceinline__ void mma_commit_pair(uint64_t* bar, uint16_t cta_mask) {
     asm volatile(
         "tcgen05.commit.cta_group::2.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
-            smem_u32(bar)),
-        "h"(cta_mask)
-        : "memory");
-}
-
-// Like mma_commit, but the arrival goes to `bar` in every CTA of `cta_mask`.
-__device__ __forceinline__ void mma_commit_multicast(uint64_t* bar, uint16_t cta_mask) {
-    asm volatile(
-        "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64 [%0], %1;" ::"r"(
             smem_u32(bar)),
         "h"(cta_mask)
         : "memory");

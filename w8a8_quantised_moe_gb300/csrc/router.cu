@@ -127,7 +127,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
     __syncthreads();
     tc_fence_after();
     const uint32_t tmem = *tmem_slot;
-    const WaitCtl ctl{abort_flag, error, timeout_ns};
+    const WaitCtl ctl{abort_flag, error, timeout_ns, 0u};
 
     if (warp == 0) {
         if (lane == 0) {

@@ -42,6 +42,18 @@
  *   - Calls on different streams are safe when their workspaces differ.
  *   - The calls are deterministic: the same inputs give bit-identical
  *     outputs.
+ *   - Fault injection for tests of the error paths: the environment variable
+ *     MOE_INJECT (read at every call; a comma-separated list) fakes faults.
+ *     On the host, reaching no GPU: "ws_short": the workspace check fails as
+ *     if the workspace were one byte short (MOE_ERR_WORKSPACE_TOO_SMALL);
+ *     "bad_ptr": the pointer check fails as if a data pointer were null
+ *     (MOE_ERR_INVALID_ARG); "launch_fail": every kernel launch fails before
+ *     anything is queued (MOE_ERR_CUDA).  On the GPU: "stall": every
+ *     tensor-core expert or linear GEMM launch starts with its producer
+ *     waiting, within the wait limit (moe_w8a8_set_wait_timeout_ns), on a
+ *     barrier that nothing completes, so that the limit runs out and the
+ *     kernel takes its abort path (MOE_ERR_DEVICE_TIMEOUT from
+ *     moe_w8a8_device_error; outputs undefined).  Unset in normal use.
  */
 #ifndef MOE_W8A8_H
 #define MOE_W8A8_H
@@ -212,16 +224,29 @@ MOE_W8A8_API moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, 
  *   before anything is launched.
  * Set-up: the first call on each device looks up that device's address of
  *   the array (with the device current) and caches it; make that first call
- *   before any stream capture.
+ *   before any stream capture.  The cached address belongs to the device's
+ *   primary context: after cudaDeviceReset (or anything else that destroys
+ *   that context) this entry point must not be called again in the process.
  * Sharing: every call on a device uses the same array, which keeps the last
  *   call's contents (the call clears what must start at zero).  Calls that
  *   overlap on the GPU -- on different streams, or from several host threads
  *   -- race on the array and give undefined results; serialise them.
- * Errors: as moe_w8a8_linear; a device-side timeout marks the output as
- *   undefined but cannot be read back through moe_w8a8_device_error.
+ * Waits: the kernels' spin-waits use the limit of
+ *   moe_w8a8_set_wait_timeout_ns, like every other entry point.
+ * Errors: as moe_w8a8_linear.  A device-side timeout sets the array's own
+ *   sticky error word (the output is then undefined); read it with
+ *   moe_w8a8_linear_static_error.
  * ------------------------------------------------------------------------- */
 MOE_W8A8_API moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* w_q, const float* w_scale,
                                                  int64_t M, int64_t N, int64_t K, uint16_t* y, void* stream);
+
+/* moe_w8a8_linear_static_error -- synchronise `stream`, then read and clear
+ * the sticky device error word of moe_w8a8_linear_static's static scratch on
+ * the current device (set by any earlier call on that device since it was
+ * last read).  Returns MOE_OK, MOE_ERR_DEVICE_TIMEOUT, MOE_ERR_DEVICE, or
+ * MOE_ERR_CUDA if the synchronisation or the read failed.  Allocates
+ * nothing; like the entry point, it must not overlap a call on the GPU. */
+MOE_W8A8_API moe_status_t moe_w8a8_linear_static_error(void* stream);
 
 /* ---------------------------------------------------------------------------
  * The FP8 (E4M3) layer.  "DeepSeek V4 950 FP8 inference on H100" (lpnh.cn):
@@ -398,7 +423,9 @@ MOE_W8A8_API uint64_t moe_w8a8_set_wait_timeout_ns(uint64_t ns);
  * automatic choice where its shape rule fails: K a multiple of 128 and at
  * most 28672, output channels a multiple of 16 for the gate/up GEMM and of
  * 64 otherwise).  Every path computes the same bits.  Returns the previous
- * setting, or -2 (and changes nothing) for a value outside [-1, 4].
+ * setting, or -2 (and changes nothing) for a value outside [-1, 4].  The
+ * FP8 layer has kernels of its own: while a path is forced, its entry points
+ * return MOE_ERR_NOT_IMPLEMENTED and launch nothing.
  * ------------------------------------------------------------------------- */
 MOE_W8A8_API int moe_w8a8_set_gemm_path(int path);
 

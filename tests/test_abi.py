@@ -179,3 +179,55 @@ def test_smoothed_entry_points_reject_bad_arguments(lib):
     assert q(FAKE, 4, 128, FAKE + 4, FAKE, FAKE, None) == INVALID
     assert q(FAKE, 4, 0, FAKE, FAKE, FAKE, None) == SHAPE
     assert q(FAKE, 0, 128, FAKE, FAKE, FAKE, None) == OK
+
+
+# ---- host-side fault injection (MOE_INJECT): every host status code ----
+
+NOT_IMPL, CUDA = -6, -4
+
+
+def test_injected_faults_take_each_host_error_path(lib, monkeypatch):
+    need = lib.moe_w8a8_linear_workspace_size(64, 256, 256)
+    monkeypatch.setenv("MOE_INJECT", "ws_short")
+    assert _fwd(lib) == WS_SMALL
+    assert _fwd_host(lib) == WS_SMALL
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need, None) == WS_SMALL
+    monkeypatch.setenv("MOE_INJECT", "bad_ptr")
+    assert _fwd(lib) == INVALID
+    assert _fwd_host(lib) == INVALID
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need, None) == INVALID
+    assert lib.moe_w8a8_linear_static(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, None) == INVALID
+    assert lib.moe_w8a8_quantize_weights(FAKE, 4, 64, FAKE, FAKE, None) == INVALID
+    monkeypatch.setenv("MOE_INJECT", "launch_fail")
+    assert _fwd(lib) == CUDA
+    assert lib.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need, None) == CUDA
+    assert lib.moe_w8a8_linear_static(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, None) == CUDA
+    assert lib.moe_w8a8_quantize_weights(FAKE, 4, 64, FAKE, FAKE, None) == CUDA
+    assert lib.moe_w8a8_fp8_quantize_weights(FAKE, 4, 64, FAKE, FAKE, None) == CUDA
+    # several faults at once: the argument checks come first
+    monkeypatch.setenv("MOE_INJECT", "launch_fail,ws_short")
+    assert _fwd(lib) == WS_SMALL
+    # the checks themselves still run: a real shape error wins over an injected fault
+    assert _fwd(lib, H=100) == SHAPE
+    monkeypatch.delenv("MOE_INJECT")
+    assert _fwd(lib, T=0) == OK
+
+
+def test_fp8_layer_refuses_a_forced_int8_kernel(lib):
+    T, H, I, E, k = 16, 256, 512, 8, 2
+    need = lib.moe_w8a8_workspace_size(T, H, I, E, k)
+    prev = lib.moe_w8a8_set_gemm_path(3)
+    try:
+        assert lib.moe_w8a8_fp8_forward(FAKE, FAKE, None, FAKE, FAKE, FAKE, FAKE, T, H, I, E, k, FAKE, FAKE, need,
+                                        None) == NOT_IMPL
+        assert _fwd_host(lib, fn="moe_w8a8_fp8_forward_host") == NOT_IMPL
+    finally:
+        lib.moe_w8a8_set_gemm_path(prev)
+
+
+def test_every_host_status_code_is_produced():
+    # the codes the tests above produce; the two device codes are produced on
+    # the GPU (test_gpu_timeout.py) and by moe_w8a8_device_error
+    produced = {OK, INVALID, SHAPE, WS_SMALL, CUDA, NOT_IMPL}
+    device = {-5, -7}
+    assert set(_lib.STATUS) == produced | device

@@ -40,6 +40,7 @@ EXPORTS = (
     "moe_w8a8_set_profile_events",
     "moe_w8a8_launch_count",
     "moe_w8a8_linear_static",
+    "moe_w8a8_linear_static_error",
     "moe_w8a8_fp8_quantize_weights",
     "moe_w8a8_fp8_forward",
     "moe_w8a8_fp8_forward_debug",
@@ -93,6 +94,7 @@ def load(path: str = LIB_PATH):
             "moe_w8a8_set_profile_events": ([ctypes.c_void_p, i32], i32),
             "moe_w8a8_launch_count": ([], ctypes.c_uint64),
             "moe_w8a8_linear_static": ([vp, vp, vp, i64, i64, i64, vp, vp], i32),
+            "moe_w8a8_linear_static_error": ([vp], i32),
             "moe_w8a8_fp8_quantize_weights": ([vp, i64, i64, vp, vp, vp], i32),
             "moe_w8a8_fp8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
             "moe_w8a8_fp8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,

@@ -73,6 +73,26 @@ bool moe_shape_ok(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
 
 bool pdl_default() { return t_events == nullptr && !pdl_env_off(); }
 
+uint64_t current_timeout_ns() { return g_timeout_ns.load(); }
+
+bool injected(InjectFault f) {
+    const char* v = std::getenv("MOE_INJECT");
+    if (v == nullptr || v[0] == '\0') return false;
+    const char* name = f == kInjectWsShort ? "ws_short"
+                       : f == kInjectBadPtr ? "bad_ptr"
+                       : f == kInjectLaunchFail ? "launch_fail"
+                                                : "stall";
+    const size_t n = std::strlen(name);
+    for (const char* p = v; *p != '\0';) {
+        const char* end = std::strchr(p, ',');
+        const size_t len = end ? (size_t)(end - p) : std::strlen(p);
+        if (len == n && std::strncmp(p, name, n) == 0) return true;
+        if (!end) break;
+        p = end + 1;
+    }
+    return false;
+}
+
 namespace {
 std::atomic<uint64_t> g_launches{0};
 }
@@ -170,11 +190,15 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     if (smooth != nullptr && !aligned16(smooth)) return MOE_ERR_INVALID_ARG;
     const void* ptrs[] = {x, router_w, w13_q, w13_scale, w2_q, w2_scale, y, workspace};
     for (const void* p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+        if (p == nullptr || !aligned16(p) || injected(kInjectBadPtr)) return MOE_ERR_INVALID_ARG;
     if (router_bias != nullptr && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     const FwdLayout L = fwd_layout(T, H, I, E, k);
+    if (injected(kInjectWsShort) && workspace_bytes >= L.total) workspace_bytes = L.total - 1;
     if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    // the FP8 layer has its own GEMM kernels: a forced INT8 kernel choice
+    // (moe_w8a8_set_gemm_path) cannot be honoured there
+    if (fp8 && g_gemm_path.load() >= 0) return MOE_ERR_NOT_IMPLEMENTED;
 
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const int S = (int)(T * k);
@@ -260,6 +284,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g1.fb_count = counts + 0;
     g1.error = err;
     g1.timeout_ns = timeout;
+    g1.stall = injected(kInjectStall) ? 1 : 0;
     if ((e = mark(3, st)) != cudaSuccess) return from_cuda(e);
     e = fp8 ? launch_grouped_gemm_fp8(Epi::GateUp, g1, st, pdl) : launch_grouped_gemm(Epi::GateUp, shape1, g1, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
@@ -294,6 +319,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     g2.fb_count = counts + 1;
     g2.error = err;
     g2.timeout_ns = timeout;
+    g2.stall = g1.stall;
     if ((e = mark(5, st)) != cudaSuccess) return from_cuda(e);
     e = fp8 ? launch_grouped_gemm_fp8(Epi::ScaleF32, g2, st, pdl)
             : launch_grouped_gemm(Epi::ScaleF32, shape2, g2, st, pdl);
@@ -375,11 +401,14 @@ moe_status_t forward_host_impl(const uint16_t* x_host, const float* router_w, co
     if (T == 0) return MOE_OK;
     const void* ptrs[] = {x_host, y_host, x_dev, y_dev, router_w, w13_q, w13_scale, w2_q, w2_scale, workspace};
     for (const void* p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+        if (p == nullptr || !aligned16(p) || injected(kInjectBadPtr)) return MOE_ERR_INVALID_ARG;
     if (router_bias != nullptr && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
     if (chunks < 0 || chunks > kMaxChunks) return MOE_ERR_INVALID_ARG;
-    if (workspace_bytes < fwd_layout(T, H, I, E, k).total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    const size_t need = fwd_layout(T, H, I, E, k).total;
+    if (injected(kInjectWsShort) && workspace_bytes >= need) workspace_bytes = need - 1;
+    if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    if (fp8 && g_gemm_path.load() >= 0) return MOE_ERR_NOT_IMPLEMENTED;
     int n = chunks == 0 ? auto_chunks(T, H, I, E) : chunks;
     if (n > T) n = (int)T;
     cudaStream_t cs = static_cast<cudaStream_t>(stream);
@@ -461,8 +490,10 @@ moe_status_t moe_w8a8_fp8_quantize_weights(const float* w, int64_t rows, int64_t
                                            void* stream) {
     if (rows < 0 || K < 4 || K > (int64_t(1) << 20) || K % 4 != 0) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
-    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale))
+    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale) ||
+        injected(kInjectBadPtr))
         return MOE_ERR_INVALID_ARG;
+    if (injected(kInjectLaunchFail)) return MOE_ERR_CUDA;
     return from_cuda(
         launch_quantize_weights_fp8(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream)));
 }
@@ -490,8 +521,10 @@ moe_status_t moe_w8a8_quantize_weights(const float* w, int64_t rows, int64_t K, 
                                        float* w_scale, void* stream) {
     if (rows < 0 || K < 1 || K > (int64_t(1) << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
-    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale))
+    if (!w || !w_q || !w_scale || !aligned16(w) || !aligned16(w_q) || !aligned16(w_scale) ||
+        injected(kInjectBadPtr))
         return MOE_ERR_INVALID_ARG;
+    if (injected(kInjectLaunchFail)) return MOE_ERR_CUDA;
     return from_cuda(launch_quantize_weights(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream)));
 }
 
@@ -539,8 +572,9 @@ moe_status_t moe_w8a8_quantize_weights_smoothed(const float* w, int64_t rows, in
     if (rows < 0 || K < 1 || K > (int64_t(1) << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
     if (rows == 0) return MOE_OK;
     if (!w || !col_scale || !w_q || !w_scale || !aligned16(w) || !aligned16(col_scale) || !aligned16(w_q) ||
-        !aligned16(w_scale))
+        !aligned16(w_scale) || injected(kInjectBadPtr))
         return MOE_ERR_INVALID_ARG;
+    if (injected(kInjectLaunchFail)) return MOE_ERR_CUDA;
     return from_cuda(
         launch_quantize_weights(w, rows, (int)K, w_q, w_scale, static_cast<cudaStream_t>(stream), col_scale));
 }
@@ -580,9 +614,12 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     if (M == 0) return MOE_OK;  // nothing is read or written
     const void* ptrs[] = {x, w_q, w_scale, y, workspace};
     for (const void* p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+        if (p == nullptr || !aligned16(p) || injected(kInjectBadPtr)) return MOE_ERR_INVALID_ARG;
     if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    if (injected(kInjectWsShort) && workspace_bytes >= need) workspace_bytes = need - 1;
     if (workspace_bytes < need) return MOE_ERR_WORKSPACE_TOO_SMALL;
+    // a faked launch failure is reported before the first CUDA call (the memset)
+    if (injected(kInjectLaunchFail)) return MOE_ERR_CUDA;
     cudaStream_t st = static_cast<cudaStream_t>(stream);
     const LinLayout L = lin_layout(M, N, K);
     float* s_x = at<float>(workspace, L.s_x);
@@ -620,6 +657,7 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     g.fb_count = counts;
     g.error = at<int>(workspace, L.err);
     g.timeout_ns = g_timeout_ns.load();
+    g.stall = injected(kInjectStall) ? 1 : 0;
     if ((e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st, pdl_default())) != cudaSuccess)
         return from_cuda(e);
     return from_cuda(mark(2, st));

@@ -278,7 +278,7 @@ struct F8Cfg {
     static constexpr int kXch = kTileM * kXchStride * 4;
     static constexpr int kOffXch = NS * kStage;
     static constexpr int kOffBars = kOffXch + kXch;
-    static constexpr int kNumBars = 2 * NS + 2 * ND + 2;
+    static constexpr int kNumBars = 2 * NS + 2 * ND + 3;  // ..., teardown, epi_bar, stall_bar
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;  // [2][BN] activation scales
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4;
@@ -331,6 +331,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     uint64_t* acc_empty = acc_full + ND;  // [ND] 4 epilogue warps
     uint64_t* teardown = acc_empty + ND;
     uint64_t* epi_bar = teardown + 1;
+    uint64_t* stall_bar = epi_bar + 1;  // test hook: nothing arrives on it
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     float* row_scale_s = reinterpret_cast<float*>(smem + C::kOffRowInfo);  // [2][BN]
@@ -353,6 +354,7 @@ __global__ void __launch_bounds__(kF8Threads, 1)
         }
         mbar_init(teardown, 1);
         mbar_init(epi_bar, 4);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
@@ -400,9 +402,15 @@ __global__ void __launch_bounds__(kF8Threads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
+        // three boxes a stage (weight rows 0-63 and 64-127, activation rows);
+        // lanes 0-2 issue one each in the same warp instruction (a bulk
+        // tensor copy costs its issuing thread ~200 cycles); lane 0 owns the
+        // waits and the arrival
+        if (lane < 3) {
             uint32_t it = 0;
-            bool ok = true;
+            int ok = 1;
+            if (lane == 0) ok = !args.stall || mbar_wait(stall_bar, 0, ctl);  // the test hook's wait runs out
+            ok = __shfl_sync(0x7u, ok, 0);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int g, cb, row0, nvalid;
                 f8_decode_tile<BN>(tiles, tile, g, cb, row0, nvalid);
@@ -417,21 +425,26 @@ __global__ void __launch_bounds__(kF8Threads, 1)
                 const int bi = f8_box_index(nvalid);
                 const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
                 const uint32_t stage_bytes = (uint32_t)(C::kStageA + f8_box_rows<BN>(bi) * kF8BK);
+                const CUtensorMap* map = lane == 2 ? mb : &tmap_w;
+                const int row = lane == 0 ? wrow0 : lane == 1 ? wrow1 : row0;
+                const int off = lane == 0 ? 0 : lane == 1 ? C::kStageA / 2 : C::kStageA;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % NS, ph = (it / NS) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
-                    tma_load_2d(st, &tmap_w, &full[s], kb * kF8BK, wrow0);
-                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kb * kF8BK, wrow1);
-                    tma_load_2d(st + C::kStageA, mb, &full[s], kb * kF8BK, row0);
+                    if (lane == 0) {
+                        ok = mbar_wait(&empty[s], ph ^ 1u, ctl);
+                        if (ok) mbar_arrive_expect_tx(&full[s], stage_bytes);
+                    }
+                    ok = __shfl_sync(0x7u, ok, 0);
+                    if (!ok) break;
+                    tma_load_2d(smem + s * C::kStage + off, map, &full[s], kb * kF8BK, row);
                 }
             }
             // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
-                mbar_wait_drain(&full[s], (last / NS) & 1u);
-            }
+            if (lane == 0)
+                for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                    const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                    mbar_wait_drain(&full[s], (last / NS) & 1u);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer

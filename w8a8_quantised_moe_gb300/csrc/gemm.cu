@@ -69,7 +69,7 @@ struct Cfg {
     static constexpr int kXch = kTileM * kXchStride * 4;  // gate/up exchange, 32 columns
     static constexpr int kOffXch = NS * kStage;
     static constexpr int kOffBars = kOffXch + kXch;
-    static constexpr int kNumBars = 3 * NS + 2 * ND + 2;
+    static constexpr int kNumBars = 3 * NS + 2 * ND + 3;  // ..., teardown, epi_bar, stall_bar
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;  // [2][BN] scales, [2][BN] flags
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
@@ -150,6 +150,7 @@ __global__ void __launch_bounds__(kThreads, 1)
     uint64_t* acc_empty = acc_full + ND;  // [ND]
     uint64_t* teardown = acc_empty + ND;
     uint64_t* epi_bar = teardown + 1;
+    uint64_t* stall_bar = epi_bar + 1;  // test hook: nothing arrives on it
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -174,6 +175,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         }
         mbar_init(teardown, 1);
         mbar_init(epi_bar, 4);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
@@ -221,9 +223,18 @@ __global__ void __launch_bounds__(kThreads, 1)
 
     if (warp == 0) {
         // ---------------------------------------------------------- producer
-        if (lane == 0) {
+        // A stage is 2 * kNumSubA weight boxes and BK / 64 activation boxes;
+        // lane l issues box l, all in the same warp instruction (a bulk tensor
+        // copy costs its issuing thread ~200 cycles).  Lane 0 owns the waits
+        // and the arrival.
+        constexpr int kBoxes = 2 * C::kNumSubA + BK / 64;
+        static_assert(kBoxes <= 32, "boxes per stage");
+        constexpr uint32_t kMask = kBoxes == 32 ? 0xffffffffu : ((1u << kBoxes) - 1u);
+        if (lane < kBoxes) {
             uint32_t it = 0;
-            bool ok = true;
+            int ok = 1;
+            if (lane == 0) ok = !args.stall || mbar_wait(stall_bar, 0, ctl);  // the test hook's wait runs out
+            ok = __shfl_sync(kMask, ok, 0);
             for (int tile = blockIdx.x; ok && tile < total_tiles; tile += gridDim.x) {
                 int g, cb, row0, nvalid;
                 decode_tile<BN>(tiles, tile, g, cb, row0, nvalid);
@@ -238,27 +249,31 @@ __global__ void __launch_bounds__(kThreads, 1)
                 const int bi = box_index<BN>(nvalid);
                 const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
                 const uint32_t stage_bytes = (uint32_t)(C::kStageA + box_rows<BN>(bi) * 128 * (BK / 64));
+                // this lane's box: lanes [0, 2 * kNumSubA) rows 0-63 / 64-127 of weight
+                // sub-tile l / 2; the rest the activation K halves
+                const bool is_w = lane < 2 * C::kNumSubA;
+                const int sa = lane >> 1, hh = lane - 2 * C::kNumSubA;
+                const CUtensorMap* map = is_w ? &tmap_w : mb;
+                const int row = is_w ? ((lane & 1) ? wrow1 : wrow0) : row0;
+                const int off = is_w ? sa * C::kSubA + (lane & 1) * (C::kSubA / 2) : C::kStageA + hh * BN * 128;
+                const int kx_off = is_w ? sa * (BK == 64 ? 64 : 128) : hh * 64;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % NS, ph = (it / NS) & 1u;
-                    if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(&full[s], stage_bytes);
-#pragma unroll
-                    for (int sa = 0; sa < C::kNumSubA; ++sa) {  // rows 0-63 and 64-127 of each sub-tile
-                        const int kx = kb * BK + sa * (BK == 64 ? 64 : 128);
-                        tma_load_2d(st + sa * C::kSubA, &tmap_w, &full[s], kx, wrow0);
-                        tma_load_2d(st + sa * C::kSubA + C::kSubA / 2, &tmap_w, &full[s], kx, wrow1);
+                    if (lane == 0) {
+                        ok = mbar_wait(&empty[s], ph ^ 1u, ctl);
+                        if (ok) mbar_arrive_expect_tx(&full[s], stage_bytes);
                     }
-#pragma unroll
-                    for (int hh = 0; hh < BK / 64; ++hh)
-                        tma_load_2d(st + C::kStageA + hh * BN * 128, mb, &full[s], kb * BK + hh * 64, row0);
+                    ok = __shfl_sync(kMask, ok, 0);
+                    if (!ok) break;
+                    tma_load_2d(smem + s * C::kStage + off, map, &full[s], kb * BK + kx_off, row);
                 }
             }
             // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
-                mbar_wait_drain(&full[s], (last / NS) & 1u);
-            }
+            if (lane == 0)
+                for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                    const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                    mbar_wait_drain(&full[s], (last / NS) & 1u);
+                }
         }
     } else if (warp == 1) {
         // ------------------------------------------------------ MMA issuer
@@ -505,6 +520,18 @@ bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes
     const cuuint32_t box[2] = {box_inner, box_outer};
     const cuuint32_t estr[2] = {1, 1};
     return enc(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
+               CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool make_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swz) {
+    EncodeFn enc = get_encode_fn();
+    if (!enc) return false;
+    const cuuint64_t d[3] = {dims[0], dims[1], dims[2]};
+    const cuuint64_t st[2] = {strides[0], strides[1]};
+    const cuuint32_t b[3] = {box[0], box[1], box[2]};
+    const cuuint32_t estr[3] = {1, 1, 1};
+    return enc(map, dt, 3, const_cast<void*>(base), d, st, b, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, swz,
                CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 

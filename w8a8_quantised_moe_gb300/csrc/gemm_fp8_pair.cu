@@ -57,7 +57,7 @@ struct P8Cfg {
     static constexpr int kXchRegion = kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf;
     static constexpr int kOffXch = NS * kStage;
     static constexpr int kOffBars = kOffXch + kXchRegion;
-    static constexpr int kNumBars = 3 * NS + 2 * kP8ND + 2;
+    static constexpr int kNumBars = 3 * NS + 2 * kP8ND + 3;  // ..., teardown, epi_bar, stall_bar
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;  // [2][BN] activation scales
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4;
@@ -140,6 +140,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
     uint64_t* acc_empty = acc_full + kP8ND;   // [ND], used in the even CTA
     uint64_t* teardown = acc_empty + kP8ND;
     uint64_t* epi_bar = teardown + 1;
+    uint64_t* stall_bar = epi_bar + 1;  // test hook: nothing arrives on it
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -166,6 +167,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
         }
         mbar_init(teardown, 1);
         mbar_init(epi_bar, 4);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
@@ -216,9 +218,16 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
 
     if (warp == 0) {
         // ------------------------------------------------ stage TMA (both CTAs)
-        if (lane == 0) {
+        // A stage is three boxes (weight rows 0-63 and 64-127, activation
+        // rows); lanes 0-2 issue one each in the same warp instruction, since
+        // a bulk tensor copy costs its issuing thread ~200 cycles.  Lane 0
+        // owns the waits and the arrival.
+        if (lane < 3) {
             uint32_t it = 0;
-            bool ok = true;
+            // the test hook stalls the even CTA only (the odd one is aborted through its peer flag)
+            int ok = 1;
+            if (lane == 0) ok = !(args.stall && rank == 0) || mbar_wait(stall_bar, 0, ctl);
+            ok = __shfl_sync(0x7u, ok, 0);
             for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
                 int g, cp, row0, nvalid;
                 p8_decode_tile<BN>(tiles, tile, g, cp, row0, nvalid);
@@ -236,22 +245,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kP8Threads, 1)
                 const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
                 const int brow = row0 + (int)rank * half;
                 const uint32_t bytes = (uint32_t)(C::kStageA + p8_box_rows<C::kHalf>(bi) * kP8BK);
+                // this lane's box: its tensor map, row and offset in the stage
+                const CUtensorMap* map = lane == 2 ? mb : &tmap_w;
+                const int row = lane == 0 ? wrow0 : lane == 1 ? wrow1 : brow;
+                const int off = lane == 0 ? 0 : lane == 1 ? C::kStageA / 2 : C::kStageA;
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
                     const uint32_t s = it % NS, ph = (it / NS) & 1u;
                     // stage s is free once the MMAs of stage it - NS completed
-                    if (!mbar_wait_cluster(&empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + s * C::kStage;
-                    mbar_arrive_expect_tx(&full[s], bytes);
-                    tma_load_2d(st, &tmap_w, &full[s], kb * kP8BK, wrow0);
-                    tma_load_2d(st + C::kStageA / 2, &tmap_w, &full[s], kb * kP8BK, wrow1);
-                    tma_load_2d(st + C::kStageA, mb, &full[s], kb * kP8BK, brow);
+                    if (lane == 0) {
+                        ok = mbar_wait_cluster(&empty[s], ph ^ 1u, ctl);
+                        if (ok) mbar_arrive_expect_tx(&full[s], bytes);
+                    }
+                    ok = __shfl_sync(0x7u, ok, 0);
+                    if (!ok) break;
+                    tma_load_2d(smem + s * C::kStage + off, map, &full[s], kb * kP8BK, row);
                 }
             }
             // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
-                mbar_wait_drain(&full[s], (last / NS) & 1u);
-            }
+            if (lane == 0)
+                for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                    const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                    mbar_wait_drain(&full[s], (last / NS) & 1u);
+                }
         }
     } else if (warp == 1 && rank != 0) {
         // ------------------------------------------- relay (odd CTA)

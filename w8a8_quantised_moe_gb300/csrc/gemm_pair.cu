@@ -18,21 +18,24 @@
 // matters because the issuing thread shares its SM sub-partition with a
 // converter and an epilogue warp.
 //
-// Roles per CTA (352 threads): warp 0 loads the int8 weight rows (ring of NQ
-// stages, deep: weights stream from HBM once), warp 10 loads this CTA's half of
-// the activation rows (ring of NB stages: they are re-read from L2 by every
-// channel-block pair), warp 1 allocates TMEM and in the even CTA issues the
-// MMAs, warps 2-5 convert, warps 6-9 run the epilogue.
+// Roles per CTA (384 threads; 512 with a second converter group): warp 0
+// loads the int8 weight rows (ring of NQ stages, deep: weights stream from HBM
+// once), warp 10 loads this CTA's half of the activation rows (ring of NB
+// stages: they are re-read from L2 by every channel-block pair), one bulk
+// copy a stage each; warp 1 allocates TMEM and in the even CTA issues the
+// MMAs with warp 11 (alternate stages); warps 2-5 convert (warps 12-15 too,
+// each group half of every stage's K columns, for the scale epilogues);
+// warps 6-9 run the epilogue.
 // Synchronisation (every wait bounded; see ptx.cuh):
-//   q_full/q_empty[NQ]  int8 stage landed / read by the 4 converter warps
+//   q_full/q_empty[NQ]  int8 stage landed / read by the converter warps
 //   b_full[NB]          this CTA's activation half landed
 //   done[NB]            committed by the even CTA's MMAs of a stage to both
 //                       CTAs: its activation slot, and the A slot (it % NA) it
 //                       read, are free again
-//   a_ready[j]          even CTA, 8 arrivals (4 converter warps x 2 CTAs):
+//   a_ready[j]          even CTA, 8 arrivals per converter group (4 warps x 2 CTAs):
 //                       tensor-memory A slot j holds the stage's weights in both
-//                       CTAs.  A converter waited on its own b_full first, so
-//                       this also covers both halves of B.
+//                       CTAs.  Group 0's converters waited on their CTA's
+//                       b_full first, so this also covers both halves of B.
 //   acc_full[d]         per CTA, committed to both: accumulator d complete
 //   acc_empty[d]        even CTA, 8 arrivals (4 epilogue warps x 2 CTAs)
 // Shared memory of the odd CTA is read by the even CTA's MMAs, and both CTAs
@@ -52,6 +55,7 @@ namespace moe {
 namespace {
 
 constexpr int kPairBK = 128;  // K per stage
+
 #ifndef MOE_P_ND
 #define MOE_P_ND 2
 #endif
@@ -70,13 +74,26 @@ constexpr int kPairND = MOE_P_ND;  // accumulator buffers
 #endif
 constexpr int kIssuers = MOE_P_ISSUERS;
 static_assert(kIssuers == 1 || kIssuers == 2, "one or two MMA issuers");
-// + warp 10, the activation producer, and warp 11, the second MMA issuer
-constexpr int kPairThreads = kThreads + 32 * kIssuers;
+// Converter groups: each of the G groups of four warps (one per TMEM lane
+// quadrant) converts 128 / G of the K columns of every stage, so that a
+// stage's conversion takes less time.  Measured per-stage timestamps put a
+// stage near 1100 cycles of which the conversion is ~250-400; the gain
+// depends on the tile mix: with two groups the down GEMM of the prefill layer
+// drops from 191 to 185 us and the 256-expert layer's gate/up GEMM from 2.00
+// to 1.96 ms, while the prefill gate/up GEMM rises from 345 to 354 us.  So
+// the gate/up GEMM runs one group, the scale epilogues two.
+// + warp 10, the activation producer, warp 11, the second MMA issuer, and
+// warps 12-15, the second converter group (if any)
 constexpr int kPairBWarp = 10;
 constexpr int kPairMma2Warp = 11;
+constexpr int kPairConv1Warp0 = 12;
+__host__ __device__ constexpr int pair_threads(int conv_groups) { return kThreads + 32 * kIssuers + 128 * (conv_groups - 1); }
 
-template <int BN_, int NQ_, int NB_, int NA_>
+template <int BN_, int NQ_, int NB_, int NA_, bool kStore_, int CONV_>
 struct PairCfg {
+    static constexpr int kConv = CONV_;                 // converter groups
+    static constexpr int kThreadsPerCta = pair_threads(CONV_);
+    static_assert(CONV_ == 1 || (CONV_ == 2 && kIssuers == 2 && kThreadsPerCta == 512), "warp layout");
     static constexpr int BN = BN_;        // activation rows per pair tile (MMA N, at most)
     static constexpr int NQ = NQ_;        // int8 weight stages (deep: weights stream from HBM)
     static constexpr int NB = NB_;        // activation stages
@@ -94,11 +111,13 @@ struct PairCfg {
     static constexpr int kOffQ = 0;
     static constexpr int kOffB = kOffQ + NQ * kQStage;
     static constexpr int kOffXch = kOffB + NB * kBStage;
-    static constexpr int kXchRegion = kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf;
+    // GateUp exchanges g and u; the scale epilogues stage two TMA-store blocks
+    static constexpr bool kStore = kStore_;
+    static constexpr int kXchRegion = kStore ? (kXch > 2 * kStoreBuf ? kXch : 2 * kStoreBuf) : kXch;
     static constexpr int kOffBars = kOffXch + kXchRegion;
     // q_full, q_empty, b_full, done, a_ready, acc_full, acc_empty, tile_go,
-    // one teardown barrier per issuer, epi_bar
-    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 3 * kPairND + kIssuers + 1;
+    // one teardown barrier per issuer, epi_bar, stall_bar
+    static constexpr int kNumBars = 2 * NQ + 2 * NB + NA + 3 * kPairND + kIssuers + 2;
     static constexpr int kOffTiles = kOffBars + kNumBars * 8;
     static constexpr int kOffRowInfo = kOffTiles + (kMaxExperts + 1) * 4 * 2;
     static constexpr int kOffMisc = kOffRowInfo + 2 * BN * 4 * 2;
@@ -113,20 +132,30 @@ struct PairCfg {
     static_assert(kSmem <= 232448, "shared memory budget");
 };
 
-// Tensor memory holds the A slots and two accumulators.  Measured on the
-// prefill and linear workloads: 192-wide tiles with two A slots beat 160-wide
-// tiles with three (wider MMAs amortise the issuing thread's per-stage cost).
-// Weights and activations have separate rings (weights stream from HBM once,
-// activations are re-read from L2 by every channel-block pair).  Measured:
-// four activation stages matter (two or three are clearly slower), a deeper
-// weight ring gains nothing.
-#ifndef MOE_P_BN  // pair tile width, int8 weight stages, activation stages, A slots
+// Tensor memory holds the A slots and two accumulators (192-wide tiles with
+// two A slots).  Weights and activations have separate rings (weights stream
+// from HBM once, activations are re-read from L2 by every channel-block
+// pair).  Measured: four activation stages matter (two or three are clearly
+// slower).  The weight ring is as deep as shared memory allows: a weight
+// stage lands ~3500 cycles after its TMA is issued, about three stages.
+#ifndef MOE_P_BN  // pair tile width, A slots
 #define MOE_P_BN 192
-#define MOE_P_NQ 4
-#define MOE_P_NB 4
 #define MOE_P_NA 2
 #endif
-using CfgPair = PairCfg<MOE_P_BN, MOE_P_NQ, MOE_P_NB, MOE_P_NA>;
+#ifndef MOE_P_NB_GU  // activation stages: GateUp, scale epilogues
+#define MOE_P_NB_GU 4
+#define MOE_P_NB_SC 4
+#endif
+#ifndef MOE_P_NQ_GU  // int8 weight stages: GateUp (no store staging), scale epilogues
+#define MOE_P_NQ_GU 6
+#define MOE_P_NQ_SC 5
+#endif
+#ifndef MOE_P_CONV_GU  // converter groups: GateUp, scale epilogues
+#define MOE_P_CONV_GU 1
+#define MOE_P_CONV_SC 2
+#endif
+using CfgPairGU = PairCfg<MOE_P_BN, MOE_P_NQ_GU, MOE_P_NB_GU, MOE_P_NA, false, MOE_P_CONV_GU>;
+using CfgPairSc = PairCfg<MOE_P_BN, MOE_P_NQ_SC, MOE_P_NB_SC, MOE_P_NA, true, MOE_P_CONV_SC>;
 
 // Box heights of the per-CTA activation tensor maps: a CTA of a tile with
 // half-width h loads the smallest box that covers h rows.
@@ -153,7 +182,7 @@ __device__ __forceinline__ void decode_pair_tile(const Tiles& t, int tile, int& 
 }
 
 template <class C, int EPI>
-__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
+__global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreadsPerCta, 1)
     grouped_gemm_pair_kernel(const __grid_constant__ CUtensorMap tmap_w, const __grid_constant__ CUtensorMap tmap_b0,
                              const __grid_constant__ CUtensorMap tmap_b1, const __grid_constant__ CUtensorMap tmap_b2,
                              const __grid_constant__ CUtensorMap tmap_b3, const __grid_constant__ CUtensorMap tmap_out,
@@ -171,7 +200,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     uint64_t* acc_empty = acc_full + kPairND;  // [ND], used in the even CTA
     uint64_t* tile_go = acc_empty + kPairND;  // [ND], even CTA: the tile's overwriting MMAs are issued
     uint64_t* teardown = tile_go + kPairND;   // [kIssuers], one per issuer
-    uint64_t* epi_bar = teardown + kIssuers;  // the last barrier of the block (kNumBars)
+    uint64_t* epi_bar = teardown + kIssuers;
+    uint64_t* stall_bar = epi_bar + 1;  // the last barrier of the block; test hook: nothing arrives on it
     int* tile_start = reinterpret_cast<int*>(smem + C::kOffTiles);
     int* row_start = tile_start + (kMaxExperts + 1);
     uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(smem + C::kOffMisc);
@@ -190,13 +220,13 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     if (threadIdx.x == 0) {
         for (int s = 0; s < NQ; ++s) {
             mbar_init(&q_full[s], 1);
-            mbar_init(&q_empty[s], 4);
+            mbar_init(&q_empty[s], 4 * C::kConv);
         }
         for (int s = 0; s < NB; ++s) {
             mbar_init(&b_full[s], 1);
             mbar_init(&done[s], 1);
         }
-        for (int j = 0; j < C::NA; ++j) mbar_init(&a_ready[j], 8);
+        for (int j = 0; j < C::NA; ++j) mbar_init(&a_ready[j], 8 * C::kConv);
         for (int d = 0; d < kPairND; ++d) {
             mbar_init(&acc_full[d], kIssuers);
             mbar_init(&tile_go[d], 1);
@@ -204,6 +234,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
         }
         for (int r = 0; r < kIssuers; ++r) mbar_init(&teardown[r], 1);
         mbar_init(epi_bar, 4);
+        mbar_init(stall_bar, 1);
         *abort_flag = 0;
         fence_barrier_init();
         tma_prefetch_desc(&tmap_w);
@@ -252,64 +283,50 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     const WaitCtl ctl{abort_flag, args.error, args.timeout_ns,
                       cluster_addr(const_cast<const int*>(abort_flag), rank ^ 1u)};
 
-    if (warp == 0) {
-        // ------------------------------------------------- int8 weight TMA
+    if (warp == 0 || warp == kPairBWarp) {
+        // ---------------------------------------- TMA producers (both CTAs)
+        // warp 0 loads the int8 weight stages, warp 10 this CTA's half of the
+        // activation rows, one bulk copy a stage each: a 3-D box holds the 64
+        // gate and 64 up weight rows (GateUp) or a 2-D box the 128 consecutive
+        // rows; the activation box holds both 64-wide K halves as two
+        // [rows][128 B] sub-tiles rows * 128 bytes apart.
+        const bool wprod = warp == 0;
+        const uint32_t NR = wprod ? (uint32_t)NQ : (uint32_t)NB;  // ring depth
         if (lane == 0) {
             uint32_t it = 0;
-            bool ok = true;
+            // the test hook stalls the even CTA's weight producer only: the odd CTA
+            // learns of the abort through its peer abort flag
+            bool ok = !(wprod && args.stall && rank == 0) || mbar_wait(stall_bar, 0, ctl);
             for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
                 int g, cp, row0, nvalid;
                 decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
                 const int cb = 2 * cp + (int)rank;
-                int wrow0, wrow1;
-                if (EPI == (int)Epi::GateUp) {
-                    wrow0 = g * args.w_rows_per_group + cb * 64;
-                    wrow1 = wrow0 + args.up_offset;
-                } else {
-                    wrow0 = g * args.w_rows_per_group + cb * kTileM;
-                    wrow1 = wrow0 + 64;
-                }
-                for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % NQ, ph = (it / NQ) & 1u;
-                    if (!mbar_wait(&q_empty[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + C::kOffQ + s * C::kQStage;
-                    mbar_arrive_expect_tx(&q_full[s], (uint32_t)C::kQStage);
-                    tma_load_2d(st, &tmap_w, &q_full[s], kb * kPairBK, wrow0);
-                    tma_load_2d(st + C::kQStage / 2, &tmap_w, &q_full[s], kb * kPairBK, wrow1);
-                }
-            }
-            // drain: every fill issued must land before the CTA may exit
-            for (uint32_t s = 0; s < (uint32_t)NQ && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NQ);
-                mbar_wait_drain(&q_full[s], (last / NQ) & 1u);
-            }
-        }
-    } else if (warp == kPairBWarp) {
-        // ---------------------------------------------- activation-half TMA
-        if (lane == 0) {
-            uint32_t it = 0;
-            bool ok = true;
-            for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
-                int g, cp, row0, nvalid;
-                decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
+                const int wrow = g * args.w_rows_per_group + cb * (EPI == (int)Epi::GateUp ? 64 : kTileM);
                 const int half = ((nvalid + 15) & ~15) >> 1;  // activation rows per CTA
                 const int bi = pair_box_index(half);
                 const CUtensorMap* mb = bi == 0 ? &tmap_b0 : bi == 1 ? &tmap_b1 : bi == 2 ? &tmap_b2 : &tmap_b3;
-                const int brow = row0 + (int)rank * half;
-                const uint32_t bytes = (uint32_t)(2 * pair_box_rows<C::kHalf>(bi) * 128);
+                const uint32_t bbytes = (uint32_t)(2 * pair_box_rows<C::kHalf>(bi) * 128);
                 for (int kb = 0; kb < nkb; ++kb, ++it) {
-                    const uint32_t s = it % NB, ph = (it / NB) & 1u;
-                    // slot s is free once the MMAs of stage it - NB completed
-                    if (!mbar_wait_cluster(&done[s], ph ^ 1u, ctl)) { ok = false; break; }
-                    uint8_t* st = smem + C::kOffB + s * C::kBStage;
-                    mbar_arrive_expect_tx(&b_full[s], bytes);
-                    tma_load_2d(st, mb, &b_full[s], kb * kPairBK, brow);
-                    tma_load_2d(st + C::kSubB, mb, &b_full[s], kb * kPairBK + 64, brow);
+                    const uint32_t s = it % NR, ph = (it / NR) & 1u;
+                    if (wprod) {
+                        if (!mbar_wait(&q_empty[s], ph ^ 1u, ctl)) { ok = false; break; }
+                        uint8_t* st = smem + C::kOffQ + s * C::kQStage;
+                        mbar_arrive_expect_tx(&q_full[s], (uint32_t)C::kQStage);
+                        if (EPI == (int)Epi::GateUp) tma_load_3d(st, &tmap_w, &q_full[s], kb * kPairBK, wrow, 0);
+                        else tma_load_2d(st, &tmap_w, &q_full[s], kb * kPairBK, wrow);
+                    } else {
+                        // slot s is free once the MMAs of stage it - NB completed
+                        if (!mbar_wait_cluster(&done[s], ph ^ 1u, ctl)) { ok = false; break; }
+                        uint8_t* st = smem + C::kOffB + s * C::kBStage;
+                        mbar_arrive_expect_tx(&b_full[s], bbytes);
+                        tma_load_3d(st, mb, &b_full[s], 0, row0 + (int)rank * half, 2 * kb);
+                    }
                 }
             }
-            for (uint32_t s = 0; s < (uint32_t)NB && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NB);
-                mbar_wait_drain(&b_full[s], (last / NB) & 1u);
+            // drain: every fill issued must land before the CTA may exit
+            for (uint32_t s = 0; s < NR && s < it; ++s) {
+                const uint32_t last = it - 1 - ((it - 1 - s) % NR);
+                mbar_wait_drain(wprod ? &q_full[s] : &b_full[s], (last / NR) & 1u);
             }
         }
     } else if (warp == 1 || (kIssuers == 2 && warp == kPairMma2Warp)) {
@@ -331,6 +348,9 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 decode_pair_tile<BN>(tiles, tile, g, cp, row0, nvalid);
                 const uint32_t n_mma = (uint32_t)((nvalid + 15) & ~15);
                 const uint32_t idesc = idesc_f16_f32(2 * kTileM, n_mma);
+                // the second K half of B starts box-rows * 128 bytes into the stage
+                const uint64_t b_sub16 =
+                    (uint64_t)((pair_box_rows<C::kHalf>(pair_box_index((int)n_mma >> 1)) * 128) >> 4);
                 const uint32_t d = tl % kPairND;
                 if (role == 0) {
                     if (!mbar_wait_cluster(&acc_empty[d], ((tl / kPairND) & 1u) ^ 1u, ctl)) break;
@@ -346,8 +366,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                     if (!mbar_wait_cluster(&a_ready[j], (itk / C::NA) & 1u, ctl)) { ok = false; break; }
                     tc_fence_after();
                     const uint32_t b_base = smem_u32(smem + C::kOffB + s * C::kBStage);
-                    mma8_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols, smem_desc_sw128(b_base),
-                                         (uint64_t)(C::kSubB >> 4), idesc, kb != 0 ? 1u : 0u);
+                    mma8_f16_tmem_a_pair(tmem + d_col, tmem + j * C::kACols, smem_desc_sw128(b_base), b_sub16, idesc,
+                                         kb != 0 ? 1u : 0u);
                     if (kIssuers > 1 && kb == 0) {  // the overwriting MMAs are issued
                         tc_fence_before();
                         mbar_arrive(&tile_go[d]);
@@ -361,9 +381,14 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
             mma_commit_pair(&teardown[role], 1);
             mbar_wait_drain(&teardown[role], 0);
         }
-    } else if (warp >= 2 && warp < kEpiWarp0) {
+    } else if ((warp >= 2 && warp < kEpiWarp0) ||
+               (C::kConv == 2 && warp >= kPairConv1Warp0 && warp < kPairConv1Warp0 + 4)) {
         // ------------------------------------------------------- converters
+        // Group cg (warps 2-5: 0; warps 12-15: 1) converts K columns
+        // [cg * 128 / G, (cg + 1) * 128 / G) of every stage; warp w serves TMEM
+        // lane quadrant w % 4.
         const int q = warp & 3;
+        const int cg = (C::kConv == 2 && warp >= kPairConv1Warp0) ? 1 : 0;
         const int row = q * 32 + lane;
         const uint32_t a_ready_leader = cluster_addr(&a_ready[0], 0);
         uint32_t it = 0;
@@ -380,7 +405,8 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + j * C::kACols;
                 const uint32_t swz = (uint32_t)(row & 7);  // 128-byte swizzle: chunk c at c ^ (row & 7)
 #pragma unroll
-                for (int hh = 0; hh < 2; ++hh) {  // 64 K per tcgen05.st
+                for (int h2 = 0; h2 < 2 / C::kConv; ++h2) {  // 64 K per tcgen05.st
+                    const int hh = h2 + cg;
                     uint32_t v[32];
 #pragma unroll
                     for (int c = 0; c < 4; ++c)
@@ -390,9 +416,10 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
                 __syncwarp();
                 if (lane == 0) mbar_arrive(&q_empty[qs]);  // the int8 stage has been read
                 // the even CTA's MMAs read this CTA's half of B once the
-                // arrival below is observed: it follows this wait (placed after
-                // the conversion, so that activation latency overlaps it)
-                if (!warp_wait(&b_full[bs], (it / NB) & 1u, ctl)) { ok = false; break; }
+                // arrival below is observed: group 0's arrival follows this
+                // wait (placed after the conversion, so that activation latency
+                // overlaps it), and a_ready completes only with group 0
+                if (cg == 0 && !warp_wait(&b_full[bs], (it / NB) & 1u, ctl)) { ok = false; break; }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
@@ -523,7 +550,7 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(kPairThreads, 1)
     if (!*abort_flag) fallback_rows<EPI>(args, row_start, n_groups);
 }
 
-int max_pair_clusters(const void* kern, int smem) {
+int max_pair_clusters(const void* kern, int smem, int threads) {
     cudaLaunchConfig_t cfg = {};
     cudaLaunchAttribute attr[1];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -531,7 +558,7 @@ int max_pair_clusters(const void* kern, int smem) {
     attr[0].val.clusterDim.y = 1;
     attr[0].val.clusterDim.z = 1;
     cfg.gridDim = dim3(2 * (unsigned)num_sms(), 1, 1);
-    cfg.blockDim = dim3(kPairThreads, 1, 1);
+    cfg.blockDim = dim3((unsigned)threads, 1, 1);
     cfg.dynamicSmemBytes = (size_t)smem;
     cfg.attrs = attr;
     cfg.numAttrs = 1;
@@ -551,20 +578,33 @@ cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st, bool pdl) {
     static int clusters = 0;
     std::call_once(once, [&] {
         attr_err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, C::kSmem);
-        if (attr_err == cudaSuccess) clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), C::kSmem);
+        if (attr_err == cudaSuccess) clusters = max_pair_clusters(reinterpret_cast<const void*>(kern), C::kSmem, C::kThreadsPerCta);
     });
     if (attr_err != cudaSuccess) return attr_err;
 
     CUtensorMap tw, tb[4];
     const uint64_t w_rows = (uint64_t)args.n_groups * args.w_rows_per_group;
-    if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, 128, 64,
-                            CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    for (int i = 0; i < 4; ++i)
-        if (!make_tensor_map_2d(&tb[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, 2, args.act16, args.K,
-                                (uint64_t)args.total_rows, 64, pair_box_rows<C::kHalf>(i),
+    if (EPI == (int)Epi::GateUp) {
+        // (k, row, half): half 1 is the up row up_offset rows below the gate row
+        const uint64_t dims[3] = {(uint64_t)args.K, w_rows - (uint64_t)args.up_offset, 2};
+        const uint64_t strides[2] = {(uint64_t)args.K, (uint64_t)args.up_offset * (uint64_t)args.K};
+        const uint32_t box[3] = {128, 64, 2};
+        if (!make_tensor_map_3d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, args.w, dims, strides, box,
                                 CU_TENSOR_MAP_SWIZZLE_128B))
             return cudaErrorInvalidValue;
+    } else if (!make_tensor_map_2d(&tw, CU_TENSOR_MAP_DATA_TYPE_UINT8, 1, args.w, args.K, w_rows, 128, kTileM,
+                                   CU_TENSOR_MAP_SWIZZLE_128B)) {
+        return cudaErrorInvalidValue;
+    }
+    for (int i = 0; i < 4; ++i) {
+        // (element within a 64-wide K chunk, row, K chunk)
+        const uint64_t dims[3] = {64, (uint64_t)args.total_rows, (uint64_t)args.K / 64};
+        const uint64_t strides[2] = {(uint64_t)args.K * 2, 128};
+        const uint32_t box[3] = {64, (uint32_t)pair_box_rows<C::kHalf>(i), 2};
+        if (!make_tensor_map_3d(&tb[i], CU_TENSOR_MAP_DATA_TYPE_FLOAT16, args.act16, dims, strides, box,
+                                CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+    }
 
     CUtensorMap tout = tw;  // unused by GateUp
     if (EPI == (int)Epi::ScaleF32 &&
@@ -580,7 +620,7 @@ cudaError_t launch_pair_impl(const GemmArgs& args, cudaStream_t st, bool pdl) {
     long n = clusters;
     if (max_tiles < n) n = max_tiles;
     if (n < 1) n = 1;
-    return launch_kernel(kern, dim3((unsigned)(2 * n)), dim3(kPairThreads), C::kSmem, st, pdl, tw, tb[0], tb[1],
+    return launch_kernel(kern, dim3((unsigned)(2 * n)), dim3(C::kThreadsPerCta), C::kSmem, st, pdl, tw, tb[0], tb[1],
                          tb[2], tb[3], tout, args);
 }
 
@@ -591,9 +631,9 @@ bool pair_gemm_supported(const GemmArgs& args) { return args.n_cb >= 2 && (args.
 cudaError_t launch_grouped_gemm_pair(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl) {
     if (args.total_rows == 0) return cudaSuccess;
     switch (epi) {
-        case Epi::GateUp: return launch_pair_impl<CfgPair, 0>(args, st, pdl);
-        case Epi::ScaleF32: return launch_pair_impl<CfgPair, 1>(args, st, pdl);
-        case Epi::ScaleBF16: return launch_pair_impl<CfgPair, 2>(args, st, pdl);
+        case Epi::GateUp: return launch_pair_impl<CfgPairGU, 0>(args, st, pdl);
+        case Epi::ScaleF32: return launch_pair_impl<CfgPairSc, 1>(args, st, pdl);
+        case Epi::ScaleBF16: return launch_pair_impl<CfgPairSc, 2>(args, st, pdl);
     }
     return cudaErrorInvalidValue;
 }

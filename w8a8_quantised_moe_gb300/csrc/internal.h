@@ -19,6 +19,8 @@ constexpr int kRouterSmallT = 128;      // up to this many tokens the router run
 constexpr int kMaxExperts = 256;
 constexpr int kMaxTopK = 8;
 constexpr uint64_t kDefaultTimeoutNs = 2000000000ull;
+// The process-wide limit of every in-kernel wait (moe_w8a8_set_wait_timeout_ns).
+uint64_t current_timeout_ns();
 
 // Bits of the sticky device error word (first int of a workspace).
 constexpr int kErrTimeout = 1;  // a pipeline wait ran out of time
@@ -66,6 +68,8 @@ struct GemmArgs {
     const int32_t* fb_count; // number of entries of fb_list
     int* error;              // sticky device error word
     uint64_t timeout_ns;
+    int stall;               // test hook (MOE_INJECT=stall): the producer first waits on a barrier that
+                             // nothing completes, so that the wait limit runs out
 };
 
 // Launch plan of the router GEMM: experts padded to E_pad (a multiple of 16,
@@ -180,6 +184,22 @@ bool pdl_default();
 // Kernels launched through launch_kernel since the library was loaded.
 void count_launch();
 
+// Host-side fault injection for tests of the error paths.  The environment
+// variable MOE_INJECT (read at every call; a comma-separated list) names the
+// faults to fake; none of them reaches the GPU:
+//   ws_short     an entry point's workspace size check fails as if the
+//                workspace were one byte short (MOE_ERR_WORKSPACE_TOO_SMALL)
+//   bad_ptr      its pointer check fails as if a data pointer were null
+//                (MOE_ERR_INVALID_ARG)
+//   launch_fail  every kernel launch fails with cudaErrorLaunchFailure before
+//                anything is queued (the entry point returns MOE_ERR_CUDA)
+//   stall        every grouped GEMM launch starts with its producer waiting,
+//                within the wait limit, on a barrier that nothing completes:
+//                the limit runs out and the kernel takes its abort path (the
+//                one fault that reaches the GPU; a test of the timeout path)
+enum InjectFault : int { kInjectWsShort = 1, kInjectBadPtr = 2, kInjectLaunchFail = 4, kInjectStall = 8 };
+bool injected(InjectFault f);
+
 template <typename... KArgs, typename... Args>
 cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st, bool pdl,
                           Args... args) {
@@ -193,6 +213,7 @@ cudaError_t launch_kernel(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t 
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = pdl ? 1 : 0;
+    if (injected(kInjectLaunchFail)) return cudaErrorLaunchFailure;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kern, static_cast<KArgs>(args)...);
     if (e == cudaSuccess) count_launch();
     return e;
@@ -269,5 +290,11 @@ int num_sms();
 bool make_tensor_map_2d(CUtensorMap* map, CUtensorMapDataType dt, int elem_bytes, const void* base,
                         uint64_t inner, uint64_t outer, uint32_t box_inner, uint32_t box_outer,
                         CUtensorMapSwizzle swz);
+// 3-D tiled tensor map: dims[0] contiguous, dims[1] and dims[2] with the
+// given byte strides (any order of strides).  One box of box[0] x box[1] x
+// box[2] lands in shared memory as box[2] consecutive [box[1]][box[0]]
+// tiles: one bulk copy where two 2-D boxes were needed.
+bool make_tensor_map_3d(CUtensorMap* map, CUtensorMapDataType dt, const void* base, const uint64_t (&dims)[3],
+                        const uint64_t (&strides)[2], const uint32_t (&box)[3], CUtensorMapSwizzle swz);
 
 }  // namespace moe

@@ -130,22 +130,29 @@ __global__ void __launch_bounds__(kRThreads, 1)
     const WaitCtl ctl{abort_flag, error, timeout_ns, 0u};
 
     if (warp == 0) {
-        if (lane == 0) {
+        // four boxes a stage (the x tile, the three weight parts); lanes 0-3
+        // issue one each in the same warp instruction (a bulk tensor copy
+        // costs its issuing thread ~200 cycles); lane 0 owns the waits
+        if (lane < 4) {
             uint32_t it = 0;
+            const CUtensorMap* map = lane == 0 ? &tmap_x : &tmap_w;
+            const int row = lane == 0 ? t0 : (lane - 1) * E_pad + e0;
+            const int off = lane == 0 ? 0 : C::kStageA + (lane - 1) * C::kStageB;
             for (int kb = kb0; kb < kb1; ++kb, ++it) {
                 const uint32_t s = it % NS, ph = (it / NS) & 1u;
-                if (!mbar_wait(&empty[s], ph ^ 1u, ctl)) break;
-                uint8_t* st = smem + s * C::kStage;
-                mbar_arrive_expect_tx(&full[s], C::kStage);
-                tma_load_2d(st, &tmap_x, &full[s], kb * kRBK, t0);
-#pragma unroll
-                for (int sp = 0; sp < 3; ++sp)
-                    tma_load_2d(st + C::kStageA + sp * C::kStageB, &tmap_w, &full[s], kb * kRBK, sp * E_pad + e0);
+                int ok = 1;
+                if (lane == 0) {
+                    ok = mbar_wait(&empty[s], ph ^ 1u, ctl);
+                    if (ok) mbar_arrive_expect_tx(&full[s], C::kStage);
+                }
+                if (!__shfl_sync(0xfu, ok, 0)) break;
+                tma_load_2d(smem + s * C::kStage + off, map, &full[s], kb * kRBK, row);
             }
-            for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
-                const uint32_t last = it - 1 - ((it - 1 - s) % NS);
-                mbar_wait_drain(&full[s], (last / NS) & 1u);
-            }
+            if (lane == 0)
+                for (uint32_t s = 0; s < (uint32_t)NS && s < it; ++s) {
+                    const uint32_t last = it - 1 - ((it - 1 - s) % NS);
+                    mbar_wait_drain(&full[s], (last / NS) & 1u);
+                }
         }
     } else if (warp == 1) {
         if (lane == 0) {
@@ -208,9 +215,24 @@ __global__ void __launch_bounds__(kRThreads, 1)
 // lane l holds the logits of experts l + 32 i (experts >= E are never taken).
 // Ties go to the lower expert index; choice j of token r ends in lane j as
 // my_e[r] and its softmax weight over the selected logits, my_w[r].
+// A NaN logit (non-finite input, outside the layer's contract) ranks as
+// -inf, so that every choice is still a valid expert index; the return value
+// (the same in every lane) says whether the warp saw one, and the caller
+// records it in the device error word.
 template <int EPT, int NT>
-__device__ __forceinline__ void warp_topk(const float (&v)[NT][EPT], int E, int k, int lane, int (&my_e)[NT],
+__device__ __forceinline__ bool warp_topk(const float (&v_in)[NT][EPT], int E, int k, int lane, int (&my_e)[NT],
                                           float (&my_w)[NT]) {
+    float v[NT][EPT];
+    bool nan_seen = false;
+#pragma unroll
+    for (int r = 0; r < NT; ++r)
+#pragma unroll
+        for (int i = 0; i < EPT; ++i) {
+            const float x = v_in[r][i];
+            const bool nan = x != x;
+            nan_seen |= nan && (lane + 32 * i) < E;
+            v[r][i] = nan ? -INFINITY : x;
+        }
     bool taken[NT][EPT];
     float sel0[NT], den[NT], my_v[NT];
 #pragma unroll
@@ -265,6 +287,7 @@ __device__ __forceinline__ void warp_topk(const float (&v)[NT][EPT], int E, int 
     }
 #pragma unroll
     for (int r = 0; r < NT; ++r) my_w[r] = __fdiv_rn(my_v[r], den[r]);
+    return __any_sync(0xffffffffu, nan_seen);
 }
 
 // One 32-token chunk, by a whole CTA of 256 threads; `mask` is shared memory
@@ -274,7 +297,8 @@ template <int EPT>
 __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, int T, int E, int E_pad,
                                            const float* __restrict__ bias, int k, int chunk,
                                            int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                           int32_t* __restrict__ rank, int32_t* __restrict__ hist, uint32_t* mask) {
+                                           int32_t* __restrict__ rank, int32_t* __restrict__ hist, uint32_t* mask,
+                                           int* __restrict__ error) {
     constexpr int EP = 32 * EPT;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int t0 = chunk * kRouterTokens;
@@ -318,7 +342,7 @@ __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, 
         }
     int my_e[4];
     float my_w[4];
-    warp_topk<EPT, 4>(vv, E, k, lane, my_e, my_w);
+    if (warp_topk<EPT, 4>(vv, E, k, lane, my_e, my_w) && lane == 0) atomicOr(error, kErrDevice);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
         const int t = t0 + warp * 4 + r;
@@ -344,11 +368,12 @@ template <int EPT>
 __global__ void __launch_bounds__(256) topk_kernel(const float* __restrict__ P, int KS, int T, int E, int E_pad,
                                                    const float* __restrict__ bias, int k,
                                                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
-                                                   int32_t* __restrict__ rank, int32_t* __restrict__ hist) {
+                                                   int32_t* __restrict__ rank, int32_t* __restrict__ hist,
+                                                   int* __restrict__ error) {
     __shared__ uint32_t mask[32 * EPT];
     pdl_wait();
     pdl_trigger();
-    topk_chunk<EPT>(P, KS, T, E, E_pad, bias, k, blockIdx.x, topk_ids, topk_w, rank, hist, mask);
+    topk_chunk<EPT>(P, KS, T, E, E_pad, bias, k, blockIdx.x, topk_ids, topk_w, rank, hist, mask, error);
 }
 
 // Few tokens (T <= kRouterSmallT): the router GEMM is far too small for the
@@ -486,7 +511,8 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float* __restr
                                                             int32_t* __restrict__ hist,
                                                             int32_t* __restrict__ offsets,
                                                             int32_t* __restrict__ counts,
-                                                            unsigned int* __restrict__ ticket) {
+                                                            unsigned int* __restrict__ ticket,
+                                                            int* __restrict__ error) {
     constexpr int EP = 32 * EPT;
     __shared__ float part[8][EP];
     __shared__ uint32_t mask[kRFMaxChunks * kMaxExperts];
@@ -533,7 +559,7 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float* __restr
         }
         int my_e[1];
         float my_w[1];
-        warp_topk<EPT, 1>(v, E, k, lane, my_e, my_w);
+        if (warp_topk<EPT, 1>(v, E, k, lane, my_e, my_w) && lane == 0) atomicOr(error, kErrDevice);
         if (lane < k) {
             topk_ids[(size_t)t * k + lane] = my_e[0];
             topk_w[(size_t)t * k + lane] = my_w[0];
@@ -625,20 +651,20 @@ cudaError_t launch_router_gemm(const uint16_t* x, const uint16_t* wsplit, int T,
 }
 
 cudaError_t launch_topk(const float* P, const RouterPlan& p, int T, int E, const float* bias, int k,
-                        int32_t* topk_ids, float* topk_w, int32_t* rank, int32_t* hist, cudaStream_t st,
+                        int32_t* topk_ids, float* topk_w, int32_t* rank, int32_t* hist, int* error, cudaStream_t st,
                         bool pdl) {
     const dim3 grid((T + kRouterTokens - 1) / kRouterTokens), block(256);
     if (E <= 32)
         return launch_kernel(topk_kernel<1>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
-                             topk_w, rank, hist);
+                             topk_w, rank, hist, error);
     if (E <= 64)
         return launch_kernel(topk_kernel<2>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
-                             topk_w, rank, hist);
+                             topk_w, rank, hist, error);
     if (E <= 128)
         return launch_kernel(topk_kernel<4>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
-                             topk_w, rank, hist);
+                             topk_w, rank, hist, error);
     return launch_kernel(topk_kernel<8>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k, topk_ids,
-                         topk_w, rank, hist);
+                         topk_w, rank, hist, error);
 }
 
 }  // namespace
@@ -692,15 +718,15 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
         const dim3 grid(T), block(256);
         if (E <= 32)
             return launch_kernel(router_finish_kernel<1>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
-                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket, error);
         if (E <= 64)
             return launch_kernel(router_finish_kernel<2>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
-                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket, error);
         if (E <= 128)
             return launch_kernel(router_finish_kernel<4>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
-                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+                                 topk_ids, topk_w, rank, hist, offsets, counts, ticket, error);
         return launch_kernel(router_finish_kernel<8>, grid, block, 0, st, pdl, P, p.KS, T, E, p.E_pad, bias, k,
-                             topk_ids, topk_w, rank, hist, offsets, counts, ticket);
+                             topk_ids, topk_w, rank, hist, offsets, counts, ticket, error);
     }
     e = launch_kernel(router_split_kernel, dim3((H + 31) / 32, (p.E_pad + 31) / 32), dim3(256), 0, st, false, Wr, H,
                       E, p.E_pad, wsplit);
@@ -716,7 +742,7 @@ cudaError_t launch_router(const uint16_t* x, const float* Wr, const float* bias,
         default: e = launch_router_gemm<128, 3>(x, wsplit, T, H, E, p.E_pad, p.n_eb, p.KS, p.kb_per_slice, P, error, timeout_ns, st, pdl); break;
     }
     if (e != cudaSuccess) return e;
-    return launch_topk(P, p, T, E, bias, k, topk_ids, topk_w, rank, hist, st, pdl);
+    return launch_topk(P, p, T, E, bias, k, topk_ids, topk_w, rank, hist, error, st, pdl);
 }
 
 }  // namespace moe

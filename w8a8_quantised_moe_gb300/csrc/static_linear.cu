@@ -26,7 +26,10 @@ void* g_scratch_ptr[kMaxDevices] = {};
 
 // Device address of the current device's copy of the scratch array.  In host
 // code the array's name is only a host-side stand-in, so the address is
-// looked up once per device, with that device current, and cached.
+// looked up once per device, with that device current, and cached.  The
+// cached address belongs to the device's primary context: it stays valid
+// until that context is destroyed (cudaDeviceReset), after which this entry
+// point must not be called again in the process.
 cudaError_t scratch_address(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
@@ -58,7 +61,8 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     if (L.total > kStaticScratchBytes) return MOE_ERR_UNSUPPORTED_SHAPE;  // beyond the static scratch
     const void* ptrs[] = {x, w_q, w_scale, y};
     for (const void* p : ptrs)
-        if (p == nullptr || !aligned16(p)) return MOE_ERR_INVALID_ARG;
+        if (p == nullptr || !aligned16(p) || injected(kInjectBadPtr)) return MOE_ERR_INVALID_ARG;
+    if (injected(kInjectLaunchFail)) return MOE_ERR_CUDA;  // faked before any CUDA call
 
     void* scratch = nullptr;
     cudaError_t e = scratch_address(&scratch);
@@ -74,9 +78,10 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     const GemmShape shape = pick_gemm_shape(M, 1, K, Epi::ScaleBF16, N, 0);
     int8_t* q8 = shape == GemmShape::Skinny ? reinterpret_cast<int8_t*>(q16) : nullptr;
 
-    // the scratch keeps the previous call's contents: clear the error word
-    // and the exact-path counters, which must start at zero
-    if (cudaMemsetAsync(err, 0, sizeof(int), st) != cudaSuccess) return MOE_ERR_CUDA;
+    // the scratch keeps the previous call's contents: clear the exact-path
+    // counters, which must start at zero.  The error word (zero when the
+    // library is loaded) is sticky: moe_w8a8_linear_static_error reads and
+    // clears it.
     if (cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
                              q8 ? nullptr : q16, q8, flag, list, counts, st, false);
@@ -100,7 +105,24 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     g.fb_list = list;
     g.fb_count = counts;
     g.error = err;
-    g.timeout_ns = kDefaultTimeoutNs;
+    g.timeout_ns = current_timeout_ns();
+    g.stall = injected(kInjectStall) ? 1 : 0;
     e = launch_grouped_gemm(Epi::ScaleBF16, shape, g, st, false);
     return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+extern "C" moe_status_t moe_w8a8_linear_static_error(void* stream) {
+    void* scratch = nullptr;
+    if (scratch_address(&scratch) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess) return MOE_ERR_CUDA;
+    int* err = reinterpret_cast<int*>(static_cast<char*>(scratch) + lin_layout(0, 0, 0).err);
+    int host = 0;
+    if (cudaMemcpy(&host, err, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess) return MOE_ERR_CUDA;
+    if (host != 0) {
+        const int zero = 0;
+        if (cudaMemcpy(err, &zero, sizeof(int), cudaMemcpyHostToDevice) != cudaSuccess) return MOE_ERR_CUDA;
+    }
+    if (host & kErrTimeout) return MOE_ERR_DEVICE_TIMEOUT;
+    if (host & kErrDevice) return MOE_ERR_DEVICE;
+    return MOE_OK;
 }

@@ -45,6 +45,11 @@ CASES = {
     # router bias, top-4, skewed experts
     "top4_zipf": TINY.replace(T=500, H=384, I=256, E=16, k=4, bias="zipf", zipf_s=1.2),
     "one_token": TINY.replace(T=1, H=256, I=512, E=8, k=2),
+    # the most experts and choices the library takes: 256 experts, top-8,
+    # softmax-renormalised weights, router bias (few tokens: one-CTA tiles;
+    # more: about 60 rows per expert)
+    "experts_256_top8": TINY.replace(T=100, H=256, I=128, E=256, k=8, bias="normal", bias_std=0.5),
+    "experts_256_top8_many": TINY.replace(T=2000, H=256, I=256, E=256, k=8, bias="normal", bias_std=0.5),
 }
 
 

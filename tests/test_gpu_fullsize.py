@@ -22,6 +22,11 @@ properties that hold at any size:
 The FP8 layer is checked the same way, except that its fp32 accumulators
 are bounded against the exact dot products of the E4M3 codes instead of
 compared bit for bit.
+
+Besides, y of every token of the decode and prefill layers (INT8), of every
+token of the FP8 decode layer and 2048 tokens of the FP8 prefill layer, and of
+256 tokens of the 256-expert layer is compared with the oracle's own
+end-to-end forward on the same inputs, within the layer's tolerance.
 """
 import numpy as np
 import pytest
@@ -197,7 +202,7 @@ def _assert_fp8_acc_close(acc, a_codes, w_codes):
     assert (err <= FP8_ACC_REL * mag).all(), float((err / np.maximum(mag, 1e-300)).max())
 
 
-@pytest.mark.parametrize("name", ["decode", "prefill"])
+@pytest.mark.parametrize("name", ["decode", "prefill", "wide"])
 def test_full_size_fp8_layer_sampled_against_oracle(name):
     cfg = wl.CONFIGS[name]
     seed = 0
@@ -352,3 +357,67 @@ def test_full_size_smoothed_layer_sampled_against_oracle(name):
         np.testing.assert_array_equal(y_gpu[i], oracle.combine(o_gpu, one, topk_w[t][None])[0])
         y_ref[i] = oracle.combine(o_own, one, w_ref[i][None])[0]
     assert_y_close(y_gpu, y_ref)
+
+
+# ---- y of (nearly) every token against the oracle's own forward -------------
+
+def _oracle_expert_weights(cfg, seed, experts, quant):
+    """[E][...] weight arrays for the oracle: the experts in `experts`
+    quantised by the oracle from the same fp32 draws, the rest zero (the
+    oracle reads only the experts its tokens route to)."""
+    code = np.uint8 if quant is oracle.quantize_rows_fp8 else np.int8
+    w13_q = np.zeros((cfg.E, 2 * cfg.I, cfg.H), code)
+    w13_s = np.zeros((cfg.E, 2 * cfg.I), np.float32)
+    w2_q = np.zeros((cfg.E, cfg.H, cfg.I), code)
+    w2_s = np.zeros((cfg.E, cfg.H), np.float32)
+    for e in experts:
+        w13_q[e], w13_s[e] = quant(wl.expert_weight_fp32(cfg, "w13", e, seed, device="cuda").cpu().numpy())
+        w2_q[e], w2_s[e] = quant(wl.expert_weight_fp32(cfg, "w2", e, seed, device="cuda").cpu().numpy())
+    return w13_q, w13_s, w2_q, w2_s
+
+
+# the decode and prefill layers whole; 256 tokens of the 256-expert layer
+# (its 11 GB of weights make the oracle's quantisation the cost, not its forward)
+EVERY = {"decode": None, "prefill": None, "wide": 256}
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill", "wide"])
+def test_full_size_layer_output_of_every_token_against_oracle(name):
+    cfg = wl.CONFIGS[name]
+    seed = 0
+    inp = wl.make_moe_inputs(cfg, seed)
+    args = (bf16_to_dev(inp.x), torch.from_numpy(inp.Wr).cuda(),
+            None if inp.bias is None else torch.from_numpy(inp.bias).cuda(), *_device_weights(cfg, seed), cfg.k)
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    y = moe.forward(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    y_gpu = bf16_from_dev(y)
+    del args, ws
+    torch.cuda.empty_cache()
+    n = EVERY[name]
+    tok = np.arange(cfg.T) if n is None else np.sort(np.random.default_rng(11).choice(cfg.T, n, replace=False))
+    ids_ref, _, _ = oracle.router(inp.x[tok], inp.Wr, inp.bias, cfg.k)
+    weights = _oracle_expert_weights(cfg, seed, sorted(set(ids_ref.ravel().tolist())), oracle.quantize_rows)
+    y_ref = oracle.moe_forward(inp.x[tok], inp.Wr, inp.bias, *weights, cfg.k)
+    assert_y_close(y_gpu[tok], y_ref)
+
+
+@pytest.mark.parametrize("name", ["decode", "prefill"])
+def test_full_size_fp8_layer_output_of_many_tokens_against_oracle(name):
+    cfg = wl.CONFIGS[name]
+    seed = 0
+    inp = wl.make_moe_inputs(cfg, seed)
+    args = (bf16_to_dev(inp.x), torch.from_numpy(inp.Wr).cuda(),
+            None if inp.bias is None else torch.from_numpy(inp.bias).cuda(), *_fp8_device_weights(cfg, seed), cfg.k)
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    y = moe.fp8_forward(*args, workspace=ws)
+    assert moe.device_error(ws) == 0
+    y_gpu = bf16_from_dev(y)
+    del args, ws
+    torch.cuda.empty_cache()
+    # the FP8 oracle sums in binary64 per product: 2048 of the prefill layer's tokens
+    tok = np.arange(cfg.T) if cfg.T <= 2048 else np.sort(np.random.default_rng(12).choice(cfg.T, 2048, replace=False))
+    ids_ref, _, _ = oracle.router(inp.x[tok], inp.Wr, inp.bias, cfg.k)
+    weights = _oracle_expert_weights(cfg, seed, sorted(set(ids_ref.ravel().tolist())), oracle.quantize_rows_fp8)
+    y_ref = oracle.moe_forward_fp8(inp.x[tok], inp.Wr, inp.bias, *weights, cfg.k)
+    assert_y_close(y_gpu[tok], y_ref)

@@ -57,6 +57,8 @@ CASES = {
     "tensor_router_min": TINY.replace(T=129, H=512, I=256, E=12, k=2),
     # the most experts and choices the library takes, few tokens
     "experts_256_top8": TINY.replace(T=100, H=256, I=128, E=256, k=8),
+    # 256 experts, top-8, about 60 rows per expert: the one-CTA tensor-core GEMMs
+    "experts_256_top8_many": TINY.replace(T=2000, H=256, I=256, E=256, k=8, bias="normal", bias_std=0.5),
 }
 
 

@@ -24,6 +24,9 @@ CASES = {
     "pair_tiles": TINY.replace(T=1000, H=512, I=256, E=4, k=2),
     # router bias, top-4
     "top4_bias": TINY.replace(T=77, H=384, I=256, E=16, k=4, bias="normal", bias_std=0.5),
+    # the most experts and choices the library takes: 256 experts, top-8, router bias
+    "experts_256_top8": TINY.replace(T=100, H=256, I=128, E=256, k=8, bias="normal", bias_std=0.5),
+    "experts_256_top8_many": TINY.replace(T=2000, H=256, I=256, E=256, k=8, bias="normal", bias_std=0.5),
 }
 
 

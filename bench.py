@@ -356,6 +356,18 @@ def traffic_from_profiles(config_name, kernel, fmt="int8"):
     return ent.get("dram_bytes_per_launch")
 
 
+def tensor_rate_from_profiles(fmt="int8"):
+    """The measured tcgen05 rate (TOPS) of the format's MMA kind, from the
+    committed summary of the contraction-rate program, or None."""
+    path = os.path.join(ROOT, "profiles", "tensor_rates.json")
+    if not os.path.exists(path):
+        return None
+    with open(path) as f:
+        table = json.load(f)
+    ent = table.get("e4m3" if fmt == "fp8" else "f16_int8_values")
+    return None if not ent else ent.get("tops")
+
+
 def run_ours(args, ranks: Ranks):
     import torch
     import w8a8_quantised_moe_gb300 as moe
@@ -493,6 +505,10 @@ def run_ours(args, ranks: Ranks):
         achieved = w["bytes"] / (dom_ms * 1e-3) / 1e9
         roof = {"bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s"}
     roof["frac"] = roof["achieved"] / roof["peak"]
+    probe = tensor_rate_from_profiles(fmt)
+    if roof["bound"] == "tensor" and probe:  # the MMA kind's own measured rate, beside the cuBLAS peak
+        roof["probe"] = {"peak": probe, "frac": achieved / probe, "unit": "TFLOP/s",
+                         "source": "profiles/tcgen05_rates.md"}
     gemm_fmt = "fp8" if fmt == "fp8" else "int8"  # the smoothed layer runs the INT8 GEMM kernels
     roof["traffic"] = traffic_from_profiles(args.config + ("_fp8" if fmt == "fp8" else ""), dom, gemm_fmt)
     roof["kernel"] = dom

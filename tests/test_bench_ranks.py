@@ -83,3 +83,34 @@ def test_reference_arm_line_on_the_host(fmt):
         assert key in line, key
     assert line["cpu_baseline"]["kind"] == "oracle"
     assert line["e2e"]["h2d_bytes_per_step"] == 0
+
+
+def test_committed_profile_tables_are_read_for_the_current_sources():
+    """`roofline.traffic` comes from the committed ncu table only while the
+    GEMM sources hash as they did at capture; the tensor rates are read as
+    committed."""
+    import json
+    with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
+        table = json.load(f)
+    for cfg, fmt in (("prefill", "int8"), ("decode", "int8"), ("prefill_fp8", "fp8"), ("decode_fp8", "fp8")):
+        ent = table[cfg]["gemm1_gateup"]
+        want = ent["dram_bytes_per_launch"] if ent["gemm_src_sha256_16"] == bench.gemm_source_sha(fmt) else None
+        assert bench.traffic_from_profiles(cfg, "gemm1_gateup", fmt) == want
+    assert bench.traffic_from_profiles("no_such_workload", "gemm1_gateup") is None
+    f16, e4m3 = bench.tensor_rate_from_profiles("int8"), bench.tensor_rate_from_profiles("fp8")
+    assert f16 > 0 and e4m3 > f16
+
+
+def test_contraction_rate_program_compiles_for_sm103a(tmp_path):
+    """The program behind the committed tensor rates builds with the library's
+    headers (nvcc cross-compiles here; running it needs a GB300)."""
+    import shutil
+    import subprocess
+    from w8a8_quantised_moe_gb300 import build as lib_build
+    if shutil.which(lib_build.nvcc()) is None and not os.path.exists(lib_build.nvcc()):
+        pytest.skip("nvcc not found")
+    pkg = os.path.join(ROOT, "w8a8_quantised_moe_gb300")
+    r = subprocess.run([lib_build.nvcc(), "-gencode", "arch=compute_103a,code=sm_103a", "-O3", "-std=c++17",
+                        "-I", os.path.join(ROOT, "include"), "-I", pkg, os.path.join(pkg, "peak_int8.cu"),
+                        "-o", str(tmp_path / "peak_int8")], capture_output=True, text=True, timeout=300)
+    assert r.returncode == 0, r.stderr[-2000:]

@@ -217,12 +217,17 @@ def test_linear_golden_example():
 @pytest.mark.parametrize("M,N,K,path", [(1, 128, 128, "auto"), (37, 256, 384, "auto"), (300, 384, 1280, "auto"),
                                         (130, 128, 4096, "auto"), (500, 512, 1024, "auto"),
                                         (3, 384, 640, "auto"), (8, 1024, 2048, "auto"), (37, 256, 384, "skinny"),
-                                        (9, 128, 1280, "narrow"), (5000, 128, 256, "auto")])
+                                        (9, 128, 1280, "narrow"), (5000, 128, 256, "auto"),
+                                        (1500, 128, 1280, "auto"), (1300, 256, 2560, "auto"),
+                                        (1250, 128, 7168, "auto")])
 def test_linear_bit_exact(M, N, K, path):
     """M <= 8 rows take the dp4a kernel by default; 37 rows forced onto it
     pass in five chunks of up to 8 rows, the last one ragged; K = 384 and 640
-    end on a half-filled 256-byte weight stage.  5000
-    rows take the warp-per-token quantiser, fewer the CTA-per-token one."""
+    end on a half-filled 256-byte weight stage.  Above 8 rows per SM the
+    quantiser takes one to eight warps per row by row length: 5000 x 256 one
+    warp, 1500 x 1280 two, 1300 x 2560 four (2.5 vectors per lane: the
+    warps' shares end unevenly), 1250 x 7168 eight; fewer rows take the
+    CTA-per-token quantiser."""
     cfg = wl.LINEAR
     x = wl.draw_activations(7, cfg.cfg_id, M, K, max(1, K // 100))
     w32 = (np.random.default_rng(M + N + K).standard_normal((N, K)) * 0.02).astype(np.float32)

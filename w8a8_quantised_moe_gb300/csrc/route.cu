@@ -4,7 +4,7 @@
 //                        first slot of every (chunk, expert).
 //   permute_quant_kernel slot of every (token, choice); per-token dynamic INT8
 //                        quantisation of x, scattered into the token's slots
-//                        (one warp per token).
+//                        (one to eight warps per token, by row length).
 //   permute_quant_cta_kernel  the same with one CTA per token, the row held in
 //                        registers: for few tokens (decode), where a warp per
 //                        token leaves most of the GPU idle.
@@ -122,51 +122,72 @@ __global__ void __launch_bounds__(kScanThreads) scan_kernel(int32_t* __restrict_
     }
 }
 
-// One warp per token.  With topk_ids == nullptr the token's single "slot" is
-// the token itself (the dense linear layer).  Besides the codes, every token
-// gets the L1 norm of its code row; rows above kExactL1 are flagged in each
-// of their slots and listed for the exact path of the GEMM.
-// A warp per token, 8 per CTA: the amax pass and the code pass each read the
-// row (the second mostly from cache).  (Measured at T = 8192: staging rows
-// through shared memory with cp.async, 4 tokens per CTA, was slower: 53
-// against 52 us.)  Registers are capped for 8 CTAs per SM, so that the 1024
-// CTAs of T = 8192 run in one wave instead of 6 per SM and a tail of 112
-// (measured: 54 -> 51 us; the kernel is issue-bound, 55 % issue-active).
+// WPT warps per token (1, 2, 4 or 8), 8 warps per CTA.  With topk_ids ==
+// nullptr the token's single "slot" is the token itself (the dense linear
+// layer).  Besides the codes, every token gets the L1 norm of its code row;
+// rows above kExactL1 are flagged in each of their slots and listed for the
+// exact path of the GEMM.
+// Each warp of a token takes every WPT-th 16-byte vector of the row; the row
+// maximum and the L1 norm are combined through shared memory.  The amax pass
+// and the code pass each read the row (the second mostly from cache).  Split
+// rows keep more loads in flight per SM than one warp per token, whose single
+// load in flight per lane left the dense linear layer's quantiser at a third
+// of the HBM rate.  (Measured at T = 8192 with one warp per token: staging
+// rows through shared memory with cp.async, 4 tokens per CTA, was slower: 53
+// against 52 us.)  Registers are capped for 8 CTAs per SM (measured with one
+// warp per token at T = 8192: 54 -> 51 us; unrolling the loops spills).
 constexpr int kPqWarps = 8;
 
+template <int WPT>
 __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids,
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
     int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    static_assert(WPT == 1 || WPT == 2 || WPT == 4 || WPT == 8, "warps per token");
+    __shared__ float red_max[kPqWarps];
+    __shared__ int red_l1[kPqWarps];
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-    const int t = blockIdx.x * kPqWarps + warp;
+    const int sub = warp % WPT;  // this warp's share of the token's row
+    const int t = blockIdx.x * (kPqWarps / WPT) + warp / WPT;
     pdl_wait();
     pdl_trigger();
-    if (t >= T) return;
+    if (WPT == 1 && t >= T) return;
+    const bool live = t < T;  // with WPT > 1 every warp reaches the block barriers
     int my_slot = t;
-    if (topk_ids != nullptr && lane < k) {
+    if (live && topk_ids != nullptr && lane < k) {
         const int e = topk_ids[(size_t)t * k + lane];
         my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + lane];
-        slot_of[(size_t)t * k + lane] = my_slot;
-        slot_token[my_slot] = t;
+        if (sub == 0) {
+            slot_of[(size_t)t * k + lane] = my_slot;
+            slot_token[my_slot] = t;
+        }
     }
     const int nk = (topk_ids != nullptr) ? k : 1;
-    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
-    const int nv = H / 8;  // 8 bf16 per 16-byte vector
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)(live ? t : 0) * H);
+    const int nv = live ? H / 8 : 0;  // 8 bf16 per 16-byte vector
     float amax = 0.f;
-    for (int i = lane; i < nv; i += 32) amax = fmaxf(amax, absmax8(__ldg(row + i)));
+    for (int i = sub * 32 + lane; i < nv; i += 32 * WPT) amax = fmaxf(amax, absmax8(__ldg(row + i)));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (WPT > 1) {
+        if (lane == 0) red_max[warp] = amax;
+        __syncthreads();
+        const int w0 = warp - sub;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) amax = fmaxf(amax, red_max[w0 + w]);
+    }
     const float s = __fdiv_rn(amax, 127.0f);
-    if (lane == 0) s_x[t] = s;
-    if (lane < nk) s_slot[my_slot] = s;
+    if (live && sub == 0) {
+        if (lane == 0) s_x[t] = s;
+        if (lane < nk) s_slot[my_slot] = s;
+    }
     int slots[kMaxTopK];  // slot j of the token is lane j's my_slot (taken before the lanes diverge)
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
     int l1 = 0;
-    for (int i = lane; i < nv; i += 32) {
+    for (int i = sub * 32 + lane; i < nv; i += 32 * WPT) {
         int q[8];
         quant8(__ldg(row + i), s, q, l1);
         if (q16 != nullptr) {
@@ -180,8 +201,16 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) l1 += __shfl_xor_sync(0xffffffffu, l1, off);
+    if (WPT > 1) {
+        if (lane == 0) red_l1[warp] = l1;
+        __syncthreads();
+        if (sub != 0) return;
+        l1 = 0;
+#pragma unroll
+        for (int w = 0; w < WPT; ++w) l1 += red_l1[warp + w];
+    }
     const int flagged = l1 > kExactL1 ? 1 : 0;
-    if (lane < nk) {
+    if (live && lane < nk) {
         flags[my_slot] = flagged;
         if (flagged) fb_list[atomicAdd(fb_count, 1)] = my_slot;
     }
@@ -476,8 +505,28 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
     if ((long)T <= (long)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kPqVec)
         return launch_kernel(permute_quant_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist, T,
                              H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
-    return launch_kernel(permute_quant_kernel, dim3((T + kPqWarps - 1) / kPqWarps), dim3(32 * kPqWarps), 0, st, pdl,
-                         x, topk_ids, rank, hist, T, H, E, k,
+    // warps per token: about four 16-byte vectors per lane (measured on the
+    // three layer shapes, quantiser time in us for 1 / 2 / 4 / 8 warps per
+    // token: H = 4096, T = 4096, one slot: 34.1 / 31.8 / 27.9 / 29.3;
+    // H = 4096, T = 8192, top-2: 51.5 / 45.2 / 43.2 / 50.4; H = 7168,
+    // T = 4096, top-8: 102.4 / 100.2 / 94.7 / 90.4)
+#ifndef MOE_PQ_WPT
+    const int per_lane4 = (H / 8 + 127) / 128;
+    const int wpt = per_lane4 <= 1 ? 1 : per_lane4 <= 2 ? 2 : per_lane4 <= 4 ? 4 : 8;
+#else
+    const int wpt = MOE_PQ_WPT;
+#endif
+    const dim3 grid((unsigned)(((long)T * wpt + kPqWarps - 1) / kPqWarps)), block(32 * kPqWarps);
+    if (wpt == 8)
+        return launch_kernel(permute_quant_kernel<8>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+    if (wpt == 4)
+        return launch_kernel(permute_quant_kernel<4>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+    if (wpt == 2)
+        return launch_kernel(permute_quant_kernel<2>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+    return launch_kernel(permute_quant_kernel<1>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
                          slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
 }
 

@@ -17,8 +17,14 @@
 // Each tensor-core case runs one issuing thread per CTA (or pair) that keeps
 // its accumulator busy back to back, one CTA per SM; the issuing CTA times
 // itself with clock64 from the first issue to the completion of the last MMA,
-// and the whole grid is timed with CUDA events.  Every wait is bounded
-// (2 s, then an error flag).  Prints one JSON line.
+// and the whole grid is timed with CUDA events.
+// Then, in cycles per K = 128 stage of 256 x 192 pair MMAs (768 at the full
+// rate), what the pair GEMM adds to that stream: waits between blocks, busy
+// warps beside the issuer, tensor-memory traffic, and the A-slot pipeline
+// (refilling warps that wait for a free slot, convert, store and signal the
+// issuer) in several shapes and handshakes, with per-segment time stamps and
+// a per-fill trace of one CTA pair.
+// Every wait is bounded (2 s, then an error flag).  Prints one JSON line.
 #include <cstdint>
 #include <cstdio>
 #include <cuda_fp16.h>
@@ -138,6 +144,318 @@ __global__ void __launch_bounds__(128, 1) tc_rate(int blocks, long long* cycles,
     }
 }
 
+// Interference cases: the 256 x 192 CTA-pair MMA stream above with one
+// ingredient of the pair GEMM added at a time, to tell which one slows a
+// K = 128 stage (a block of 8 MMAs, 768 cycles at the full rate) down.
+//   kWaitPrev   the issuer keeps at most two blocks in flight: before block i
+//               it waits for the commit of block i - 2 (as the pair GEMM's
+//               two A slots allow)
+//   kWaitSelf   before block i it waits for the commit of block i - 1 (the
+//               commit-to-wake latency, serially)
+//   kAlu        four more warps per CTA (one per SM sub-partition, so one
+//               shares the issuer's) issue independent FMAs back to back
+//   kTmemSt     four more warps store 32 columns to tensor memory in a loop
+//   kTmemLd     four more warps load 32 columns from tensor memory in a loop
+enum Load : int { kWaitPrev = 1, kWaitSelf = 2, kAlu = 3, kTmemSt = 4, kTmemLd = 5 };
+
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* err) {
+    if (wait_bounded(bar, parity)) return true;
+    atomicOr(err, 2);
+    return false;
+}
+
+template <int LOAD>
+__global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycles, int* err) {
+    constexpr int N = 192;
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t done_bar, done[2];
+    __shared__ uint32_t tmem_slot;
+    __shared__ volatile int stop;
+    const int tid = threadIdx.x, warp = tid >> 5;
+    const uint32_t rank = cluster_ctarank();
+    for (int i = tid; i < (N / 2) * 128 / 2; i += blockDim.x)
+        reinterpret_cast<uint16_t*>(sm)[i] = f16_bits_of_int(static_cast<int>((i * 2654435761u) >> 9) % 128 - 64);
+    if (tid == 0) {
+        mbar_init(&done_bar, 1);
+        mbar_init(&done[0], 1);
+        mbar_init(&done[1], 1);
+        stop = 0;
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(&tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    if (warp < 4) {  // defined A operand in both slots
+        uint32_t r[32];
+        for (int c = 0; c < 128; c += 32) {
+#pragma unroll
+            for (int j = 0; j < 32; ++j) r[j] = static_cast<uint32_t>(f16_bits_of_int((tid * 7 + (c + j) * 13) % 128 - 64)) * 0x10001u;
+            tmem_st_32(tmem + lane_base + kACol + c, r);
+        }
+        tmem_wait_st();
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+
+    const uint32_t idesc = idesc_f16_f32(256, N);
+    if (tid == 0 && rank == 0) {
+        const uint64_t bd = smem_desc_sw128(smem_u32(sm));
+        const long long c0 = clock64();
+        for (int blk = 0; blk < blocks; ++blk) {
+            const int slot = blk & 1;
+            if (LOAD == kWaitPrev && blk >= 2 && !wait_phase(&done[slot], ((blk - 2) >> 1) & 1, err)) break;
+            if (LOAD == kWaitSelf && blk >= 1 && !wait_phase(&done[slot ^ 1], ((blk - 1) >> 1) & 1, err)) break;
+            mma8_f16_tmem_a_pair(tmem, tmem + kACol, bd, 0, idesc, blk ? 1u : 0u);
+            if (LOAD == kWaitPrev || LOAD == kWaitSelf) mma_commit_pair(&done[slot], 3);
+        }
+        mma_commit_pair(&done_bar, 3);
+        wait_phase(&done_bar, 0, err);
+        cycles[blockIdx.x / 2] = clock64() - c0;
+    }
+    if (tid == 0 && rank == 1) wait_phase(&done_bar, 0, err);
+    if (tid == 0 && (LOAD == kWaitPrev || LOAD == kWaitSelf)) {
+        // every commit of the blocks has landed in this CTA before it leaves
+        for (int s = 0; s < 2 && s < blocks; ++s) wait_phase(&done[s], (((blocks - s + 1) >> 1) - 1) & 1, err);
+    }
+    if (tid == 0) stop = 1;
+
+    if (warp >= 4 && LOAD >= kAlu && LOAD <= kTmemLd) {
+        const uint64_t t0 = global_timer_ns();
+        uint32_t r[32];
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(tid + j);
+#pragma unroll
+        for (int j = 0; j < 32; ++j) r[j] = 0x3c003c00u;
+        for (int it = 0; !stop; ++it) {
+            if (LOAD == kAlu) {
+#pragma unroll
+                for (int k = 0; k < 16; ++k)
+#pragma unroll
+                    for (int j = 0; j < 8; ++j) f[j] = fmaf(f[j], 0.999f, 0.25f);
+            } else if (LOAD == kTmemSt) {
+                tmem_st_32(tmem + lane_base + 384 + (it & 3) * 32, r);
+                tmem_wait_st();
+            } else {
+                tmem_ld_32(tmem + lane_base + 384 + (it & 3) * 32, r);
+                tmem_wait_ld();
+            }
+            if ((it & 15) == 0 && global_timer_ns() - t0 > 2000000000ull) {
+                atomicOr(err, 4);
+                break;
+            }
+        }
+        float acc = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) acc += f[j] + __uint_as_float(r[j]);
+        if (acc == 1234.5f) atomicOr(err, 8);
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
+// The A-slot pipeline on its own, in the shapes a pair GEMM could use:
+// NSLOT tensor-memory A slots, each holding the K of MPS MMAs (MPS x 8
+// 32-bit columns), refilled by four warps per CTA
+// that wait for the slot's previous readers, spend `delay` dependent FMAs per
+// 64 columns (the conversion), store the slot and arrive on the even CTA's
+// a_ready (REMOTE: the odd CTA's warps too; else only the even CTA's); with
+// ST false they store nothing.  The issuer waits a_ready, issues the slot's
+// MMAs (256 x 192) and commits them to both CTAs' done barrier of the slot.
+constexpr int kTraceFrom = 200, kTrace = 48;  // per-fill time stamps of CTA 0 for fills [200, 248)
+
+// Handshake variants of the A-slot pipeline (timing only; 1, 2 and 5 drop an
+// ordering the real kernels need):
+//   0  as described above
+//   1  the issuer omits tcgen05.fence::after_thread_sync after a_ready
+//   2  the refilling warps omit both tcgen05 fences
+//   3  the conversion is a spin on clock64 for 7 x `delay` cycles, no FMAs
+//   4  the issuer polls a_ready with test_wait (no suspension) instead of try_wait
+//   5  a_ready is a shared-memory counter (relaxed remote red.add), polled by
+//      the issuer with volatile loads
+//   6  the refilling warps do not wait for the slot to be free (a_ready as
+//      in 5, which tolerates their running ahead)
+//   7  the issuer does not wait for a_ready, nor the refilling warps for free
+//      slots: the MMA stream beside the refilling work, uncoupled
+enum Handshake : int { kHsBase = 0, kHsNoIssuerFence = 1, kHsNoConvFence = 2, kHsClockSpin = 3, kHsTestWait = 4,
+                       kHsCounter = 5, kHsConvNoWait = 6, kHsIssuerNoWait = 7 };
+
+__device__ __forceinline__ bool mbar_test_wait(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tmbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\tselp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
+template <int NSLOT, int MPS, bool ST, bool REMOTE, int HS = kHsBase, int G = 1, int N = 192, int ISS = 1>
+__global__ void __launch_bounds__(128 + 128 * G, 1) handoff_rate(int fills, int delay, long long* cycles, int* err,
+                                                                 long long* seg) {
+    constexpr uint32_t kCols = MPS * 8;  // columns per slot
+    static_assert(NSLOT * kCols <= 256 && kCols % 32 == 0, "A slots fit columns 256-511");
+    extern __shared__ uint8_t raw[];
+    uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
+    __shared__ uint64_t done_bar, done[NSLOT], a_ready[NSLOT];
+    __shared__ uint32_t a_count[NSLOT];
+    __shared__ uint32_t tmem_slot;
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    const uint32_t rank = cluster_ctarank();
+    for (int i = tid; i < (N / 2) * 128 / 2; i += blockDim.x)
+        reinterpret_cast<uint16_t*>(sm)[i] = f16_bits_of_int(static_cast<int>((i * 2654435761u) >> 9) % 128 - 64);
+    if (tid == 0) {
+        mbar_init(&done_bar, ISS);  // one final commit per issuer
+        for (int j = 0; j < NSLOT; ++j) {
+            mbar_init(&done[j], 1);
+            mbar_init(&a_ready[j], REMOTE ? 8 : 4);  // one group's 4 warps in each CTA
+            a_count[j] = 0;
+        }
+        fence_barrier_init();
+    }
+    if (warp == 0) {
+        tmem_alloc_pair(&tmem_slot, kTmemCols);
+        tmem_relinquish_pair();
+    }
+    fence_proxy_async_smem();
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    const uint32_t tmem = tmem_slot;
+    const uint32_t lane_base = static_cast<uint32_t>((warp & 3) * 32) << 16;
+    const uint32_t idesc = idesc_f16_f32(256, N);
+    // issuers: warp 0 lane 0, and with ISS == 2 warp 3 lane 0 too, taking alternate fills
+    const int issuer = warp == 0 ? 0 : (ISS == 2 && warp == 3 ? 1 : -1);
+    if (rank == 0 && lane == 0 && issuer >= 0) {
+        const uint64_t bd = smem_desc_sw128(smem_u32(sm));
+        const long long c0 = clock64();
+        long long s_wait = 0, s_issue = 0;
+        const bool stamp = blockIdx.x == 0 && issuer == 0;
+        for (int f = issuer; f < fills; f += ISS) {
+            const int slot = f % NSLOT;
+            const long long t0 = clock64();
+            if (HS == kHsTestWait) {
+                const uint64_t g0 = global_timer_ns();
+                bool ok = true;
+                while (!mbar_test_wait(&a_ready[slot], (f / NSLOT) & 1))
+                    if (global_timer_ns() - g0 > 2000000000ull) { ok = false; break; }
+                if (!ok) { atomicOr(err, 2); break; }
+            } else if (HS == kHsCounter || HS == kHsConvNoWait) {
+                const uint32_t want = (REMOTE ? 8u : 4u) * static_cast<uint32_t>(f / NSLOT + 1);
+                const uint64_t g0 = global_timer_ns();
+                bool ok = true;
+                while (*reinterpret_cast<volatile uint32_t*>(&a_count[slot]) < want)
+                    if (global_timer_ns() - g0 > 2000000000ull) { ok = false; break; }
+                if (!ok) { atomicOr(err, 2); break; }
+            } else if (HS != kHsIssuerNoWait && !wait_phase(&a_ready[slot], (f / NSLOT) & 1, err)) {
+                break;
+            }
+            if (HS != kHsNoIssuerFence) tc_fence_after();
+            const long long t1 = clock64();
+            s_wait += t1 - t0;
+            if (stamp && f >= kTraceFrom && f < kTraceFrom + kTrace) seg[8 + (f - kTraceFrom) * 4 + 0] = t1;
+            const uint32_t a = tmem + kACol + slot * kCols;
+            if (MPS == 8) {
+                mma8_f16_tmem_a_pair(tmem, a, bd, 0, idesc, f ? 1u : 0u);
+            } else {
+#pragma unroll
+                for (int m = 0; m < MPS; ++m)
+                    mma_f16_tmem_a_pair(tmem, a + m * 8, bd + static_cast<uint64_t>((m & 3) * 2), idesc, (f | m) ? 1u : 0u);
+            }
+            mma_commit_pair(&done[slot], 3);
+            const long long t2 = clock64();
+            s_issue += t2 - t1;
+            if (stamp && f >= kTraceFrom && f < kTraceFrom + kTrace) seg[8 + (f - kTraceFrom) * 4 + 1] = t2;
+        }
+        mma_commit_pair(&done_bar, 3);
+        wait_phase(&done_bar, 0, err);
+        cycles[issuer * 1024 + blockIdx.x / 2] = clock64() - c0;
+        if (stamp) {
+            seg[0] = s_wait;
+            seg[1] = s_issue;
+        }
+    }
+    if (tid == 0 && rank == 1) wait_phase(&done_bar, 0, err);
+    if (warp >= 4 && (REMOTE || rank == 0 || ST)) {
+        long long s_done = 0, s_delay = 0, s_store = 0, s_arrive = 0;
+        uint32_t r[32];
+        const int group = (warp - 4) / 4;  // G groups of four warps take alternate fills
+        for (int f = group; f < fills; f += G) {
+            const int slot = f % NSLOT;
+            bool ok = true;
+            const long long t0 = clock64();
+            // (with the issuer not waiting, the slot's phases can run two ahead of
+            // a parity wait: the refilling warps then do not wait either)
+            if (HS != kHsConvNoWait && HS != kHsIssuerNoWait && lane == 0 && f >= NSLOT)
+                ok = wait_phase(&done[slot], ((f - NSLOT) / NSLOT) & 1, err);
+            if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
+            if (HS != kHsNoConvFence) tc_fence_after();
+            const long long t1 = clock64();
+            float v = static_cast<float>(lane);
+            const int d_end = delay * MPS / 8;
+            if (HS == kHsClockSpin) {
+                while (clock64() - t1 < 7 * d_end) v += 1.0f;
+            } else {
+                for (int d = 0; d < d_end; ++d) v = fmaf(v, 0.999f, 0.25f);
+            }
+            const uint32_t bits = v == 1234.5f ? 0x3c003c00u : 0x3c003c01u;
+            const long long t2 = clock64();
+            if (ST) {
+#pragma unroll
+                for (int j = 0; j < 32; ++j) r[j] = bits;
+#pragma unroll
+                for (uint32_t c = 0; c < kCols; c += 32) tmem_st_32(tmem + lane_base + kACol + slot * kCols + c, r);
+                tmem_wait_st();
+            } else if (bits == 0x3c003c00u) {
+                atomicOr(err, 8);
+            }
+            const long long t3 = clock64();
+            if (HS != kHsNoConvFence) tc_fence_before();
+            __syncwarp();
+            if (lane == 0 && (REMOTE || rank == 0)) {
+                if (HS == kHsCounter || HS == kHsConvNoWait)
+                    asm volatile("red.shared::cluster.add.u32 [%0], 1;" ::"r"(cluster_addr(&a_count[slot], 0)) : "memory");
+                else
+                    mbar_arrive_cluster(cluster_addr(&a_ready[slot], 0));
+            }
+            const long long t4 = clock64();
+            if (blockIdx.x == 0 && tid == 128 && f >= kTraceFrom && f < kTraceFrom + kTrace) {
+                seg[8 + (f - kTraceFrom) * 4 + 2] = t1;  // the slot's previous fill observed complete
+                seg[8 + (f - kTraceFrom) * 4 + 3] = t4;  // arrived on a_ready
+            }
+            s_done += t1 - t0;
+            s_delay += t2 - t1;
+            s_store += t3 - t2;
+            s_arrive += t4 - t3;
+        }
+        if (blockIdx.x == 0 && tid == 128) {  // warp 4 of the even CTA
+            seg[2] = s_done;
+            seg[3] = s_delay;
+            seg[4] = s_store;
+            seg[5] = s_arrive;
+        }
+    }
+    if (tid == 0) {  // every commit of the fills has landed in this CTA before it leaves
+        for (int j = 0; j < NSLOT && j < fills; ++j)
+            wait_phase(&done[j], (((fills - j + NSLOT - 1) / NSLOT) - 1) & 1, err);
+    }
+    tc_fence_before();
+    cluster_sync_all();
+    tc_fence_after();
+    if (warp == 0) tmem_dealloc_pair(tmem, kTmemCols);
+}
+
 // mma.sync m16n8k32 s8 x s8 -> s32, eight independent accumulator chains per warp
 __global__ void __launch_bounds__(256) s8_rate(int iters, long long* cycles, int* sink) {
     uint32_t a[4], b[2];
@@ -220,6 +538,77 @@ bool run_tc(int nsm, int blocks, long long* d_cyc, int* d_err, Result* out) {
     return timed(launch, issuers, per_issuer * issuers, per_issuer / (PAIR ? 2 : 1), d_cyc, out);
 }
 
+// cycles per 8-MMA block of the slowest issuer, for one interference case
+template <int LOAD>
+bool run_pipe(int nsm, int blocks, long long* d_cyc, int* d_err, double* cycles_per_block) {
+    auto kern = pipe_rate<LOAD>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return false;
+    const int grid = nsm & ~1;
+    long long h[2048];
+    for (int rep = 0; rep < 2; ++rep) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(256);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, blocks, d_cyc, d_err) != cudaSuccess) return false;
+        if (cudaDeviceSynchronize() != cudaSuccess) return false;
+    }
+    if (cudaMemcpy(h, d_cyc, (grid / 2) * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+    long long mx = 1;
+    for (int i = 0; i < grid / 2; ++i) mx = h[i] > mx ? h[i] : mx;
+    *cycles_per_block = static_cast<double>(mx) / blocks;
+    return true;
+}
+
+// cycles per K = 128 (8 MMAs) of the slowest issuer, for one A-slot pipeline
+template <int NSLOT, int MPS, bool ST, bool REMOTE, int HS = kHsBase, int G = 1, int N = 192, int ISS = 1>
+bool run_handoff(int nsm, int fills, int delay, long long* d_cyc, int* d_err, double* cycles_per_k128,
+                 double* seg_per_fill = nullptr, long long* trace = nullptr) {
+    auto kern = handoff_rate<NSLOT, MPS, ST, REMOTE, HS, G, N, ISS>;
+    if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
+        return false;
+    const int grid = nsm & ~1;
+    long long h[2048];
+    for (int rep = 0; rep < 2; ++rep) {
+        cudaLaunchConfig_t cfg = {};
+        cfg.gridDim = dim3(grid);
+        cfg.blockDim = dim3(128 + 128 * G);
+        cfg.dynamicSmemBytes = kSmemBytes;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (cudaLaunchKernelEx(&cfg, kern, fills, delay, d_cyc, d_err, d_cyc + 2048) != cudaSuccess) return false;
+        if (cudaDeviceSynchronize() != cudaSuccess) return false;
+    }
+    long long mx = 1;
+    for (int is = 0; is < ISS; ++is) {
+        if (cudaMemcpy(h, d_cyc + is * 1024, (grid / 2) * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess)
+            return false;
+        for (int i = 0; i < grid / 2; ++i) mx = h[i] > mx ? h[i] : mx;
+    }
+    *cycles_per_k128 = static_cast<double>(mx) / fills * (8.0 / MPS);
+    if (seg_per_fill) {
+        if (cudaMemcpy(h, d_cyc + 2048, 6 * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+        for (int i = 0; i < 6; ++i) seg_per_fill[i] = static_cast<double>(h[i]) / fills;
+    }
+    if (trace && cudaMemcpy(trace, d_cyc + 2048 + 8, kTrace * 4 * sizeof(long long), cudaMemcpyDeviceToHost) !=
+                     cudaSuccess)
+        return false;
+    return true;
+}
+
 void print(const char* name, const Result& r, bool last) {
     printf("\"%s\": {\"ops_per_clk_per_sm\": %.0f, \"tops\": %.1f, \"sm_mhz\": %.0f}%s", name, r.ops_per_clk_sm,
            r.tops, r.mhz, last ? "" : ", ");
@@ -255,9 +644,104 @@ int main() {
     };
     const double s8_per_cta = 2.0 * 16 * 8 * 32 * 8.0 * 8.0 * s8_iters;  // 8 warps x 8 chains
     if (!timed(s8_launch, s8_blocks, s8_per_cta * s8_blocks, s8_per_cta * 4, d_cyc, &r[6])) return 3;
+    // interference cases: cycles per K = 128 stage (8 pair MMAs, 768 at the full rate)
+    const int pb = 2000;
+    double cpb[16];
+    int n_pipe = 0;
+    const int delays[] = {0, 64, 128, 192};
+    ok = run_pipe<0>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kWaitPrev>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kWaitSelf>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kAlu>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kTmemSt>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kTmemLd>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]);
+    // A-slot pipelines: [slots x MMAs per slot, stores, remote arrivals] x conversion delays
+    double hof[6][4], seg2[4][6], seg3[4][6];
+    static long long trace[kTrace * 4];
+    for (int i = 0; i < 4; ++i) {
+        const int d = delays[i];
+        ok = ok && run_handoff<2, 8, true, true>(nsm, pb, d, d_cyc, d_err, &hof[0][i], seg2[i]) &&
+             run_handoff<2, 8, false, true>(nsm, pb, d, d_cyc, d_err, &hof[1][i]) &&
+             run_handoff<2, 8, true, false>(nsm, pb, d, d_cyc, d_err, &hof[2][i]) &&
+             run_handoff<3, 8, true, true>(nsm, pb, d, d_cyc, d_err, &hof[3][i], seg3[i], i == 1 ? trace : nullptr) &&
+             run_handoff<4, 4, true, true>(nsm, 2 * pb, d, d_cyc, d_err, &hof[4][i]) &&
+             run_handoff<4, 8, true, true>(nsm, pb, d, d_cyc, d_err, &hof[5][i]);
+    }
+    // handshake variants, 2 and 3 slots, delay 64
+    double hs[8][2], grp[3][4], n160[3][4], two_iss[4][4];
+    ok = ok && run_handoff<2, 8, true, true, kHsBase>(nsm, pb, 64, d_cyc, d_err, &hs[0][0]) &&
+         run_handoff<3, 8, true, true, kHsBase>(nsm, pb, 64, d_cyc, d_err, &hs[0][1]) &&
+         run_handoff<2, 8, true, true, kHsNoIssuerFence>(nsm, pb, 64, d_cyc, d_err, &hs[1][0]) &&
+         run_handoff<3, 8, true, true, kHsNoIssuerFence>(nsm, pb, 64, d_cyc, d_err, &hs[1][1]) &&
+         run_handoff<2, 8, true, true, kHsNoConvFence>(nsm, pb, 64, d_cyc, d_err, &hs[2][0]) &&
+         run_handoff<3, 8, true, true, kHsNoConvFence>(nsm, pb, 64, d_cyc, d_err, &hs[2][1]) &&
+         run_handoff<2, 8, true, true, kHsClockSpin>(nsm, pb, 64, d_cyc, d_err, &hs[3][0]) &&
+         run_handoff<3, 8, true, true, kHsClockSpin>(nsm, pb, 64, d_cyc, d_err, &hs[3][1]) &&
+         run_handoff<2, 8, true, true, kHsTestWait>(nsm, pb, 64, d_cyc, d_err, &hs[4][0]) &&
+         run_handoff<3, 8, true, true, kHsTestWait>(nsm, pb, 64, d_cyc, d_err, &hs[4][1]) &&
+         run_handoff<2, 8, true, true, kHsCounter>(nsm, pb, 64, d_cyc, d_err, &hs[5][0]) &&
+         run_handoff<3, 8, true, true, kHsCounter>(nsm, pb, 64, d_cyc, d_err, &hs[5][1]) &&
+         run_handoff<2, 8, true, true, kHsConvNoWait>(nsm, pb, 64, d_cyc, d_err, &hs[6][0]) &&
+         run_handoff<3, 8, true, true, kHsConvNoWait>(nsm, pb, 64, d_cyc, d_err, &hs[6][1]) &&
+         run_handoff<2, 8, true, true, kHsIssuerNoWait>(nsm, pb, 64, d_cyc, d_err, &hs[7][0]) &&
+         run_handoff<3, 8, true, true, kHsIssuerNoWait>(nsm, pb, 64, d_cyc, d_err, &hs[7][1]);
+    // two refill groups taking alternate fills: slots 2, 3, 4 x delays
+    for (int i = 0; i < 4; ++i)
+        ok = ok && run_handoff<2, 8, true, true, kHsBase, 2>(nsm, pb, delays[i], d_cyc, d_err, &grp[0][i]) &&
+             run_handoff<3, 8, true, true, kHsBase, 2>(nsm, pb, delays[i], d_cyc, d_err, &grp[1][i]) &&
+             run_handoff<4, 8, true, true, kHsBase, 2>(nsm, pb, delays[i], d_cyc, d_err, &grp[2][i]) &&
+             run_handoff<2, 8, true, true, kHsBase, 1, 160>(nsm, pb, delays[i], d_cyc, d_err, &n160[0][i]) &&
+             run_handoff<3, 8, true, true, kHsBase, 1, 160>(nsm, pb, delays[i], d_cyc, d_err, &n160[1][i]) &&
+             run_handoff<3, 8, true, true, kHsBase, 2, 160>(nsm, pb, delays[i], d_cyc, d_err, &n160[2][i]) &&
+             run_handoff<3, 8, true, true, kHsBase, 2, 160, 2>(nsm, pb, delays[i], d_cyc, d_err, &two_iss[0][i]) &&
+             run_handoff<3, 8, true, true, kHsBase, 2, 192, 2>(nsm, pb, delays[i], d_cyc, d_err, &two_iss[1][i]) &&
+             run_handoff<2, 8, true, true, kHsBase, 2, 192, 2>(nsm, pb, delays[i], d_cyc, d_err, &two_iss[2][i]) &&
+             run_handoff<2, 8, true, true, kHsBase, 1, 192, 2>(nsm, pb, delays[i], d_cyc, d_err, &two_iss[3][i]);
+    if (!ok) {
+        fprintf(stderr, "interference launch failed: %s\n", cudaGetErrorString(cudaGetLastError()));
+        return 3;
+    }
     int h_err[4] = {};
     cudaMemcpy(h_err, d_err, sizeof(h_err), cudaMemcpyDeviceToHost);
-    printf("{\"sms\": %d, \"wait_timeouts\": %d, ", nsm, h_err[0]);
+    printf("{\"sms\": %d, \"wait_timeouts\": %d, \"pipe_errors\": %d, ", nsm, h_err[0] & 1, h_err[0] & ~1);
+    printf("\"stage_cycles_pair_n192\": {\"alone\": %.0f, \"wait_prev\": %.0f, \"wait_self\": %.0f, \"alu_warps\": %.0f, "
+           "\"tmem_st_warps\": %.0f, \"tmem_ld_warps\": %.0f", cpb[0], cpb[1], cpb[2], cpb[3], cpb[4], cpb[5]);
+    printf("}, \"handoff_cycles_per_k128_by_delay\": {\"delays\": [%d, %d, %d, %d]", delays[0], delays[1], delays[2],
+           delays[3]);
+    const char* names[6] = {"slots2_k128", "slots2_k128_no_store", "slots2_k128_local_arrivals", "slots3_k128",
+                            "slots4_k64", "slots4_k128"};
+    for (int c = 0; c < 6; ++c)
+        printf(", \"%s\": [%.0f, %.0f, %.0f, %.0f]", names[c], hof[c][0], hof[c][1], hof[c][2], hof[c][3]);
+    printf("}, \"handoff_segments_per_fill\": {\"order\": [\"issuer_wait_a_ready\", \"issuer_issue_commit\", "
+           "\"conv_wait_done\", \"conv_delay\", \"conv_store\", \"conv_arrive\"]");
+    for (int i = 0; i < 4; ++i) {
+        printf(", \"slots2_delay_%d\": [%.0f, %.0f, %.0f, %.0f, %.0f, %.0f]", delays[i], seg2[i][0], seg2[i][1],
+               seg2[i][2], seg2[i][3], seg2[i][4], seg2[i][5]);
+        printf(", \"slots3_delay_%d\": [%.0f, %.0f, %.0f, %.0f, %.0f, %.0f]", delays[i], seg3[i][0], seg3[i][1],
+               seg3[i][2], seg3[i][3], seg3[i][4], seg3[i][5]);
+    }
+    printf("}, \"handshake_variants_delay_64_slots_2_3\": {");
+    const char* hs_names[8] = {"base", "no_issuer_fence", "no_converter_fences", "clock_spin_conversion",
+                               "issuer_test_wait", "shared_counter", "converters_do_not_wait", "issuer_does_not_wait"};
+    for (int v = 0; v < 8; ++v) printf("%s\"%s\": [%.0f, %.0f]", v ? ", " : "", hs_names[v], hs[v][0], hs[v][1]);
+    printf("}, \"two_refill_groups_by_delay\": {\"slots2\": [%.0f, %.0f, %.0f, %.0f], \"slots3\": [%.0f, %.0f, %.0f, %.0f], "
+           "\"slots4\": [%.0f, %.0f, %.0f, %.0f]", grp[0][0], grp[0][1], grp[0][2], grp[0][3], grp[1][0], grp[1][1],
+           grp[1][2], grp[1][3], grp[2][0], grp[2][1], grp[2][2], grp[2][3]);
+    printf("}, \"n160_by_delay\": {\"slots2_one_group\": [%.0f, %.0f, %.0f, %.0f], \"slots3_one_group\": [%.0f, %.0f, %.0f, %.0f], "
+           "\"slots3_two_groups\": [%.0f, %.0f, %.0f, %.0f]", n160[0][0], n160[0][1], n160[0][2], n160[0][3], n160[1][0],
+           n160[1][1], n160[1][2], n160[1][3], n160[2][0], n160[2][1], n160[2][2], n160[2][3]);
+    printf("}, \"two_issuers_by_delay\": {");
+    const char* ti_names[4] = {"n160_slots3_two_groups", "n192_slots3_two_groups", "n192_slots2_two_groups",
+                               "n192_slots2_one_group"};
+    for (int c = 0; c < 4; ++c)
+        printf("%s\"%s\": [%.0f, %.0f, %.0f, %.0f]", c ? ", " : "", ti_names[c], two_iss[c][0], two_iss[c][1],
+               two_iss[c][2], two_iss[c][3]);
+    printf("}, \"trace_slots3_delay_64\": {\"fields\": [\"issuer_woke\", \"issuer_committed\", \"conv_slot_free\", "
+           "\"conv_arrived\"], \"from_fill\": %d, \"rows\": [", kTraceFrom);
+    for (int f = 0; f < kTrace; ++f)
+        printf("%s[%lld, %lld, %lld, %lld]", f ? ", " : "", trace[f * 4] - trace[0], trace[f * 4 + 1] - trace[0],
+               trace[f * 4 + 2] - trace[0], trace[f * 4 + 3] - trace[0]);
+    printf("]}, ");
     print("tcgen05_f16_int8_values_smem_a_m128_n256", r[0], false);
     print("tcgen05_f16_int8_values_tmem_a_m128_n256", r[1], false);
     print("tcgen05_f16_int8_values_pair_tmem_a_m256_n192", r[2], false);

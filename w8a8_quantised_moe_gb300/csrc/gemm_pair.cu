@@ -55,6 +55,10 @@ namespace moe {
 namespace {
 
 constexpr int kPairBK = 128;  // K per stage
+#ifndef MOE_P_EARLY
+#define MOE_P_EARLY 1
+#endif
+constexpr bool kEarlyTests = MOE_P_EARLY != 0;  // converters test the next barriers early
 
 #ifndef MOE_P_ND
 #define MOE_P_ND 2
@@ -391,16 +395,28 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreadsPerCta, 1
         const int cg = (C::kConv == 2 && warp >= kPairConv1Warp0) ? 1 : 0;
         const int row = q * 32 + lane;
         const uint32_t a_ready_leader = cluster_addr(&a_ready[0], 0);
-        uint32_t it = 0;
+        uint32_t it = 0, qs = 0, qph = 0;  // the stage and its weight-ring slot and phase parity
+        bool q_ready = false;              // the stage's weights were seen landed by the early test
         bool ok = true;
         for (int tile = cluster; ok && tile < total_tiles; tile += n_clusters) {
             for (int kb = 0; kb < nkb; ++kb, ++it) {
-                const uint32_t qs = it % NQ, bs = it % NB, j = it % C::NA;
-                if (!warp_wait(&q_full[qs], (it / NQ) & 1u, ctl)) { ok = false; break; }
+                const uint32_t bs = it % NB, j = it % C::NA;
+                if (!q_ready && !warp_wait(&q_full[qs], qph, ctl)) { ok = false; break; }
                 if (it >= (uint32_t)C::NA) {  // A slot j is free once the MMAs of stage it - NA completed
                     const uint32_t p = it - C::NA;
                     if (!warp_wait_cluster(&done[p % NB], (p / NB) & 1u, ctl)) { ok = false; break; }
                 }
+                // Early tests, answered while this stage converts: a satisfied
+                // wait still costs its latency (measured ~120-140 cycles under
+                // this kernel's load), so the next stage's weights and (group
+                // 0) this stage's activations are tested now and their waits
+                // skipped when already complete.  Neither phase can be behind
+                // the one tested: this warp consumed the weight slot's previous
+                // fill, and the activation slot's previous fill was waited
+                // on by group 0 before its previous a_ready arrival.
+                const uint32_t qs1 = qs + 1u == (uint32_t)NQ ? 0u : qs + 1u, qph1 = qs1 == 0u ? qph ^ 1u : qph;
+                const bool q_next = kEarlyTests && mbar_test(&q_full[qs1], qph1);
+                const bool b_now = kEarlyTests && cg == 0 && mbar_test(&b_full[bs], (it / NB) & 1u);
                 const uint8_t* src = smem + C::kOffQ + qs * C::kQStage + row * 128;
                 const uint32_t taddr = tmem + ((uint32_t)(q * 32) << 16) + j * C::kACols;
                 const uint32_t swz = (uint32_t)(row & 7);  // 128-byte swizzle: chunk c at c ^ (row & 7)
@@ -419,11 +435,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreadsPerCta, 1
                 // arrival below is observed: group 0's arrival follows this
                 // wait (placed after the conversion, so that activation latency
                 // overlaps it), and a_ready completes only with group 0
-                if (cg == 0 && !warp_wait(&b_full[bs], (it / NB) & 1u, ctl)) { ok = false; break; }
+                if (cg == 0 && !__all_sync(0xffffffffu, b_now) && !warp_wait(&b_full[bs], (it / NB) & 1u, ctl)) {
+                    ok = false;
+                    break;
+                }
                 tmem_wait_st();
                 tc_fence_before();
                 __syncwarp();
                 if (lane == 0) mbar_arrive_cluster(a_ready_leader + j * 8);
+                q_ready = __all_sync(0xffffffffu, q_next);
+                qs = qs1;
+                qph = qph1;
             }
         }
     } else if (warp >= kEpiWarp0 && warp < kEpiWarp0 + 4) {

@@ -69,6 +69,22 @@ struct WaitCtl {
     uint32_t peer_abort;  // shared::cluster address, or 0
 };
 
+// Non-blocking test of the phase with parity `parity` (mbarrier.test_wait:
+// the thread is never suspended).  Used to learn early, while other work is
+// in flight, whether a later wait can be skipped; a completed phase stays
+// complete until its consumer releases the resource.
+__device__ __forceinline__ bool mbar_test(uint64_t* bar, uint32_t parity) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    return ok != 0;
+}
+
 // Records a timed-out wait: aborts this CTA (and its pair peer) and sets the
 // timeout bit of the device error word.  The remote store reaches the peer
 // before either CTA passes the pair's final cluster barrier.

@@ -224,8 +224,8 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
                 __syncthreads();
                 staged_row0 = row0;
             }
-#pragma unroll 1
             constexpr int kItems = EPI == (int)Epi::GateUp ? kSkItemsGateUp : kSkItemsScale;
+#pragma unroll 1
             for (int it = 0; it < kItems; ++it) {
                 const int item = warp * kItems + it;
                 const int first = EPI == (int)Epi::GateUp ? unit * kSkUnitGateUp + item * (kSkRows / 2)

@@ -156,7 +156,11 @@ __global__ void __launch_bounds__(128, 1) tc_rate(int blocks, long long* cycles,
 //               shares the issuer's) issue independent FMAs back to back
 //   kTmemSt     four more warps store 32 columns to tensor memory in a loop
 //   kTmemLd     four more warps load 32 columns from tensor memory in a loop
-enum Load : int { kWaitPrev = 1, kWaitSelf = 2, kAlu = 3, kTmemSt = 4, kTmemLd = 5 };
+//   kSmemLd     four more warps read shared memory (16-byte loads) in a loop
+//   kSmemLdSt   four more warps read and write shared memory in a loop
+// (the pair GEMM's SM also takes its TMA writes and its converters' reads
+// through shared memory, next to the MMAs' operand reads)
+enum Load : int { kWaitPrev = 1, kWaitSelf = 2, kAlu = 3, kTmemSt = 4, kTmemLd = 5, kSmemLd = 6, kSmemLdSt = 7 };
 
 __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* err) {
     if (wait_bounded(bar, parity)) return true;
@@ -165,7 +169,8 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t parity, int* 
 }
 
 template <int LOAD>
-__global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycles, int* err) {
+__global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycles, int* err, int mma_on,
+                                                    long long* lsu_iters) {
     constexpr int N = 192;
     extern __shared__ uint8_t raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(raw) + 1023) & ~uintptr_t(1023));
@@ -210,7 +215,11 @@ __global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycle
     if (tid == 0 && rank == 0) {
         const uint64_t bd = smem_desc_sw128(smem_u32(sm));
         const long long c0 = clock64();
-        for (int blk = 0; blk < blocks; ++blk) {
+        if (!mma_on) {  // the same time without MMAs: the load warps alone
+            while (clock64() - c0 < 768ll * blocks) {
+            }
+        }
+        for (int blk = 0; mma_on && blk < blocks; ++blk) {
             const int slot = blk & 1;
             if (LOAD == kWaitPrev && blk >= 2 && !wait_phase(&done[slot], ((blk - 2) >> 1) & 1, err)) break;
             if (LOAD == kWaitSelf && blk >= 1 && !wait_phase(&done[slot ^ 1], ((blk - 1) >> 1) & 1, err)) break;
@@ -228,7 +237,7 @@ __global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycle
     }
     if (tid == 0) stop = 1;
 
-    if (warp >= 4 && LOAD >= kAlu && LOAD <= kTmemLd) {
+    if (warp >= 4 && LOAD >= kAlu && LOAD <= kSmemLdSt) {
         const uint64_t t0 = global_timer_ns();
         uint32_t r[32];
         float f[8];
@@ -236,7 +245,8 @@ __global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycle
         for (int j = 0; j < 8; ++j) f[j] = static_cast<float>(tid + j);
 #pragma unroll
         for (int j = 0; j < 32; ++j) r[j] = 0x3c003c00u;
-        for (int it = 0; !stop; ++it) {
+        int it = 0;
+        for (; !stop; ++it) {
             if (LOAD == kAlu) {
 #pragma unroll
                 for (int k = 0; k < 16; ++k)
@@ -245,9 +255,19 @@ __global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycle
             } else if (LOAD == kTmemSt) {
                 tmem_st_32(tmem + lane_base + 384 + (it & 3) * 32, r);
                 tmem_wait_st();
-            } else {
+            } else if (LOAD == kTmemLd) {
                 tmem_ld_32(tmem + lane_base + 384 + (it & 3) * 32, r);
                 tmem_wait_ld();
+            } else {
+                // a 32 KB region past the B operand (which ends at 12 KB)
+                uint4* reg = reinterpret_cast<uint4*>(sm + 16384);
+                const int base = ((warp - 4) * 32 + (tid & 31) + (it & 15) * 128) & 2047;
+#pragma unroll
+                for (int k = 0; k < 8; ++k) {
+                    const uint4 x = reg[(base + k * 256) & 2047];
+                    r[k] ^= x.x ^ x.y ^ x.z ^ x.w;
+                    if (LOAD == kSmemLdSt) reg[(base + k * 256 + 1024) & 2047] = make_uint4(r[k], x.x, x.y, x.z);
+                }
             }
             if ((it & 15) == 0 && global_timer_ns() - t0 > 2000000000ull) {
                 atomicOr(err, 4);
@@ -258,6 +278,7 @@ __global__ void __launch_bounds__(256, 1) pipe_rate(int blocks, long long* cycle
 #pragma unroll
         for (int j = 0; j < 8; ++j) acc += f[j] + __uint_as_float(r[j]);
         if (acc == 1234.5f) atomicOr(err, 8);
+        if ((tid & 31) == 0 && blockIdx.x < 64) lsu_iters[blockIdx.x * 4 + (warp - 4)] = it;
     }
     tc_fence_before();
     cluster_sync_all();
@@ -540,7 +561,8 @@ bool run_tc(int nsm, int blocks, long long* d_cyc, int* d_err, Result* out) {
 
 // cycles per 8-MMA block of the slowest issuer, for one interference case
 template <int LOAD>
-bool run_pipe(int nsm, int blocks, long long* d_cyc, int* d_err, double* cycles_per_block) {
+bool run_pipe(int nsm, int blocks, long long* d_cyc, int* d_err, double* cycles_per_block, int mma_on = 1,
+              double* lsu_bytes_per_clk = nullptr) {
     auto kern = pipe_rate<LOAD>;
     if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes) != cudaSuccess)
         return false;
@@ -558,13 +580,21 @@ bool run_pipe(int nsm, int blocks, long long* d_cyc, int* d_err, double* cycles_
         attr[0].val.clusterDim.z = 1;
         cfg.attrs = attr;
         cfg.numAttrs = 1;
-        if (cudaLaunchKernelEx(&cfg, kern, blocks, d_cyc, d_err) != cudaSuccess) return false;
+        if (cudaLaunchKernelEx(&cfg, kern, blocks, d_cyc, d_err, mma_on, d_cyc + 3072) != cudaSuccess) return false;
         if (cudaDeviceSynchronize() != cudaSuccess) return false;
     }
     if (cudaMemcpy(h, d_cyc, (grid / 2) * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
     long long mx = 1;
     for (int i = 0; i < grid / 2; ++i) mx = h[i] > mx ? h[i] : mx;
     *cycles_per_block = static_cast<double>(mx) / blocks;
+    if (lsu_bytes_per_clk) {  // the load warps of CTAs 0-63: 4 KB read (8 KB read + written) per iteration
+        long long it[256];
+        if (cudaMemcpy(it, d_cyc + 3072, 256 * sizeof(long long), cudaMemcpyDeviceToHost) != cudaSuccess) return false;
+        double tot = 0;
+        for (int i = 0; i < 256; ++i) tot += static_cast<double>(it[i]);
+        const double per_iter = LOAD == kSmemLdSt ? 8192.0 : 4096.0;
+        *lsu_bytes_per_clk = tot / 64.0 * per_iter / static_cast<double>(mx);
+    }
     return true;
 }
 
@@ -654,7 +684,15 @@ int main() {
          run_pipe<kWaitSelf>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
          run_pipe<kAlu>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
          run_pipe<kTmemSt>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
-         run_pipe<kTmemLd>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]);
+         run_pipe<kTmemLd>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kSmemLd>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]) &&
+         run_pipe<kSmemLdSt>(nsm, pb, d_cyc, d_err, &cpb[n_pipe++]);
+    // the load warps' own shared-memory rate, B/clk per SM, beside the MMA stream and alone
+    double lsu[4] = {0, 0, 0, 0}, dummy = 0;
+    ok = ok && run_pipe<kSmemLd>(nsm, pb, d_cyc, d_err, &dummy, 1, &lsu[0]) &&
+         run_pipe<kSmemLd>(nsm, pb, d_cyc, d_err, &dummy, 0, &lsu[1]) &&
+         run_pipe<kSmemLdSt>(nsm, pb, d_cyc, d_err, &dummy, 1, &lsu[2]) &&
+         run_pipe<kSmemLdSt>(nsm, pb, d_cyc, d_err, &dummy, 0, &lsu[3]);
     // A-slot pipelines: [slots x MMAs per slot, stores, remote arrivals] x conversion delays
     double hof[6][4], seg2[4][6], seg3[4][6];
     static long long trace[kTrace * 4];
@@ -705,7 +743,10 @@ int main() {
     cudaMemcpy(h_err, d_err, sizeof(h_err), cudaMemcpyDeviceToHost);
     printf("{\"sms\": %d, \"wait_timeouts\": %d, \"pipe_errors\": %d, ", nsm, h_err[0] & 1, h_err[0] & ~1);
     printf("\"stage_cycles_pair_n192\": {\"alone\": %.0f, \"wait_prev\": %.0f, \"wait_self\": %.0f, \"alu_warps\": %.0f, "
-           "\"tmem_st_warps\": %.0f, \"tmem_ld_warps\": %.0f", cpb[0], cpb[1], cpb[2], cpb[3], cpb[4], cpb[5]);
+           "\"tmem_st_warps\": %.0f, \"tmem_ld_warps\": %.0f, \"smem_ld_warps\": %.0f, \"smem_ld_st_warps\": %.0f",
+           cpb[0], cpb[1], cpb[2], cpb[3], cpb[4], cpb[5], cpb[6], cpb[7]);
+    printf("}, \"smem_bytes_per_clk_of_load_warps\": {\"ld_beside_mma\": %.1f, \"ld_alone\": %.1f, "
+           "\"ld_st_beside_mma\": %.1f, \"ld_st_alone\": %.1f", lsu[0], lsu[1], lsu[2], lsu[3]);
     printf("}, \"handoff_cycles_per_k128_by_delay\": {\"delays\": [%d, %d, %d, %d]", delays[0], delays[1], delays[2],
            delays[3]);
     const char* names[6] = {"slots2_k128", "slots2_k128_no_store", "slots2_k128_local_arrivals", "slots3_k128",

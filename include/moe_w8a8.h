@@ -53,7 +53,20 @@
  *     waiting, within the wait limit (moe_w8a8_set_wait_timeout_ns), on a
  *     barrier that nothing completes, so that the limit runs out and the
  *     kernel takes its abort path (MOE_ERR_DEVICE_TIMEOUT from
- *     moe_w8a8_device_error; outputs undefined).  Unset in normal use.
+ *     moe_w8a8_device_error; outputs undefined).  "bad_slot", honoured only
+ *     by the checked build below: after the quantiser the first slot index
+ *     is overwritten with an out-of-range value, which the combine's check
+ *     reports (MOE_ERR_DEVICE; that token's output undefined).  Unset in
+ *     normal use.
+ *
+ *   Checked build.  Compiled with -DMOE_CHECKED=1 (libmoe_w8a8_checked.so,
+ *     `python -m w8a8_quantised_moe_gb300.build --checked`), the kernels
+ *     range-check every index they take from data rather than from their
+ *     launch shape (expert ids, slots, expert offsets, exact-path lists,
+ *     gathered rows).  An index out of range sets the device error word
+ *     (MOE_ERR_DEVICE from moe_w8a8_device_error) and the access is skipped,
+ *     where the normal build would read or write out of bounds.  The same
+ *     entry points and results; a debugging aid, not the fast path.
  */
 #ifndef MOE_W8A8_H
 #define MOE_W8A8_H

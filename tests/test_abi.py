@@ -37,6 +37,19 @@ def test_library_exports_every_declared_symbol(lib):
         assert hasattr(lib, name), name
 
 
+def test_checked_build_compiles_and_exports_every_declared_symbol():
+    """The checked build (-DMOE_CHECKED=1: data-derived indices range-checked
+    in the kernels) is a separate library beside the normal one; it builds
+    and loads here, and rejects the same bad arguments on the host."""
+    checked = _lib.open_library(lib_build.build(checked=True))
+    for name in declared_functions():
+        assert hasattr(checked, name), name
+    need = checked.moe_w8a8_linear_workspace_size(64, 256, 256)
+    assert need > 0
+    assert checked.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 256, 256, FAKE, FAKE, need - 1, None) == WS_SMALL
+    assert checked.moe_w8a8_linear(FAKE, FAKE, FAKE, 64, 200, 256, FAKE, FAKE, need, None) == SHAPE
+
+
 def test_status_strings(lib):
     for code, name in _lib.STATUS.items():
         assert lib.moe_w8a8_status_string(code).decode() == name

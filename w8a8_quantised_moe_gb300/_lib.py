@@ -74,46 +74,56 @@ def load(path: str = LIB_PATH):
     with _lock:
         if _lib is not None:
             return _lib
-        if not os.path.exists(path):
-            raise ImportError(f"CUDA library not built: {path} (run __graft_entry__.build())")
-        lib = ctypes.CDLL(path)
-        i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
-        decl = {
-            "moe_w8a8_status_string": ([i32], ctypes.c_char_p),
-            "moe_w8a8_version": ([], i32),
-            "moe_w8a8_quantize_weights": ([vp, i64, i64, vp, vp, vp], i32),
-            "moe_w8a8_workspace_size": ([i64, i64, i64, i64, i64], sz),
-            "moe_w8a8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
-            "moe_w8a8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
+        _lib = open_library(path)
+        return _lib
+
+
+def open_library(path: str):
+    """A separately loaded copy of a build of the library (e.g. the checked
+    build), its C signatures declared; load() is not affected."""
+    if not os.path.exists(path):
+        raise ImportError(f"CUDA library not built: {path} (run __graft_entry__.build())")
+    lib = ctypes.CDLL(path)
+    _declare(lib)
+    return lib
+
+
+def _declare(lib) -> None:
+    i64, vp, sz, i32 = ctypes.c_int64, ctypes.c_void_p, ctypes.c_size_t, ctypes.c_int
+    decl = {
+        "moe_w8a8_status_string": ([i32], ctypes.c_char_p),
+        "moe_w8a8_version": ([], i32),
+        "moe_w8a8_quantize_weights": ([vp, i64, i64, vp, vp, vp], i32),
+        "moe_w8a8_workspace_size": ([i64, i64, i64, i64, i64], sz),
+        "moe_w8a8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
+        "moe_w8a8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
+                                    ctypes.POINTER(DebugBuffers)], i32),
+        "moe_w8a8_linear_workspace_size": ([i64, i64, i64], sz),
+        "moe_w8a8_linear": ([vp, vp, vp, i64, i64, i64, vp, vp, sz, vp], i32),
+        "moe_w8a8_device_error": ([vp, vp], i32),
+        "moe_w8a8_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_uint64),
+        "moe_w8a8_set_gemm_path": ([i32], i32),
+        "moe_w8a8_set_profile_events": ([ctypes.c_void_p, i32], i32),
+        "moe_w8a8_launch_count": ([], ctypes.c_uint64),
+        "moe_w8a8_linear_static": ([vp, vp, vp, i64, i64, i64, vp, vp], i32),
+        "moe_w8a8_linear_static_error": ([vp], i32),
+        "moe_w8a8_fp8_quantize_weights": ([vp, i64, i64, vp, vp, vp], i32),
+        "moe_w8a8_fp8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
+        "moe_w8a8_fp8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
                                         ctypes.POINTER(DebugBuffers)], i32),
-            "moe_w8a8_linear_workspace_size": ([i64, i64, i64], sz),
-            "moe_w8a8_linear": ([vp, vp, vp, i64, i64, i64, vp, vp, sz, vp], i32),
-            "moe_w8a8_device_error": ([vp, vp], i32),
-            "moe_w8a8_set_wait_timeout_ns": ([ctypes.c_uint64], ctypes.c_uint64),
-            "moe_w8a8_set_gemm_path": ([i32], i32),
-            "moe_w8a8_set_profile_events": ([ctypes.c_void_p, i32], i32),
-            "moe_w8a8_launch_count": ([], ctypes.c_uint64),
-            "moe_w8a8_linear_static": ([vp, vp, vp, i64, i64, i64, vp, vp], i32),
-            "moe_w8a8_linear_static_error": ([vp], i32),
-            "moe_w8a8_fp8_quantize_weights": ([vp, i64, i64, vp, vp, vp], i32),
-            "moe_w8a8_fp8_forward": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp], i32),
-            "moe_w8a8_fp8_forward_debug": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
-                                            ctypes.POINTER(DebugBuffers)], i32),
-            "moe_w8a8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz, vp,
-                                       vp, i32], i32),
-            "moe_w8a8_fp8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz,
-                                           vp, vp, i32], i32),
-            "moe_w8a8_host_chunks": ([i64, i64, i64, i64], i32),
-            "moe_w8a8_quantize_weights_smoothed": ([vp, i64, i64, vp, vp, vp, vp], i32),
-            "moe_w8a8_forward_smooth": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
-                                         ctypes.POINTER(DebugBuffers)], i32),
-        }
-        for name, (args, res) in decl.items():
-            fn = getattr(lib, name)
-            fn.argtypes = args
-            fn.restype = res
-        _lib = lib
-        return lib
+        "moe_w8a8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz, vp,
+                                   vp, i32], i32),
+        "moe_w8a8_fp8_forward_host": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, vp, vp, sz,
+                                       vp, vp, i32], i32),
+        "moe_w8a8_host_chunks": ([i64, i64, i64, i64], i32),
+        "moe_w8a8_quantize_weights_smoothed": ([vp, i64, i64, vp, vp, vp, vp], i32),
+        "moe_w8a8_forward_smooth": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
+                                     ctypes.POINTER(DebugBuffers)], i32),
+    }
+    for name, (args, res) in decl.items():
+        fn = getattr(lib, name)
+        fn.argtypes = args
+        fn.restype = res
 
 
 def check(status: int, what: str) -> None:

@@ -78,9 +78,10 @@ uint64_t current_timeout_ns() { return g_timeout_ns.load(); }
 bool injected(InjectFault f) {
     const char* v = std::getenv("MOE_INJECT");
     if (v == nullptr || v[0] == '\0') return false;
-    const char* name = f == kInjectWsShort ? "ws_short"
-                       : f == kInjectBadPtr ? "bad_ptr"
+    const char* name = f == kInjectWsShort      ? "ws_short"
+                       : f == kInjectBadPtr     ? "bad_ptr"
                        : f == kInjectLaunchFail ? "launch_fail"
+                       : f == kInjectBadSlot    ? "bad_slot"
                                                 : "stall";
     const size_t n = std::strlen(name);
     for (const char* p = v; *p != '\0';) {
@@ -251,17 +252,21 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     if ((e = mark(2, st)) != cudaSuccess) return from_cuda(e);
     if (fp8)
         e = launch_permute_quant_fp8(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                                     s_x, s_slot, reinterpret_cast<uint8_t*>(q_x8), st, pdl);
+                                     s_x, s_slot, reinterpret_cast<uint8_t*>(q_x8), err, st, pdl);
     else if (smooth)
         // the router's weight split is dead once the router has run: its region
         // (6 * E_pad * H >= 4 * E * H bytes) holds the smoothing reciprocals
         e = launch_permute_quant_smooth(x, smooth, reinterpret_cast<float*>(wsplit), topk_ids, rank, hist, (int)T,
                                         (int)H, (int)E, (int)k, slot_of, slot_token, s_x, s_slot,
-                                        q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
+                                        q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, err, st, pdl);
     else
         e = launch_permute_quant(x, topk_ids, rank, hist, (int)T, (int)H, (int)E, (int)k, slot_of, slot_token,
-                                 s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, st, pdl);
+                                 s_x, s_slot, q_x8 ? nullptr : q_x16, q_x8, flag1, list1, counts + 0, err, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
+    // test hook of the checked build: an out-of-range slot index for the
+    // combine's checks to catch (0x7f7f7f7f; the normal build ignores it)
+    if (kChecked && injected(kInjectBadSlot) && (e = cudaMemsetAsync(slot_of, 0x7f, 4, st)) != cudaSuccess)
+        return from_cuda(e);
 
     GemmArgs g1{};
     g1.w = w13_q;
@@ -326,7 +331,7 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     if (e != cudaSuccess) return from_cuda(e);
 
     if ((e = mark(6, st)) != cudaSuccess) return from_cuda(e);
-    e = launch_combine(o, slot_of, topk_w, (int)T, (int)H, (int)k, y, st, pdl);
+    e = launch_combine(o, slot_of, topk_w, (int)T, (int)H, (int)k, y, err, st, pdl);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(7, st)) != cudaSuccess) return from_cuda(e);
 
@@ -348,14 +353,14 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
         if (q_h8 && (e = cp(dbg->q_h, q_h8, (size_t)S * I)) != cudaSuccess) return from_cuda(e);
         if ((e = cp(dbg->s_slot, s_slot, Sb)) != cudaSuccess) return from_cuda(e);
         if (dbg->q_slot) {  // every slot's row, in slot order
-            e = q_x8 ? launch_s8_rows_gather(q_x8, nullptr, S, (int)H, 1, dbg->q_slot, st)
-                     : launch_f16_rows_to_s8(q_x16, nullptr, S, (int)H, 1, dbg->q_slot, st);
+            e = q_x8 ? launch_s8_rows_gather(q_x8, nullptr, S, (int)H, 1, S, dbg->q_slot, err, st)
+                     : launch_f16_rows_to_s8(q_x16, nullptr, S, (int)H, 1, S, dbg->q_slot, err, st);
             if (e != cudaSuccess) return from_cuda(e);
         }
         if (dbg->q_x) {
             // token t's quantised row sits in each of its slots; take the first
-            e = q_x8 ? launch_s8_rows_gather(q_x8, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st)
-                     : launch_f16_rows_to_s8(q_x16, slot_of, (int)T, (int)H, (int)k, dbg->q_x, st);
+            e = q_x8 ? launch_s8_rows_gather(q_x8, slot_of, (int)T, (int)H, (int)k, S, dbg->q_x, err, st)
+                     : launch_f16_rows_to_s8(q_x16, slot_of, (int)T, (int)H, (int)k, S, dbg->q_x, err, st);
             if (e != cudaSuccess) return from_cuda(e);
         }
     }
@@ -634,7 +639,7 @@ moe_status_t moe_w8a8_linear(const uint16_t* x, const int8_t* w_q, const float* 
     if ((e = cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st)) != cudaSuccess) return from_cuda(e);
     // the quantiser follows a memset: a plain launch; the GEMM may overlap its tail
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q8 ? nullptr : q16, q8, flag, list, counts, st, false);
+                             q8 ? nullptr : q16, q8, flag, list, counts, at<int>(workspace, L.err), st, false);
     if (e != cudaSuccess) return from_cuda(e);
     if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
     GemmArgs g{};

@@ -86,18 +86,20 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ rank,
     const int32_t* __restrict__ base, int T, int H, int E, int k, int32_t* __restrict__ slot_of,
     int32_t* __restrict__ slot_token, float* __restrict__ s_x, float* __restrict__ s_slot,
-    uint8_t* __restrict__ q8) {
+    uint8_t* __restrict__ q8, int* __restrict__ error) {
     const int lane = threadIdx.x & 31;
     const int t = blockIdx.x * 8 + (threadIdx.x >> 5);
     pdl_wait();
     pdl_trigger();
     if (t >= T) return;
-    int my_slot = t;
+    int my_slot = t;  // -1: out of range (checked build), its writes skipped
     if (lane < k) {
         const int e = topk_ids[(size_t)t * k + lane];
-        my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + lane];
+        my_slot = in_range(e, 0, E, error) ? base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + lane]
+                                           : -1;
+        if (my_slot >= 0 && !in_range(my_slot, 0, (long long)T * k, error)) my_slot = -1;
         slot_of[(size_t)t * k + lane] = my_slot;
-        slot_token[my_slot] = t;
+        if (!kChecked || my_slot >= 0) slot_token[my_slot] = t;
     }
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
     const int nv = H / 8;  // 8 bf16 per 16-byte vector
@@ -111,7 +113,7 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_kernel(
     amax = warp_max_f(amax);
     const float s = __fdiv_rn(amax, kE4m3Max);
     if (lane == 0) s_x[t] = s;
-    if (lane < k) s_slot[my_slot] = s;
+    if (lane < k && (!kChecked || my_slot >= 0)) s_slot[my_slot] = s;
     int slots[kMaxTopK];  // taken before the lanes' loop trip counts differ
 #pragma unroll
     for (int j = 0; j < kMaxTopK; ++j) slots[j] = __shfl_sync(0xffffffffu, my_slot, j);
@@ -119,7 +121,8 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_kernel(
         const uint4 v = __ldg(row + i);
         const uint2 c = make_uint2(e4m3_codes4(bf16_lo(v.x), bf16_hi(v.x), bf16_lo(v.y), bf16_hi(v.y), s),
                                    e4m3_codes4(bf16_lo(v.z), bf16_hi(v.z), bf16_lo(v.w), bf16_hi(v.w), s));
-        for (int j = 0; j < k; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = c;
+        for (int j = 0; j < k; ++j)
+            if (!kChecked || slots[j] >= 0) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = c;
     }
 }
 
@@ -168,7 +171,7 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_cta_kernel(
     const uint16_t* __restrict__ x, const int32_t* __restrict__ topk_ids, const int32_t* __restrict__ rank,
     const int32_t* __restrict__ base, int T, int H, int E, int k, int32_t* __restrict__ slot_of,
     int32_t* __restrict__ slot_token, float* __restrict__ s_x, float* __restrict__ s_slot,
-    uint8_t* __restrict__ q8) {
+    uint8_t* __restrict__ q8, int* __restrict__ error) {
     __shared__ float red[8];
     __shared__ int slots_s[kMaxTopK];
     const int tid = threadIdx.x;
@@ -178,9 +181,11 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_cta_kernel(
     if (t >= T) return;
     if (tid < k) {
         const int e = topk_ids[(size_t)t * k + tid];
-        const int my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid];
+        int my_slot = in_range(e, 0, E, error) ? base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid]
+                                               : -1;  // -1: out of range (checked build), its writes skipped
+        if (my_slot >= 0 && !in_range(my_slot, 0, (long long)T * k, error)) my_slot = -1;
         slot_of[(size_t)t * k + tid] = my_slot;
-        slot_token[my_slot] = t;
+        if (!kChecked || my_slot >= 0) slot_token[my_slot] = t;
         slots_s[tid] = my_slot;
     }
     const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
@@ -198,14 +203,15 @@ __global__ void __launch_bounds__(256) permute_quant_fp8_cta_kernel(
     amax = cta_max_f(amax, red);  // its barrier also publishes slots_s
     const float s = __fdiv_rn(amax, kE4m3Max);
     if (tid == 0) s_x[t] = s;
-    if (tid < k) s_slot[slots_s[tid]] = s;
+    if (tid < k && (!kChecked || slots_s[tid] >= 0)) s_slot[slots_s[tid]] = s;
 #pragma unroll
     for (int i = 0; i < kF8Vec; ++i) {
         const int idx = tid + 256 * i;
         if (idx >= nv) break;
         const uint2 c = make_uint2(e4m3_codes4(bf16_lo(v[i].x), bf16_hi(v[i].x), bf16_lo(v[i].y), bf16_hi(v[i].y), s),
                                    e4m3_codes4(bf16_lo(v[i].z), bf16_hi(v[i].z), bf16_lo(v[i].w), bf16_hi(v[i].w), s));
-        for (int j = 0; j < k; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = c;
+        for (int j = 0; j < k; ++j)
+            if (!kChecked || slots_s[j] >= 0) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = c;
     }
 }
 
@@ -371,12 +377,17 @@ __global__ void __launch_bounds__(kF8Threads, 1)
     pdl_trigger();
     if (warp == 2) {  // tile table: tiles of group g = ceil(rows_g / BN) * n_cb
         int carry = 0;
+        bool bad = false;  // checked build: an offset out of order or range
         for (int base = 0; base < n_groups; base += 32) {
             const int g = base + lane;
             int r0 = 0, r1 = 0;
             if (g < n_groups) {
                 r0 = args.offsets ? args.offsets[g] : 0;
                 r1 = args.offsets ? args.offsets[g + 1] : args.total_rows;
+                if (!group_rows_ok(r0, r1, args.total_rows, args.error)) {
+                    bad = true;
+                    r0 = r1 = 0;
+                }
                 row_start[g] = r0;
                 if (g == n_groups - 1) row_start[n_groups] = r1;
             }
@@ -391,6 +402,12 @@ __global__ void __launch_bounds__(kF8Threads, 1)
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) tile_start[n_groups] = carry;
+        if (kChecked && __any_sync(0xffffffffu, bad)) {  // an empty, consistent table: no tile runs
+            for (int g = lane; g <= n_groups; g += 32) {
+                row_start[g] = 0;
+                tile_start[g] = 0;
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();
@@ -601,14 +618,14 @@ cudaError_t launch_quantize_weights_fp8(const float* w, int64_t rows, int K, uin
 
 cudaError_t launch_permute_quant_fp8(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                      const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
-                                     int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, cudaStream_t st,
-                                     bool pdl) {
+                                     int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, int* error,
+                                     cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
     if ((long)T <= 8L * num_sms() && H <= 256 * 8 * kF8Vec)  // few tokens: a CTA per token
         return launch_kernel(permute_quant_fp8_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
-                             T, H, E, k, slot_of, slot_token, s_x, s_slot, q8);
+                             T, H, E, k, slot_of, slot_token, s_x, s_slot, q8, error);
     return launch_kernel(permute_quant_fp8_kernel, dim3((T + 7) / 8), dim3(256), 0, st, pdl, x, topk_ids, rank, hist,
-                         T, H, E, k, slot_of, slot_token, s_x, s_slot, q8);
+                         T, H, E, k, slot_of, slot_token, s_x, s_slot, q8, error);
 }
 
 cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t* q8, cudaStream_t st, bool pdl) {

@@ -124,13 +124,22 @@ __device__ __forceinline__ float dequant(float acc, float s_act, float s_w) {
     return __fmul_rn(__fmul_rn(acc, s_act), s_w);
 }
 
+// Checked build: whether group g's rows [r0, r1) lie within [0, total)
+// (records kErrDevice when not).  A kernel whose offsets fail it empties its
+// whole tile (or unit) table, so that no tile reads or writes outside the
+// rows, and reports the error.
+__device__ __forceinline__ bool group_rows_ok(int r0, int r1, int total, int* error) {
+    return in_range(r0, 0, (long long)r1 + 1, error) && in_range(r1, 0, (long long)total + 1, error);
+}
+
 // Exact CUDA-core path for the rows the certificate rejected: one warp per
 // (row, output channel), int32 dot products over K, spread over every warp of
 // the grid.
 template <int EPI>
 __device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_groups) {
-    const int n_fb = *args.fb_count;
+    int n_fb = *args.fb_count;
     if (n_fb <= 0) return;
+    if (!in_range(n_fb, 0, (long long)args.total_rows + 1, args.error)) n_fb = args.total_rows;
     const int lane = threadIdx.x & 31;
     const int per_row = (EPI == (int)Epi::GateUp) ? args.up_offset : args.w_rows_per_group;
     const long n_items = (long)n_fb * per_row;
@@ -140,6 +149,7 @@ __device__ void fallback_rows(const GemmArgs& args, const int* row_start, int n_
     for (long item = (long)blockIdx.x * warps + (threadIdx.x >> 5); item < n_items;
          item += (long)gridDim.x * warps) {
         const int row = args.fb_list[item / per_row];
+        if (!in_range(row, 0, args.total_rows, args.error)) continue;  // checked build
         const int n = (int)(item % per_row);
         const int g = last_le(row_start, n_groups, row);
         const __half* a = act + (size_t)row * args.K;

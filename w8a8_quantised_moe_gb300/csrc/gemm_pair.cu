@@ -256,12 +256,17 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreadsPerCta, 1
     pdl_trigger();
     if (warp == 2) {  // tile table: pair tiles of group g = ceil(rows_g / BN) * n_cp
         int carry = 0;
+        bool bad = false;  // checked build: an offset out of order or range
         for (int base = 0; base < n_groups; base += 32) {
             const int g = base + lane;
             int r0 = 0, r1 = 0;
             if (g < n_groups) {
                 r0 = args.offsets ? args.offsets[g] : 0;
                 r1 = args.offsets ? args.offsets[g + 1] : args.total_rows;
+                if (!group_rows_ok(r0, r1, args.total_rows, args.error)) {
+                    bad = true;
+                    r0 = r1 = 0;
+                }
                 row_start[g] = r0;
                 if (g == n_groups - 1) row_start[n_groups] = r1;
             }
@@ -276,6 +281,12 @@ __global__ void __cluster_dims__(2, 1, 1) __launch_bounds__(C::kThreadsPerCta, 1
             carry += __shfl_sync(0xffffffffu, incl, 31);
         }
         if (lane == 0) tile_start[n_groups] = carry;
+        if (kChecked && __any_sync(0xffffffffu, bad)) {  // an empty, consistent table: no tile runs
+            for (int g = lane; g <= n_groups; g += 32) {
+                row_start[g] = 0;
+                tile_start[g] = 0;
+            }
+        }
     }
     tc_fence_before();
     __syncthreads();

@@ -173,12 +173,17 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
 
     if (warp == 0) {  // unit table: exclusive prefix of per_group over the non-empty groups
         int carry = 0;
+        bool bad = false;  // checked build: an offset out of order or range
         for (int g0 = 0; g0 < G; g0 += 32) {
             const int g = g0 + lane;
             int r0 = 0, r1 = 0;
             if (g < G) {
                 r0 = args.offsets ? args.offsets[g] : 0;
                 r1 = args.offsets ? args.offsets[g + 1] : args.total_rows;
+                if (!group_rows_ok(r0, r1, args.total_rows, args.error)) {
+                    bad = true;
+                    r0 = r1 = 0;
+                }
                 row_start[g] = r0;
             }
             const int v = (g < G && r1 > r0) ? per_group : 0;
@@ -194,6 +199,12 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
         if (lane == 0) {
             unit_start[G] = carry;
             row_start[G] = args.offsets ? args.offsets[G] : args.total_rows;
+        }
+        if (kChecked && __any_sync(0xffffffffu, bad)) {  // an empty, consistent table: no unit runs
+            for (int g = lane; g <= G; g += 32) {
+                row_start[g] = 0;
+                unit_start[g] = 0;
+            }
         }
     }
     __syncthreads();

@@ -26,6 +26,18 @@ uint64_t current_timeout_ns();
 constexpr int kErrTimeout = 1;  // a pipeline wait ran out of time
 constexpr int kErrDevice = 2;   // a device-side consistency check failed
 
+// Checked build (-DMOE_CHECKED=1): every index a kernel takes from data
+// rather than from its launch shape (expert ids, slots, expert offsets,
+// exact-path lists, gathered rows) is range-checked before its access; an
+// index outside its range sets kErrDevice in the error word and the access
+// is skipped (or the range clamped), where the normal build would read or
+// write out of bounds.  Without the flag in_range() is the constant true and
+// the checks compile away.
+#ifndef MOE_CHECKED
+#define MOE_CHECKED 0
+#endif
+constexpr bool kChecked = MOE_CHECKED != 0;
+
 // Epilogue variants of the grouped GEMM.
 enum class Epi : int {
     GateUp = 0,    // h = silu(g) * u, fp32 out (first expert GEMM)
@@ -104,6 +116,14 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 // finishing and the next one's set-up.  The first kernel of each entry point
 // is launched without it (it then serialises like a plain launch).
 #ifdef __CUDACC__
+// Checked build: true when lo <= v < hi, else records kErrDevice (when error
+// is given) and returns false.  Always true in the normal build.
+__device__ __forceinline__ bool in_range(long long v, long long lo, long long hi, int* error) {
+    if (!kChecked || (v >= lo && v < hi)) return true;
+    if (error != nullptr) atomicOr(error, kErrDevice);
+    return false;
+}
+
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
@@ -197,7 +217,11 @@ void count_launch();
 //                within the wait limit, on a barrier that nothing completes:
 //                the limit runs out and the kernel takes its abort path (the
 //                one fault that reaches the GPU; a test of the timeout path)
-enum InjectFault : int { kInjectWsShort = 1, kInjectBadPtr = 2, kInjectLaunchFail = 4, kInjectStall = 8 };
+// kInjectBadSlot: after the quantiser, one slot index is overwritten with an
+// out-of-range value; honoured only by the checked build, whose combine
+// catches it (the normal build ignores it).
+enum InjectFault : int { kInjectWsShort = 1, kInjectBadPtr = 2, kInjectLaunchFail = 4, kInjectStall = 8,
+                         kInjectBadSlot = 16 };
 bool injected(InjectFault f);
 
 template <typename... KArgs, typename... Args>
@@ -237,7 +261,7 @@ cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int3
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
-                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, int* error, cudaStream_t st,
                                  bool pdl);
 // The same with SmoothQuant-folded activations per expert: each (token,
 // choice) row is x[t] times the reciprocals of smooth[e] ([E][H]), quantised
@@ -247,19 +271,21 @@ cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, 
                                         const int32_t* topk_ids, const int32_t* rank, const int32_t* hist, int T,
                                         int H, int E, int k, int32_t* slot_of, int32_t* slot_token, float* s_x,
                                         float* s_slot, uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
-                                        int32_t* fb_count, cudaStream_t st, bool pdl);
+                                        int32_t* fb_count, int* error, cudaStream_t st, bool pdl);
 cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q16, int8_t* q8,
                            int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st, bool pdl);
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
-                           int H, int k, uint16_t* y, cudaStream_t st, bool pdl);
+                           int H, int k, uint16_t* y, int* error, cudaStream_t st, bool pdl);
 // col_scale (optional, [K]): the row quantised is w[r][k] * col_scale[k].
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
                                     cudaStream_t st, const float* col_scale = nullptr);
+// out[r][:] = the codes of q16[row_of[r * stride]][:] (row_of == nullptr:
+// identity); src_rows bounds row_of's values (checked build).
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
-                                  int row_stride_of, int8_t* q8, cudaStream_t st);
+                                  int row_stride_of, int src_rows, int8_t* q8, int* error, cudaStream_t st);
 // out[r][:] = q8[row_of[r * stride]][:] (row_of == nullptr: identity).
 cudaError_t launch_s8_rows_gather(const int8_t* q8, const int32_t* row_of, int rows, int K, int row_stride_of,
-                                  int8_t* out, cudaStream_t st);
+                                  int src_rows, int8_t* out, int* error, cudaStream_t st);
 GemmShape choose_gemm_shape(long rows, long groups, long K);
 // choose_gemm_shape unless a test forced a path (moe_w8a8_set_gemm_path);
 // a forced Skinny falls back to the automatic choice where unsupported.
@@ -279,8 +305,8 @@ cudaError_t launch_grouped_gemm_skinny(Epi epi, const GemmArgs& args, cudaStream
 cudaError_t launch_quantize_weights_fp8(const float* w, int64_t rows, int K, uint8_t* q, float* s, cudaStream_t st);
 cudaError_t launch_permute_quant_fp8(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                      const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
-                                     int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, cudaStream_t st,
-                                     bool pdl);
+                                     int32_t* slot_token, float* s_x, float* s_slot, uint8_t* q8, int* error,
+                                     cudaStream_t st, bool pdl);
 cudaError_t launch_requant_fp8(const float* h, int S, int I, float* s_h, uint8_t* q8, cudaStream_t st, bool pdl);
 cudaError_t launch_grouped_gemm_fp8(Epi epi, const GemmArgs& args, cudaStream_t st, bool pdl);
 

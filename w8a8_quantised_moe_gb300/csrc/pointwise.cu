@@ -179,7 +179,8 @@ template <int KMAX>  // k <= KMAX (register budget of the loads in flight)
 __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ o,
                                                       const int32_t* __restrict__ slot_of,
                                                       const float* __restrict__ topk_w, int T,
-                                                      int H, int k, uint16_t* __restrict__ y) {
+                                                      int H, int k, uint16_t* __restrict__ y,
+                                                      int* __restrict__ error) {
     const int t = blockIdx.x;
     pdl_wait();
     pdl_trigger();
@@ -187,7 +188,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
     __shared__ int32_t slot[kMaxTopK];
     __shared__ float w[kMaxTopK];
     if (threadIdx.x < k) {
-        slot[threadIdx.x] = slot_of[(size_t)t * k + threadIdx.x];
+        const int sl = slot_of[(size_t)t * k + threadIdx.x];
+        // checked build: a slot out of range contributes nothing (-1)
+        slot[threadIdx.x] = in_range(sl, 0, (long long)T * k, blockIdx.y == 0 ? error : nullptr) ? sl : -1;
         w[threadIdx.x] = topk_w[(size_t)t * k + threadIdx.x];
     }
     __syncthreads();
@@ -196,7 +199,9 @@ __global__ void __launch_bounds__(256) combine_kernel(const float* __restrict__ 
         float4 v[KMAX];
 #pragma unroll
         for (int j = 0; j < KMAX; ++j)  // independent loads first
-            if (j < k) v[j] = reinterpret_cast<const float4*>(o + (size_t)slot[j] * H)[i];
+            if (j < k)
+                v[j] = (!kChecked || slot[j] >= 0) ? reinterpret_cast<const float4*>(o + (size_t)slot[j] * H)[i]
+                                                   : make_float4(0.f, 0.f, 0.f, 0.f);
         float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
 #pragma unroll
         for (int j = 0; j < KMAX; ++j) {  // then the sum in top-k order
@@ -267,19 +272,23 @@ __global__ void __launch_bounds__(256) quantize_weights_kernel(const float* __re
 
 // q8[r][:] = int8(q16[row_of[r * stride]][:]) (row_of == nullptr: identity).
 __global__ void f16_rows_to_s8_kernel(const uint16_t* __restrict__ q16, const int32_t* __restrict__ row_of,
-                                      int rows, int K, int stride, int8_t* __restrict__ q8) {
+                                      int rows, int K, int stride, int src_rows, int8_t* __restrict__ q8,
+                                      int* __restrict__ error) {
     const int r = blockIdx.x;
     if (r >= rows) return;
     const int src = row_of ? row_of[(size_t)r * stride] : r;
+    if (!in_range(src, 0, src_rows, threadIdx.x == 0 ? error : nullptr)) return;  // checked build
     for (int i = threadIdx.x; i < K; i += blockDim.x)
         q8[(size_t)r * K + i] = (int8_t)__half2int_rn(__ushort_as_half(q16[(size_t)src * K + i]));
 }
 
 __global__ void s8_rows_gather_kernel(const int8_t* __restrict__ q8, const int32_t* __restrict__ row_of, int rows,
-                                      int K, int stride, int8_t* __restrict__ out) {
+                                      int K, int stride, int src_rows, int8_t* __restrict__ out,
+                                      int* __restrict__ error) {
     const int r = blockIdx.x;
     if (r >= rows) return;
     const int src = row_of ? row_of[(size_t)r * stride] : r;
+    if (!in_range(src, 0, src_rows, threadIdx.x == 0 ? error : nullptr)) return;  // checked build
     const uint4* s = reinterpret_cast<const uint4*>(q8 + (size_t)src * K);
     uint4* d = reinterpret_cast<uint4*>(out + (size_t)r * K);
     for (int i = threadIdx.x; i < K / 16; i += blockDim.x) d[i] = s[i];
@@ -288,9 +297,9 @@ __global__ void s8_rows_gather_kernel(const int8_t* __restrict__ q8, const int32
 }  // namespace
 
 cudaError_t launch_s8_rows_gather(const int8_t* q8, const int32_t* row_of, int rows, int K, int row_stride_of,
-                                  int8_t* out, cudaStream_t st) {
+                                  int src_rows, int8_t* out, int* error, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    s8_rows_gather_kernel<<<rows, 256, 0, st>>>(q8, row_of, rows, K, row_stride_of, out);
+    s8_rows_gather_kernel<<<rows, 256, 0, st>>>(q8, row_of, rows, K, row_stride_of, src_rows, out, error);
     return cudaGetLastError();
 }
 
@@ -314,16 +323,16 @@ cudaError_t launch_requant(const float* h, int S, int I, float* s_h, uint16_t* q
 }
 
 cudaError_t launch_combine(const float* o, const int32_t* slot_of, const float* topk_w, int T,
-                           int H, int k, uint16_t* y, cudaStream_t st, bool pdl) {
+                           int H, int k, uint16_t* y, int* error, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
     const int blocks = (H / 4 + 255) / 256;
     int split = (4 * num_sms() + T - 1) / T;
     if (split > blocks) split = blocks;
     if (split < 1) split = 1;
     const dim3 grid(T, split), block(256);
-    if (k <= 2) return launch_kernel(combine_kernel<2>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
-    if (k <= 4) return launch_kernel(combine_kernel<4>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
-    return launch_kernel(combine_kernel<kMaxTopK>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y);
+    if (k <= 2) return launch_kernel(combine_kernel<2>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y, error);
+    if (k <= 4) return launch_kernel(combine_kernel<4>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y, error);
+    return launch_kernel(combine_kernel<kMaxTopK>, grid, block, 0, st, pdl, o, slot_of, topk_w, T, H, k, y, error);
 }
 
 cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t* q, float* s,
@@ -340,9 +349,9 @@ cudaError_t launch_quantize_weights(const float* w, int64_t rows, int K, int8_t*
 }
 
 cudaError_t launch_f16_rows_to_s8(const uint16_t* q16, const int32_t* row_of, int rows, int K,
-                                  int row_stride_of, int8_t* q8, cudaStream_t st) {
+                                  int row_stride_of, int src_rows, int8_t* q8, int* error, cudaStream_t st) {
     if (rows == 0) return cudaSuccess;
-    f16_rows_to_s8_kernel<<<rows, 256, 0, st>>>(q16, row_of, rows, K, row_stride_of, q8);
+    f16_rows_to_s8_kernel<<<rows, 256, 0, st>>>(q16, row_of, rows, K, row_stride_of, src_rows, q8, error);
     return cudaGetLastError();
 }
 

@@ -144,7 +144,8 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
-    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count,
+    int* __restrict__ error) {
     static_assert(WPT == 1 || WPT == 2 || WPT == 4 || WPT == 8, "warps per token");
     __shared__ float red_max[kPqWarps];
     __shared__ int red_l1[kPqWarps];
@@ -155,13 +156,15 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     pdl_trigger();
     if (WPT == 1 && t >= T) return;
     const bool live = t < T;  // with WPT > 1 every warp reaches the block barriers
-    int my_slot = t;
+    int my_slot = t;  // -1: out of range (checked build), its writes skipped
     if (live && topk_ids != nullptr && lane < k) {
         const int e = topk_ids[(size_t)t * k + lane];
-        my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + lane];
+        my_slot = in_range(e, 0, E, error) ? base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + lane]
+                                           : -1;
+        if (my_slot >= 0 && !in_range(my_slot, 0, (long long)T * k, error)) my_slot = -1;
         if (sub == 0) {
             slot_of[(size_t)t * k + lane] = my_slot;
-            slot_token[my_slot] = t;
+            if (!kChecked || my_slot >= 0) slot_token[my_slot] = t;
         }
     }
     const int nk = (topk_ids != nullptr) ? k : 1;
@@ -181,7 +184,7 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
     const float s = __fdiv_rn(amax, 127.0f);
     if (live && sub == 0) {
         if (lane == 0) s_x[t] = s;
-        if (lane < nk) s_slot[my_slot] = s;
+        if (lane < nk && (!kChecked || my_slot >= 0)) s_slot[my_slot] = s;
     }
     int slots[kMaxTopK];  // slot j of the token is lane j's my_slot (taken before the lanes diverge)
 #pragma unroll
@@ -192,11 +195,13 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
         quant8(__ldg(row + i), s, q, l1);
         if (q16 != nullptr) {
             const uint4 ov = pack_codes_f16(q);
-            for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
+            for (int j = 0; j < nk; ++j)
+                if (!kChecked || slots[j] >= 0) reinterpret_cast<uint4*>(q16 + (size_t)slots[j] * H)[i] = ov;
         }
         if (q8 != nullptr) {
             const uint2 ov8 = pack_codes_s8(q);
-            for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = ov8;
+            for (int j = 0; j < nk; ++j)
+                if (!kChecked || slots[j] >= 0) reinterpret_cast<uint2*>(q8 + (size_t)slots[j] * H)[i] = ov8;
         }
     }
 #pragma unroll
@@ -210,7 +215,7 @@ __global__ void __launch_bounds__(32 * kPqWarps, 8) permute_quant_kernel(
         for (int w = 0; w < WPT; ++w) l1 += red_l1[warp + w];
     }
     const int flagged = l1 > kExactL1 ? 1 : 0;
-    if (live && lane < nk) {
+    if (live && lane < nk && (!kChecked || my_slot >= 0)) {
         flags[my_slot] = flagged;
         if (flagged) fb_list[atomicAdd(fb_count, 1)] = my_slot;
     }
@@ -225,7 +230,8 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8,
-    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    int32_t* __restrict__ flags, int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count,
+    int* __restrict__ error) {
     __shared__ float red_max[8];
     __shared__ int red_l1[8];
     __shared__ int slots_s[kMaxTopK];
@@ -236,12 +242,14 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
     if (t >= T) return;
     const int nk = (topk_ids != nullptr) ? k : 1;
     if (tid < nk) {
-        int my_slot = t;
+        int my_slot = t;  // -1: out of range (checked build), its writes skipped
         if (topk_ids != nullptr) {
             const int e = topk_ids[(size_t)t * k + tid];
-            my_slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid];
+            my_slot = in_range(e, 0, E, error) ? base[(size_t)(t / kRouterTokens) * E + e] + rank[(size_t)t * k + tid]
+                                               : -1;
+            if (my_slot >= 0 && !in_range(my_slot, 0, (long long)T * k, error)) my_slot = -1;
             slot_of[(size_t)t * k + tid] = my_slot;
-            slot_token[my_slot] = t;
+            if (!kChecked || my_slot >= 0) slot_token[my_slot] = t;
         }
         slots_s[tid] = my_slot;
     }
@@ -269,7 +277,7 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (tid == 0) s_x[t] = s;
-    if (tid < nk) s_slot[slots_s[tid]] = s;
+    if (tid < nk && (!kChecked || slots_s[tid] >= 0)) s_slot[slots_s[tid]] = s;
     int l1 = 0;
 #pragma unroll
     for (int i = 0; i < kPqVec; ++i) {
@@ -279,11 +287,13 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
         quant8(v[i], s, q, l1);
         if (q16 != nullptr) {
             const uint4 ov = pack_codes_f16(q);
-            for (int j = 0; j < nk; ++j) reinterpret_cast<uint4*>(q16 + (size_t)slots_s[j] * H)[idx] = ov;
+            for (int j = 0; j < nk; ++j)
+                if (!kChecked || slots_s[j] >= 0) reinterpret_cast<uint4*>(q16 + (size_t)slots_s[j] * H)[idx] = ov;
         }
         if (q8 != nullptr) {
             const uint2 ov8 = pack_codes_s8(q);
-            for (int j = 0; j < nk; ++j) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = ov8;
+            for (int j = 0; j < nk; ++j)
+                if (!kChecked || slots_s[j] >= 0) reinterpret_cast<uint2*>(q8 + (size_t)slots_s[j] * H)[idx] = ov8;
         }
     }
 #pragma unroll
@@ -295,8 +305,10 @@ __global__ void __launch_bounds__(256) permute_quant_cta_kernel(
 #pragma unroll
         for (int i = 0; i < 8; ++i) tot += red_l1[i];
         const int flagged = tot > kExactL1 ? 1 : 0;
-        flags[slots_s[tid]] = flagged;
-        if (flagged) fb_list[atomicAdd(fb_count, 1)] = slots_s[tid];
+        if (!kChecked || slots_s[tid] >= 0) {
+            flags[slots_s[tid]] = flagged;
+            if (flagged) fb_list[atomicAdd(fb_count, 1)] = slots_s[tid];
+        }
     }
 }
 
@@ -334,7 +346,7 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
-    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count, int* __restrict__ error) {
     const int lane = threadIdx.x & 31;
     const int64_t c = (int64_t)blockIdx.x * 8 + (threadIdx.x >> 5);  // choice t * k + j
     pdl_wait();
@@ -342,7 +354,9 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_kernel(
     if (c >= (int64_t)T * k) return;
     const int t = (int)(c / k);
     const int e = topk_ids[c];
+    if (!in_range(e, 0, E, error)) return;  // checked build: the choice is skipped
     const int slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[c];
+    if (!in_range(slot, 0, (long long)T * k, error)) return;
     if (lane == 0) {
         slot_of[c] = slot;
         slot_token[slot] = t;
@@ -401,7 +415,7 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
     const int32_t* __restrict__ rank, const int32_t* __restrict__ base, int T, int H, int E, int k,
     int32_t* __restrict__ slot_of, int32_t* __restrict__ slot_token, float* __restrict__ s_x,
     float* __restrict__ s_slot, uint16_t* __restrict__ q16, int8_t* __restrict__ q8, int32_t* __restrict__ flags,
-    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count) {
+    int32_t* __restrict__ fb_list, int32_t* __restrict__ fb_count, int* __restrict__ error) {
     __shared__ float red_max[8];
     __shared__ int red_l1[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -411,7 +425,9 @@ __global__ void __launch_bounds__(256) permute_quant_smooth_cta_kernel(
     if (c >= (int64_t)T * k) return;
     const int t = (int)(c / k);
     const int e = topk_ids[c];
+    if (!in_range(e, 0, E, error)) return;  // checked build: the choice is skipped (CTA-uniform)
     const int slot = base[(size_t)(t / kRouterTokens) * E + e] + rank[c];
+    if (!in_range(slot, 0, (long long)T * k, error)) return;
     if (tid == 0) {
         slot_of[c] = slot;
         slot_token[slot] = t;
@@ -494,7 +510,7 @@ cudaError_t launch_scan(int32_t* hist, int nchunk, int E, int32_t* offsets, int3
 cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, const int32_t* rank,
                                  const int32_t* hist, int T, int H, int E, int k, int32_t* slot_of,
                                  int32_t* slot_token, float* s_x, float* s_slot, uint16_t* q16, int8_t* q8,
-                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, cudaStream_t st,
+                                 int32_t* flags, int32_t* fb_list, int32_t* fb_count, int* error, cudaStream_t st,
                                  bool pdl) {
     if (T == 0) return cudaSuccess;
     // few tokens: one CTA per token (measured at T = 8192: a warp per token
@@ -504,7 +520,7 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
 #endif
     if ((long)T <= (long)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kPqVec)
         return launch_kernel(permute_quant_cta_kernel, dim3(T), dim3(256), 0, st, pdl, x, topk_ids, rank, hist, T,
-                             H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+                             H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count, error);
     // warps per token: about four 16-byte vectors per lane (measured on the
     // three layer shapes, quantiser time in us for 1 / 2 / 4 / 8 warps per
     // token: H = 4096, T = 4096, one slot: 34.1 / 31.8 / 27.9 / 29.3;
@@ -519,29 +535,29 @@ cudaError_t launch_permute_quant(const uint16_t* x, const int32_t* topk_ids, con
     const dim3 grid((unsigned)(((long)T * wpt + kPqWarps - 1) / kPqWarps)), block(32 * kPqWarps);
     if (wpt == 8)
         return launch_kernel(permute_quant_kernel<8>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
-                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count, error);
     if (wpt == 4)
         return launch_kernel(permute_quant_kernel<4>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
-                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count, error);
     if (wpt == 2)
         return launch_kernel(permute_quant_kernel<2>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
-                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+                             slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count, error);
     return launch_kernel(permute_quant_kernel<1>, grid, block, 0, st, pdl, x, topk_ids, rank, hist, T, H, E, k,
-                         slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count);
+                         slot_of, slot_token, s_x, s_slot, q16, q8, flags, fb_list, fb_count, error);
 }
 
 cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, float* rcp,
                                         const int32_t* topk_ids, const int32_t* rank, const int32_t* hist, int T,
                                         int H, int E, int k, int32_t* slot_of, int32_t* slot_token, float* s_x,
                                         float* s_slot, uint16_t* q16, int8_t* q8, int32_t* flags, int32_t* fb_list,
-                                        int32_t* fb_count, cudaStream_t st, bool pdl) {
+                                        int32_t* fb_count, int* error, cudaStream_t st, bool pdl) {
     if (T == 0) return cudaSuccess;
     const int64_t n = (int64_t)T * k;
     // few slots: a CTA per slot (as the plain quantiser's threshold), reciprocals formed in place
     if (n <= (int64_t)MOE_PQ_CTA_TOKENS_PER_SM * num_sms() && H <= 256 * 8 * kSmVec)
         return launch_kernel(permute_quant_smooth_cta_kernel, dim3((unsigned)n), dim3(256), 0, st, pdl, x, smooth,
                              topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
-                             fb_list, fb_count);
+                             fb_list, fb_count, error);
     // many slots: the reciprocal table once, then a warp per slot
     const int64_t n4 = (int64_t)E * H / 4;
     int64_t blocks = (n4 + 255) / 256;
@@ -550,7 +566,7 @@ cudaError_t launch_permute_quant_smooth(const uint16_t* x, const float* smooth, 
     if (e != cudaSuccess) return e;
     return launch_kernel(permute_quant_smooth_kernel, dim3((unsigned)((n + 7) / 8)), dim3(256), 0, st, pdl, x, rcp,
                          topk_ids, rank, hist, T, H, E, k, slot_of, slot_token, s_x, s_slot, q16, q8, flags,
-                         fb_list, fb_count);
+                         fb_list, fb_count, error);
 }
 
 }  // namespace moe

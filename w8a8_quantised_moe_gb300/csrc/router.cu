@@ -349,7 +349,7 @@ __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, 
         if (t < T && lane < k) {
             topk_ids[(size_t)t * k + lane] = my_e[r];
             topk_w[(size_t)t * k + lane] = my_w[r];
-            atomicOr(&mask[my_e[r]], 1u << (warp * 4 + r));
+            if (in_range(my_e[r], 0, E, error)) atomicOr(&mask[my_e[r]], 1u << (warp * 4 + r));
         }
     }
     __syncthreads();
@@ -358,7 +358,7 @@ __device__ __forceinline__ void topk_chunk(const float* __restrict__ P, int KS, 
         const int r = i / k, t = t0 + r;
         if (t < T) {
             const int e = topk_ids[(size_t)t * k + (i % k)];
-            rank[(size_t)t * k + (i % k)] = __popc(mask[e] & ((1u << r) - 1u));
+            rank[(size_t)t * k + (i % k)] = in_range(e, 0, E, error) ? __popc(mask[e] & ((1u << r) - 1u)) : 0;
         }
     }
     for (int e = tid; e < E; e += 256) hist[(size_t)chunk * E + e] = __popc(mask[e]);
@@ -579,13 +579,14 @@ __global__ void __launch_bounds__(256) router_finish_kernel(const float* __restr
     for (int i = tid; i < T * k; i += 256) {
         const int tk = i / k;
         const int e = __ldcg(topk_ids + i);
-        atomicOr(&mask[(tk / kRouterTokens) * E + e], 1u << (tk % kRouterTokens));
+        if (in_range(e, 0, E, error)) atomicOr(&mask[(tk / kRouterTokens) * E + e], 1u << (tk % kRouterTokens));
     }
     __syncthreads();
     for (int i = tid; i < T * k; i += 256) {
         const int tk = i / k;
         const int e = __ldcg(topk_ids + i);
-        rank[i] = __popc(mask[(tk / kRouterTokens) * E + e] & ((1u << (tk % kRouterTokens)) - 1u));
+        rank[i] = in_range(e, 0, E, error) ? __popc(mask[(tk / kRouterTokens) * E + e] & ((1u << (tk % kRouterTokens)) - 1u))
+                                           : 0;
     }
     // per expert: first slot of each chunk relative to the expert, and its total
     int32_t tot = 0;

@@ -84,7 +84,7 @@ extern "C" moe_status_t moe_w8a8_linear_static(const uint16_t* x, const int8_t* 
     // clears it.
     if (cudaMemsetAsync(counts, 0, 2 * sizeof(int32_t), st) != cudaSuccess) return MOE_ERR_CUDA;
     e = launch_permute_quant(x, nullptr, nullptr, nullptr, (int)M, (int)K, 1, 1, nullptr, nullptr, s_x, s_x,
-                             q8 ? nullptr : q16, q8, flag, list, counts, st, false);
+                             q8 ? nullptr : q16, q8, flag, list, counts, err, st, false);
     if (e != cudaSuccess) return MOE_ERR_CUDA;
     GemmArgs g{};
     g.w = w_q;

@@ -37,6 +37,7 @@ METRIC = "W8A8 MoE layer tokens/s at 1 GB300; % of INT8-tensor / HBM roofline"
 L2_FLUSH_BYTES = 256 << 20
 STAGES = ["router_topk", "scan", "permute_quant", "gemm1_gateup", "requant", "gemm2_down", "combine"]
 LIN_STAGES = ["quant", "gemm"]
+FUSED_STAGES = ["fused_layer"]
 
 
 def parse_args(argv=None):
@@ -49,6 +50,8 @@ def parse_args(argv=None):
     p.add_argument("--format", default="int8", choices=["int8", "fp8", "int8-smooth"],
                    help="int8: the W8A8 INT8 layer; fp8: its E4M3 variant; int8-smooth: the INT8 layer with "
                         "SmoothQuant-folded activations, per-expert factors (MoE configs only)")
+    p.add_argument("--fused", action="store_true",
+                   help="the INT8 MoE layer as one persistent kernel (moe_w8a8_forward_fused; T <= 128)")
     p.add_argument("--seed", type=int, default=0)
     p.add_argument("--cpu-seconds", type=float, default=12.0, help="target CPU time of the oracle sample")
     p.add_argument("--no-cpu-baseline", action="store_true")
@@ -327,7 +330,8 @@ def layer_roofline_us(cfg, offsets, peaks, fmt="int8"):
 
 
 GEMM_SOURCES = {
-    "int8": ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
+    "int8": ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_skinny.cuh", "gemm_common.cuh", "ptx.cuh",
+             "internal.h"),
     "fp8": ("fp8.cu", "gemm_fp8_pair.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
 }
 
@@ -381,6 +385,8 @@ def run_ours(args, ranks: Ranks):
     fmt = args.format
     if linear and fmt != "int8":
         raise SystemExit(f"--format {fmt} applies to the MoE configs")
+    if args.fused and (linear or fmt != "int8" or not moe.fused_supported(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)):
+        raise SystemExit("--fused takes an INT8 MoE config that moe_w8a8_fused_supported accepts (T <= 128)")
     if fmt == "int8-smooth":
         smooth_dev = torch.from_numpy(wl.smoothing_factors(cfg, args.seed + ranks.rank)).to(dev)
 
@@ -389,6 +395,11 @@ def run_ours(args, ranks: Ranks):
 
         def fwd_debug(*a, fields=None, **kw):
             return moe.forward_smooth(*a[:3], smooth_dev, *a[3:], fields=fields, **kw)
+    elif args.fused:
+        fwd = moe.forward_fused
+
+        def fwd_debug(*a, fields=None, **kw):
+            return moe.forward_fused(*a, fields=fields, **kw)
     else:
         fwd = moe.fp8_forward if fmt == "fp8" else moe.forward
         fwd_debug = moe.fp8_forward_debug if fmt == "fp8" else moe.forward_debug
@@ -416,7 +427,7 @@ def run_ours(args, ranks: Ranks):
 
         def step(xin, out):
             return fwd(xin, Wr, bias, w13_q, w13_s, w2_q, w2_s, cfg.k, workspace=ws, out=out)
-        stage_names = STAGES
+        stage_names = FUSED_STAGES if args.fused else STAGES
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
     lib = moe._lib.load()
 
@@ -492,6 +503,9 @@ def run_ours(args, ranks: Ranks):
 
     # dominant kernel and its roofline
     work = algorithmic_work(cfg, offsets, peaks)
+    if args.fused:  # one kernel: the whole layer's bytes and flops
+        _, _, lb, lf = layer_roofline_us(cfg, offsets, peaks, fmt)
+        work = {"fused_layer": {"flops": lf, "bytes": lb}}
     dom = max(work, key=lambda k: stage_ms[k])
     dom_ms = stage_ms[dom]
     w = work[dom]
@@ -592,6 +606,9 @@ def run_ours(args, ranks: Ranks):
         "gpu_launches": int(launches),
         "clocks": clocks.summary(),
     }
+    if args.fused:
+        out["config"]["layer_kernel"] = "one persistent cooperative kernel (moe_w8a8_forward_fused)"
+        out["e2e"]["note"] = "through moe_w8a8_forward_host (the multi-kernel layer; no host entry for the fused one)"
     if not linear:
         out["config"]["touched_experts"] = int((np.diff(offsets) > 0).sum())
         out["config"]["top12_share"] = float(np.sort(shares)[::-1][:12].sum())

@@ -198,6 +198,38 @@ MOE_W8A8_API moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float*
                                     const moe_w8a8_debug_t* dbg);
 
 /* ---------------------------------------------------------------------------
+ * moe_w8a8_forward_fused -- the same layer for few tokens as ONE persistent
+ * kernel ("Tencent Hunyuan AI Infra on Hopper", section 1.3: gate, top-k,
+ * routing pre-processing, both expert GEMMs and the weighted aggregation in
+ * one fused operator).  Router, top-k and routing tables, per-token
+ * quantisation, gate/up GEMM with its epilogue, requantisation, down GEMM and
+ * combine run as phases of one cooperative launch separated by grid-wide
+ * barriers, with the arithmetic of moe_w8a8_forward: y and every
+ * intermediate equal moe_w8a8_forward's bit for bit.
+ *
+ * Arguments, workspace (moe_w8a8_workspace_size) and errors as
+ * moe_w8a8_forward_debug; `dbg` may be NULL.  Shapes: those for which
+ * moe_w8a8_fused_supported returns 1 (T <= 128, I <= 8192, and the decode
+ * GEMM's unit shapes: I a multiple of 16 and H of 64); others return
+ * MOE_ERR_UNSUPPORTED_SHAPE.  One launch on `stream` (plus the copies into
+ * `dbg`); it occupies every SM until it ends.  Every barrier wait is bounded
+ * by moe_w8a8_set_wait_timeout_ns: one that runs out makes every CTA skip the
+ * remaining phases (y is then undefined) and is reported by
+ * moe_w8a8_device_error as MOE_ERR_DEVICE_TIMEOUT.  MOE_INJECT=stall makes
+ * one CTA skip a barrier arrival, so that the limit runs out.
+ * ------------------------------------------------------------------------- */
+MOE_W8A8_API moe_status_t moe_w8a8_forward_fused(const uint16_t* x, const float* router_w,
+                                    const float* router_bias, const int8_t* w13_q,
+                                    const float* w13_scale, const int8_t* w2_q,
+                                    const float* w2_scale, int64_t T, int64_t H, int64_t I,
+                                    int64_t E, int64_t top_k, uint16_t* y, void* workspace,
+                                    size_t workspace_bytes, void* stream,
+                                    const moe_w8a8_debug_t* dbg);
+
+/* 1 if moe_w8a8_forward_fused takes the shape, else 0. */
+MOE_W8A8_API int moe_w8a8_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k);
+
+/* ---------------------------------------------------------------------------
  * moe_w8a8_linear -- one W8A8 linear layer, the dense form of the expert
  * GEMM: per-token dynamic quantisation of x, exact INT8 GEMM, and the
  * per-token x per-channel scale outer product in the epilogue

@@ -226,6 +226,38 @@ def test_injected_faults_take_each_host_error_path(lib, monkeypatch):
     assert _fwd(lib, T=0) == OK
 
 
+def _fused(lib, T=16, H=256, I=512, E=8, k=2, ptrs=None, ws_bytes=None):
+    p = dict(x=FAKE, rw=FAKE, w13=FAKE, s13=FAKE, w2=FAKE, s2=FAKE, y=FAKE, ws=FAKE)
+    p.update(ptrs or {})
+    need = lib.moe_w8a8_workspace_size(T, H, I, E, k)
+    return lib.moe_w8a8_forward_fused(p["x"], p["rw"], None, p["w13"], p["s13"], p["w2"], p["s2"], T, H, I, E, k,
+                                      p["y"], p["ws"], need if ws_bytes is None else ws_bytes, None, None)
+
+
+def test_fused_layer_shapes_and_argument_checks(lib, monkeypatch):
+    ok = lib.moe_w8a8_fused_supported
+    assert ok(1, 256, 128, 1, 1) and ok(64, 4096, 1536, 64, 2) and ok(128, 7168, 2048, 256, 8)
+    assert not ok(129, 4096, 1536, 64, 2)     # more tokens than the few-token router takes
+    assert not ok(64, 4096, 16384, 64, 2)     # a row of h beyond one CTA's registers
+    assert not ok(64, 4096, 1544, 64, 2)      # not a shape of the forward at all
+    assert not ok(64, 4032, 1536, 64, 2)      # H not a multiple of 128
+    assert not ok(0, 4096, 1536, 64, 2)
+    assert _fused(lib, T=129) == SHAPE
+    assert _fused(lib, I=16384) == SHAPE
+    assert _fused(lib, T=0) == OK  # no tokens: nothing is launched
+    for name in ("x", "rw", "w13", "s13", "w2", "s2", "y", "ws"):
+        assert _fused(lib, ptrs={name: None}) == INVALID, name
+        assert _fused(lib, ptrs={name: FAKE + 4}) == INVALID, name
+    assert _fused(lib, ptrs={"ws": FAKE + 16}) == INVALID
+    assert _fused(lib, ws_bytes=1024) == WS_SMALL
+    monkeypatch.setenv("MOE_INJECT", "ws_short")
+    assert _fused(lib) == WS_SMALL
+    monkeypatch.setenv("MOE_INJECT", "bad_ptr")
+    assert _fused(lib) == INVALID
+    monkeypatch.setenv("MOE_INJECT", "launch_fail")
+    assert _fused(lib) == CUDA
+
+
 def test_fp8_layer_refuses_a_forced_int8_kernel(lib):
     T, H, I, E, k = 16, 256, 512, 8, 2
     need = lib.moe_w8a8_workspace_size(T, H, I, E, k)

@@ -20,7 +20,8 @@ from ._lib import MoeError, STATUS
 
 __all__ = [
     "MoeError", "STATUS", "quantize_weights", "workspace_size", "new_workspace", "forward", "forward_debug",
-    "forward_host", "host_chunks", "quantize_weights_smoothed", "forward_smooth", "linear_workspace_size", "linear",
+    "forward_host", "host_chunks", "quantize_weights_smoothed", "forward_smooth", "forward_fused",
+    "fused_supported", "linear_workspace_size", "linear",
     "device_error", "set_wait_timeout_ns", "set_gemm_path", "GEMM_PATHS", "version",
     "fp8_quantize_weights", "fp8_forward", "fp8_forward_debug", "fp8_forward_host",
 ]
@@ -237,6 +238,38 @@ def forward_debug(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, to
     return y, out
 
 
+
+def fused_supported(T, H, I, E, top_k) -> bool:
+    """Whether ``forward_fused`` takes the shape (few tokens: T <= 128)."""
+    return bool(_lib.load().moe_w8a8_fused_supported(T, H, I, E, top_k))
+
+
+def forward_fused(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k, fields=(), workspace=None,
+                  out=None, stream=None):
+    """The MoE layer as one persistent kernel (few tokens; see
+    include/moe_w8a8.h): the same result as ``forward`` bit for bit.  Returns
+    y, or (y, dict of the intermediates named in ``fields``) when ``fields``
+    is given (None: all)."""
+    torch = _torch()
+    T, H, I, E = _forward_args(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, top_k)
+    if workspace is None:
+        workspace = new_workspace(workspace_size(T, H, I, E, top_k), x.device)
+    y = out if out is not None else torch.empty((T, H), dtype=torch.bfloat16, device=x.device)
+    _need(y, torch.bfloat16, (T, H), "out")
+    fields = tuple(_DEBUG_FIELDS) if fields is None else tuple(fields)
+    bufs, dumps = None, {}
+    if fields:
+        bufs = _lib.DebugBuffers()
+        for name in fields:
+            dt, shape = _DEBUG_FIELDS[name]
+            t = torch.zeros(shape(T, H, I, E, top_k), dtype=getattr(torch, dt), device=x.device)
+            dumps[name] = t
+            setattr(bufs, name, t.data_ptr())
+    _lib.check(_lib.load().moe_w8a8_forward_fused(
+        _ptr(x), _ptr(router_w), _ptr(router_bias), _ptr(w13_q), _ptr(w13_scale), _ptr(w2_q), _ptr(w2_scale),
+        T, H, I, E, top_k, _ptr(y), _ptr(workspace), workspace.numel() * workspace.element_size(),
+        _stream(stream), ctypes.byref(bufs) if bufs is not None else None), "moe_w8a8_forward_fused")
+    return (y, dumps) if fields else y
 
 # ---- SmoothQuant-folded activations, calibrated per expert ------------------
 

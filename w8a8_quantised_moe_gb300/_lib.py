@@ -49,6 +49,8 @@ EXPORTS = (
     "moe_w8a8_host_chunks",
     "moe_w8a8_quantize_weights_smoothed",
     "moe_w8a8_forward_smooth",
+    "moe_w8a8_forward_fused",
+    "moe_w8a8_fused_supported",
 )
 
 
@@ -119,6 +121,9 @@ def _declare(lib) -> None:
         "moe_w8a8_quantize_weights_smoothed": ([vp, i64, i64, vp, vp, vp, vp], i32),
         "moe_w8a8_forward_smooth": ([vp, vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
                                      ctypes.POINTER(DebugBuffers)], i32),
+        "moe_w8a8_forward_fused": ([vp, vp, vp, vp, vp, vp, vp, i64, i64, i64, i64, i64, vp, vp, sz, vp,
+                                    ctypes.POINTER(DebugBuffers)], i32),
+        "moe_w8a8_fused_supported": ([i64, i64, i64, i64, i64], i32),
     }
     for name, (args, res) in decl.items():
         fn = getattr(lib, name)

@@ -20,8 +20,8 @@ LIB = os.path.join(PKG, "libmoe_w8a8.so")
 BUILD_CHECKED = os.path.join(PKG, "_build_checked")
 LIB_CHECKED = os.path.join(PKG, "libmoe_w8a8_checked.so")
 SOURCES = ["api.cu", "route.cu", "router.cu", "pointwise.cu", "gemm.cu", "gemm_pair.cu", "gemm_skinny.cu",
-           "static_linear.cu", "fp8.cu", "gemm_fp8_pair.cu"]
-HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh"]
+           "static_linear.cu", "fp8.cu", "gemm_fp8_pair.cu", "fused.cu"]
+HEADERS = ["internal.h", "ptx.cuh", "gemm_common.cuh", "gemm_skinny.cuh", "router_small.cuh"]
 
 NVCC_FLAGS = [
     "-gencode", "arch=compute_103a,code=sm_103a",

@@ -52,11 +52,16 @@ bool pdl_env_off() {
 
 size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
-// Byte offset, within the first 256 bytes of the workspace (the error
-// region, zeroed once by the caller), of the small-batch router's ticket.
-constexpr size_t kTicketOffset = 128;
-
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// The dp4a GEMM's scheduling words in a workspace's error region (the GEMM
+// leaves them zero).  Taken by the one-kernel layer, whose gate/up GEMM phase
+// they shortened (decode layer: 122.5 -> 118.7 us); the separate dp4a
+// kernels deal their units round-robin (measured: the decode layer 201.3 us
+// round-robin, 203.4 us taking units from the counter).
+unsigned int* sched_words(int* err) {
+    return reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(err) + kSchedOffset);
+}
 
 moe_status_t from_cuda(cudaError_t e) { return e == cudaSuccess ? MOE_OK : MOE_ERR_CUDA; }
 
@@ -367,6 +372,129 @@ moe_status_t forward_impl(const uint16_t* x, const float* router_w, const float*
     return MOE_OK;
 }
 
+// The one-kernel layer (fused.cu) on the forward's workspace layout.
+moe_status_t forward_fused_impl(const uint16_t* x, const float* router_w, const float* router_bias,
+                                const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                                const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E, int64_t k,
+                                uint16_t* y, void* workspace, size_t workspace_bytes, void* stream,
+                                const moe_w8a8_debug_t* dbg) {
+    if (!moe_shape_ok(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (T == 0) return MOE_OK;
+    if (!fused_supported(T, H, I, E, k)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    const void* ptrs[] = {x, router_w, w13_q, w13_scale, w2_q, w2_scale, y, workspace};
+    for (const void* p : ptrs)
+        if (p == nullptr || !aligned16(p) || injected(kInjectBadPtr)) return MOE_ERR_INVALID_ARG;
+    if (router_bias != nullptr && !aligned16(router_bias)) return MOE_ERR_INVALID_ARG;
+    if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return MOE_ERR_INVALID_ARG;
+    const FwdLayout L = fwd_layout(T, H, I, E, k);
+    if (injected(kInjectWsShort) && workspace_bytes >= L.total) workspace_bytes = L.total - 1;
+    if (workspace_bytes < L.total) return MOE_ERR_WORKSPACE_TOO_SMALL;
+
+    cudaStream_t st = static_cast<cudaStream_t>(stream);
+    const int S = (int)(T * k);
+    const RouterPlan rp = router_plan(T, H, E);
+    FusedArgs a{};
+    a.x = x;
+    a.Wr = router_w;
+    a.bias = router_bias;
+    a.T = (int)T;
+    a.H = (int)H;
+    a.I = (int)I;
+    a.E = (int)E;
+    a.k = (int)k;
+    a.E_pad = rp.E_pad;
+    a.KS = rp.KS;
+    a.hs = rp.hs;
+    a.P = at<float>(workspace, L.logits);
+    a.topk_ids = at<int32_t>(workspace, L.topk_ids);
+    a.topk_w = at<float>(workspace, L.topk_w);
+    a.rank = at<int32_t>(workspace, L.rank);
+    a.hist = at<int32_t>(workspace, L.hist);
+    a.offsets = at<int32_t>(workspace, L.offsets);
+    a.counts = at<int32_t>(workspace, L.counts);
+    a.error = at<int>(workspace, L.err);
+    a.ticket = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(a.error) + kTicketOffset);
+    a.bar = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(a.error) + kFusedCtlOffset);
+    a.abort = reinterpret_cast<int*>(reinterpret_cast<char*>(a.error) + kFusedCtlOffset + 4);
+    a.exits = reinterpret_cast<unsigned int*>(reinterpret_cast<char*>(a.error) + kFusedCtlOffset + 8);
+    a.slot_of = at<int32_t>(workspace, L.slot_of);
+    a.slot_token = at<int32_t>(workspace, L.slot_token);
+    a.s_x = at<float>(workspace, L.s_x);
+    a.s_slot = at<float>(workspace, L.s_slot);
+    a.q_tok = at<int8_t>(workspace, L.q_x16);  // T * H bytes of the S * H * 2
+    a.h = at<float>(workspace, L.h);
+    a.s_h = at<float>(workspace, L.s_h);
+    a.q_h = at<int8_t>(workspace, L.q_h16);
+    a.o = at<float>(workspace, L.o);
+    a.y = y;
+    a.timeout_ns = g_timeout_ns.load();
+    a.stall = injected(kInjectStall) ? 1 : 0;
+
+    GemmArgs& g1 = a.g1;
+    g1.sched = sched_words(a.error);
+    g1.w = w13_q;
+    g1.act8 = a.q_tok;
+    g1.K = (int)H;
+    g1.n_groups = (int)E;
+    g1.total_rows = S;
+    g1.offsets = a.offsets;
+    g1.w_rows_per_group = (int)(2 * I);
+    g1.up_offset = (int)I;
+    g1.w_scale = w13_scale;
+    g1.act_scale = a.s_slot;
+    g1.out = a.h;
+    g1.ld_out = (int)I;
+    g1.acc_out = dbg ? dbg->acc1 : nullptr;
+    g1.error = a.error;
+    g1.timeout_ns = a.timeout_ns;
+    GemmArgs& g2 = a.g2;
+    g2.sched = g1.sched;
+    g2.w = w2_q;
+    g2.act8 = a.q_h;
+    g2.K = (int)I;
+    g2.n_groups = (int)E;
+    g2.total_rows = S;
+    g2.offsets = a.offsets;
+    g2.w_rows_per_group = (int)H;
+    g2.w_scale = w2_scale;
+    g2.act_scale = a.s_h;
+    g2.out = a.o;
+    g2.ld_out = (int)H;
+    g2.acc_out = dbg ? dbg->acc2 : nullptr;
+    g2.error = a.error;
+    g2.timeout_ns = a.timeout_ns;
+
+    cudaError_t e;
+    if ((e = mark(0, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = launch_moe_fused(a, st)) != cudaSuccess) return from_cuda(e);
+    if ((e = mark(1, st)) != cudaSuccess) return from_cuda(e);
+
+    if (dbg) {
+        auto cp = [&](void* dst, const void* src, size_t bytes) -> cudaError_t {
+            if (!dst) return cudaSuccess;
+            return cudaMemcpyAsync(dst, src, bytes, cudaMemcpyDeviceToDevice, st);
+        };
+        const size_t Sb = (size_t)S * 4;
+        if ((e = cp(dbg->topk_ids, a.topk_ids, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->topk_w, a.topk_w, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->offsets, a.offsets, (size_t)(E + 1) * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->slot_of, a.slot_of, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->slot_token, a.slot_token, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_x, a.s_x, (size_t)T * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->q_x, a.q_tok, (size_t)T * H)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->h, a.h, (size_t)S * I * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_h, a.s_h, Sb)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->q_h, a.q_h, (size_t)S * I)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->o, a.o, (size_t)S * H * 4)) != cudaSuccess) return from_cuda(e);
+        if ((e = cp(dbg->s_slot, a.s_slot, Sb)) != cudaSuccess) return from_cuda(e);
+        if (dbg->q_slot) {  // every slot's row: its token's codes
+            e = launch_s8_rows_gather(a.q_tok, a.slot_token, S, (int)H, 1, (int)T, dbg->q_slot, a.error, st);
+            if (e != cudaSuccess) return from_cuda(e);
+        }
+    }
+    return MOE_OK;
+}
+
 // Host-resident activations: x copied in and y copied out in token chunks on
 // a copy stream, overlapping the layer's compute on another chunk.  Tokens
 // are independent in the layer, so each chunk is a whole forward of its own
@@ -603,6 +731,19 @@ moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float* router_w,
                                     const moe_w8a8_debug_t* dbg) {
     return forward_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
                         workspace, workspace_bytes, stream, dbg);
+}
+
+int moe_w8a8_fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t top_k) {
+    return moe_shape_ok(T, H, I, E, top_k) && fused_supported(T, H, I, E, top_k) ? 1 : 0;
+}
+
+moe_status_t moe_w8a8_forward_fused(const uint16_t* x, const float* router_w, const float* router_bias,
+                                    const int8_t* w13_q, const float* w13_scale, const int8_t* w2_q,
+                                    const float* w2_scale, int64_t T, int64_t H, int64_t I, int64_t E,
+                                    int64_t top_k, uint16_t* y, void* workspace, size_t workspace_bytes,
+                                    void* stream, const moe_w8a8_debug_t* dbg) {
+    return forward_fused_impl(x, router_w, router_bias, w13_q, w13_scale, w2_q, w2_scale, T, H, I, E, top_k, y,
+                              workspace, workspace_bytes, stream, dbg);
 }
 
 size_t moe_w8a8_linear_workspace_size(int64_t M, int64_t N, int64_t K) {

@@ -82,7 +82,53 @@ struct GemmArgs {
     uint64_t timeout_ns;
     int stall;               // test hook (MOE_INJECT=stall): the producer first waits on a barrier that
                              // nothing completes, so that the wait limit runs out
+    unsigned int* sched;     // Skinny only, optional: two words, zero between launches, through which
+                             // CTAs take work units in turn (nullptr: a fixed round-robin deal)
 };
+
+// The one-kernel layer for few tokens (fused.cu).  Pointers into the
+// forward's workspace (FwdLayout) except x, Wr, bias, the weights (in g1, g2)
+// and y.  q_tok: int8 codes [T][H] token-major; q_h: int8 [S][I]; g1 and g2
+// as the multi-kernel forward fills them for the dp4a kernel, with g1.act8 =
+// q_tok (rows gathered through slot_token).  bar, abort, exits: words of the
+// workspace's error region that are zero between calls.
+struct FusedArgs {
+    const uint16_t* x;
+    const float* Wr;
+    const float* bias;
+    int T, H, I, E, k, E_pad, KS, hs;
+    float* P;
+    int32_t *topk_ids;
+    float* topk_w;
+    int32_t *rank, *hist, *offsets, *counts;
+    unsigned int* ticket;
+    int32_t *slot_of, *slot_token;
+    float *s_x, *s_slot;
+    int8_t* q_tok;
+    float *h, *s_h;
+    int8_t* q_h;
+    float* o;
+    uint16_t* y;
+    GemmArgs g1, g2;
+    unsigned int* bar;
+    int* abort;
+    unsigned int* exits;
+    int* error;
+    uint64_t timeout_ns;
+    int stall;  // test hook (MOE_INJECT=stall): CTA 0 skips one barrier arrival, every wait runs out
+};
+// Shapes the one-kernel layer takes: T <= kRouterSmallT, both GEMMs on the
+// dp4a kernel's unit shapes, a row of x and of h in one CTA's registers.
+bool fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
+cudaError_t launch_moe_fused(const FusedArgs& a, cudaStream_t st);
+
+// Byte offsets, within the first 256 bytes of the workspace (the error
+// region, zeroed once by the caller and left zero by every call), of the
+// few-token router's ticket and of the one-kernel layer's barrier words.
+constexpr size_t kTicketOffset = 128;
+constexpr size_t kFusedCtlOffset = 192;
+// the two counter words of the dp4a GEMM's unit scheduling (GemmArgs::sched)
+constexpr size_t kSchedOffset = 224;
 
 // Launch plan of the router GEMM: experts padded to E_pad (a multiple of 16,
 // or of 128 above 128), NB experts per CTA, the hidden dimension cut into KS
@@ -137,6 +183,20 @@ __device__ __forceinline__ void cp_async16(void* smem_dst, const void* gmem_src)
 }
 __device__ __forceinline__ void cp_async_wait_all() {
     asm volatile("cp.async.commit_group;\n\tcp.async.wait_group 0;" ::: "memory");
+}
+// cp_async16 that writes 16 zero bytes instead when !valid (gmem_src is then
+// not read); commit of the copies issued since the last commit, and the wait
+// until at most N committed groups are still in flight.
+__device__ __forceinline__ void cp_async16_zfill(void* smem_dst, const void* gmem_src, bool valid) {
+    asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(
+                     static_cast<uint32_t>(__cvta_generic_to_shared(smem_dst))),
+                 "l"(gmem_src), "r"(valid ? 16 : 0)
+                 : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
+template <int N>
+__device__ __forceinline__ void cp_async_wait() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(N) : "memory");
 }
 
 // Quantisation code of v for the scale s = amax / 127 of its row:

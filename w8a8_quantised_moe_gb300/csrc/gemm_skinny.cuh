@@ -38,53 +38,59 @@ __device__ __forceinline__ int dot16(const uint4 w, const uint4 a, int acc) {
     return __dp4a((int)w.w, (int)a.w, acc);
 }
 
-// One warp item: kSkRows weight rows x RC staged activation rows (rc valid),
-// dot products over K, then the epilogue of the valid (row, channel) pairs.
-// GateUp: rows are gate c, gate c+1, up c, up c+1 (c = first channel).
-// Each batch issues NB 512-byte steps of every row before using any (NB * 2
-// KB in flight per warp): measured on the down GEMM of the decode layer
-// (K = 1536), 69.6 us against 76 us with two steps per batch.
-template <int EPI, int RC, int NB = (RC <= 4 ? 4 : 2)>
-__device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* __restrict__ act_s, int rc,
-                                            int row0, int g, int first, int lane) {
+// A warp item: kSkRows weight rows x RC staged activation rows (rc valid),
+// dot products over K in batches of kSkNB 512-byte steps per row (every load
+// of a batch issued before any is used), then the epilogue of the valid (row,
+// channel) pairs.  GateUp: rows are gate c, gate c+1, up c, up c+1 (c = first
+// channel).  The first batch of a warp's next item (in this step or the
+// next) is issued before the current item's epilogue, so that it is in
+// flight through the epilogue and the CTA's staging barrier.
+constexpr int kSkNB = 4;
+
+__device__ __forceinline__ int skinny_first(int EPI, int unit, int item) {
+    return EPI == (int)Epi::GateUp ? unit * kSkUnitGateUp + item * (kSkRows / 2) : unit * kSkUnitScale + item * kSkRows;
+}
+
+template <int EPI>
+__device__ __forceinline__ void skinny_load(uint4 (&wv)[kSkNB][kSkRows], const GemmArgs& args, int g, int first,
+                                            int n, int lane) {
     const int K = args.K;
-    const int8_t* w = static_cast<const int8_t*>(args.w);
-    const int8_t* wr[kSkRows];
-    int wrow[kSkRows];  // weight row within the group
+    const int8_t* w = static_cast<const int8_t*>(args.w) + (size_t)g * args.w_rows_per_group * K;
 #pragma unroll
     for (int j = 0; j < kSkRows; ++j) {
-        if (EPI == (int)Epi::GateUp) wrow[j] = (j >> 1) * args.up_offset + first + (j & 1);
-        else wrow[j] = first + j;
-        wr[j] = w + ((size_t)g * args.w_rows_per_group + wrow[j]) * K;
-    }
-    int acc[kSkRows][RC];
+        const int wrow = EPI == (int)Epi::GateUp ? (j >> 1) * args.up_offset + first + (j & 1) : first + j;
+        const int8_t* wr = w + (size_t)wrow * K;
 #pragma unroll
-    for (int j = 0; j < kSkRows; ++j)
-#pragma unroll
-        for (int r = 0; r < RC; ++r) acc[j][r] = 0;
-
-    for (int k0 = lane * 16; k0 < K; k0 += NB * 512) {
-        uint4 wv[NB][kSkRows];
-#pragma unroll
-        for (int b = 0; b < NB; ++b) {  // every load of the batch first
-            const int k = k0 + b * 512;
-#pragma unroll
-            for (int j = 0; j < kSkRows; ++j) wv[b][j] = k < K ? ld_stream16(wr[j] + k) : make_uint4(0u, 0u, 0u, 0u);
+        for (int b = 0; b < kSkNB; ++b) {
+            const int k = (n * kSkNB + b) * 512 + lane * 16;
+            wv[b][j] = k < K ? ld_stream16(wr + k) : make_uint4(0u, 0u, 0u, 0u);
         }
+    }
+}
+
+// acc[j][r] += batch n's products (int32: exact in any order).
+template <int RC>
+__device__ __forceinline__ void skinny_accum(const uint4 (&wv)[kSkNB][kSkRows], const int8_t* __restrict__ act_s,
+                                             int K, int n, int lane, int (&acc)[kSkRows][RC]) {
 #pragma unroll
-        for (int b = 0; b < NB; ++b) {
-            const int k = k0 + b * 512;
-            if (k < K) {
+    for (int b = 0; b < kSkNB; ++b) {
+        const int k = (n * kSkNB + b) * 512 + lane * 16;
+        if (k < K) {
 #pragma unroll
-                for (int r = 0; r < RC; ++r) {
-                    const uint4 a = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k);
+            for (int r = 0; r < RC; ++r) {
+                const uint4 a = *reinterpret_cast<const uint4*>(act_s + (size_t)r * K + k);
 #pragma unroll
-                    for (int j = 0; j < kSkRows; ++j) acc[j][r] = dot16(wv[b][j], a, acc[j][r]);
-                }
+                for (int j = 0; j < kSkRows; ++j) acc[j][r] = dot16(wv[b][j], a, acc[j][r]);
             }
         }
     }
+}
 
+// The item's epilogue: reduction across the warp, then the valid (row,
+// channel) outputs.
+template <int EPI, int RC>
+__device__ __forceinline__ void skinny_epilogue(const GemmArgs& args, int (&acc)[kSkRows][RC], int rc, int row0,
+                                                int g, int first, int lane) {
     const float* sw = args.w_scale + (size_t)g * args.w_rows_per_group;
     if (EPI == (int)Epi::GateUp) {
         // value (c, r, gate/up) at ((c * RC) + r) * 2 + gu: the reduction ends
@@ -138,6 +144,43 @@ __device__ __forceinline__ void skinny_item(const GemmArgs& args, const int8_t* 
     }
 }
 
+// A step: unit u (group g, unit index within the group) and one chunk of up
+// to kSkChunk of the group's activation rows, [row0, min(row0 + kSkChunk,
+// r_end)).
+struct SkStep {
+    int g, unit, row0, r_end;
+};
+
+__host__ __device__ constexpr int skinny_items(int EPI) { return EPI == (int)Epi::GateUp ? kSkItemsGateUp : kSkItemsScale; }
+
+// This warp's items of step `cur`; wv holds the first batch of the first
+// item on entry and, on return, the first batch of `next`'s first item
+// (when next_ok).
+template <int EPI, int RC>
+__device__ __forceinline__ void skinny_step(const GemmArgs& args, const int8_t* __restrict__ act_s,
+                                            const SkStep& cur, const SkStep& next, bool next_ok, int nbat,
+                                            uint4 (&wv)[kSkNB][kSkRows], int warp, int lane) {
+    constexpr int kItems = skinny_items(EPI);
+    const int rc = min(kSkChunk, cur.r_end - cur.row0);
+#pragma unroll 1
+    for (int it = 0; it < kItems; ++it) {
+        const int first = skinny_first(EPI, cur.unit, warp * kItems + it);
+        int acc[kSkRows][RC];
+#pragma unroll
+        for (int j = 0; j < kSkRows; ++j)
+#pragma unroll
+            for (int r = 0; r < RC; ++r) acc[j][r] = 0;
+#pragma unroll 1
+        for (int n = 0; n < nbat; ++n) {
+            if (n > 0) skinny_load<EPI>(wv, args, cur.g, first, n, lane);
+            skinny_accum<RC>(wv, act_s, args.K, n, lane, acc);
+        }
+        if (it + 1 < kItems) skinny_load<EPI>(wv, args, cur.g, skinny_first(EPI, cur.unit, warp * kItems + it + 1), 0, lane);
+        else if (next_ok) skinny_load<EPI>(wv, args, next.g, skinny_first(EPI, next.unit, warp * kItems), 0, lane);
+        skinny_epilogue<EPI, RC>(args, acc, rc, cur.row0, cur.g, first, lane);
+    }
+}
+
 // Where skinny_run's activation rows come from.
 enum SkSrc : int {
     kSkSrcRows = 0,    // rows [total_rows][K] of act8
@@ -146,19 +189,41 @@ enum SkSrc : int {
 
 __host__ __device__ constexpr int skinny_smem_bytes(int K) { return kSkChunk * K; }
 
+// Copies rows row0 .. row0 + rc of the group table into act_s, zeros up to
+// the step's row shape (coherent L2 loads: the rows may have been written
+// earlier in the same launch, before a grid-wide barrier).
+template <int SRC>
+__device__ __forceinline__ void skinny_stage(int8_t* act_s, const int8_t* act, int K, int row0, int rc,
+                                             const int* map_s) {
+    const int RC = rc <= 2 ? 2 : rc <= 4 ? 4 : 8;
+    const int n16 = RC * K / 16;
+    uint4* dst = reinterpret_cast<uint4*>(act_s);
+    if (SRC == kSkSrcGather) {
+        const int row16 = K / 16;
+        for (int i = threadIdx.x; i < n16; i += kSkThreads) {
+            const int r = i / row16;
+            dst[i] = r < rc ? __ldcg(reinterpret_cast<const uint4*>(act + (size_t)map_s[row0 + r] * K) + (i - r * row16))
+                            : make_uint4(0, 0, 0, 0);
+        }
+    } else {
+        const int valid16 = rc * K / 16;
+        const uint4* src = reinterpret_cast<const uint4*>(act + (size_t)row0 * K);
+        for (int i = threadIdx.x; i < n16; i += kSkThreads) dst[i] = i < valid16 ? __ldcg(src + i) : make_uint4(0, 0, 0, 0);
+    }
+}
+
 // Persistent grid over work units = (non-empty group, block of weight rows);
-// per unit the group's activation rows pass through shared memory in chunks
-// of kSkChunk rows (zero-padded to the kernel's chunk shape).  CTA `bid` of
-// `nblk` starts with unit bid; its next units are bid + nblk, bid + 2 nblk,
-// ... or, with args.sched, taken in turn from a counter (one taken a unit
-// ahead, so the atomic's latency is hidden), which evens out CTAs whose units
-// took longer.  act_s: skinny_smem_bytes(K) bytes; unit_start, row_start:
-// kMaxExperts + 1 ints; next_s: two ints (shared memory: the unit taken from
-// the counter reaches all threads through them, in turn).  The activation
-// rows are read through L2 (coherent loads): they may have been written
-// earlier in the same launch, before a grid-wide barrier.  kSkSrcGather:
-// row_map [total_rows] gives each row's source row in act8 (map_rows rows),
-// copied to map_s (total_rows ints of shared memory) first.
+// a step is one unit and one chunk of up to kSkChunk of its group's
+// activation rows, staged in shared memory (zero-padded to the step's row
+// shape).  CTA `bid` of `nblk` starts with unit bid; its next units are
+// bid + nblk, bid + 2 nblk, ... or, with args.sched, taken in turn from a
+// counter (one taken a unit ahead, so the atomic's latency is hidden), which
+// evens out CTAs whose units took longer.  act_s: skinny_smem_bytes(K) bytes;
+// unit_start, row_start: kMaxExperts + 1 ints; next_s: two ints (shared
+// memory: the unit taken from the counter reaches all threads through them,
+// in turn).  kSkSrcGather: row_map [total_rows] gives each row's source row
+// in act8 (map_rows rows), copied to map_s (total_rows ints of shared memory)
+// first.
 template <int EPI, int SRC = kSkSrcRows>
 __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, int* unit_start, int* row_start,
                                            int* next_s, int bid, int nblk, const int32_t* row_map = nullptr,
@@ -215,68 +280,66 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
     const int total_units = unit_start[G];
     const int K = args.K;
     const int8_t* act = args.act8;
+    const int nbat = (K + kSkNB * 512 - 1) / (kSkNB * 512);
+    auto step_of = [&](int u) {  // the first step of unit u
+        SkStep st;
+        st.g = last_le(unit_start, G, u);
+        st.unit = u - unit_start[st.g];
+        st.row0 = row_start[st.g];
+        st.r_end = row_start[st.g + 1];
+        return st;
+    };
 
-    // un: the unit taken after u; grab: thread 0's request for the one after
-    // un, in flight.  next_s slot ph is written next (a slot is rewritten only
-    // after a barrier past its reads).
+    // un: the unit taken after the current one; grab: thread 0's request for
+    // the one after un, in flight.  next_s slot ph is written next (a slot is
+    // rewritten only after a barrier past its reads).
     int un = bid + nblk, ph = 1;
     unsigned grab = 0u;
     if (dyn) {
         un = bid < total_units ? next_s[0] : total_units;
         if (threadIdx.x == 0 && un < total_units) grab = nblk + atomicAdd(args.sched, 1u);
     }
-    int staged_row0 = -1;  // first activation row in act_s (row ranges of groups are disjoint)
-    for (int u = bid; u < total_units;) {
-        const int g = last_le(unit_start, G, u);
-        const int unit = u - unit_start[g];
-        const int r_begin = row_start[g], r_end = row_start[g + 1];
-        for (int row0 = r_begin; row0 < r_end; row0 += kSkChunk) {
-            const int rc = min(kSkChunk, r_end - row0);
-            const int RC = rc <= 2 ? 2 : rc <= 4 ? 4 : 8;
-            if (row0 != staged_row0) {
-                // stage rows row0 .. row0 + rc, zeros up to RC
-                __syncthreads();  // every warp is done with the previous rows
-                const int n16 = RC * K / 16;
-                const int valid16 = rc * K / 16;
-                uint4* dst = reinterpret_cast<uint4*>(act_s);
-                if (SRC == kSkSrcGather) {
-                    const int row16 = K / 16;
-                    for (int i = threadIdx.x; i < n16; i += kSkThreads) {
-                        const int r = i / row16;
-                        dst[i] = r < rc ? __ldcg(reinterpret_cast<const uint4*>(act + (size_t)map_s[row0 + r] * K) +
-                                                 (i - r * row16))
-                                        : make_uint4(0, 0, 0, 0);
-                    }
-                } else {
-                    const uint4* src = reinterpret_cast<const uint4*>(act + (size_t)row0 * K);
-                    for (int i = threadIdx.x; i < n16; i += kSkThreads)
-                        dst[i] = i < valid16 ? __ldcg(src + i) : make_uint4(0, 0, 0, 0);
-                }
-                __syncthreads();
-                staged_row0 = row0;
-            }
-            constexpr int kItems = EPI == (int)Epi::GateUp ? kSkItemsGateUp : kSkItemsScale;
-#pragma unroll 1
-            for (int it = 0; it < kItems; ++it) {
-                const int item = warp * kItems + it;
-                const int first = EPI == (int)Epi::GateUp ? unit * kSkUnitGateUp + item * (kSkRows / 2)
-                                                           : unit * kSkUnitScale + item * kSkRows;
-                if (RC == 2) skinny_item<EPI, 2>(args, act_s, rc, row0, g, first, lane);
-                else if (RC == 4) skinny_item<EPI, 4>(args, act_s, rc, row0, g, first, lane);
-                else skinny_item<EPI, 8>(args, act_s, rc, row0, g, first, lane);
-            }
-        }
-        // the next unit
-        u = un;
-        if (!dyn) {
-            un += nblk;
-        } else {
-            if (threadIdx.x == 0) next_s[ph] = un < total_units ? (int)grab : total_units;
+    if (bid >= total_units) un = total_units;
+    SkStep cur{};
+    uint4 wv[kSkNB][kSkRows];
+    bool have = bid < total_units;
+    if (have) {
+        cur = step_of(bid);
+        skinny_load<EPI>(wv, args, cur.g, skinny_first(EPI, cur.unit, warp * skinny_items(EPI)), 0, lane);
+        skinny_stage<SRC>(act_s, act, K, cur.row0, min(kSkChunk, cur.r_end - cur.row0), map_s);
+    }
+    __syncthreads();
+    while (have) {
+        // the step after this one
+        SkStep nxt = cur;
+        const bool new_unit = cur.row0 + kSkChunk >= cur.r_end;
+        bool next_ok = true;
+        if (!new_unit) nxt.row0 = cur.row0 + kSkChunk;
+        else if ((next_ok = un < total_units)) nxt = step_of(un);
+        const int rc = min(kSkChunk, cur.r_end - cur.row0);
+        if (rc <= 2) skinny_step<EPI, 2>(args, act_s, cur, nxt, next_ok, nbat, wv, warp, lane);
+        else if (rc <= 4) skinny_step<EPI, 4>(args, act_s, cur, nxt, next_ok, nbat, wv, warp, lane);
+        else skinny_step<EPI, 8>(args, act_s, cur, nxt, next_ok, nbat, wv, warp, lane);
+        // the next step's rows, unless they are this step's (distinct groups
+        // never share a first row); every warp's next batch is in flight
+        const bool restage = next_ok && nxt.row0 != cur.row0;
+        if (dyn && new_unit && threadIdx.x == 0) next_s[ph] = un < total_units ? (int)grab : total_units;
+        if (restage || (dyn && new_unit)) __syncthreads();  // every warp is done with act_s / next_s is set
+        if (restage) {
+            skinny_stage<SRC>(act_s, act, K, nxt.row0, min(kSkChunk, nxt.r_end - nxt.row0), map_s);
             __syncthreads();
-            un = next_s[ph];
-            ph ^= 1;
-            if (threadIdx.x == 0 && un < total_units) grab = nblk + atomicAdd(args.sched, 1u);
         }
+        if (new_unit) {
+            if (!dyn) {
+                un += nblk;
+            } else {
+                un = next_s[ph];
+                ph ^= 1;
+                if (threadIdx.x == 0 && un < total_units) grab = nblk + atomicAdd(args.sched, 1u);
+            }
+        }
+        cur = nxt;
+        have = next_ok;
     }
     if (dyn) {  // the last CTA out leaves the counter words zero for the next launch
         __syncthreads();

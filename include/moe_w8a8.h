@@ -208,10 +208,9 @@ MOE_W8A8_API moe_status_t moe_w8a8_forward_debug(const uint16_t* x, const float*
  * intermediate equal moe_w8a8_forward's bit for bit.
  *
  * Arguments, workspace (moe_w8a8_workspace_size) and errors as
- * moe_w8a8_forward_debug; `dbg` may be NULL.  Shapes: those for which
- * moe_w8a8_fused_supported returns 1 (T <= 128, I <= 8192, and the decode
- * GEMM's unit shapes: I a multiple of 16 and H of 64); others return
- * MOE_ERR_UNSUPPORTED_SHAPE.  One launch on `stream` (plus the copies into
+ * moe_w8a8_forward_debug; `dbg` may be NULL.  Shapes: those of
+ * moe_w8a8_forward with T <= 128 (moe_w8a8_fused_supported returns 1); others
+ * return MOE_ERR_UNSUPPORTED_SHAPE.  One launch on `stream` (plus the copies into
  * `dbg`); it occupies every SM until it ends.  Every barrier wait is bounded
  * by moe_w8a8_set_wait_timeout_ns: one that runs out makes every CTA skip the
  * remaining phases (y is then undefined) and is reported by

@@ -8,10 +8,10 @@ intermediate of the debug dump (routing, slot maps, scales, codes, the raw
 int32 accumulators of both GEMMs, h, o).  y is also compared with the oracle
 directly.  Shapes: one token, a few tokens per expert, the 128-token maximum,
 a single expert, 256 experts with top-8 and a router bias (most experts
-empty), and the decode layer at full size.  Then the failure path: with
-MOE_INJECT=stall one CTA skips a barrier arrival, the 2 ms wait limit runs
-out everywhere, MOE_ERR_DEVICE_TIMEOUT is reported, and the next calls on the
-same workspace are exact again."""
+empty), rows of h longer than 8192, and the decode layer at full size.  Then
+the failure path: with MOE_INJECT=stall one CTA skips a barrier arrival, the
+2 ms wait limit runs out everywhere, MOE_ERR_DEVICE_TIMEOUT is reported, and
+the next calls on the same workspace are exact again."""
 import numpy as np
 import pytest
 import torch
@@ -33,6 +33,7 @@ SHAPES = {
     "max_tokens": TINY.replace(T=128, H=512, I=384, E=64, k=4),
     "one_expert": TINY.replace(T=32, H=256, I=128, E=1, k=1),
     "top8_bias": TINY.replace(T=100, H=256, I=128, E=256, k=8, bias="normal", bias_std=0.5),
+    "long_rows": TINY.replace(T=8, H=256, I=8320, E=2, k=1),  # rows of h longer than 8192
 }
 
 

@@ -151,6 +151,7 @@ FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     L.s_h = take(S * 4);
     L.q_h16 = take(S * I * 2);
     L.o = take(S * H * 4);
+    L.fctl = take(2 * E * 4);  // the one-kernel layer's per-expert hand-off words
     L.total = off;
     return L;
 }
@@ -448,7 +449,9 @@ moe_status_t forward_fused_impl(const uint16_t* x, const float* router_w, const 
     g1.error = a.error;
     g1.timeout_ns = a.timeout_ns;
     GemmArgs& g2 = a.g2;
-    g2.sched = g1.sched;
+    g2.sched = g1.sched + 2;
+    a.done1 = at<unsigned int>(workspace, L.fctl);
+    a.ready2 = at<int>(workspace, L.fctl + E * 4);
     g2.w = w2_q;
     g2.act8 = a.q_h;
     g2.K = (int)I;

@@ -128,46 +128,87 @@ __device__ void quant_token(const FusedArgs& a, int t) {
     __syncthreads();  // red_max is reused by the next token of this CTA
 }
 
-// Phase B, in the CTA that built the routing tables: slot of every (token,
-// choice) = first slot of (its chunk, expert) + its rank there; the slot's
-// token and activation scale.
-__device__ void build_slots(const FusedArgs& a) {
-    __syncthreads();  // this CTA's table writes (hist, rank) are visible to all its threads
-    const int S = a.T * a.k;
-    for (int i = threadIdx.x; i < S; i += blockDim.x) {
-        const int t = i / a.k;
+// After the top-k phase, in every CTA: the routing tables in shared memory
+// (the slot of (token t, choice j) routed to expert e is offsets[e] plus the
+// number of earlier tokens routed to e: the multi-kernel forward's order), so
+// that no CTA waits for one CTA to build them.  offs_s [E + 1], map_s [S]
+// (slot -> token), ssl_s [S] (slot -> activation scale), mask_s [chunks][E]
+// (token bits of every 32-token chunk per expert).  CTA 0 also writes the
+// global copies (offsets, slot_of, slot_token, s_slot) that the combine and
+// the debug dumps read.
+__device__ void build_tables(const FusedArgs& a, int* offs_s, int* map_s, float* ssl_s, uint32_t* mask_s) {
+    __shared__ int32_t wsum[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int T = a.T, k = a.k, E = a.E, S = T * k;
+    const int nchunk = (T + kRouterTokens - 1) / kRouterTokens;
+    for (int i = tid; i < nchunk * E; i += blockDim.x) mask_s[i] = 0u;
+    __syncthreads();
+    for (int i = tid; i < S; i += blockDim.x) {
+        const int t = i / k;
+        const int e = __ldcg(a.topk_ids + i);
+        if (in_range(e, 0, E, a.error)) atomicOr(&mask_s[(t / kRouterTokens) * E + e], 1u << (t % kRouterTokens));
+    }
+    __syncthreads();
+    // exclusive prefix over the experts of their token counts (E <= 256 = blockDim)
+    int32_t tot = 0;
+    if (tid < E)
+        for (int c = 0; c < nchunk; ++c) tot += __popc(mask_s[c * E + tid]);
+    int32_t incl = tot;
+#pragma unroll
+    for (int off = 1; off < 32; off <<= 1) {
+        const int32_t o = __shfl_up_sync(0xffffffffu, incl, off);
+        if (lane >= off) incl += o;
+    }
+    if (lane == 31) wsum[warp] = incl;
+    __syncthreads();
+    int32_t before = 0, all = 0;
+#pragma unroll
+    for (int w = 0; w < 8; ++w) {
+        if (w < warp) before += wsum[w];
+        all += wsum[w];
+    }
+    if (tid < E) offs_s[tid] = before + incl - tot;
+    if (tid == 0) offs_s[E] = all;
+    __syncthreads();
+    for (int i = tid; i < S; i += blockDim.x) {
+        const int t = i / k, c = t / kRouterTokens;
         const int e = __ldcg(a.topk_ids + i);
         int slot = -1;
-        if (in_range(e, 0, a.E, a.error)) {
-            slot = __ldcg(a.hist + (size_t)(t / kRouterTokens) * a.E + e) + __ldcg(a.rank + i);
+        if (in_range(e, 0, E, a.error)) {
+            slot = offs_s[e] + __popc(mask_s[c * E + e] & ((1u << (t % kRouterTokens)) - 1u));
+            for (int cc = 0; cc < c; ++cc) slot += __popc(mask_s[cc * E + e]);
             if (!in_range(slot, 0, S, a.error)) slot = -1;
         }
-        a.slot_of[i] = slot;
         if (!kChecked || slot >= 0) {
-            a.slot_token[slot] = t;
-            a.s_slot[slot] = __ldcg(a.s_x + t);
+            const float sx = __ldcg(a.s_x + t);
+            map_s[slot] = t;
+            ssl_s[slot] = sx;
+            if (blockIdx.x == 0) {
+                a.slot_token[slot] = t;
+                a.s_slot[slot] = sx;
+            }
         }
+        if (blockIdx.x == 0) a.slot_of[i] = slot;
     }
+    if (blockIdx.x == 0)
+        for (int e = tid; e <= E; e += blockDim.x) a.offsets[e] = offs_s[e];
+    __syncthreads();
 }
 
-// Phase D, slot row r of h: s_h[r] = amax / 127 and its int8 codes (one CTA,
-// the row in registers: I <= 256 * 4 * 8).  The arithmetic of the
-// multi-kernel forward's requantiser.
-constexpr int kFrVec = 8;
-
+// Slot row r of h: s_h[r] = amax / 127 and its int8 codes (one CTA; the
+// arithmetic of the multi-kernel forward's requantiser).  The row is read
+// twice (the second time from L2) so that few registers are live here: this
+// runs inside the gate/up GEMM's loop, next to its weights in flight.
 __device__ void requant_row(const FusedArgs& a, int r) {
     __shared__ float red_max[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int I = a.I;
     const float4* row = reinterpret_cast<const float4*>(a.h + (size_t)r * I);
     const int nv = I / 4;
-    float4 v[kFrVec];
     float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < kFrVec; ++i) {
-        const int idx = tid + 256 * i;
-        v[i] = idx < nv ? __ldcg(row + idx) : make_float4(0.f, 0.f, 0.f, 0.f);
-        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v[i].x)), fmaxf(fabsf(v[i].y), fabsf(v[i].z))), fabsf(v[i].w));
+    for (int idx = tid; idx < nv; idx += blockDim.x) {
+        const float4 v = __ldcg(row + idx);
+        amax = fmaxf(fmaxf(fmaxf(amax, fabsf(v.x)), fmaxf(fabsf(v.y), fabsf(v.z))), fabsf(v.w));
     }
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
@@ -178,18 +219,94 @@ __device__ void requant_row(const FusedArgs& a, int r) {
     for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
     const float s = __fdiv_rn(amax, 127.0f);
     if (tid == 0) a.s_h[r] = s;
-#pragma unroll
-    for (int i = 0; i < kFrVec; ++i) {
-        const int idx = tid + 256 * i;
-        if (idx >= nv) break;
-        const int c0 = quant_code_div(v[i].x, s), c1 = quant_code_div(v[i].y, s), c2 = quant_code_div(v[i].z, s),
-                  c3 = quant_code_div(v[i].w, s);
+    for (int idx = tid; idx < nv; idx += blockDim.x) {
+        const float4 v = __ldcg(row + idx);
+        const int c0 = quant_code_div(v.x, s), c1 = quant_code_div(v.y, s), c2 = quant_code_div(v.z, s),
+                  c3 = quant_code_div(v.w, s);
         reinterpret_cast<uint32_t*>(a.q_h + (size_t)r * I)[idx] =
             (uint32_t)(uint8_t)c0 | ((uint32_t)(uint8_t)c1 << 8) | ((uint32_t)(uint8_t)c2 << 16) |
             ((uint32_t)(uint8_t)c3 << 24);
     }
-    __syncthreads();  // red_max is reused by the next row of this CTA
+    __syncthreads();  // red_max is reused by the next row
 }
+
+// Hand-offs between the two GEMM phases, without a grid barrier: a CTA
+// counts each gate/up unit it finishes on its expert's counter; the CTA that
+// finishes an expert's last unit requantises that expert's rows of h (phase
+// D of the multi-kernel forward) and raises its ready flag; a CTA waits for
+// an expert's flag before it stages that expert's rows for the down GEMM.  A
+// CTA moves to the down GEMM as soon as the gate/up units run out, so the
+// down GEMM's first experts overlap the gate/up GEMM's last units.  The
+// counter's result is read one unit after the increment (the warp does not
+// wait for the atomic); the last increment's at the end.
+__device__ void requant_expert(const FusedArgs& a, const int* offs_s, int e) {
+    for (int r = offs_s[e]; r < offs_s[e + 1]; ++r) requant_row(a, r);
+    __syncthreads();
+    if (threadIdx.x == 0) {
+        __threadfence();  // the expert's q_h and s_h before its flag
+        atomicExch(a.ready2 + e, 1);
+    }
+}
+
+struct FusedGateUpHook {
+    static constexpr bool kWaits = false;
+    static constexpr bool kCounts = true;
+    const FusedArgs* a;
+    const int* offs_s;
+    int* req_s;  // two ints of shared memory, used in turn
+    unsigned per_group;
+    int pend_g = -1;  // thread 0: the expert of the increment in flight, and its result
+    unsigned pend_old = 0;
+    int ph = 0;
+    __device__ __forceinline__ bool ready(int) { return true; }
+    __device__ __forceinline__ void unit_end_pre() {
+        if (threadIdx.x == 0) {
+            req_s[ph] = (pend_g >= 0 && pend_old == per_group - 1u) ? pend_g : -1;
+            pend_g = -1;
+        }
+    }
+    __device__ __forceinline__ void unit_end_post(int g) {
+        const int r = req_s[ph];
+        ph ^= 1;
+        if (r >= 0) requant_expert(*a, offs_s, r);
+        if (threadIdx.x == 0) {
+            __threadfence();  // this unit's h (every warp's, ordered by the barrier before)
+            pend_old = atomicAdd(a->done1 + g, 1u);
+            pend_g = g;
+        }
+    }
+    __device__ __forceinline__ void end() {
+        __syncthreads();
+        unit_end_pre();
+        __syncthreads();
+        const int r = req_s[ph];
+        ph ^= 1;
+        if (r >= 0) requant_expert(*a, offs_s, r);
+    }
+};
+
+struct FusedDownHook {
+    static constexpr bool kWaits = true;
+    static constexpr bool kCounts = false;
+    const FusedArgs* a;
+    // bounded wait for expert g's flag; false when the launch gave up
+    __device__ __forceinline__ bool ready(int g) {
+        const uint64_t t0 = global_timer_ns();
+        for (uint32_t i = 0;; ++i) {
+            if (ld_acquire_u32(reinterpret_cast<const unsigned*>(a->ready2 + g)) != 0u) return true;
+            if (*reinterpret_cast<volatile int*>(a->abort)) return false;
+            if ((i & 15u) == 15u && global_timer_ns() - t0 > a->timeout_ns) {
+                atomicExch(a->abort, 1);
+                atomicOr(a->error, kErrTimeout);
+                return false;
+            }
+            __nanosleep(64);
+        }
+    }
+    __device__ __forceinline__ void unit_end_pre() {}
+    __device__ __forceinline__ void unit_end_post(int) {}
+    __device__ __forceinline__ void end() {}
+};
 
 // Phase F, token t, part `part` of `nparts` of its columns: the weighted sum
 // of its k slot rows of o in top-k order (the multi-kernel forward's combine).
@@ -237,11 +354,11 @@ __device__ void combine_part(const FusedArgs& a, int t, int part, int nparts) {
 // down GEMM phase 69.7 -> 68.0 us.  The same for the gate/up GEMM's first
 // units during the routing phases made those phases 5 us longer, for 1.6 us
 // gained in the GEMM: not done.)
-__device__ void prefetch_gemm2(const FusedArgs& a, int bid) {
+__device__ void prefetch_gemm2(const FusedArgs& a, const int* offs_s, int bid) {
     const int per_group = a.H / kSkUnitScale;
     int u = bid;
     for (int g = 0; g < a.E; ++g) {
-        if (__ldcg(a.offsets + g + 1) == __ldcg(a.offsets + g)) continue;
+        if (offs_s[g + 1] == offs_s[g]) continue;
         if (u < per_group) {
             const int8_t* w = static_cast<const int8_t*>(a.g2.w) + ((size_t)g * a.H + (size_t)u * kSkUnitScale) * a.I;
             prefetch_l2_bulk(w, (uint32_t)((size_t)kSkUnitScale * a.I));
@@ -273,12 +390,21 @@ __global__ void __launch_bounds__(kSkThreads, 2) moe_fused_kernel(const FusedArg
     extern __shared__ __align__(16) float4 fused_smem[];  // router slice, then the GEMMs' activation rows
     __shared__ int unit_start[kMaxExperts + 1];
     __shared__ int row_start[kMaxExperts + 1];
-    __shared__ int next_s[2];
-    __shared__ int map_s[kRouterSmallT * kMaxTopK];  // slot -> token, for the gate/up GEMM's row gather
+    __shared__ int next_s[3];
+    __shared__ int req_s[2];
+    __shared__ int map_s[kRouterSmallT * kMaxTopK];    // slot -> token: the gate/up GEMM's row gather
+    __shared__ float ssl_s[kRouterSmallT * kMaxTopK];  // slot -> activation scale
+    __shared__ int offs_s[kMaxExperts + 1];            // expert slot offsets
+    __shared__ uint32_t mask_s[kRFMaxChunks * kMaxExperts];
     const int bid = blockIdx.x, nblk = gridDim.x;
     const int S = a.T * a.k;
 
     // A: router partials | per-token quantisation
+    if (bid == 0)
+        for (int e = threadIdx.x; e < a.E; e += blockDim.x) {
+            a.done1[e] = 0u;
+            a.ready2[e] = 0;
+        }
     for (int w = bid; w < a.KS + a.T; w += nblk) {
         if (w < a.KS) router_partial_body(a.x, a.Wr, a.T, a.H, a.E, a.E_pad, a.hs, a.P, fused_smem, w);
         else quant_token(a, w - a.KS);
@@ -286,30 +412,31 @@ __global__ void __launch_bounds__(kSkThreads, 2) moe_fused_kernel(const FusedArg
     }
     if (!grid_barrier(a, 1)) return fused_exit(a);
 
-    // B: top-k per token; the last token's CTA builds the tables and slot maps
-    for (int t = bid; t < a.T; t += nblk) {
-        if (router_finish_body<EPT>(a.P, a.KS, a.T, a.E, a.E_pad, a.bias, a.k, a.topk_ids, a.topk_w, a.rank,
-                                    a.hist, a.offsets, a.counts, a.ticket, a.error, t, a.T))
-            build_slots(a);
-        __syncthreads();
-    }
+    // B: top-k per token
+    for (int t = bid; t < a.T; t += nblk)
+        router_finish_body<EPT, false>(a.P, a.KS, a.T, a.E, a.E_pad, a.bias, a.k, a.topk_ids, a.topk_w, a.rank,
+                                       a.hist, a.offsets, a.counts, a.ticket, a.error, t, a.T);
     // the test hook stalls CTA 0 here: it never arrives, every wait runs out
     if (!grid_barrier(a, 2, a.stall != 0 && bid == 0)) return fused_exit(a);
 
-    // C: gate/up GEMM over the slots, rows gathered from the token-major codes
-    skinny_run<(int)Epi::GateUp, kSkSrcGather>(a.g1, reinterpret_cast<int8_t*>(fused_smem), unit_start, row_start,
-                                               next_s, bid, nblk, a.slot_token, a.T, map_s);
-    if (threadIdx.x == 0) prefetch_gemm2(a, bid);
+    // C: the routing tables (every CTA), then the gate/up GEMM over the
+    // slots, rows gathered from the token-major codes
+    build_tables(a, offs_s, map_s, ssl_s, mask_s);
+    GemmArgs g1 = a.g1;
+    g1.offsets = offs_s;
+    g1.act_scale = ssl_s;
+    FusedGateUpHook up_hook{&a, offs_s, req_s, (unsigned)(a.I / kSkUnitGateUp)};
+    skinny_run<(int)Epi::GateUp, kSkSrcGather>(g1, reinterpret_cast<int8_t*>(fused_smem), unit_start, row_start,
+                                               next_s, bid, nblk, nullptr, a.T, map_s, up_hook);
+    if (threadIdx.x == 0) prefetch_gemm2(a, offs_s, bid);
+
+    // D + E: each expert's rows requantised by the CTA that finished its last
+    // gate/up unit; the down GEMM, each expert after its flag
+    GemmArgs g2 = a.g2;
+    g2.offsets = offs_s;
+    skinny_run<(int)Epi::ScaleF32, kSkSrcRows>(g2, reinterpret_cast<int8_t*>(fused_smem), unit_start, row_start,
+                                               next_s, bid, nblk, nullptr, 0, nullptr, FusedDownHook{&a});
     if (!grid_barrier(a, 3)) return fused_exit(a);
-
-    // D: requantise h
-    for (int r = bid; r < S; r += nblk) requant_row(a, r);
-    if (!grid_barrier(a, 4)) return fused_exit(a);
-
-    // E: down GEMM
-    skinny_run<(int)Epi::ScaleF32, kSkSrcRows>(a.g2, reinterpret_cast<int8_t*>(fused_smem), unit_start, row_start,
-                                               next_s, bid, nblk);
-    if (!grid_barrier(a, 5)) return fused_exit(a);
 
     // F: combine, each token's columns in nparts parts
     const int blocks = (a.H / 4 + 255) / 256;
@@ -332,19 +459,27 @@ template <int EPT>
 cudaError_t launch_fused_impl(const FusedArgs& a, size_t smem, cudaStream_t st) {
     if (injected(kInjectLaunchFail)) return cudaErrorLaunchFailure;
     auto kern = moe_fused_kernel<EPT>;
+    // the shared-memory attribute and the resident CTAs per SM, per
+    // shared-memory size (queried once: host time here delays the launch)
     static std::mutex mu;
-    static size_t smem_set = 0;
+    static size_t smem_set = 0, occ_smem = 0;
+    static int occ_cached = 0;
+    int occ = 0;
+    cudaError_t e = cudaSuccess;
     {
         std::lock_guard<std::mutex> lock(mu);
         if (smem > smem_set) {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+            e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
             if (e != cudaSuccess) return e;
             smem_set = smem;
         }
+        if (occ_smem != smem || occ_cached == 0) {
+            e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ_cached, kern, kSkThreads, smem);
+            if (e != cudaSuccess) return e;
+            occ_smem = smem;
+        }
+        occ = occ_cached;
     }
-    int occ = 0;
-    cudaError_t e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&occ, kern, kSkThreads, smem);
-    if (e != cudaSuccess) return e;
     if (occ < 1) return cudaErrorInvalidConfiguration;
     if (occ > 2) occ = 2;
     cudaLaunchConfig_t cfg = {};
@@ -366,7 +501,7 @@ cudaError_t launch_fused_impl(const FusedArgs& a, size_t smem, cudaStream_t st) 
 
 bool fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     if (T < 1 || T > kRouterSmallT || E > kMaxExperts || k > kMaxTopK) return false;
-    if (H > 256 * 8 * kFqVec || I > 256 * 4 * kFrVec) return false;  // a row in one CTA's registers
+    if (H > 256 * 8 * kFqVec) return false;  // a row of x in one CTA's registers
     if (!skinny_shape_supported(Epi::GateUp, H, 2 * I, I) || !skinny_shape_supported(Epi::ScaleF32, I, H, 0))
         return false;
     return fused_smem_bytes(T, H, I, E) <= 200 * 1024;  // with the static shared memory, within 227 KB

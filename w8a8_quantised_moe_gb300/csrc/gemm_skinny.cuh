@@ -181,6 +181,21 @@ __device__ __forceinline__ void skinny_step(const GemmArgs& args, const int8_t* 
     }
 }
 
+// Hooks through which the one-kernel layer hands work between its GEMMs
+// inside skinny_run; SkNoHook: none (compiled away).
+struct SkNoHook {
+    static constexpr bool kWaits = false;   // ready() may wait
+    static constexpr bool kCounts = false;  // unit_end_*() need a barrier at every unit's end
+    // thread 0, before group g's rows are staged: false = give up (the CTA stops its units)
+    __device__ __forceinline__ bool ready(int) { return true; }
+    // thread 0, before the barrier that ends a unit
+    __device__ __forceinline__ void unit_end_pre() {}
+    // every thread, after it: the unit (of group g) is complete in every warp
+    __device__ __forceinline__ void unit_end_post(int) {}
+    // every thread, after the CTA's last unit
+    __device__ __forceinline__ void end() {}
+};
+
 // Where skinny_run's activation rows come from.
 enum SkSrc : int {
     kSkSrcRows = 0,    // rows [total_rows][K] of act8
@@ -219,15 +234,15 @@ __device__ __forceinline__ void skinny_stage(int8_t* act_s, const int8_t* act, i
 // bid + nblk, bid + 2 nblk, ... or, with args.sched, taken in turn from a
 // counter (one taken a unit ahead, so the atomic's latency is hidden), which
 // evens out CTAs whose units took longer.  act_s: skinny_smem_bytes(K) bytes;
-// unit_start, row_start: kMaxExperts + 1 ints; next_s: two ints (shared
-// memory: the unit taken from the counter reaches all threads through them,
-// in turn).  kSkSrcGather: row_map [total_rows] gives each row's source row
+// unit_start, row_start: kMaxExperts + 1 ints; next_s: three ints (shared
+// memory: the unit taken from the counter reaches all threads through the
+// first two, in turn; the third carries a hook's give-up).  kSkSrcGather: row_map [total_rows] gives each row's source row
 // in act8 (map_rows rows), copied to map_s (total_rows ints of shared memory)
-// first.
-template <int EPI, int SRC = kSkSrcRows>
+// first; with row_map == nullptr, map_s already holds it.
+template <int EPI, int SRC = kSkSrcRows, class Hook = SkNoHook>
 __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, int* unit_start, int* row_start,
                                            int* next_s, int bid, int nblk, const int32_t* row_map = nullptr,
-                                           int map_rows = 0, int* map_s = nullptr) {
+                                           int map_rows = 0, int* map_s = nullptr, Hook hook = Hook()) {
     const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int G = args.n_groups;
     const int unit_rows = EPI == (int)Epi::GateUp ? kSkUnitGateUp : kSkUnitScale;
@@ -270,7 +285,7 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
             }
         }
     }
-    if (SRC == kSkSrcGather)
+    if (SRC == kSkSrcGather && row_map != nullptr)
         for (int r = threadIdx.x; r < args.total_rows; r += kSkThreads) {
             const int m = row_map[r];
             map_s[r] = in_range(m, 0, map_rows, args.error) ? m : 0;
@@ -306,7 +321,12 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
     if (have) {
         cur = step_of(bid);
         skinny_load<EPI>(wv, args, cur.g, skinny_first(EPI, cur.unit, warp * skinny_items(EPI)), 0, lane);
-        skinny_stage<SRC>(act_s, act, K, cur.row0, min(kSkChunk, cur.r_end - cur.row0), map_s);
+        if (Hook::kWaits) {
+            if (threadIdx.x == 0) next_s[2] = hook.ready(cur.g) ? 0 : 1;
+            __syncthreads();
+            have = next_s[2] == 0;
+        }
+        if (have) skinny_stage<SRC>(act_s, act, K, cur.row0, min(kSkChunk, cur.r_end - cur.row0), map_s);
     }
     __syncthreads();
     while (have) {
@@ -324,7 +344,12 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
         // never share a first row); every warp's next batch is in flight
         const bool restage = next_ok && nxt.row0 != cur.row0;
         if (dyn && new_unit && threadIdx.x == 0) next_s[ph] = un < total_units ? (int)grab : total_units;
-        if (restage || (dyn && new_unit)) __syncthreads();  // every warp is done with act_s / next_s is set
+        if (new_unit) hook.unit_end_pre();
+        if (Hook::kWaits && restage && threadIdx.x == 0) next_s[2] = hook.ready(nxt.g) ? 0 : 1;
+        // every warp is done with act_s / next_s is set / a hook's word is set
+        if (restage || (dyn && new_unit) || (Hook::kCounts && new_unit)) __syncthreads();
+        if (new_unit) hook.unit_end_post(cur.g);
+        if (Hook::kWaits && restage && next_s[2] != 0) break;  // every thread alike
         if (restage) {
             skinny_stage<SRC>(act_s, act, K, nxt.row0, min(kSkChunk, nxt.r_end - nxt.row0), map_s);
             __syncthreads();
@@ -341,6 +366,7 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
         cur = nxt;
         have = next_ok;
     }
+    hook.end();
     if (dyn) {  // the last CTA out leaves the counter words zero for the next launch
         __syncthreads();
         if (threadIdx.x == 0) {

@@ -110,6 +110,8 @@ struct FusedArgs {
     float* o;
     uint16_t* y;
     GemmArgs g1, g2;
+    unsigned int* done1;  // [E] gate/up GEMM units finished per expert
+    int* ready2;          // [E] nonzero once the expert's rows of h are requantised
     unsigned int* bar;
     int* abort;
     unsigned int* exits;
@@ -118,7 +120,7 @@ struct FusedArgs {
     int stall;  // test hook (MOE_INJECT=stall): CTA 0 skips one barrier arrival, every wait runs out
 };
 // Shapes the one-kernel layer takes: T <= kRouterSmallT, both GEMMs on the
-// dp4a kernel's unit shapes, a row of x and of h in one CTA's registers.
+// dp4a kernel's unit shapes, a row of x in one CTA's registers.
 bool fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 cudaError_t launch_moe_fused(const FusedArgs& a, cudaStream_t st);
 
@@ -127,7 +129,8 @@ cudaError_t launch_moe_fused(const FusedArgs& a, cudaStream_t st);
 // few-token router's ticket and of the one-kernel layer's barrier words.
 constexpr size_t kTicketOffset = 128;
 constexpr size_t kFusedCtlOffset = 192;
-// the two counter words of the dp4a GEMM's unit scheduling (GemmArgs::sched)
+// the counter words of the dp4a GEMMs' unit scheduling (GemmArgs::sched;
+// two per GEMM)
 constexpr size_t kSchedOffset = 224;
 
 // Launch plan of the router GEMM: experts padded to E_pad (a multiple of 16,
@@ -143,7 +146,7 @@ RouterPlan router_plan(int64_t T, int64_t H, int64_t E);
 // Forward workspace layout (byte offsets; every region 256-byte aligned).
 struct FwdLayout {
     size_t err, counts, wsplit, logits, topk_ids, topk_w, rank, hist, offsets, slot_of, slot_token, s_x,
-        s_slot, flag1, list1, flag2, list2, q_x16, h, s_h, q_h16, o, total;
+        s_slot, flag1, list1, flag2, list2, q_x16, h, s_h, q_h16, o, fctl, total;
 };
 FwdLayout fwd_layout(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k);
 

@@ -217,8 +217,9 @@ __device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__
 
 // The body of router_finish_kernel for token t of a grid of n_cta CTAs (one
 // per token); the CTA that takes the last ticket builds the routing tables
-// and returns true (every thread), the others return false.
-template <int EPT>
+// and returns true (every thread), the others return false.  TABLES = false:
+// the token's choices only (no ticket, no tables; returns false).
+template <int EPT, bool TABLES = true>
 __device__ __forceinline__ bool router_finish_body(const float* __restrict__ P, int KS, int T, int E, int E_pad,
                                                    const float* __restrict__ bias, int k,
                                                    int32_t* __restrict__ topk_ids, float* __restrict__ topk_w,
@@ -276,6 +277,10 @@ __device__ __forceinline__ bool router_finish_body(const float* __restrict__ P, 
         }
     }
 
+    if (!TABLES) {
+        __syncthreads();  // part is reused by the CTA's next token
+        return false;
+    }
     // ---- the last CTA: chunk masks, ranks, then the prefix sums
     __threadfence();  // this CTA's choices are visible device-wide before the ticket
     __syncthreads();

@@ -34,9 +34,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) grouped_gemm_skinny_kernel(cons
     __shared__ int unit_start[kMaxExperts + 1];
     __shared__ int row_start[kMaxExperts + 1];
     __shared__ int next_s[3];
-    pdl_wait();  // the previous kernel's outputs (offsets, codes, scales) are visible from here
-    pdl_trigger();
-    skinny_run<EPI>(args, act_s, unit_start, row_start, next_s, blockIdx.x, gridDim.x);
+    skinny_run<EPI, kSkSrcRows, SkNoHook, true>(args, act_s, unit_start, row_start, next_s, blockIdx.x, gridDim.x);
 }
 
 template <int EPI>

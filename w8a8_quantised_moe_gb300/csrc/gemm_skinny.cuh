@@ -239,7 +239,12 @@ __device__ __forceinline__ void skinny_stage(int8_t* act_s, const int8_t* act, i
 // first two, in turn; the third carries a hook's give-up).  kSkSrcGather: row_map [total_rows] gives each row's source row
 // in act8 (map_rows rows), copied to map_s (total_rows ints of shared memory)
 // first; with row_map == nullptr, map_s already holds it.
-template <int EPI, int SRC = kSkSrcRows, class Hook = SkNoHook>
+// PDL (a separate kernel launched with programmatic dependent launch): the
+// unit table is built, and thread 0 prefetches its first unit's weights into
+// L2, before the wait for the previous kernel (the expert offsets and the
+// weights were complete before that kernel started; the activation rows and
+// scales are read only after the wait).
+template <int EPI, int SRC = kSkSrcRows, class Hook = SkNoHook, bool PDL = false>
 __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, int* unit_start, int* row_start,
                                            int* next_s, int bid, int nblk, const int32_t* row_map = nullptr,
                                            int map_rows = 0, int* map_s = nullptr, Hook hook = Hook()) {
@@ -290,9 +295,25 @@ __device__ __forceinline__ void skinny_run(const GemmArgs& args, int8_t* act_s, 
             const int m = row_map[r];
             map_s[r] = in_range(m, 0, map_rows, args.error) ? m : 0;
         }
-    if (dyn && threadIdx.x == 0) next_s[0] = nblk + (int)atomicAdd(args.sched, 1u);  // used if bid has a unit
     __syncthreads();
     const int total_units = unit_start[G];
+    if (PDL) {
+        if (threadIdx.x == 0 && bid < total_units) {
+            const int g = last_le(unit_start, G, bid);
+            const int first = skinny_first(EPI, bid - unit_start[g], 0);
+            const int8_t* w = static_cast<const int8_t*>(args.w) + ((size_t)g * args.w_rows_per_group + first) * args.K;
+            if (EPI == (int)Epi::GateUp) {  // the unit's gate rows and its up rows
+                prefetch_l2_bulk(w, (uint32_t)((size_t)kSkUnitGateUp * args.K));
+                prefetch_l2_bulk(w + (size_t)args.up_offset * args.K, (uint32_t)((size_t)kSkUnitGateUp * args.K));
+            } else {
+                prefetch_l2_bulk(w, (uint32_t)((size_t)kSkUnitScale * args.K));
+            }
+        }
+        pdl_wait();
+        pdl_trigger();
+    }
+    if (dyn && threadIdx.x == 0) next_s[0] = nblk + (int)atomicAdd(args.sched, 1u);  // used if bid has a unit
+    __syncthreads();
     const int K = args.K;
     const int8_t* act = args.act8;
     const int nbat = (K + kSkNB * 512 - 1) / (kSkNB * 512);

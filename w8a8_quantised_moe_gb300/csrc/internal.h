@@ -162,8 +162,16 @@ LinLayout lin_layout(int64_t M, int64_t N, int64_t K);
 // previous grid has completed and its memory is visible, before its first
 // global memory access.  Every kernel of the layer calls pdl_wait() first and
 // pdl_trigger() right after it, so at most two grids overlap: the one
-// finishing and the next one's set-up.  The first kernel of each entry point
-// is launched without it (it then serialises like a plain launch).
+// finishing and the next one's set-up.  One exception: the one-CTA-per-row
+// requantiser (few rows: decode) triggers before it waits, so that the down
+// GEMM's CTAs take the SMs that the gate/up GEMM's last CTAs leave and
+// prefetch their first weights there; each grid still waits for its
+// predecessor's completion, and a dependent grid launches only once every
+// CTA of its predecessor is running, so no grid can hold the SMs that an
+// earlier one still needs.  The first kernel of each entry point is launched
+// without PDL (it then serialises like a plain launch).  The dp4a GEMM reads
+// the expert offsets and its weights before its wait (both complete before
+// its predecessor started).
 #ifdef __CUDACC__
 // Checked build: true when lo <= v < hi, else records kErrDevice (when error
 // is given) and returns false.  Always true in the normal build.

@@ -113,8 +113,11 @@ __global__ void __launch_bounds__(256) requant_cta_kernel(const float* __restric
     __shared__ int red_l1[8];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int r = blockIdx.x;
-    pdl_wait();
+    // the next kernel (the down GEMM) may launch before this one waits: its
+    // CTAs then take the SMs that the gate/up GEMM's last CTAs leave, and
+    // prefetch their first weights while those finish
     pdl_trigger();
+    pdl_wait();
     if (r >= S) return;
     const float4* row = reinterpret_cast<const float4*>(h + (size_t)r * I);
     const int nv = I / 4;

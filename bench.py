@@ -331,7 +331,7 @@ def layer_roofline_us(cfg, offsets, peaks, fmt="int8"):
 
 GEMM_SOURCES = {
     "int8": ("gemm.cu", "gemm_pair.cu", "gemm_skinny.cu", "gemm_skinny.cuh", "gemm_common.cuh", "ptx.cuh",
-             "internal.h"),
+             "internal.h", "fused.cu", "router_small.cuh"),
     "fp8": ("fp8.cu", "gemm_fp8_pair.cu", "gemm_common.cuh", "ptx.cuh", "internal.h"),
 }
 

@@ -79,55 +79,6 @@ __device__ bool grid_barrier(const FusedArgs& a, unsigned n, bool skip_arrival =
     return ok_s != 0;
 }
 
-// Phase A, token t: s_x[t] = amax / 127 and the codes of x[t] (one CTA of
-// 256 threads, the row in registers: H <= 256 * 8 * 8).  The arithmetic of
-// the multi-kernel forward's per-token quantiser.
-constexpr int kFqVec = 8;
-
-__device__ void quant_token(const FusedArgs& a, int t) {
-    __shared__ float red_max[8];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int H = a.H;
-    const uint4* row = reinterpret_cast<const uint4*>(a.x + (size_t)t * H);
-    const int nv = H / 8;
-    uint4 v[kFqVec];
-    float amax = 0.f;
-#pragma unroll
-    for (int i = 0; i < kFqVec; ++i) {
-        const int idx = tid + 256 * i;
-        v[i] = idx < nv ? __ldg(row + idx) : make_uint4(0u, 0u, 0u, 0u);
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            amax = fmaxf(amax, fabsf(__uint_as_float((w[j] & 0xffffu) << 16)));
-            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
-        }
-    }
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
-    if (lane == 0) red_max[warp] = amax;
-    __syncthreads();
-    amax = red_max[0];
-#pragma unroll
-    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
-    const float s = __fdiv_rn(amax, 127.0f);
-    if (tid == 0) a.s_x[t] = s;
-#pragma unroll
-    for (int i = 0; i < kFqVec; ++i) {
-        const int idx = tid + 256 * i;
-        if (idx >= nv) break;
-        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
-        int q[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            q[2 * j] = quant_code_div(__uint_as_float((w[j] & 0xffffu) << 16), s);
-            q[2 * j + 1] = quant_code_div(__uint_as_float(w[j] & 0xffff0000u), s);
-        }
-        reinterpret_cast<uint2*>(a.q_tok + (size_t)t * H)[idx] = pack_codes_s8(q);
-    }
-    __syncthreads();  // red_max is reused by the next token of this CTA
-}
-
 // After the top-k phase, in every CTA: the routing tables in shared memory
 // (the slot of (token t, choice j) routed to expert e is offsets[e] plus the
 // number of earlier tokens routed to e: the multi-kernel forward's order), so
@@ -407,7 +358,7 @@ __global__ void __launch_bounds__(kSkThreads, 2) moe_fused_kernel(const FusedArg
         }
     for (int w = bid; w < a.KS + a.T; w += nblk) {
         if (w < a.KS) router_partial_body(a.x, a.Wr, a.T, a.H, a.E, a.E_pad, a.hs, a.P, fused_smem, w);
-        else quant_token(a, w - a.KS);
+        else quant_token_body(a.x, a.H, w - a.KS, a.s_x, a.q_tok);
         __syncthreads();  // the slice's shared memory is reused by the next item
     }
     if (!grid_barrier(a, 1)) return fused_exit(a);
@@ -501,7 +452,7 @@ cudaError_t launch_fused_impl(const FusedArgs& a, size_t smem, cudaStream_t st) 
 
 bool fused_supported(int64_t T, int64_t H, int64_t I, int64_t E, int64_t k) {
     if (T < 1 || T > kRouterSmallT || E > kMaxExperts || k > kMaxTopK) return false;
-    if (H > 256 * 8 * kFqVec) return false;  // a row of x in one CTA's registers
+    if (H > 256 * 8 * kQtVec) return false;  // a row of x in one CTA's registers
     if (!skinny_shape_supported(Epi::GateUp, H, 2 * I, I) || !skinny_shape_supported(Epi::ScaleF32, I, H, 0))
         return false;
     return fused_smem_bytes(T, H, I, E) <= 200 * 1024;  // with the static shared memory, within 227 KB

@@ -126,6 +126,58 @@ __device__ __forceinline__ void cp_async4(void* smem_dst, const void* gmem_src) 
                  : "memory");
 }
 
+// Per-token dynamic quantisation of row t of x (bf16 [.][H]) by one CTA of
+// 256 threads, the row held in registers (H <= 256 * 8 * kQtVec): s_x[t] =
+// amax / 127 and the token's codes, written once (token-major) to q_tok
+// [.][H].  The arithmetic of the per-slot quantisers of route.cu; the
+// one-kernel layer runs it beside the router's partial logits, its gate/up
+// GEMM gathering rows through the slot -> token map.
+constexpr int kQtVec = 8;
+
+__device__ __forceinline__ void quant_token_body(const uint16_t* __restrict__ x, int H, int t, float* __restrict__ s_x,
+                                                 int8_t* __restrict__ q_tok) {
+    __shared__ float red_max[8];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const uint4* row = reinterpret_cast<const uint4*>(x + (size_t)t * H);
+    const int nv = H / 8;
+    uint4 v[kQtVec];
+    float amax = 0.f;
+#pragma unroll
+    for (int i = 0; i < kQtVec; ++i) {
+        const int idx = tid + 256 * i;
+        v[i] = idx < nv ? __ldg(row + idx) : make_uint4(0u, 0u, 0u, 0u);
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            amax = fmaxf(amax, fabsf(__uint_as_float((w[j] & 0xffffu) << 16)));
+            amax = fmaxf(amax, fabsf(__uint_as_float(w[j] & 0xffff0000u)));
+        }
+    }
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) amax = fmaxf(amax, __shfl_xor_sync(0xffffffffu, amax, off));
+    if (lane == 0) red_max[warp] = amax;
+    __syncthreads();
+    amax = red_max[0];
+#pragma unroll
+    for (int i = 1; i < 8; ++i) amax = fmaxf(amax, red_max[i]);
+    const float s = __fdiv_rn(amax, 127.0f);
+    if (tid == 0) s_x[t] = s;
+#pragma unroll
+    for (int i = 0; i < kQtVec; ++i) {
+        const int idx = tid + 256 * i;
+        if (idx >= nv) break;
+        const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+        int q[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            q[2 * j] = quant_code_div(__uint_as_float((w[j] & 0xffffu) << 16), s);
+            q[2 * j + 1] = quant_code_div(__uint_as_float(w[j] & 0xffff0000u), s);
+        }
+        reinterpret_cast<uint2*>(q_tok + (size_t)t * H)[idx] = pack_codes_s8(q);
+    }
+    __syncthreads();  // red_max is reused by the CTA's next token
+}
+
 // The body of router_partial_kernel for slice s; rp_smem: the kernel's dynamic
 // shared memory (router_plan's partial_smem bytes).
 __device__ __forceinline__ void router_partial_body(const uint16_t* __restrict__ x, const float* __restrict__ Wr,

@@ -2,33 +2,38 @@
 // persistent kernel: router, top-k and routing tables, per-token activation
 // quantisation, the gate/up GEMM with the SiLU-times-up epilogue, the
 // requantisation of its output, the down GEMM and the weighted combine run as
-// phases of a single cooperative launch, separated by grid-wide barriers.
+// phases of a single cooperative launch.
 //
 // "Tencent Hunyuan AI Infra on Hopper" (pnsm.cn), section 1.3, describes the
 // fused MoE operator as one kernel that runs gate, top-k, the routing
 // pre-processing, both expert GEMMs and the weighted aggregation in turn.
 // Here the phases reuse the device bodies of the multi-kernel forward (the
-// few-token router of router_small.cuh, the dp4a work-unit loop of
-// gemm_skinny.cuh) and the same quantisation arithmetic, so that every
-// intermediate and the output equal that forward's bit for bit.  Two things
-// differ from it: the activation codes are written once per token (not once
-// per slot) in the first phase, next to the router, and the gate/up GEMM
-// gathers its rows through the slot -> token map; and no kernel boundary
-// separates the phases, only a barrier.
+// few-token router and the per-token quantiser of router_small.cuh, the dp4a
+// work-unit loop of gemm_skinny.cuh) and the same arithmetic, so that every
+// intermediate and the output equal that forward's bit for bit.  What differs
+// from it: the activation codes are written once per token (not once per
+// slot), next to the router, and the gate/up GEMM gathers its rows through the
+// slot -> token map; the routing tables are built by every CTA in its own
+// shared memory; and no kernel boundary separates the phases.
 //
 // Phases (CTA b of nblk, all CTAs resident: a cooperative launch):
 //   A  router partial logits of K slice s (CTAs s < KS) and, on the next T
 //      CTAs, the per-token quantisation of x (codes token-major)
-//   B  per token: slice sums, bias, top-k and softmax weights; the CTA that
-//      finishes last builds the routing tables and the slot maps
-//   C  gate/up GEMM (dp4a), epilogue h = silu(gate) * up
-//   D  per slot row of h: s_h = amax / 127 and its int8 codes
-//   E  down GEMM (dp4a), o = (acc * s_h) * s_w
+//                                                        -- grid barrier 1
+//   B  per token: slice sums, bias, top-k and softmax weights
+//                                                        -- grid barrier 2
+//   C  every CTA: the routing tables (shared memory); the gate/up GEMM (dp4a),
+//      epilogue h = silu(gate) * up, units taken from a counter
+//   D  the CTA that finishes an expert's last gate/up unit requantises the
+//      expert's rows of h (s_h = amax / 127, int8 codes) and raises its flag
+//   E  down GEMM (dp4a), o = (acc * s_h) * s_w; an expert's rows are staged
+//      after its flag, so the down GEMM starts while the gate/up GEMM's last
+//      units run                                         -- grid barrier 3
 //   F  y[t] = bf16(sum_j w[t][j] * o[slot(t, j)]) in top-k order
-// Every wait (the barriers) is bounded by the library's wait limit; a CTA
-// that runs out sets the timeout bit of the error word and an abort flag,
-// after which every CTA skips the remaining phases and returns.  The last CTA
-// to return clears the barrier words for the next call.
+// Every wait (the barriers, the experts' flags) is bounded by the library's
+// wait limit; a CTA that runs out sets the timeout bit of the error word and
+// an abort flag, after which every CTA skips the remaining phases and
+// returns.  The last CTA to return clears the barrier words for the next call.
 #include <mutex>
 
 #include "gemm_common.cuh"

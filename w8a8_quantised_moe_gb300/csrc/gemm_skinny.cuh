@@ -1,7 +1,7 @@
 // gemm_skinny.cuh -- the dp4a grouped GEMM's work-unit loop as a device
 // function: the body of grouped_gemm_skinny_kernel (gemm_skinny.cu) and of the
-// GEMM phases of the fused decode kernel (fused.cu).  What it computes and
-// why it is shaped so: gemm_skinny.cu.
+// GEMM phases of the one-kernel layer (fused.cu).  What it computes and why
+// it is shaped so: gemm_skinny.cu.
 #pragma once
 
 #include "gemm_common.cuh"

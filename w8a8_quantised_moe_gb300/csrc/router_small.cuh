@@ -1,6 +1,7 @@
-// router_small.cuh -- the top-k selection and the few-token (CUDA-core)
-// router as device functions: used by router.cu's kernels and by the fused
-// decode kernel (fused.cu), which must route exactly as they do.
+// router_small.cuh -- the top-k selection, the few-token (CUDA-core) router
+// and a per-token quantiser as device functions: used by router.cu's kernels
+// and by the one-kernel layer (fused.cu), which must route and quantise
+// exactly as the multi-kernel layer does.
 #pragma once
 
 #include <cuda_bf16.h>

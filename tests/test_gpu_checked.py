@@ -8,8 +8,8 @@ Checked through the C ABI of the checked library, loaded beside the normal
 one:
   * on valid inputs it gives the normal build's results bit for bit (MoE
     layers on each GEMM kernel and quantiser form, with a router bias and
-    top-8, the FP8 layer, the linear layer) and leaves the error word clear;
-    one layer is also compared with the oracle;
+    top-8, the FP8 layer, the linear layer, the one-kernel layer) and leaves
+    the error word clear; one layer is also compared with the oracle;
   * a slot index out of range, planted by its test hook after the quantiser
     (MOE_INJECT=bad_slot overwrites slot_of[0] with 0x7f7f7f7f), is caught by
     the combine's check: MOE_ERR_DEVICE, no fault, every other token's output
@@ -115,6 +115,34 @@ def test_checked_build_equals_normal_build_linear(libs):
         assert lib.moe_w8a8_device_error(ws.data_ptr(), _stream()) == OK
         outs.append(bf16_from_dev(y))
     np.testing.assert_array_equal(outs[1], outs[0])
+
+
+FUSED_SHAPES = {  # T <= 128: the shapes the one-kernel layer takes
+    "tiny": TINY,
+    "decode": SHAPES["decode"],
+    "top8": TINY.replace(T=100, H=256, I=128, E=256, k=8, bias="normal", bias_std=0.5),
+}
+
+
+@pytest.mark.parametrize("name", list(FUSED_SHAPES))
+def test_checked_build_equals_normal_build_one_kernel_layer(libs, name):
+    normal, checked = libs
+    layer = Layer(FUSED_SHAPES[name])
+    x, Wr, bias, w13, s13, w2, s2, k = layer.device_args()
+    T, H = x.shape
+    E, I = w13.shape[0], w13.shape[1] // 2
+    ptr = lambda t: None if t is None else t.data_ptr()  # noqa: E731
+    outs = []
+    for lib in (normal, checked):
+        ws = moe.new_workspace(moe.workspace_size(T, H, I, E, k))
+        y = torch.empty((T, H), dtype=torch.bfloat16, device="cuda")
+        assert lib.moe_w8a8_forward_fused(ptr(x), ptr(Wr), ptr(bias), ptr(w13), ptr(s13), ptr(w2), ptr(s2), T, H, I,
+                                          E, k, ptr(y), ptr(ws), ws.numel(), _stream(), None) == OK
+        assert lib.moe_w8a8_device_error(ws.data_ptr(), _stream()) == OK
+        outs.append(bf16_from_dev(y))
+    np.testing.assert_array_equal(outs[1], outs[0])
+    y_multi, _ = _forward(normal, layer)
+    np.testing.assert_array_equal(outs[0], y_multi)
 
 
 def test_checked_build_reports_a_slot_out_of_range(libs, monkeypatch):

@@ -8,7 +8,8 @@ intermediate of the debug dump (routing, slot maps, scales, codes, the raw
 int32 accumulators of both GEMMs, h, o).  y is also compared with the oracle
 directly.  Shapes: one token, a few tokens per expert, the 128-token maximum,
 a single expert, 256 experts with top-8 and a router bias (most experts
-empty), rows of h longer than 8192, and the decode layer at full size.  Then
+empty), rows of h longer than 8192, the decode layer at full size, and the
+256-expert layer's shape at 128 tokens.  Then
 the failure path: with MOE_INJECT=stall one CTA skips a barrier arrival, the
 2 ms wait limit runs out everywhere, MOE_ERR_DEVICE_TIMEOUT is reported, and
 the next calls on the same workspace are exact again."""
@@ -97,6 +98,31 @@ def test_fused_decode_layer_at_full_size():
     sel = np.arange(0, cfg.T, 8)  # the oracle on every 8th token
     y_o = oracle.moe_forward(inp.x[sel], inp.Wr, inp.bias, layer.w13_q, layer.s13, layer.w2_q, layer.s2, cfg.k)
     assert_y_close(y_f[sel], y_o)
+
+
+def test_fused_wide_layer_at_128_tokens():
+    """T = 128, H = 7168, I = 2048, E = 256, top-8 with a router bias (the
+    256-expert layer's shape at the one-kernel layer's token limit; random
+    int8 weights drawn on the device): bit for bit the multi-kernel layer."""
+    cfg = wl.CONFIGS["wide"].replace(T=128)
+    inp = wl.make_moe_inputs(cfg, 0)
+    g = torch.Generator(device="cuda").manual_seed(11)
+    w13 = torch.randint(-127, 128, (cfg.E, 2 * cfg.I, cfg.H), dtype=torch.int8, generator=g, device="cuda")
+    w2 = torch.randint(-127, 128, (cfg.E, cfg.H, cfg.I), dtype=torch.int8, generator=g, device="cuda")
+    s13 = torch.rand((cfg.E, 2 * cfg.I), generator=g, device="cuda") * 1e-3 + 1e-4
+    s2 = torch.rand((cfg.E, cfg.H), generator=g, device="cuda") * 1e-3 + 1e-4
+    x = torch.from_numpy(np.ascontiguousarray(inp.x).view(np.int16)).view(torch.bfloat16).cuda()
+    bias = None if inp.bias is None else torch.from_numpy(inp.bias).cuda()
+    args = (x, torch.from_numpy(inp.Wr).cuda(), bias, w13, s13, w2, s2, cfg.k)
+    assert moe.fused_supported(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k)
+    ws = moe.new_workspace(moe.workspace_size(cfg.T, cfg.H, cfg.I, cfg.E, cfg.k))
+    fields = ("topk_ids", "offsets", "slot_token", "s_h", "q_h")
+    y_p, d_p = moe.forward_debug(*args, fields=fields, workspace=ws)
+    y_f, d_f = moe.forward_fused(*args, fields=fields, workspace=ws)
+    assert moe.device_error(ws) == OK
+    np.testing.assert_array_equal(bf16_from_dev(y_f), bf16_from_dev(y_p))
+    for field in fields:
+        np.testing.assert_array_equal(d_f[field].cpu().numpy(), d_p[field].cpu().numpy(), err_msg=field)
 
 
 def test_forced_timeout_in_the_fused_layer_then_exact_again(monkeypatch):

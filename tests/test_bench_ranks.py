@@ -92,10 +92,12 @@ def test_committed_profile_tables_are_read_for_the_current_sources():
     import json
     with open(os.path.join(ROOT, "profiles", "traffic.json")) as f:
         table = json.load(f)
-    for cfg, fmt in (("prefill", "int8"), ("decode", "int8"), ("prefill_fp8", "fp8"), ("decode_fp8", "fp8")):
-        ent = table[cfg]["gemm1_gateup"]
+    for cfg, kernel, fmt in (("prefill", "gemm1_gateup", "int8"), ("decode", "gemm1_gateup", "int8"),
+                             ("decode", "fused_layer", "int8"), ("prefill_fp8", "gemm1_gateup", "fp8"),
+                             ("decode_fp8", "gemm1_gateup", "fp8")):
+        ent = table[cfg][kernel]
         want = ent["dram_bytes_per_launch"] if ent["gemm_src_sha256_16"] == bench.gemm_source_sha(fmt) else None
-        assert bench.traffic_from_profiles(cfg, "gemm1_gateup", fmt) == want
+        assert bench.traffic_from_profiles(cfg, kernel, fmt) == want
     assert bench.traffic_from_profiles("no_such_workload", "gemm1_gateup") is None
     f16, e4m3 = bench.tensor_rate_from_profiles("int8"), bench.tensor_rate_from_profiles("fp8")
     assert f16 > 0 and e4m3 > f16
